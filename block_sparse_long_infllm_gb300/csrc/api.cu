@@ -1,0 +1,262 @@
+// api.cu -- the C ABI of libinfllmv2.so (declared in include/infllmv2.h): argument checks,
+// workspace carving and kernel launches.  Nothing here allocates device memory: the caller
+// owns every buffer, as in the static-memory design of "CPM.cu：端侧大模型推理的 CUDA 加速引擎"
+// (section 4, preallocated KV cache).
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "infllmv2.h"
+#include "internal.h"
+
+using infllmv2::Params;
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr int kMaxDevices = 64;
+constexpr int kMaxLen = 1 << 28;
+
+// Device error word: bits of infllmv2::kDevErr*, set by kernels, read and cleared by
+// infllmv2_sync_status.
+__device__ int g_device_error;
+
+std::mutex g_err_mutex;
+int* g_err_ptr[kMaxDevices] = {};
+
+int* device_error_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_err_mutex);
+    if (g_err_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_group(int G) { return G == 1 || G == 2 || G == 4 || G == 8 || G == 16; }
+
+// Checks the parameter struct; fills the kernel-side copy (with the scale resolved for d).
+int check_params(const infllmv2_params* in, int d, Params* out) {
+    if (in == nullptr) return INFLLMV2_ERR_INVALID_ARG;
+    const infllmv2_params& p = *in;
+    if (p.kernel_size <= 0 || p.kernel_stride <= 0 || p.topk < 0 || p.n_init_blocks < 0 ||
+        p.n_local_blocks < 1 || p.dense_len < 0 || !(p.softmax_scale >= 0.f) || !isfinite(p.softmax_scale))
+        return INFLLMV2_ERR_INVALID_ARG;
+    if (p.block_size != 64 && p.block_size != 128) return INFLLMV2_ERR_UNSUPPORTED;
+    if (p.kernel_size > p.block_size || p.kernel_stride > p.block_size) return INFLLMV2_ERR_UNSUPPORTED;
+    out->block_size = p.block_size;
+    out->kernel_size = p.kernel_size;
+    out->kernel_stride = p.kernel_stride;
+    out->topk = p.topk;
+    out->n_init = p.n_init_blocks;
+    out->n_local = p.n_local_blocks;
+    out->dense_len = p.dense_len;
+    out->scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf(static_cast<float>(d > 0 ? d : 1));
+    return INFLLMV2_OK;
+}
+
+int check_heads(int Hq, int Hkv, int d) {
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return INFLLMV2_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return INFLLMV2_ERR_UNSUPPORTED;
+    if (!supported_group(Hq / Hkv)) return INFLLMV2_ERR_UNSUPPORTED;
+    return INFLLMV2_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? INFLLMV2_OK : INFLLMV2_ERR_CUDA; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int n_blocks(int L_max, int bs) { return (L_max + bs - 1) / bs; }
+
+// Decode workspace: scores | idx | counts | split partials, each 256-byte aligned.
+struct DecodeWs {
+    size_t scores, idx, counts, part, total;
+};
+
+// Sized for tree verification (one extra split per row) whether or not a mask is passed.
+DecodeWs decode_ws(int B, int n_draft, int Hkv, int d, int L_max, const Params& p) {
+    DecodeWs w{};
+    const int S_cap = infllmv2::selection_capacity(p, L_max);
+    int bps, nsc, ns;
+    infllmv2::decode_split_shape(S_cap, p.block_size, true, &bps, &nsc, &ns);
+    const size_t rows = static_cast<size_t>(B) * Hkv * n_draft;
+    w.scores = 0;
+    w.idx = align256(w.scores + rows * n_blocks(L_max, p.block_size) * sizeof(float));
+    w.counts = align256(w.idx + rows * S_cap * sizeof(int));
+    w.part = align256(w.counts + rows * sizeof(int));
+    w.total = align256(w.part + infllmv2::decode_partial_bytes(B, n_draft, Hkv, d, ns));
+    return w;
+}
+
+int blocks_per_score_cta(const Params& p) { return 2048 / p.block_size; }
+
+}  // namespace
+
+extern "C" {
+
+const char* infllmv2_status_string(int status) {
+    switch (status) {
+        case INFLLMV2_OK: return "ok";
+        case INFLLMV2_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad size or range)";
+        case INFLLMV2_ERR_UNSUPPORTED: return "unsupported configuration (head dim, group size, block size)";
+        case INFLLMV2_ERR_WORKSPACE: return "workspace missing or too small";
+        case INFLLMV2_ERR_CUDA: return "CUDA runtime error";
+        case INFLLMV2_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
+        case INFLLMV2_ERR_DEVICE_INDEX: return "device saw kv_len or a selected block id out of range";
+        case INFLLMV2_ERR_NOT_IMPLEMENTED: return "not implemented";
+        default: return "unknown status";
+    }
+}
+
+int infllmv2_version(void) { return kVersion; }
+
+int infllmv2_sync_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return INFLLMV2_ERR_CUDA;
+    int* ep = device_error_ptr();
+    if (ep == nullptr) return INFLLMV2_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, ep, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return INFLLMV2_ERR_CUDA;
+    if (word != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(ep, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return INFLLMV2_ERR_CUDA;
+    }
+    if (word & infllmv2::kDevErrTimeout) return INFLLMV2_ERR_DEVICE_TIMEOUT;
+    if (word & infllmv2::kDevErrIndex) return INFLLMV2_ERR_DEVICE_INDEX;
+    return INFLLMV2_OK;
+}
+
+int infllmv2_selection_capacity(const infllmv2_params* params, int L_max) {
+    Params p;
+    if (L_max <= 0 || L_max > kMaxLen || check_params(params, 128, &p) != INFLLMV2_OK) return -1;
+    return infllmv2::selection_capacity(p, L_max);
+}
+
+size_t infllmv2_workspace_size(int entry, int B, int Tq, int Hq, int Hkv, int d, int L_max,
+                               const infllmv2_params* params) {
+    Params p;
+    if (B < 0 || Tq < 0 || L_max <= 0 || L_max > kMaxLen) return 0;
+    if (check_params(params, d, &p) != INFLLMV2_OK || check_heads(Hq, Hkv, d) != INFLLMV2_OK) return 0;
+    switch (entry) {
+        case INFLLMV2_ENTRY_BLOCK_SELECT: return align256(infllmv2::select_workspace_bytes(B, Tq, Hkv, L_max, p));
+        case INFLLMV2_ENTRY_SPARSE_ATTN_FWD: return 0;
+        case INFLLMV2_ENTRY_DECODE: return decode_ws(B, Tq, Hkv, d, L_max, p).total;
+        default: return 0;
+    }
+}
+
+int infllmv2_kernel_pool(const void* k_cache, void* kernel_cache, int B, int Hkv, int L_max, int M_max,
+                         int d, int tok_begin, int tok_end, const infllmv2_params* params, void* stream) {
+    Params p;
+    if (int rc = check_params(params, d, &p)) return rc;
+    if (d != 64 && d != 128) return INFLLMV2_ERR_UNSUPPORTED;
+    if (B < 0 || Hkv <= 0 || L_max <= 0 || L_max > kMaxLen || M_max < 0) return INFLLMV2_ERR_INVALID_ARG;
+    if (tok_begin < 0 || tok_begin > tok_end || tok_end > L_max) return INFLLMV2_ERR_INVALID_ARG;
+    const int c = p.kernel_size, s = p.kernel_stride;
+    const int num = tok_begin - c + 1;
+    const int j_first = num <= 0 ? 0 : (num + s - 1) / s;
+    const int j_last = tok_end >= c ? (tok_end - c) / s : -1;
+    const int n_new = j_last - j_first + 1;
+    if (B == 0 || n_new <= 0) return INFLLMV2_OK;
+    if (j_last >= M_max) return INFLLMV2_ERR_INVALID_ARG;
+    if (!k_cache || !kernel_cache || !aligned16(k_cache) || !aligned16(kernel_cache)) return INFLLMV2_ERR_INVALID_ARG;
+    return cuda_status(infllmv2::launch_kernel_pool(k_cache, kernel_cache, B, Hkv, L_max, M_max, d, j_first, n_new,
+                                                    c, s, static_cast<cudaStream_t>(stream)));
+}
+
+int infllmv2_block_select(const void* q, const void* kernel_cache, const int32_t* kv_len, int B, int Tq, int Hq,
+                          int Hkv, int d, int L_max, int M_max, int32_t* idx, int32_t* counts, int S_max,
+                          void* workspace, size_t ws_bytes, const infllmv2_params* params, void* stream) {
+    Params p;
+    if (int rc = check_params(params, d, &p)) return rc;
+    if (int rc = check_heads(Hq, Hkv, d)) return rc;
+    if (B < 0 || Tq < 0 || L_max <= 0 || L_max > kMaxLen || M_max < 0) return INFLLMV2_ERR_INVALID_ARG;
+    if (B == 0 || Tq == 0) return INFLLMV2_OK;
+    if (Tq > L_max) return INFLLMV2_ERR_INVALID_ARG;
+    if (S_max < infllmv2::selection_capacity(p, L_max)) return INFLLMV2_ERR_INVALID_ARG;
+    if (!q || !kernel_cache || !kv_len || !idx || !counts) return INFLLMV2_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kernel_cache) || !aligned16(kv_len) || !aligned16(idx) || !aligned16(counts))
+        return INFLLMV2_ERR_INVALID_ARG;
+    const size_t need = align256(infllmv2::select_workspace_bytes(B, Tq, Hkv, L_max, p));
+    if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return INFLLMV2_ERR_WORKSPACE;
+    int* err = device_error_ptr();
+    if (err == nullptr) return INFLLMV2_ERR_CUDA;
+    infllmv2::SelectArgs a{q, kernel_cache, kv_len, B, Tq, Hq, Hkv, d, L_max, M_max, 0, idx, counts, S_max,
+                           blocks_per_score_cta(p), p, err, static_cast<cudaStream_t>(stream)};
+    return cuda_status(infllmv2::launch_block_select(a, static_cast<float*>(workspace)));
+}
+
+int infllmv2_sparse_attn_fwd(const void* q, const void* k_cache, const void* v_cache, const int32_t* idx,
+                             const int32_t* counts, int S_max, const int32_t* kv_len, int B, int Tq, int Hq,
+                             int Hkv, int d, int L_max, void* o, float* lse, void* workspace, size_t ws_bytes,
+                             const infllmv2_params* params, void* stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    Params p;
+    if (int rc = check_params(params, d, &p)) return rc;
+    if (int rc = check_heads(Hq, Hkv, d)) return rc;
+    if (B < 0 || Tq < 0 || L_max <= 0 || L_max > kMaxLen) return INFLLMV2_ERR_INVALID_ARG;
+    if (B == 0 || Tq == 0) return INFLLMV2_OK;
+    if (Tq > L_max) return INFLLMV2_ERR_INVALID_ARG;
+    if (!q || !k_cache || !v_cache || !kv_len || !o) return INFLLMV2_ERR_INVALID_ARG;
+    if ((idx == nullptr) != (counts == nullptr)) return INFLLMV2_ERR_INVALID_ARG;
+    if (idx != nullptr && (S_max <= 0 || !aligned16(idx) || !aligned16(counts))) return INFLLMV2_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(kv_len))
+        return INFLLMV2_ERR_INVALID_ARG;
+    if (lse != nullptr && !aligned16(lse)) return INFLLMV2_ERR_INVALID_ARG;
+    int* err = device_error_ptr();
+    if (err == nullptr) return INFLLMV2_ERR_CUDA;
+    infllmv2::PrefillArgs a{q, k_cache, v_cache, idx, counts, S_max, kv_len, B, Tq, Hq, Hkv, d, L_max,
+                            o, lse, p, err, static_cast<cudaStream_t>(stream)};
+    return cuda_status(infllmv2::launch_prefill_attention(a));
+}
+
+int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache, const void* kernel_cache,
+                    const int32_t* kv_len, const void* draft_k, const void* draft_v, const uint64_t* tree_mask,
+                    int B, int n_draft, int Hq, int Hkv, int d, int L_max, int M_max, void* o, float* lse,
+                    int32_t* idx_out, int32_t* counts_out, int S_max, void* workspace, size_t ws_bytes,
+                    const infllmv2_params* params, void* stream) {
+    Params p;
+    if (int rc = check_params(params, d, &p)) return rc;
+    if (int rc = check_heads(Hq, Hkv, d)) return rc;
+    if (B < 0 || n_draft < 0 || L_max <= 0 || L_max > kMaxLen || M_max < 0) return INFLLMV2_ERR_INVALID_ARG;
+    const bool tree = tree_mask != nullptr;
+    if (!tree && n_draft > 1) return INFLLMV2_ERR_INVALID_ARG;
+    if (tree && n_draft > 64) return INFLLMV2_ERR_UNSUPPORTED;
+    if (B == 0 || n_draft == 0) return INFLLMV2_OK;
+    if (!q || !k_cache || !v_cache || !kernel_cache || !kv_len || !o) return INFLLMV2_ERR_INVALID_ARG;
+    if (tree && (!draft_k || !draft_v || !aligned16(draft_k) || !aligned16(draft_v) ||
+                 (reinterpret_cast<uintptr_t>(tree_mask) & 7u) != 0))
+        return INFLLMV2_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(kernel_cache) ||
+        !aligned16(kv_len) || !aligned16(o))
+        return INFLLMV2_ERR_INVALID_ARG;
+    if (lse != nullptr && !aligned16(lse)) return INFLLMV2_ERR_INVALID_ARG;
+    const int S_cap = infllmv2::selection_capacity(p, L_max);
+    if ((idx_out == nullptr) != (counts_out == nullptr)) return INFLLMV2_ERR_INVALID_ARG;
+    if (idx_out != nullptr && (S_max < S_cap || !aligned16(idx_out) || !aligned16(counts_out)))
+        return INFLLMV2_ERR_INVALID_ARG;
+    const DecodeWs w = decode_ws(B, n_draft, Hkv, d, L_max, p);
+    if (workspace == nullptr || ws_bytes < w.total || !aligned16(workspace)) return INFLLMV2_ERR_WORKSPACE;
+    int* err = device_error_ptr();
+    if (err == nullptr) return INFLLMV2_ERR_CUDA;
+    char* ws = static_cast<char*>(workspace);
+    int* idx = idx_out != nullptr ? idx_out : reinterpret_cast<int*>(ws + w.idx);
+    int* counts = counts_out != nullptr ? counts_out : reinterpret_cast<int*>(ws + w.counts);
+    const int stride = idx_out != nullptr ? S_max : S_cap;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    infllmv2::SelectArgs sa{q, kernel_cache, kv_len, B, n_draft, Hq, Hkv, d, L_max, M_max, tree ? 1 : 0, idx, counts,
+                            stride, blocks_per_score_cta(p), p, err, st};
+    if (int rc = cuda_status(infllmv2::launch_block_select(sa, reinterpret_cast<float*>(ws + w.scores)))) return rc;
+    infllmv2::DecodeArgs da{q, k_cache, v_cache, kv_len, draft_k, draft_v, tree_mask, B, n_draft, Hq, Hkv, d, L_max,
+                            o, lse, p, err, st};
+    return cuda_status(
+        infllmv2::launch_decode_attention(da, idx, counts, stride, S_cap, reinterpret_cast<float*>(ws + w.part)));
+}
+
+}  // extern "C"

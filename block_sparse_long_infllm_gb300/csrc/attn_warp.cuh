@@ -1,0 +1,179 @@
+// attn_warp.cuh -- one warp's flash-attention state for 16 query rows, fed 32 keys at a time
+// (the online-softmax form of "attention on the selected blocks only", "MiniCPM4: 如何在手机
+// 电脑上高效运行大语言模型", section 1.1 "InfLLM v2").
+//
+// Rows are the G heads of one query token (padded to 16).  QK^T and PV run as m16n8k16 warp
+// MMAs with fp32 accumulators; the softmax runs in fp32 in the log2 domain.  Operands come
+// straight from global memory with 128-bit loads, no shared memory:
+//   * QK^T: the head dimension is permuted the same way for Q and K (the sum over d does
+//     not depend on the order of its terms) so each lane's 16 bytes of a K row feed two
+//     k-steps of its B fragment;
+//   * PV: output column n of n-tile nt is head-dim element (D/8)*n + nt, so each lane
+//     reads D/8 consecutive elements of its four V rows and, in the end, owns D/4
+//     consecutive output elements of each of its two rows.
+#pragma once
+
+#include "common.cuh"
+
+namespace infllmv2 {
+
+template <int D>
+struct QFrag {
+    uint32_t a[D / 16][4];
+};
+
+template <int D>
+struct WarpAcc {
+    float o[D / 8][4];  // o[nt][0..1]: row g, o[nt][2..3]: row g+8
+    float m[2];         // running max of the scaled log2 logits, rows g and g+8
+    float l[2];         // this lane's share of the row sums
+};
+
+// Load the A fragments of 16 rows; row r's data starts at rows + r*row_stride, rows r >= n_rows
+// read as zero.
+template <int D>
+__device__ __forceinline__ void load_q(QFrag<D>& Q, const __nv_bfloat16* rows, int row_stride, int n_rows) {
+    const int g = (threadIdx.x & 31) >> 2, c = threadIdx.x & 3;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int r = g + 8 * half;
+        const bool ok = r < n_rows;
+        const __nv_bfloat16* src = rows + static_cast<size_t>(ok ? r : 0) * row_stride + 8 * c;
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+            const uint4 w = ok ? ldg_v4(src + 32 * i) : make_uint4(0, 0, 0, 0);
+            Q.a[2 * i][half] = w.x;
+            Q.a[2 * i][2 + half] = w.y;
+            Q.a[2 * i + 1][half] = w.z;
+            Q.a[2 * i + 1][2 + half] = w.w;
+        }
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void acc_init(WarpAcc<D>& A) {
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) A.o[nt][e] = 0.f;
+    A.m[0] = A.m[1] = -INFINITY;
+    A.l[0] = A.l[1] = 0.f;
+}
+
+// Feed 32 keys whose rows are k_rows[kk*D], v_rows[kk*D] (kk = 0..31); bit kk of `valid` says
+// key kk takes part.  Rows of keys that do not take part are never read.
+template <int D>
+__device__ __forceinline__ void attend32(WarpAcc<D>& A, const QFrag<D>& Q, const __nv_bfloat16* k_rows,
+                                         const __nv_bfloat16* v_rows, uint32_t valid, float scale_log2) {
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+
+    // ---- V rows for the two k-steps (keys 16kk + 2c + {0,1}, 16kk + 8 + 2c + {0,1}); issued first
+    constexpr int VW = D / 16;  // 32-bit words per lane per V row
+    uint32_t vw[2][4][VW];
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int key = 16 * kk + 2 * c + (r & 1) + 8 * (r >> 1);
+            const bool ok = (valid >> key) & 1u;
+            const uint4* src = reinterpret_cast<const uint4*>(v_rows + static_cast<size_t>(key) * D + (D / 8) * g);
+#pragma unroll
+            for (int u = 0; u < VW / 4; ++u) {
+                const uint4 w = ok ? ldg_v4_stream(src + u) : make_uint4(0, 0, 0, 0);
+                vw[kk][r][4 * u + 0] = w.x;
+                vw[kk][r][4 * u + 1] = w.y;
+                vw[kk][r][4 * u + 2] = w.z;
+                vw[kk][r][4 * u + 3] = w.w;
+            }
+        }
+    }
+
+    // ---- S = Q K^T for 4 n-tiles of 8 keys
+    float s[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+        const int key = nt * 8 + g;
+        const bool ok = (valid >> key) & 1u;
+        const __nv_bfloat16* src = k_rows + static_cast<size_t>(key) * D + 8 * c;
+        uint4 w[D / 32];
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) w[i] = ok ? ldg_v4_stream(src + 32 * i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+            mma_16816(s[nt], Q.a[2 * i], w[i].x, w[i].y);
+            mma_16816(s[nt], Q.a[2 * i + 1], w[i].z, w[i].w);
+        }
+    }
+
+    // ---- online softmax (log2 domain)
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int key = nt * 8 + 2 * c + (e & 1);
+            s[nt][e] = ((valid >> key) & 1u) ? s[nt][e] * scale_log2 : -INFINITY;
+            mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+        }
+    }
+    float ref[2], corr[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+        const float m_new = fmaxf(A.m[h], mx[h]);
+        ref[h] = m_new == -INFINITY ? 0.f : m_new;
+        corr[h] = fast_exp2(A.m[h] - ref[h]);
+        A.m[h] = m_new;
+        A.l[h] *= corr[h];
+    }
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) {
+        A.o[nt][0] *= corr[0];
+        A.o[nt][1] *= corr[0];
+        A.o[nt][2] *= corr[1];
+        A.o[nt][3] *= corr[1];
+    }
+    uint32_t pa[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+        float pv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            pv[e] = fast_exp2(s[nt][e] - ref[e >> 1]);
+            A.l[e >> 1] += pv[e];
+        }
+        const int kk = nt >> 1, hi = nt & 1;
+        pa[kk][2 * hi + 0] = pack_bf16x2(pv[0], pv[1]);
+        pa[kk][2 * hi + 1] = pack_bf16x2(pv[2], pv[3]);
+    }
+
+    // ---- O += P V
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) {
+            const uint32_t b0 = pair_halves(vw[kk][0][nt >> 1], vw[kk][1][nt >> 1], nt & 1);
+            const uint32_t b1 = pair_halves(vw[kk][2][nt >> 1], vw[kk][3][nt >> 1], nt & 1);
+            mma_16816(A.o[nt], pa[kk], b0, b1);
+        }
+    }
+}
+
+// Sum the lanes' shares of the row sums (after the last tile).
+template <int D>
+__device__ __forceinline__ void acc_finish_rowsum(WarpAcc<D>& A) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        A.l[h] += __shfl_xor_sync(0xffffffffu, A.l[h], 1);
+        A.l[h] += __shfl_xor_sync(0xffffffffu, A.l[h], 2);
+    }
+}
+
+// Head-dim element held in o[nt][e]: row half e>>1, column (D/8)*(2c + (e&1)) + nt.
+__device__ __forceinline__ int o_col(int D, int c, int nt, int e) { return (D / 8) * (2 * c + (e & 1)) + nt; }
+
+}  // namespace infllmv2

@@ -1,0 +1,104 @@
+// common.cuh -- device helpers shared by the InfLLM v2 kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace infllmv2 {
+
+// Method parameters as the kernels see them (mirrors infllmv2_params).
+struct Params {
+    int block_size;
+    int kernel_size;
+    int kernel_stride;
+    int topk;
+    int n_init;
+    int n_local;
+    int dense_len;
+    float scale;  // softmax scale, already resolved (never 0)
+};
+
+// Bits of the device error word.
+enum : int { kDevErrTimeout = 1, kDevErrIndex = 2 };
+
+__device__ __forceinline__ void raise_error(int* err, int code) {
+    if (err) atomicOr(err, code);
+}
+
+// Floor division for a possibly negative numerator and a positive divisor.
+__host__ __device__ __forceinline__ int floor_div(int a, int b) {
+    return a >= 0 ? a / b : -((-a + b - 1) / b);
+}
+
+// Number of complete semantic kernels among the first L tokens.
+__host__ __device__ __forceinline__ int kernels_in(int L, int c, int s) {
+    return L < c ? 0 : (L - c) / s + 1;
+}
+
+// Kernels sharing at least one token with block blk: j*s < (blk+1)*bs and j*s + c > blk*bs.
+__host__ __device__ __forceinline__ int first_kernel_of_block(int blk, int bs, int c, int s) {
+    int j = floor_div(blk * bs - c, s) + 1;
+    return j < 0 ? 0 : j;
+}
+__host__ __device__ __forceinline__ int last_kernel_of_block(int blk, int bs, int s) {
+    return ((blk + 1) * bs - 1) / s;
+}
+
+// 128-bit read-only global load.
+__device__ __forceinline__ uint4 ldg_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// 128-bit streaming load: read once, do not keep in L1.
+__device__ __forceinline__ uint4 ldg_v4_stream(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// D += A(16x16, row) * B(16x8, col), bf16 inputs, fp32 accumulate (legacy warp MMA).
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 2^x on the special-function unit (PTX ex2.approx; inputs of -inf give +0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Select the 16-bit element `e` (0 = low) of word pair (w0, w1) as two halves of one word:
+// result = { lo: element e of w0, hi: element e of w1 }.
+__device__ __forceinline__ uint32_t pair_halves(uint32_t w0, uint32_t w1, int e) {
+    return e == 0 ? __byte_perm(w0, w1, 0x5410) : __byte_perm(w0, w1, 0x7632);
+}
+
+// Monotone map from fp32 to uint32 (larger float -> larger key); -0 is folded into +0
+// so that equal scores always compare equal.
+__device__ __forceinline__ uint32_t ordered_key(float s) {
+    uint32_t u = __float_as_uint(s + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+}  // namespace infllmv2

@@ -1,0 +1,75 @@
+// internal.h -- launch interfaces between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace infllmv2 {
+
+struct SelectArgs {
+    const void* q;
+    const void* kernel_cache;
+    const int* kv_len;
+    int B, Tq, Hq, Hkv, d, L_max, M_max;
+    int tree;  // queries are tree drafts after the cache (all at the last cached position)
+    int* idx;
+    int* counts;
+    int S_max;
+    int blocks_per_cta;
+    Params p;
+    int* err;
+    cudaStream_t stream;
+};
+
+struct PrefillArgs {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int* idx;
+    const int* counts;
+    int S_max;
+    const int* kv_len;
+    int B, Tq, Hq, Hkv, d, L_max;
+    void* o;
+    float* lse;
+    Params p;
+    int* err;
+    cudaStream_t stream;
+};
+
+struct DecodeArgs {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int* kv_len;
+    const void* draft_k;
+    const void* draft_v;
+    const uint64_t* tree_mask;
+    int B, n_draft, Hq, Hkv, d, L_max;
+    void* o;
+    float* lse;
+    Params p;
+    int* err;
+    cudaStream_t stream;
+};
+
+cudaError_t launch_kernel_pool(const void* k_cache, void* kernel_cache, int B, int Hkv, int L_max,
+                               int M_max, int d, int j_first, int n_new, int c, int s,
+                               cudaStream_t stream);
+
+int selection_capacity(const Params& p, int L_max);
+size_t select_workspace_bytes(int B, int Tq, int Hkv, int L_max, const Params& p);
+cudaError_t launch_block_select(const SelectArgs& a, float* S);
+
+cudaError_t launch_prefill_attention(const PrefillArgs& a);
+
+void decode_split_shape(int S_cap, int bs, bool tree, int* blocks_per_split, int* n_split_cache,
+                        int* n_split);
+size_t decode_partial_bytes(int B, int n_draft, int Hkv, int d, int n_split);
+cudaError_t launch_decode_attention(const DecodeArgs& a, const int* idx, const int* counts, int idx_stride,
+                                    int S_cap, float* part);
+
+}  // namespace infllmv2

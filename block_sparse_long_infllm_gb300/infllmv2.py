@@ -1,0 +1,189 @@
+"""Python binding of libinfllmv2.so (include/infllmv2.h), argument marshalling only.
+
+Every function takes CUDA tensors (PyTorch is used for device memory and
+streams), passes their device pointers and sizes to the C ABI entry point of
+the same name, and raises `InfLLMv2Error` on a non-zero status.  No step of
+the method runs here, and there is no fallback: if the library has not been
+built, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libinfllmv2.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "infllmv2.h")
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED = -2
+ERR_WORKSPACE = -3
+ERR_CUDA = -4
+ERR_DEVICE_TIMEOUT = -5
+ERR_DEVICE_INDEX = -6
+ERR_NOT_IMPLEMENTED = -7
+
+ENTRY_BLOCK_SELECT = 1
+ENTRY_SPARSE_ATTN_FWD = 2
+ENTRY_DECODE = 3
+
+
+class InfLLMv2Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class Params(ctypes.Structure):
+    """infllmv2_params: block_size, kernel_size, kernel_stride, topk, n_init_blocks,
+    n_local_blocks, dense_len, softmax_scale (0 = 1/sqrt(d))."""
+    _fields_ = [("block_size", ctypes.c_int32), ("kernel_size", ctypes.c_int32),
+                ("kernel_stride", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("n_init_blocks", ctypes.c_int32), ("n_local_blocks", ctypes.c_int32),
+                ("dense_len", ctypes.c_int32), ("softmax_scale", ctypes.c_float)]
+
+    @classmethod
+    def make(cls, p) -> "Params":
+        if isinstance(p, Params):
+            return p
+        return cls(int(p["block_size"]), int(p["kernel_size"]), int(p["kernel_stride"]),
+                   int(p["topk"]), int(p["n_init_blocks"]), int(p["n_local_blocks"]),
+                   int(p["dense_len"]), float(p.get("softmax_scale", 0.0)))
+
+
+_lib = None
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libinfllmv2.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with block_sparse_long_infllm_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    p, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    pp = ctypes.POINTER(Params)
+    lib.infllmv2_status_string.argtypes = [i32]
+    lib.infllmv2_status_string.restype = ctypes.c_char_p
+    lib.infllmv2_version.argtypes = []
+    lib.infllmv2_sync_status.argtypes = [p]
+    lib.infllmv2_selection_capacity.argtypes = [pp, i32]
+    lib.infllmv2_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, pp]
+    lib.infllmv2_workspace_size.restype = sz
+    lib.infllmv2_kernel_pool.argtypes = [p, p, i32, i32, i32, i32, i32, i32, i32, pp, p]
+    lib.infllmv2_block_select.argtypes = [p, p, p, i32, i32, i32, i32, i32, i32, i32, p, p, i32, p, sz,
+                                          pp, p]
+    lib.infllmv2_sparse_attn_fwd.argtypes = [p, p, p, p, p, i32, p, i32, i32, i32, i32, i32, i32, p, p,
+                                             p, sz, pp, p]
+    lib.infllmv2_decode.argtypes = [p, p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, p, p, p,
+                                    p, i32, p, sz, pp, p]
+    for name in ("infllmv2_version", "infllmv2_sync_status", "infllmv2_selection_capacity",
+                 "infllmv2_kernel_pool", "infllmv2_block_select", "infllmv2_sparse_attn_fwd",
+                 "infllmv2_decode"):
+        getattr(lib, name).restype = ctypes.c_int
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/infllmv2.h declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(infllmv2_[a-z_0-9]+)\s*\(", text)))
+
+
+def status_string(status: int) -> str:
+    return load().infllmv2_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(load().infllmv2_version())
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise InfLLMv2Error(rc, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def sync_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return int(load().infllmv2_sync_status(_stream(stream)))
+
+
+def selection_capacity(params, L_max: int) -> int:
+    return int(load().infllmv2_selection_capacity(ctypes.byref(Params.make(params)), int(L_max)))
+
+
+def workspace_size(entry: int, B: int, Tq: int, Hq: int, Hkv: int, d: int, L_max: int, params) -> int:
+    return int(load().infllmv2_workspace_size(int(entry), B, Tq, Hq, Hkv, d, L_max,
+                                              ctypes.byref(Params.make(params))))
+
+
+def kernel_pool(k_cache, kernel_cache, tok_begin: int, tok_end: int, params, stream=None):
+    """Pool the kernels that become complete with tokens [tok_begin, tok_end)."""
+    B, Hkv, L_max, d = k_cache.shape
+    M_max = kernel_cache.shape[2]
+    _check(load().infllmv2_kernel_pool(_ptr(k_cache), _ptr(kernel_cache), B, Hkv, L_max, M_max, d,
+                                       int(tok_begin), int(tok_end), ctypes.byref(Params.make(params)),
+                                       _stream(stream)), "infllmv2_kernel_pool")
+
+
+def block_select(q, kernel_cache, kv_len, idx, counts, workspace, params, L_max: int, stream=None):
+    """Top-k block selection for a causal chunk (the last Tq tokens of each sequence)."""
+    B, Tq, Hq, d = q.shape
+    Hkv, M_max = kernel_cache.shape[1], kernel_cache.shape[2]
+    _check(load().infllmv2_block_select(_ptr(q), _ptr(kernel_cache), _ptr(kv_len), B, Tq, Hq, Hkv, d,
+                                        int(L_max), M_max, _ptr(idx), _ptr(counts), idx.shape[-1],
+                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        ctypes.byref(Params.make(params)), _stream(stream)),
+           "infllmv2_block_select")
+
+
+def sparse_attn_fwd(q, k_cache, v_cache, idx, counts, kv_len, o, params, lse=None, workspace=None,
+                    stream=None):
+    """Block-sparse causal attention of a chunk over its selected blocks (idx None: dense)."""
+    B, Tq, Hq, d = q.shape
+    Hkv, L_max = k_cache.shape[1], k_cache.shape[2]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().infllmv2_sparse_attn_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(idx), _ptr(counts),
+                                           0 if idx is None else idx.shape[-1], _ptr(kv_len), B, Tq, Hq,
+                                           Hkv, d, L_max, _ptr(o), _ptr(lse), _ptr(workspace), ws_bytes,
+                                           ctypes.byref(Params.make(params)), _stream(stream)),
+           "infllmv2_sparse_attn_fwd")
+
+
+def decode(q, k_cache, v_cache, kernel_cache, kv_len, o, workspace, params, lse=None, draft_k=None,
+           draft_v=None, tree_mask=None, idx_out=None, counts_out=None, stream=None):
+    """Selection + split-KV attention + merge for one decode token or a draft tree."""
+    B, n_draft, Hq, d = q.shape
+    Hkv, L_max = k_cache.shape[1], k_cache.shape[2]
+    M_max = kernel_cache.shape[2]
+    S_max = 0 if idx_out is None else idx_out.shape[-1]
+    _check(load().infllmv2_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kernel_cache), _ptr(kv_len),
+                                  _ptr(draft_k), _ptr(draft_v), _ptr(tree_mask), B, n_draft, Hq, Hkv, d,
+                                  L_max, M_max, _ptr(o), _ptr(lse), _ptr(idx_out), _ptr(counts_out), S_max,
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  ctypes.byref(Params.make(params)), _stream(stream)), "infllmv2_decode")

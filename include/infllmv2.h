@@ -1,0 +1,207 @@
+/*
+ * infllmv2.h -- C ABI of libinfllmv2.so: InfLLM v2 trainable block-sparse
+ * attention (semantic-kernel pooling, block scoring, top-k block selection,
+ * block-sparse flash attention) for NVIDIA GB300 (sm_103a).
+ *
+ * The method, as the pages describe it:
+ *   [MiniCPM4-1.1]  "MiniCPM4: 如何在手机电脑上高效运行大语言模型"
+ *                   (xugj520.cn), section 1.1 "InfLLM v2" -- context split into
+ *                   blocks; overlapping semantic kernels of 32 tokens, stride
+ *                   16; each query keeps its top-K most relevant blocks; the
+ *                   opening tokens and the sliding window are always kept;
+ *                   attention runs on the kept blocks only; kernel-level
+ *                   relevance avoids token-level work; a uint64-packed mask
+ *                   supports tree-speculative decoding.
+ *   [MiniCPM4.0-sparse] "MiniCPM40极速狂飙端侧模型的比赛结束了"
+ *                   (shadowrocket9.top), section "InfLLM v2：重新定义注意力
+ *                   机制" -- 64-token blocks, top-64 blocks, dense attention
+ *                   below 8192 tokens; its deployment guide sets
+ *                   sparse_config = {topk, block_size, dense_len}.
+ *   [CPM.cu]        "CPM.cu：端侧大模型推理的 CUDA 加速引擎" (pomoai.com),
+ *                   section 4 -- static memory (preallocated KV cache),
+ *                   CUDA graphs, chunked prefill.
+ * The pages disagree on block size (64 vs 128) and top-k (64 vs 6), so every
+ * method parameter is a runtime argument (infllmv2_params).
+ *
+ * Conventions for every entry point
+ *   - Tensors are plain device pointers, row-major, densely packed, 16-byte
+ *     aligned.  bf16 tensors are passed as void*.  Index/length arrays are
+ *     device int32.  The caller owns every buffer and the stream; the library
+ *     never allocates device memory (the static-memory design of [CPM.cu]).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     All work is enqueued on it; calls return before the GPU finishes.
+ *   - Argument errors are found on the host and returned before anything is
+ *     enqueued.  Errors only the device can see (a kv_len out of range, a
+ *     selected block past the query's own block, a wait that ran out) set a
+ *     device error word; infllmv2_sync_status() reports and clears it.
+ *   - Supported: bf16 Q/K/V; head_dim d in {64, 128}; query heads per KV head
+ *     G = Hq/Hkv in {1, 2, 4, 8, 16}; block_size in {64, 128}; kernel_size and
+ *     kernel_stride positive with kernel_size <= block_size; n_local_blocks >= 1;
+ *     at most 64 draft tokens (one uint64 mask word each).
+ *
+ * Layouts (B = batch, Tq = queries per sequence, Hq/Hkv = query/KV heads)
+ *   q            [B, Tq, Hq, d]        bf16; heads g*G .. g*G+G-1 share KV head g
+ *   k_cache      [B, Hkv, L_max, d]    bf16; token x of a sequence is row x
+ *   v_cache      [B, Hkv, L_max, d]    bf16
+ *   kernel_cache [B, Hkv, M_max, d]    bf16; kernel j = mean of tokens
+ *                                      [j*stride, j*stride + kernel_size)
+ *   kv_len       [B]                   int32; tokens in the cache, including
+ *                                      the tokens of this call
+ *   o            [B, Tq, Hq, d]        bf16
+ *   lse          [B, Hq, Tq]           fp32, natural-log sum of exp(scale*q.k)
+ *   idx          [B, Hkv, Tq, S_max]   int32 selected block ids, ascending,
+ *                                      padded with -1
+ *   counts       [B, Hkv, Tq]          int32 number of valid entries in idx
+ */
+#ifndef INFLLMV2_H_
+#define INFLLMV2_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Method parameters ([MiniCPM4-1.1]; sparse_config of [MiniCPM4.0-sparse]). */
+typedef struct infllmv2_params {
+    int32_t block_size;      /* tokens per KV block: 64 or 128                        */
+    int32_t kernel_size;     /* tokens per semantic kernel (the pages: 32)            */
+    int32_t kernel_stride;   /* token stride between kernels (the pages: 16)          */
+    int32_t topk;            /* blocks chosen by score, on top of the forced ones     */
+    int32_t n_init_blocks;   /* leading blocks always kept ("opening tokens")         */
+    int32_t n_local_blocks;  /* blocks ending at the query's own block, always kept   */
+    int32_t dense_len;       /* sequences with kv_len < dense_len attend densely      */
+    float softmax_scale;     /* 0 selects 1/sqrt(d)                                   */
+} infllmv2_params;
+
+typedef enum infllmv2_status {
+    INFLLMV2_OK = 0,
+    INFLLMV2_ERR_INVALID_ARG = -1,     /* null/misaligned pointer, bad size or range   */
+    INFLLMV2_ERR_UNSUPPORTED = -2,     /* d, G, block size ... outside the set above   */
+    INFLLMV2_ERR_WORKSPACE = -3,       /* workspace missing or smaller than required   */
+    INFLLMV2_ERR_CUDA = -4,            /* a CUDA runtime call failed (launch, ...)     */
+    INFLLMV2_ERR_DEVICE_TIMEOUT = -5,  /* a bounded device-side wait ran out           */
+    INFLLMV2_ERR_DEVICE_INDEX = -6,    /* device saw kv_len or a block id out of range */
+    INFLLMV2_ERR_NOT_IMPLEMENTED = -7
+} infllmv2_status;
+
+/* Entry ids for infllmv2_workspace_size. */
+enum {
+    INFLLMV2_ENTRY_BLOCK_SELECT = 1,
+    INFLLMV2_ENTRY_SPARSE_ATTN_FWD = 2,
+    INFLLMV2_ENTRY_DECODE = 3
+};
+
+/* Human-readable text of a status code (static storage, never NULL). */
+const char* infllmv2_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int infllmv2_version(void);
+
+/*
+ * Synchronise `stream`, then report and clear the device error word of the
+ * current device.  Returns INFLLMV2_OK, INFLLMV2_ERR_DEVICE_TIMEOUT,
+ * INFLLMV2_ERR_DEVICE_INDEX or INFLLMV2_ERR_CUDA.
+ */
+int infllmv2_sync_status(void* stream);
+
+/*
+ * Most selected blocks any query can get for these parameters and an L_max-token
+ * cache: topk + n_init + n_local, or every causal block while kv_len < dense_len
+ * (whichever is larger, capped at ceil(L_max/block_size)).  idx buffers need at
+ * least this many columns (S_max).  Returns -1 on invalid parameters.
+ */
+int infllmv2_selection_capacity(const infllmv2_params* params, int L_max);
+
+/*
+ * Bytes of device workspace an entry point needs (entry = INFLLMV2_ENTRY_*).
+ * Tq is the number of queries per sequence (n_draft for decode).  Returns 0
+ * for invalid arguments (and for entries that need none).
+ */
+size_t infllmv2_workspace_size(int entry, int B, int Tq, int Hq, int Hkv, int d, int L_max,
+                               const infllmv2_params* params);
+
+/*
+ * Step 1, semantic kernels ([MiniCPM4-1.1], semantic-kernel item):
+ *   kernel_cache[b,g,j,:] = bf16_rne( (1/kernel_size) * sum of k_cache[b,g,x,:]
+ *                           over x in [j*stride, j*stride + kernel_size) )
+ * for every kernel j whose last token lies in [tok_begin, tok_end) -- that is,
+ * the kernels that become complete once tokens [tok_begin, tok_end) are in the
+ * cache.  Call it after appending tokens (a prefill chunk, or each decode token;
+ * a new kernel completes every `stride` tokens).  Sums are exact (fp64) and
+ * rounded to bf16 once, nearest-even.
+ * Requires 0 <= tok_begin <= tok_end <= L_max and
+ * M_max >= (tok_end - kernel_size)/kernel_stride + 1.  Other kernels are untouched.
+ */
+int infllmv2_kernel_pool(const void* k_cache, void* kernel_cache, int B, int Hkv, int L_max,
+                         int M_max, int d, int tok_begin, int tok_end,
+                         const infllmv2_params* params, void* stream);
+
+/*
+ * Steps 2-3, block scores and top-k selection for a causal chunk
+ * ([MiniCPM4-1.1] dynamic block selection and local retention;
+ * [MiniCPM4.0-sparse] dense switch).  Query t of sequence b sits at position
+ * p = kv_len[b] - Tq + t (the chunk is the last Tq tokens of the cache; Tq = 1
+ * is single-token decode).  With bt = p / block_size:
+ *   S[t,g,blk] = max over heads h of group g and over kernels j that share a
+ *                token with blk and end at or before p, of q[t,h] . kernel[j]
+ *   forced     = blocks [0, n_init) and [bt - n_local + 1, bt], within [0, bt]
+ *   selected   = forced + the topk other blocks <= bt by (S desc, id asc);
+ *                every block <= bt when kv_len[b] < dense_len.
+ * Writes idx [B,Hkv,Tq,S_max] (ascending, -1 padded) and counts [B,Hkv,Tq].
+ * Needs S_max >= infllmv2_selection_capacity(params, L_max), kernels pooled up
+ * to kv_len[b], kv_len[b] in [Tq, L_max], and
+ * ws_bytes >= infllmv2_workspace_size(INFLLMV2_ENTRY_BLOCK_SELECT, ...).
+ */
+int infllmv2_block_select(const void* q, const void* kernel_cache, const int32_t* kv_len, int B,
+                          int Tq, int Hq, int Hkv, int d, int L_max, int M_max, int32_t* idx,
+                          int32_t* counts, int S_max, void* workspace, size_t ws_bytes,
+                          const infllmv2_params* params, void* stream);
+
+/*
+ * Step 4, block-sparse attention for a causal chunk ([MiniCPM4-1.1], attention
+ * on the selected blocks only; chunked prefill of [CPM.cu]).  For query t of
+ * sequence b at p = kv_len[b] - Tq + t and head h of group g:
+ *   keys = tokens x <= p of the blocks idx[b,g,t,0..counts-1]
+ *   o    = softmax_x(scale * q.k_x) v_x    (fp32 online softmax, bf16 output)
+ * idx == NULL (and counts == NULL) means dense causal attention (every block).
+ * lse may be NULL.  Selected ids must lie in [0, bt] (checked on the device).
+ * Requires ws_bytes >= infllmv2_workspace_size(INFLLMV2_ENTRY_SPARSE_ATTN_FWD, ...).
+ */
+int infllmv2_sparse_attn_fwd(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* idx, const int32_t* counts, int S_max,
+                             const int32_t* kv_len, int B, int Tq, int Hq, int Hkv, int d,
+                             int L_max, void* o, float* lse, void* workspace, size_t ws_bytes,
+                             const infllmv2_params* params, void* stream);
+
+/*
+ * Steps 2-4 for decoding: selection from the cached kernels, split-KV
+ * attention over the selected blocks, and the merge of the splits.
+ *   tree_mask == NULL: single-token decode (n_draft must be 1); the query is
+ *     the newest cached token, p = kv_len[b] - 1.
+ *   tree_mask != NULL: tree-speculative verification ([MiniCPM4-1.1] uint64
+ *     mask; [CPM.cu] tree verification inside flash attention).  n_draft <= 64
+ *     draft tokens come after kv_len[b] committed tokens; bit j of
+ *     tree_mask[b,i] says draft i attends to draft j (the mask holds the
+ *     draft's own bit and its ancestors').  Each draft selects its own blocks
+ *     from all cached kernels (bt = the last cached block) and attends to
+ *     every cached token of them plus the masked drafts, whose keys and values
+ *     come from draft_k/draft_v [B, Hkv, n_draft, d] (not pooled, not cached).
+ * q [B, n_draft, Hq, d]; o [B, n_draft, Hq, d]; lse [B, Hq, n_draft] or NULL;
+ * idx_out [B, Hkv, n_draft, S_max] / counts_out [B, Hkv, n_draft] receive the
+ * selection when not NULL (S_max is ignored when idx_out is NULL).
+ * Requires ws_bytes >= infllmv2_workspace_size(INFLLMV2_ENTRY_DECODE, ...).
+ */
+int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache,
+                    const void* kernel_cache, const int32_t* kv_len, const void* draft_k,
+                    const void* draft_v, const uint64_t* tree_mask, int B, int n_draft, int Hq,
+                    int Hkv, int d, int L_max, int M_max, void* o, float* lse, int32_t* idx_out,
+                    int32_t* counts_out, int S_max, void* workspace, size_t ws_bytes,
+                    const infllmv2_params* params, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* INFLLMV2_H_ */

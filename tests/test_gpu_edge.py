@@ -1,0 +1,156 @@
+"""GPU edge cases against the oracle: ragged and per-sequence cache lengths,
+every supported group size and head dim, both block sizes, the dense switch,
+top-k covering every block, dense attention without a selection, wide trees,
+queries that are not a multiple of the CTA tile, and device-side error words
+(reported, context still usable)."""
+import numpy as np
+import pytest
+
+import oracle
+from block_sparse_long_infllm_gb300 import synth
+
+from harness import (bf16_to_f64, bf16_to_np_bits, check_output, compare_selection, lib, n_kernels,
+                     run_gpu, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+BASE = synth.WORKLOADS["decode_32k"]
+
+
+def _parity(w, inp, params=None):
+    p = params or w.params()
+    g = run_gpu(w, inp, params=p)
+    tree = w.kind == "tree"
+    kern_ref, _ = oracle.kernel_pool(inp["k_cache"], inp["kv_len"], w.kernel_size, w.kernel_stride,
+                                     max(n_kernels(w), 1))
+    kv = inp["kv_len"]
+    # kernels past a sequence's own length are not written by the oracle: compare the written ones
+    gk = bf16_to_np_bits(g["kern"])
+    for b in range(w.B):
+        m = oracle.n_kernels(int(kv[b]), w.kernel_size, w.kernel_stride) if w.kind != "prefill" else None
+        if m is not None:
+            assert np.array_equal(gk[b, :, :m], kern_ref[b, :, :m])
+    S = oracle.block_scores(inp["q"], kern_ref, kv, w.Hkv, p, tree=tree,
+                            nblk_max=(w.L_max - 1) // w.block_size + 1)
+    oidx, ocnt, kth, _ = oracle.select(S, kv, w.Tq, p, tree=tree, S_max=g["S_cap"])
+    gidx, gcnt = g["idx"].cpu().numpy(), g["counts"].cpu().numpy()
+    rows, exact, ties, bad = compare_selection(gidx, gcnt, oidx, ocnt, S, kth)
+    assert bad == 0
+    o_ref, lse_ref = oracle.attention(inp["q"], inp["k_cache"], inp["v_cache"], kv, gidx, gcnt, p,
+                                      draft_k=inp.get("draft_k"), draft_v=inp.get("draft_v"),
+                                      tree_mask=inp.get("tree_mask"))
+    check_output(bf16_to_f64(g["o"]), o_ref)
+    assert np.max(np.abs(g["lse"].cpu().numpy() - lse_ref)) < 2e-3
+    return g, oidx, ocnt
+
+
+@pytest.mark.parametrize("G,d", [(1, 128), (2, 64), (4, 128), (8, 64), (16, 64)])
+def test_decode_group_sizes_and_ragged_lengths(cuda_lib, G, d):
+    w = BASE.scaled(B=3, L=4096, Hq=2 * G, Hkv=2, d=d, topk=8, seed=3000 + G + d)
+    inp = synth.make_inputs(w)
+    inp["kv_len"] = np.array([4096, 4096 - 37, 777], dtype=np.int32)   # ragged last blocks
+    w = w.scaled(dense_len=0)
+    _parity(w, inp)
+
+
+@pytest.mark.parametrize("bs", [64, 128])
+def test_prefill_block_sizes_ragged_chunk(cuda_lib, bs):
+    # 203 queries: not a multiple of the 4-query CTA tile; chunk starts mid-block
+    w = synth.WORKLOADS["chunked_prefill_32k"].scaled(L=3000, Tq=203, Hq=8, Hkv=2, block_size=bs,
+                                                       topk=3, n_local=2, dense_len=0, seed=3100 + bs)
+    inp = synth.make_inputs(w)
+    inp["kv_len"] = np.array([3000], dtype=np.int32)
+    _parity(w, inp)
+
+
+def test_prefill_batch_with_different_lengths(cuda_lib):
+    w = synth.WORKLOADS["tiny_prefill_2k"].scaled(B=2, L=1500, Tq=100, Hq=4, Hkv=2, d=128, seed=3200)
+    inp = synth.make_inputs(w)
+    inp["kv_len"] = np.array([1500, 611], dtype=np.int32)
+    p = w.params()
+    g = run_gpu(w, inp, pool_split=0)
+    kern_ref, _ = oracle.kernel_pool(inp["k_cache"], inp["kv_len"], 32, 16, n_kernels(w))
+    S = oracle.block_scores(inp["q"], kern_ref, inp["kv_len"], w.Hkv, p)
+    oidx, ocnt, kth, _ = oracle.select(S, inp["kv_len"], w.Tq, p, S_max=g["S_cap"])
+    gidx, gcnt = g["idx"].cpu().numpy(), g["counts"].cpu().numpy()
+    assert compare_selection(gidx, gcnt, oidx, ocnt, S, kth)[3] == 0
+    o_ref, _ = oracle.attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["kv_len"], gidx, gcnt, p)
+    check_output(bf16_to_f64(g["o"]), o_ref)
+
+
+def test_dense_switch_and_topk_covering_everything(cuda_lib):
+    # kv_len below dense_len: every block; and topk above the block count: also every block
+    for kw in (dict(dense_len=5000), dict(dense_len=0, topk=500)):
+        w = BASE.scaled(L=4096, seed=3300, **kw)
+        inp = synth.make_inputs(w)
+        g, oidx, ocnt = _parity(w, inp)
+        assert np.all(g["counts"].cpu().numpy() == 64)
+        assert np.array_equal(g["idx"].cpu().numpy()[0, 0, 0, :64], np.arange(64))
+
+
+def test_dense_prefill_without_selection(cuda_lib):
+    torch = pytest.importorskip("torch")
+    L = lib()
+    w = synth.WORKLOADS["tiny_prefill_2k"].scaled(L=700, Tq=130, Hq=4, Hkv=1, d=128, seed=3400)
+    inp = synth.make_inputs(w)
+    q, k, v, kv = (to_dev(inp[x]) for x in ("q", "k_cache", "v_cache", "kv_len"))
+    o = torch.empty_like(q)
+    L.sparse_attn_fwd(q, k, v, None, None, kv, o, w.params())
+    torch.cuda.synchronize()
+    assert L.sync_status() == 0
+    o_ref, _ = oracle.attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["kv_len"], None, None, w.params())
+    check_output(bf16_to_f64(o), o_ref)
+
+
+@pytest.mark.parametrize("n_draft", [1, 40, 64])
+def test_tree_widths(cuda_lib, n_draft):
+    w = synth.WORKLOADS["tree_verify_64k"].scaled(B=2, L=5000, Tq=n_draft, topk=6, seed=3500 + n_draft,
+                                                  tree_depth=8)
+    inp = synth.make_inputs(w)
+    inp["kv_len"] = np.array([5000, 4321], dtype=np.int32)
+    _parity(w, inp)
+
+
+def test_device_index_error_is_reported_and_context_survives(cuda_lib):
+    torch = pytest.importorskip("torch")
+    L = lib()
+    w = BASE.scaled(L=2048, seed=3600)
+    inp = synth.make_inputs(w)
+    p = w.params()
+    q, k, v = (to_dev(inp[x]) for x in ("q", "k_cache", "v_cache"))
+    kern = torch.zeros((1, 2, n_kernels(w), 128), dtype=torch.bfloat16, device="cuda")
+    L.kernel_pool(k, kern, 0, w.L, p)
+    ws = torch.empty(L.workspace_size(L.ENTRY_DECODE, 1, 1, 32, 2, 128, w.L_max, p), dtype=torch.uint8,
+                     device="cuda")
+    o = torch.empty_like(q)
+    bad_len = torch.tensor([w.L_max + 5], dtype=torch.int32, device="cuda")   # past the cache
+    L.decode(q, k, v, kern, bad_len, o, ws, p)
+    assert L.sync_status() == L.ERR_DEVICE_INDEX
+    assert L.sync_status() == 0                                            # cleared once read
+    # a selected block past the query's own block
+    idx = torch.full((1, 2, 1, L.selection_capacity(p, w.L_max)), -1, dtype=torch.int32, device="cuda")
+    idx[..., 0] = 40
+    counts = torch.ones((1, 2, 1), dtype=torch.int32, device="cuda")
+    kv = torch.tensor([100], dtype=torch.int32, device="cuda")
+    L.sparse_attn_fwd(q, k, v, idx, counts, kv, o, p)
+    assert L.sync_status() == L.ERR_DEVICE_INDEX
+    good = to_dev(inp["kv_len"])
+    L.decode(q, k, v, kern, good, o, ws, p)
+    assert L.sync_status() == 0
+
+
+def test_bad_arguments_raise(cuda_lib):
+    torch = pytest.importorskip("torch")
+    L = lib()
+    w = BASE.scaled(L=1024, seed=3700)
+    inp = synth.make_inputs(w)
+    q, k, v, kv = (to_dev(inp[x]) for x in ("q", "k_cache", "v_cache", "kv_len"))
+    kern = torch.zeros((1, 2, n_kernels(w), 128), dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(q)
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(L.InfLLMv2Error) as e:
+        L.decode(q, k, v, kern, kv, o, small, w.params())
+    assert e.value.status == L.ERR_WORKSPACE
+    with pytest.raises(L.InfLLMv2Error) as e:
+        L.kernel_pool(k, kern[:, :, :3].contiguous(), 0, w.L, w.params())
+    assert e.value.status == L.ERR_INVALID_ARG
