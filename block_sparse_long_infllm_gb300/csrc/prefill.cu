@@ -37,7 +37,7 @@ prefill_warp_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
     acc_init(A);
     const int sel_row = (b * Hkv + g) * Tq + t;
     int nsel = idx != nullptr ? counts[sel_row] : bt + 1;
-    if (nsel < 0 || nsel > S_max) {  // a caller-written count outside its idx row
+    if (idx != nullptr && (nsel < 0 || nsel > S_max)) {  // a caller-written count outside its idx row
         if (lane == 0) raise_error(err, kDevErrIndex);
         nsel = nsel < 0 ? 0 : S_max;
     }
