@@ -1,0 +1,547 @@
+#!/usr/bin/env python3
+"""Benchmark of the InfLLM v2 sparse-attention hot path on GB300.
+
+Headline: single-token decode at 128K context, batch 4 (32 query / 2 KV heads,
+head dim 128, 64-token blocks, top-64 + 1 initial + 2 local blocks) -- the
+workload "decode_128k_b4".  One step is one call of infllmv2_decode: block
+scoring over the cached semantic kernels, top-k selection, split-KV attention
+over the selected blocks and the merge of the splits, for the 4 sequences.
+The semantic-kernel cache is resident (pooled once before timing), as the
+workload states; Q, K/V and kernels are synthetic (seeded N(0,1) bf16 with
+planted blocks).  L2 is flushed (a 1 GiB write) before every timed step and
+each step is timed alone with CUDA events on the launching stream.
+
+Also reported: the 32K-context chunked prefill (4096 queries, block 128,
+top-16) as "prefill", the per-kernel stage times, the roofline of the
+dominant kernel, an end-to-end number through the C ABI with host buffers,
+and the fp64 CPU oracle's throughput on a bounded sample.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs an independent replica (the path
+shards by sequence with no exchange); value = all ranks' query tokens over
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse-attn query tok/s at 128K ctx; % of HBM / tensor-core roofline"
+UNIT = "query tok/s"
+HEADLINE = "decode_128k_b4"
+PREFILL = "chunked_prefill_32k"
+FLUSH_BYTES = 1 << 30
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--prefill-steps", type=int, default=20)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of this GPU's clocks and throttle reasons."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        import torch
+        self.proc = None
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        props = torch.cuda.get_device_properties(device)
+        self.bus = None
+        try:
+            self.bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+        except AttributeError:
+            pass
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.bus:
+            cmd.insert(1, f"--id={self.bus}")
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names[1:], parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def dev_bf16(a):
+    import numpy as np
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def source_sha(*names) -> str:
+    h = hashlib.sha1()
+    for n in names:
+        with open(os.path.join(ROOT, "block_sparse_long_infllm_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(kernel: str, sha: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was
+    taken on the current source (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and parts[0] == kernel and parts[1] == sha:
+                return float(parts[2])
+    return None
+
+
+class Flusher:
+    def __init__(self):
+        import torch
+        self.buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def __call__(self):
+        self.buf.fill_(1)
+
+
+# ------------------------------------------------------------------ decode (headline)
+
+def setup_decode(name: str):
+    import torch
+
+    from block_sparse_long_infllm_gb300 import infllmv2, synth
+    w = synth.WORKLOADS[name]
+    inp = synth.make_inputs(w)
+    p = w.params()
+    d = dict(w=w, inp=inp, p=p)
+    d["q"] = dev_bf16(inp["q"])
+    d["k"] = dev_bf16(inp["k_cache"])
+    d["v"] = dev_bf16(inp["v_cache"])
+    d["kv_len"] = torch.from_numpy(inp["kv_len"]).cuda()
+    M = (w.L - w.kernel_size) // w.kernel_stride + 1
+    d["kern"] = torch.zeros((w.B, w.Hkv, M, w.d), dtype=torch.bfloat16, device="cuda")
+    infllmv2.kernel_pool(d["k"], d["kern"], 0, w.L, p)   # resident kernel cache (not timed)
+    d["o"] = torch.empty_like(d["q"])
+    d["lse"] = torch.empty((w.B, w.Hq, w.Tq), dtype=torch.float32, device="cuda")
+    d["ws"] = torch.empty(infllmv2.workspace_size(infllmv2.ENTRY_DECODE, w.B, w.Tq, w.Hq, w.Hkv, w.d, w.L_max, p),
+                          dtype=torch.uint8, device="cuda")
+    S_cap = infllmv2.selection_capacity(p, w.L_max)
+    d["idx"] = torch.empty((w.B, w.Hkv, w.Tq, S_cap), dtype=torch.int32, device="cuda")
+    d["counts"] = torch.empty((w.B, w.Hkv, w.Tq), dtype=torch.int32, device="cuda")
+    return d
+
+
+def decode_call(d, q=None, kv_len=None, o=None):
+    from block_sparse_long_infllm_gb300 import infllmv2
+    infllmv2.decode(d["q"] if q is None else q, d["k"], d["v"], d["kern"], d["kv_len"] if kv_len is None else kv_len,
+                    d["o"] if o is None else o, d["ws"], d["p"], lse=d["lse"], idx_out=d["idx"],
+                    counts_out=d["counts"])
+
+
+def decode_algorithmic_bytes(d) -> dict:
+    """Bytes each stage must move at least: the kernel-cache scan (score) and the
+    selected K/V blocks (attend), from the selection the step made."""
+    w = d["w"]
+    M = (w.L - w.kernel_size) // w.kernel_stride + 1
+    kern_bytes = w.B * w.Hkv * M * w.d * 2
+    q_bytes = w.B * w.Tq * w.Hq * w.d * 2
+    counts = d["counts"].cpu().numpy()
+    # selected tokens: whole blocks except a partial last block past kv_len
+    idx = d["idx"].cpu().numpy()
+    L = int(d["kv_len"][0].item())
+    toks = 0
+    for b in range(w.B):
+        for g in range(w.Hkv):
+            for t in range(w.Tq):
+                blks = idx[b, g, t, :counts[b, g, t]]
+                toks += int(sum(min(w.block_size, L - int(x) * w.block_size) for x in blks))
+    kv_bytes = toks * w.d * 2 * 2
+    return dict(score=kern_bytes + q_bytes, attend=kv_bytes + q_bytes, topk=0, combine=0,
+                total=kern_bytes + kv_bytes + 2 * q_bytes, kernel_cache=kern_bytes, selected_kv=kv_bytes)
+
+
+def run_decode(args, world, rank):
+    import torch
+
+    from block_sparse_long_infllm_gb300 import infllmv2
+    d = setup_decode(HEADLINE)
+    w = d["w"]
+    flush = Flusher()
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush()
+        decode_call(d)
+    torch.cuda.synchronize()
+    if infllmv2.sync_status() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    # ---- timed region: K steps, L2 flushed before each, events around each step
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall = time.perf_counter()
+    for i in range(K):
+        flush()
+        ev[i][0].record(stream)
+        decode_call(d)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    status = infllmv2.sync_status()
+
+    # ---- stage times (a second K-step region with the library's stage events)
+    stage_n = min(K, 500)
+    infllmv2.profile_enable(True)
+    stages: dict[str, list[float]] = {}
+    for _ in range(stage_n):
+        flush()
+        decode_call(d)
+        for name, ms in infllmv2.profile_read():
+            stages.setdefault(name, []).append(ms)
+    infllmv2.profile_enable(False)
+    stage_ms = {k: statistics.median(v) for k, v in stages.items()}
+
+    alg = decode_algorithmic_bytes(d)
+    pk = peaks()
+    dom = max(("score", "attend"), key=lambda s: stage_ms.get(s, 0.0))
+    achieved = alg[dom] / (stage_ms[dom] * 1e-3) / 1e9
+    kernel_names = {"score": "score_kernel", "attend": "decode_split_kernel"}
+    sha = source_sha("select.cu" if dom == "score" else "decode.cu", "attn_warp.cuh", "common.cuh")
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": ncu_traffic(kernel_names[dom], sha),
+                "kernel": kernel_names[dom], "algorithmic_bytes": alg[dom], "peak_source": pk["source"]}
+    step_alg_gbs = alg["total"] / (total_ms / K * 1e-3) / 1e9
+
+    out = dict(metric=METRIC, value=None, unit=UNIT, n_gpus=world, steps=K, warmup=args.warmup,
+               ms_per_step=total_ms / K, higher_is_better=True, scaling="weak", vs_baseline=None,
+               dtype="bf16", data="synthetic (seeded N(0,1) bf16, planted blocks)",
+               config={"workload": HEADLINE, "batch": w.B, "kv_len": w.L, "q_heads": w.Hq, "kv_heads": w.Hkv,
+                       "head_dim": w.d, "block_size": w.block_size, "kernel": [w.kernel_size, w.kernel_stride],
+                       "topk": w.topk, "n_init": w.n_init, "n_local": w.n_local, "dense_len": w.dense_len,
+                       "parallelism": f"replicas x{world}", "l2": "flushed by a 1 GiB write before each timed step",
+                       "kernel_cache": "resident (pooled before timing)"},
+               roofline=roofline, clocks=clk, gpu_launches=4 * K, device_status=status)
+    out["value"] = world * w.B * w.Tq * K / (total_ms * 1e-3)
+    out["step"] = {"algorithmic_bytes": alg["total"], "kernel_cache_bytes": alg["kernel_cache"],
+                   "selected_kv_bytes": alg["selected_kv"], "achieved_gbs": round(step_alg_gbs, 1),
+                   "frac_hbm": round(step_alg_gbs / pk["hbm_gbs"], 4), "frac_8tbs": round(step_alg_gbs / 8000, 4),
+                   "wall_s": round(t_wall, 3)}
+    out["stages_ms"] = {k: round(v, 5) for k, v in stage_ms.items()}
+    out["e2e"] = run_decode_e2e(d, flush, n=min(K, 300))
+    return out, d
+
+
+def run_decode_e2e(d, flush, n: int) -> dict:
+    """Same step through the public call with host buffers: copy this step's query
+    (and lengths) from pinned host memory, decode, read the output back."""
+    import torch
+    w = d["w"]
+    q_host = d["q"].cpu().pin_memory()
+    kv_host = d["kv_len"].cpu().pin_memory()
+    o_host = torch.empty(d["o"].shape, dtype=d["o"].dtype).pin_memory()
+    q_dev = torch.empty_like(d["q"])
+    kv_dev = torch.empty_like(d["kv_len"])
+    stream = torch.cuda.current_stream()
+    times = []
+    for i in range(n + 3):
+        flush()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        q_dev.copy_(q_host, non_blocking=True)
+        kv_dev.copy_(kv_host, non_blocking=True)
+        decode_call(d, q=q_dev, kv_len=kv_dev)
+        o_host.copy_(d["o"], non_blocking=True)
+        stream.synchronize()
+        if i >= 3:
+            times.append(time.perf_counter() - t0)
+    h2d = q_host.numel() * q_host.element_size() + kv_host.numel() * kv_host.element_size()
+    d2h = o_host.numel() * o_host.element_size()
+    return {"value": w.B * w.Tq / statistics.mean(times), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * statistics.mean(times),
+            "note": "wall clock per step, L2 flushed before each; KV and kernel caches resident"}
+
+
+# ------------------------------------------------------------------ prefill (secondary)
+
+def run_prefill(args) -> dict:
+    import numpy as np
+    import torch
+
+    from block_sparse_long_infllm_gb300 import infllmv2, synth
+    w = synth.WORKLOADS[PREFILL]
+    inp = synth.make_inputs(w)
+    p = w.params()
+    q, k, v = dev_bf16(inp["q"]), dev_bf16(inp["k_cache"]), dev_bf16(inp["v_cache"])
+    kv_len = torch.from_numpy(inp["kv_len"]).cuda()
+    M = (w.L - w.kernel_size) // w.kernel_stride + 1
+    kern = torch.zeros((w.B, w.Hkv, M, w.d), dtype=torch.bfloat16, device="cuda")
+    infllmv2.kernel_pool(k, kern, 0, w.q_pos0, p)     # kernels of the cached prefix (not timed)
+    S_cap = infllmv2.selection_capacity(p, w.L_max)
+    idx = torch.empty((w.B, w.Hkv, w.Tq, S_cap), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((w.B, w.Hkv, w.Tq), dtype=torch.int32, device="cuda")
+    ws = torch.empty(infllmv2.workspace_size(infllmv2.ENTRY_BLOCK_SELECT, w.B, w.Tq, w.Hq, w.Hkv, w.d, w.L_max, p),
+                     dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Tq), dtype=torch.float32, device="cuda")
+    flush = Flusher()
+    stream = torch.cuda.current_stream()
+
+    def step(record=None):
+        infllmv2.kernel_pool(k, kern, w.q_pos0, w.L, p)
+        if record is not None:
+            record.append(infllmv2.profile_read())
+        infllmv2.block_select(q, kern, kv_len, idx, cnt, ws, p, w.L_max)
+        if record is not None:
+            record.append(infllmv2.profile_read())
+        infllmv2.sparse_attn_fwd(q, k, v, idx, cnt, kv_len, o, p, lse=lse)
+        if record is not None:
+            record.append(infllmv2.profile_read())
+
+    for _ in range(3):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    K = args.prefill_steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    infllmv2.profile_enable(True)
+    stages: dict[str, list[float]] = {}
+    for _ in range(max(3, K // 2)):
+        flush()
+        rec = []
+        step(rec)
+        for part in rec:
+            for name, t in part:
+                stages.setdefault(name, []).append(t)
+    infllmv2.profile_enable(False)
+    stage_ms = {kk: statistics.median(vv) for kk, vv in stages.items()}
+
+    # algorithmic FLOPs: 4 d per attended (query, head, key) and 2 d per scored (query, head, kernel)
+    counts = cnt.cpu().numpy()
+    sel = idx.cpu().numpy()
+    attended = 0
+    scored = 0
+    for t in range(w.Tq):
+        pos = w.L - w.Tq + t
+        vis_kernels = (pos + 1 - w.kernel_size) // w.kernel_stride + 1
+        scored += vis_kernels * w.Hq
+        for g in range(w.Hkv):
+            blks = sel[0, g, t, :counts[0, g, t]].astype(np.int64)
+            keys = np.minimum(pos + 1 - blks * w.block_size, w.block_size).clip(min=0).sum()
+            attended += int(keys) * (w.Hq // w.Hkv)
+    fl_attn = 4.0 * w.d * attended
+    fl_score = 2.0 * w.d * scored
+    pk = peaks()
+    att_tf = fl_attn / (stage_ms["attend"] * 1e-3) / 1e12
+    step_tf = (fl_attn + fl_score) / (ms * 1e-3) / 1e12
+    return {"workload": PREFILL, "value": w.Tq / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms, "steps": K,
+            "stages_ms": {kk: round(vv, 4) for kk, vv in stage_ms.items()},
+            "algorithmic_gflop": {"attention": fl_attn / 1e9, "score": fl_score / 1e9},
+            "keys_per_query": attended / (w.Tq * w.Hq),
+            "roofline": {"bound": "tensor", "kernel": "prefill_warp_kernel", "achieved": round(att_tf, 2),
+                         "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(att_tf / pk["bf16_tflops"], 4),
+                         "traffic": None},
+            "step_tflops": round(step_tf, 2), "step_frac": round(step_tf / pk["bf16_tflops"], 4),
+            "gpu_launches": 4 * K}
+
+
+# ------------------------------------------------------------------ oracle (CPU) baseline
+
+def oracle_rows(inp, w, kern, rows):
+    """The oracle's decode step restricted to the listed (b, g) rows and heads."""
+    import numpy as np
+
+    import oracle
+    p = w.params()
+    for (b, g, heads) in rows:
+        G = w.Hq // w.Hkv
+        hsel = list(range(g * G, g * G + heads))
+        q = np.ascontiguousarray(inp["q"][b:b + 1][:, :, hsel])
+        kern_bg = np.ascontiguousarray(kern[b:b + 1, g:g + 1])
+        kv = inp["kv_len"][b:b + 1]
+        S = oracle.block_scores(q, kern_bg, kv, 1, p)
+        idx, cnt, _, _ = oracle.select(S, kv, 1, p)
+        oracle.attention(q, np.ascontiguousarray(inp["k_cache"][b:b + 1, g:g + 1]),
+                         np.ascontiguousarray(inp["v_cache"][b:b + 1, g:g + 1]), kv, idx, cnt, p)
+
+
+def oracle_setup():
+    import oracle
+    from block_sparse_long_infllm_gb300 import synth
+    w = synth.WORKLOADS[HEADLINE]
+    inp = synth.make_inputs(w)
+    M = oracle.n_kernels(w.L, w.kernel_size, w.kernel_stride)
+    kern, _ = oracle.kernel_pool(inp["k_cache"], inp["kv_len"], w.kernel_size, w.kernel_stride, M)
+    return w, inp, kern
+
+
+def cpu_baseline(seconds: float = 12.0, prepared=None) -> dict:
+    """The oracle (as it stands) on whole decode rows of the headline workload,
+    for about `seconds` of host time."""
+    import oracle
+    w, inp, kern = prepared or oracle_setup()
+    G = w.Hq // w.Hkv
+    n = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds or n == 0:
+        b, g = divmod(n % (w.B * w.Hkv), w.Hkv)
+        oracle_rows(inp, w, kern, [(b, g, G)])
+        n += 1
+    el = time.perf_counter() - t0
+    queries = n * G / w.Hq
+    return {"value": queries / el, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} decode rows (sequence, KV head: 16 heads = 1/2 query token each) of {HEADLINE}, "
+                      f"{el:.1f} s; kernel cache precomputed as in the workload"}
+
+
+def run_reference(args, world, rank):
+    """The fp64 oracle as the reference arm: each step is one decode row of the
+    headline workload with as many of its 16 heads as keep the run within a few minutes."""
+    if rank != 0:
+        return None
+    import oracle
+    prepared = oracle_setup()
+    w, inp, kern = prepared
+    G = w.Hq // w.Hkv
+    t0 = time.perf_counter()
+    oracle_rows(inp, w, kern, [(0, 0, G)])
+    t_row = time.perf_counter() - t0
+    heads = G
+    budget = 150.0
+    while heads > 1 and (args.steps + args.warmup) * t_row * heads / G > budget:
+        heads //= 2
+    for i in range(args.warmup):
+        b, g = divmod(i % (w.B * w.Hkv), w.Hkv)
+        oracle_rows(inp, w, kern, [(b, g, heads)])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        b, g = divmod(i % (w.B * w.Hkv), w.Hkv)
+        oracle_rows(inp, w, kern, [(b, g, heads)])
+    el = time.perf_counter() - t0
+    value = args.steps * heads / w.Hq / el
+    cfg = {"workload": HEADLINE, "batch": w.B, "kv_len": w.L, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.d,
+           "block_size": w.block_size, "topk": w.topk}
+    sample = f"each step: one decode row (sequence, KV head) of {HEADLINE} with {heads} of its {G} query heads"
+    return dict(impl="reference", metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
+                warmup=args.warmup, ms_per_step=1e3 * el / args.steps, higher_is_better=True, scaling="weak",
+                vs_baseline=None, dtype="f64", data="synthetic (seeded N(0,1) bf16, planted blocks)", config=cfg,
+                cpu_baseline={"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                              "sample": sample},
+                e2e={"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0})
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_info()
+    if args.impl == "reference":
+        out = run_reference(args, world, rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    out, _ = run_decode(args, world, rank)
+    if not args.no_prefill:
+        out["prefill"] = run_prefill(args)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline()
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -96,6 +96,55 @@ DecodeWs decode_ws(int B, int n_draft, int Hkv, int d, int L_max, const Params& 
 
 int blocks_per_score_cta(const Params& p) { return 2048 / p.block_size; }
 
+// ---- stage timing
+constexpr int kMaxStages = 8;
+struct ProfState {
+    cudaEvent_t ev[kMaxStages + 1] = {};
+    const char* name[kMaxStages] = {};
+    int n = -1;  // marks recorded after the begin event of the last call
+    bool ready = false;
+};
+bool g_prof_on = false;
+ProfState g_prof[kMaxDevices];
+
+ProfState* prof_state() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    ProfState& st = g_prof[dev];
+    if (!st.ready) {
+        for (auto& e : st.ev)
+            if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        st.ready = true;
+    }
+    return &st;
+}
+
+}  // namespace
+
+namespace infllmv2 {
+
+void prof_begin(cudaStream_t stream) {
+    if (!g_prof_on) return;
+    ProfState* st = prof_state();
+    if (st == nullptr) return;
+    st->n = 0;
+    cudaEventRecord(st->ev[0], stream);
+}
+
+void prof_mark(cudaStream_t stream, const char* stage) {
+    if (!g_prof_on) return;
+    ProfState* st = prof_state();
+    if (st == nullptr || st->n < 0 || st->n >= kMaxStages) return;
+    st->name[st->n] = stage;
+    st->n += 1;
+    cudaEventRecord(st->ev[st->n], stream);
+}
+
+}  // namespace infllmv2
+
+namespace {
+using infllmv2::prof_begin;
+using infllmv2::prof_mark;
 }  // namespace
 
 extern "C" {
@@ -115,6 +164,30 @@ const char* infllmv2_status_string(int status) {
 }
 
 int infllmv2_version(void) { return kVersion; }
+
+int infllmv2_profile_enable(int on) {
+    g_prof_on = on != 0;
+    if (g_prof_on && prof_state() == nullptr) return INFLLMV2_ERR_CUDA;
+    return INFLLMV2_OK;
+}
+
+int infllmv2_profile_read(float* ms, int max_stages, int* n_stages) {
+    ProfState* st = prof_state();
+    if (st == nullptr) return INFLLMV2_ERR_CUDA;
+    const int n = st->n < 0 ? 0 : st->n;
+    if (n_stages != nullptr) *n_stages = n;
+    for (int i = 0; i < n && i < max_stages; ++i) {
+        if (cudaEventSynchronize(st->ev[i + 1]) != cudaSuccess) return INFLLMV2_ERR_CUDA;
+        if (cudaEventElapsedTime(&ms[i], st->ev[i], st->ev[i + 1]) != cudaSuccess) return INFLLMV2_ERR_CUDA;
+    }
+    return INFLLMV2_OK;
+}
+
+const char* infllmv2_profile_stage_name(int i) {
+    ProfState* st = prof_state();
+    if (st == nullptr || i < 0 || i >= st->n || st->name[i] == nullptr) return "";
+    return st->name[i];
+}
 
 int infllmv2_sync_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return INFLLMV2_ERR_CUDA;
@@ -165,8 +238,12 @@ int infllmv2_kernel_pool(const void* k_cache, void* kernel_cache, int B, int Hkv
     if (B == 0 || n_new <= 0) return INFLLMV2_OK;
     if (j_last >= M_max) return INFLLMV2_ERR_INVALID_ARG;
     if (!k_cache || !kernel_cache || !aligned16(k_cache) || !aligned16(kernel_cache)) return INFLLMV2_ERR_INVALID_ARG;
-    return cuda_status(infllmv2::launch_kernel_pool(k_cache, kernel_cache, B, Hkv, L_max, M_max, d, j_first, n_new,
-                                                    c, s, static_cast<cudaStream_t>(stream)));
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    prof_begin(st);
+    const cudaError_t e = infllmv2::launch_kernel_pool(k_cache, kernel_cache, B, Hkv, L_max, M_max, d, j_first,
+                                                       n_new, c, s, st);
+    prof_mark(st, "pool");
+    return cuda_status(e);
 }
 
 int infllmv2_block_select(const void* q, const void* kernel_cache, const int32_t* kv_len, int B, int Tq, int Hq,
@@ -188,6 +265,7 @@ int infllmv2_block_select(const void* q, const void* kernel_cache, const int32_t
     if (err == nullptr) return INFLLMV2_ERR_CUDA;
     infllmv2::SelectArgs a{q, kernel_cache, kv_len, B, Tq, Hq, Hkv, d, L_max, M_max, 0, idx, counts, S_max,
                            blocks_per_score_cta(p), p, err, static_cast<cudaStream_t>(stream)};
+    prof_begin(a.stream);
     return cuda_status(infllmv2::launch_block_select(a, static_cast<float*>(workspace)));
 }
 
@@ -213,7 +291,10 @@ int infllmv2_sparse_attn_fwd(const void* q, const void* k_cache, const void* v_c
     if (err == nullptr) return INFLLMV2_ERR_CUDA;
     infllmv2::PrefillArgs a{q, k_cache, v_cache, idx, counts, S_max, kv_len, B, Tq, Hq, Hkv, d, L_max,
                             o, lse, p, err, static_cast<cudaStream_t>(stream)};
-    return cuda_status(infllmv2::launch_prefill_attention(a));
+    prof_begin(a.stream);
+    const cudaError_t e = infllmv2::launch_prefill_attention(a);
+    prof_mark(a.stream, "attend");
+    return cuda_status(e);
 }
 
 int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache, const void* kernel_cache,
@@ -252,6 +333,7 @@ int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache, con
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     infllmv2::SelectArgs sa{q, kernel_cache, kv_len, B, n_draft, Hq, Hkv, d, L_max, M_max, tree ? 1 : 0, idx, counts,
                             stride, blocks_per_score_cta(p), p, err, st};
+    prof_begin(st);
     if (int rc = cuda_status(infllmv2::launch_block_select(sa, reinterpret_cast<float*>(ws + w.scores)))) return rc;
     infllmv2::DecodeArgs da{q, k_cache, v_cache, kv_len, draft_k, draft_v, tree_mask, B, n_draft, Hq, Hkv, d, L_max,
                             o, lse, p, err, st};

@@ -201,6 +201,7 @@ cudaError_t launch_decode_attention(const DecodeArgs& a, const int* idx, const i
                                                              idx_stride, a.n_draft, a.Hq, a.Hkv, G, a.L_max,
                                                              a.p.block_size, bps, nsc, ns, scale_log2, part, a.err);
         if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
+        prof_mark(a.stream, "attend");
         decode_combine_kernel<128><<<rows, 128, 0, a.stream>>>(part, counts, bps, nsc, ns, a.n_draft, a.Hq, a.Hkv, G,
                                                                static_cast<__nv_bfloat16*>(a.o), a.lse);
     } else {
@@ -208,9 +209,11 @@ cudaError_t launch_decode_attention(const DecodeArgs& a, const int* idx, const i
                                                             idx_stride, a.n_draft, a.Hq, a.Hkv, G, a.L_max,
                                                             a.p.block_size, bps, nsc, ns, scale_log2, part, a.err);
         if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
+        prof_mark(a.stream, "attend");
         decode_combine_kernel<64><<<rows, 128, 0, a.stream>>>(part, counts, bps, nsc, ns, a.n_draft, a.Hq, a.Hkv, G,
                                                               static_cast<__nv_bfloat16*>(a.o), a.lse);
     }
+    prof_mark(a.stream, "combine");
     return cudaGetLastError();
 }
 

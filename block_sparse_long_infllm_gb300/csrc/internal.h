@@ -56,6 +56,10 @@ struct DecodeArgs {
     cudaStream_t stream;
 };
 
+// Stage timing (infllmv2_profile_*): no-ops unless profiling is enabled.
+void prof_begin(cudaStream_t stream);
+void prof_mark(cudaStream_t stream, const char* stage);
+
 cudaError_t launch_kernel_pool(const void* k_cache, void* kernel_cache, int B, int Hkv, int L_max,
                                int M_max, int d, int j_first, int n_new, int c, int s,
                                cudaStream_t stream);

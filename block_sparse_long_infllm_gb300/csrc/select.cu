@@ -322,6 +322,7 @@ cudaError_t launch_block_select(const SelectArgs& a, float* S) {
     if (a.d == 128) e = many ? launch_score_t<128, 4, 4>(a, S) : launch_score_t<128, 4, 1>(a, S);
     else e = many ? launch_score_t<64, 4, 4>(a, S) : launch_score_t<64, 4, 1>(a, S);
     if (e != cudaSuccess) return e;
+    prof_mark(a.stream, "score");
     const int rows = a.B * a.Hkv * a.Tq;
     if (nblk_max <= 512)
         topk_kernel<128><<<rows, 128, 0, a.stream>>>(S, a.kv_len, a.Tq, a.Hkv, nblk_max, a.L_max, a.tree, p,
@@ -329,6 +330,7 @@ cudaError_t launch_block_select(const SelectArgs& a, float* S) {
     else
         topk_kernel<512><<<rows, 512, 0, a.stream>>>(S, a.kv_len, a.Tq, a.Hkv, nblk_max, a.L_max, a.tree, p,
                                                      a.idx, a.counts, a.S_max, a.err);
+    prof_mark(a.stream, "topk");
     return cudaGetLastError();
 }
 

@@ -81,7 +81,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                              p, sz, pp, p]
     lib.infllmv2_decode.argtypes = [p, p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, p, p, p,
                                     p, i32, p, sz, pp, p]
+    lib.infllmv2_profile_enable.argtypes = [i32]
+    lib.infllmv2_profile_read.argtypes = [p, i32, p]
+    lib.infllmv2_profile_stage_name.argtypes = [i32]
+    lib.infllmv2_profile_stage_name.restype = ctypes.c_char_p
     for name in ("infllmv2_version", "infllmv2_sync_status", "infllmv2_selection_capacity",
+                 "infllmv2_profile_enable", "infllmv2_profile_read",
                  "infllmv2_kernel_pool", "infllmv2_block_select", "infllmv2_sparse_attn_fwd",
                  "infllmv2_decode"):
         getattr(lib, name).restype = ctypes.c_int
@@ -131,6 +136,20 @@ def _stream(stream):
 def sync_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error status."""
     return int(load().infllmv2_sync_status(_stream(stream)))
+
+
+def profile_enable(on: bool = True):
+    """Record a CUDA event around every kernel the entry points launch."""
+    _check(load().infllmv2_profile_enable(1 if on else 0), "infllmv2_profile_enable")
+
+
+def profile_read(max_stages: int = 8) -> list[tuple[str, float]]:
+    """(stage name, milliseconds) for each kernel of the most recent call (waits for it)."""
+    lib = load()
+    ms = (ctypes.c_float * max_stages)()
+    n = ctypes.c_int(0)
+    _check(lib.infllmv2_profile_read(ms, max_stages, ctypes.byref(n)), "infllmv2_profile_read")
+    return [(lib.infllmv2_profile_stage_name(i).decode(), float(ms[i])) for i in range(min(n.value, max_stages))]
 
 
 def selection_capacity(params, L_max: int) -> int:

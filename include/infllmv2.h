@@ -200,6 +200,22 @@ int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache,
                     int32_t* counts_out, int S_max, void* workspace, size_t ws_bytes,
                     const infllmv2_params* params, void* stream);
 
+/*
+ * Stage timing (the pages' CPM.cu lists a performance-analysis module next to
+ * the inference entry; this is the library's counterpart).  While enabled,
+ * every entry point records a CUDA event on its stream before its first kernel
+ * and after each kernel it launches; infllmv2_profile_read then waits for
+ * those events and writes the elapsed milliseconds of each stage of the most
+ * recent call into ms[0 .. *n_stages-1] (at most max_stages), and
+ * infllmv2_profile_stage_name(i) names stage i ("pool", "score", "topk",
+ * "attend", "combine").  Events live in the library, per device, created on
+ * first use; enabling costs one event record per kernel.  Not thread-safe.
+ * Returns INFLLMV2_OK or INFLLMV2_ERR_CUDA.
+ */
+int infllmv2_profile_enable(int on);
+int infllmv2_profile_read(float* ms, int max_stages, int* n_stages);
+const char* infllmv2_profile_stage_name(int i);
+
 #ifdef __cplusplus
 }
 #endif

@@ -149,16 +149,16 @@ int orc_block_scores(const uint16_t* q, const uint16_t* kern, const int32_t* kv_
             if (pos < 0 || pos / bs >= nblk_max) return ORC_ERR_CAPACITY;
         }
     }
-#pragma omp parallel for collapse(3) schedule(dynamic)
+#pragma omp parallel for collapse(4) schedule(dynamic, 16)
     for (int64_t b = 0; b < B; ++b) {
         for (int64_t g = 0; g < Hkv; ++g) {
             for (int64_t ti = 0; ti < n_t; ++ti) {
-                const int64_t t = t_list[ti];
-                const int64_t pos = query_pos(kv_len[b], Tq, t, tree);
-                const int64_t bt = pos / bs;
-                const int64_t M = n_kernels(kv_len[b], c, s);
-                double* row = S + ((b * Hkv + g) * n_t + ti) * nblk_max;
                 for (int64_t blk = 0; blk < nblk_max; ++blk) {
+                    const int64_t t = t_list[ti];
+                    const int64_t pos = query_pos(kv_len[b], Tq, t, tree);
+                    const int64_t bt = pos / bs;
+                    const int64_t M = n_kernels(kv_len[b], c, s);
+                    double* row = S + ((b * Hkv + g) * n_t + ti) * nblk_max;
                     double best = -INFINITY;
                     if (blk <= bt) {
                         for (int64_t h = g * G; h < (g + 1) * G; ++h) {
