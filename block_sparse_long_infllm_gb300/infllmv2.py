@@ -81,6 +81,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                              p, sz, pp, p]
     lib.infllmv2_decode.argtypes = [p, p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, p, p, p,
                                     p, i32, p, sz, pp, p]
+    lib.infllmv2_decode_noalloc.argtypes = [p, p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, p, p,
+                                            p, p, i32, pp, p]
+    lib.infllmv2_decode_noalloc.restype = ctypes.c_int
     lib.infllmv2_profile_enable.argtypes = [i32]
     lib.infllmv2_profile_read.argtypes = [p, i32, p]
     lib.infllmv2_profile_stage_name.argtypes = [i32]
@@ -206,3 +209,22 @@ def decode(q, k_cache, v_cache, kernel_cache, kv_len, o, workspace, params, lse=
                                   L_max, M_max, _ptr(o), _ptr(lse), _ptr(idx_out), _ptr(counts_out), S_max,
                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
                                   ctypes.byref(Params.make(params)), _stream(stream)), "infllmv2_decode")
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20  # INFLLMV2_NOALLOC_SCRATCH_BYTES
+
+
+def decode_noalloc(q, k_cache, v_cache, kernel_cache, kv_len, o, params, lse=None, draft_k=None, draft_v=None,
+                   tree_mask=None, idx_out=None, counts_out=None, stream=None):
+    """infllmv2_decode without a workspace argument: for callers that cannot allocate
+    device memory; the library's fixed scratch array is used instead (see the header)."""
+    B, n_draft, Hq, d = q.shape
+    Hkv, L_max = k_cache.shape[1], k_cache.shape[2]
+    M_max = kernel_cache.shape[2]
+    S_max = 0 if idx_out is None else idx_out.shape[-1]
+    _check(load().infllmv2_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kernel_cache),
+                                          _ptr(kv_len), _ptr(draft_k), _ptr(draft_v), _ptr(tree_mask), B,
+                                          n_draft, Hq, Hkv, d, L_max, M_max, _ptr(o), _ptr(lse),
+                                          _ptr(idx_out), _ptr(counts_out), S_max,
+                                          ctypes.byref(Params.make(params)), _stream(stream)),
+           "infllmv2_decode_noalloc")

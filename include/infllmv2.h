@@ -201,6 +201,34 @@ int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache,
                     const infllmv2_params* params, void* stream);
 
 /*
+ * Allocation-free decode.  The paper has no counterpart: this entry point is
+ * for callers of this library that cannot provide a workspace -- a process whose
+ * device memory is reserved up front by its own pool, a plugin that receives
+ * only input and output pointers, or a loop that must not allocate after
+ * start-up.  It behaves exactly like infllmv2_decode (same arguments without
+ * workspace/ws_bytes, same results) but takes its scratch from one fixed array
+ * of INFLLMV2_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads the library holds until the process exits.
+ *   - Problems whose decode workspace (infllmv2_workspace_size with
+ *     INFLLMV2_ENTRY_DECODE) exceeds that size are rejected with
+ *     INFLLMV2_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on each device looks up the array's device address with
+ *     cudaGetSymbolAddress (the device must be current); make that first call
+ *     before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents (nothing
+ *     in it needs to start at zero).  Calls that overlap on the GPU -- other
+ *     streams, other host threads -- race on it; serialise them.
+ *   - It never calls cudaMalloc, cudaFree or any allocating routine.
+ */
+#define INFLLMV2_NOALLOC_SCRATCH_BYTES (16u << 20)
+int infllmv2_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                            const void* kernel_cache, const int32_t* kv_len, const void* draft_k,
+                            const void* draft_v, const uint64_t* tree_mask, int B, int n_draft,
+                            int Hq, int Hkv, int d, int L_max, int M_max, void* o, float* lse,
+                            int32_t* idx_out, int32_t* counts_out, int S_max,
+                            const infllmv2_params* params, void* stream);
+
+/*
  * Stage timing (the pages' CPM.cu lists a performance-analysis module next to
  * the inference entry; this is the library's counterpart).  While enabled,
  * every entry point records a CUDA event on its stream before its first kernel
