@@ -94,6 +94,30 @@ __device__ __forceinline__ uint32_t pair_halves(uint32_t w0, uint32_t w1, int e)
     return e == 0 ? __byte_perm(w0, w1, 0x5410) : __byte_perm(w0, w1, 0x7632);
 }
 
+// Programmatic dependent launch: a kernel launched with the programmatic-serialisation
+// attribute may start before its predecessor on the stream has finished; pdl_wait() blocks
+// until the predecessor grid has completed and its memory is visible (it returns at once for a
+// normally launched kernel).  pdl_trigger() lets the successor start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch `kern` on `stream`; with `pdl` the launch may overlap the previous kernel's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          bool pdl, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Monotone map from fp32 to uint32 (larger float -> larger key); -0 is folded into +0
 // so that equal scores always compare equal.
 __device__ __forceinline__ uint32_t ordered_key(float s) {

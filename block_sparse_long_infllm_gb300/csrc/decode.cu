@@ -41,6 +41,11 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
     const int i = (row_id / Hkv) % n_draft;
     const int b = row_id / (Hkv * n_draft);
     const int sp = blockIdx.x;
+    // q and the caches were written before this call: load Q while the selection finishes
+    QFrag<D> Q;
+    load_q(Q, q + ((static_cast<size_t>(b) * n_draft + i) * Hq + static_cast<size_t>(g) * G) * D, D, G);
+    pdl_wait();
+    pdl_trigger();
     const int L = kv_len[b];
     const bool len_ok = L >= 1 && L <= L_max;
     // splits past the row's selected blocks hold nothing; the merge never reads them
@@ -49,8 +54,6 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
     WarpAcc<D> A;
     acc_init(A);
     if (len_ok) {
-        QFrag<D> Q;
-        load_q(Q, q + ((static_cast<size_t>(b) * n_draft + i) * Hq + static_cast<size_t>(g) * G) * D, D, G);
         if (sp < n_split_cache) {
             const int sel_row = (b * Hkv + g) * n_draft + i;
             const int cnt = counts[sel_row];
@@ -123,51 +126,56 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
     }
 }
 
+// Merge of a row's split partials: D/4 threads per query head (four output elements each),
+// 512/D heads per CTA, so a batch of rows spreads over many SMs and every thread's split
+// loop issues independent loads.
 template <int D>
 __global__ void __launch_bounds__(128)
 decode_combine_kernel(const float* __restrict__ part, const int* __restrict__ counts, int blocks_per_split,
                       int n_split_cache, int n_split, int n_draft, int Hq, int Hkv, int G,
                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+    constexpr int TPH = D / 4;        // threads per head row
+    constexpr int HPC = 128 / TPH;    // head rows per CTA
     const int row_id = blockIdx.x;
+    const int r = blockIdx.y * HPC + threadIdx.x / TPH;
+    const int dq = (threadIdx.x % TPH) * 4;
     const int g = row_id % Hkv;
     const int i = (row_id / Hkv) % n_draft;
     const int b = row_id / (Hkv * n_draft);
+    pdl_wait();
+    if (r >= G) return;
     const float* src = part + static_cast<size_t>(row_id) * n_split * PartialLayout<D>::kFloats;
     // the cache splits that hold selected blocks, then the draft split (tree mode)
     const int cnt = counts[(b * Hkv + g) * n_draft + i];
     const int used = min((cnt + blocks_per_split - 1) / blocks_per_split, n_split_cache);
     const int n_read = used + (n_split - n_split_cache);
-    constexpr int Q4 = D / 4;
-    for (int e = threadIdx.x; e < G * Q4; e += blockDim.x) {
-        const int r = e / Q4, dq = (e % Q4) * 4;
-        float M = -INFINITY;
-        for (int k = 0; k < n_read; ++k) {
-            const int s = k < used ? k : n_split_cache + (k - used);
-            M = fmaxf(M, src[s * PartialLayout<D>::kFloats + r]);
-        }
-        const float ref = M == -INFINITY ? 0.f : M;
-        float l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int k = 0; k < n_read; ++k) {
-            const int s = k < used ? k : n_split_cache + (k - used);
-            const float* ps = src + s * PartialLayout<D>::kFloats;
-            const float f = fast_exp2(ps[r] - ref);
-            l += ps[16 + r] * f;
-            const float4 ov = *reinterpret_cast<const float4*>(ps + 32 + r * D + dq);
-            acc[0] += ov.x * f;
-            acc[1] += ov.y * f;
-            acc[2] += ov.z * f;
-            acc[3] += ov.w * f;
-        }
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const int h = g * G + r;
-        uint2 packed;
-        packed.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        packed.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-        *reinterpret_cast<uint2*>(o + ((static_cast<size_t>(b) * n_draft + i) * Hq + h) * D + dq) = packed;
-        if (lse != nullptr && dq == 0)
-            lse[(static_cast<size_t>(b) * Hq + h) * n_draft + i] =
-                l > 0.f ? (M + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+    float M = -INFINITY;
+    for (int k = 0; k < n_read; ++k) {
+        const int s = k < used ? k : n_split_cache + (k - used);
+        M = fmaxf(M, __ldcg(src + s * PartialLayout<D>::kFloats + r));
     }
+    const float ref = M == -INFINITY ? 0.f : M;
+    float l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < n_read; ++k) {
+        const int s = k < used ? k : n_split_cache + (k - used);
+        const float* ps = src + s * PartialLayout<D>::kFloats;
+        const float f = fast_exp2(__ldcg(ps + r) - ref);
+        l += __ldcg(ps + 16 + r) * f;
+        const float4 ov = __ldcg(reinterpret_cast<const float4*>(ps + 32 + r * D + dq));
+        acc[0] += ov.x * f;
+        acc[1] += ov.y * f;
+        acc[2] += ov.z * f;
+        acc[3] += ov.w * f;
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const int h = g * G + r;
+    uint2 packed;
+    packed.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    packed.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(o + ((static_cast<size_t>(b) * n_draft + i) * Hq + h) * D + dq) = packed;
+    if (lse != nullptr && dq == 0)
+        lse[(static_cast<size_t>(b) * Hq + h) * n_draft + i] =
+            l > 0.f ? (M + log2f(l)) * 0.69314718055994530942f : -INFINITY;
 }
 
 size_t decode_partial_bytes(int B, int n_draft, int Hkv, int d, int n_split) {
@@ -190,31 +198,32 @@ cudaError_t launch_decode_attention(const DecodeArgs& a, const int* idx, const i
     const int G = a.Hq / a.Hkv;
     const int rows = a.B * a.n_draft * a.Hkv;
     const float scale_log2 = a.p.scale * 1.4426950408889634f;
-    dim3 grid(ns, rows);
     const auto* qp = static_cast<const __nv_bfloat16*>(a.q);
     const auto* kp = static_cast<const __nv_bfloat16*>(a.k_cache);
     const auto* vp = static_cast<const __nv_bfloat16*>(a.v_cache);
     const auto* dkp = static_cast<const __nv_bfloat16*>(a.draft_k);
     const auto* dvp = static_cast<const __nv_bfloat16*>(a.draft_v);
+    auto* op = static_cast<__nv_bfloat16*>(a.o);
+    cudaError_t e;
     if (a.d == 128) {
-        decode_split_kernel<128><<<grid, 128, 0, a.stream>>>(qp, kp, vp, dkp, dvp, a.tree_mask, a.kv_len, idx, counts,
-                                                             idx_stride, a.n_draft, a.Hq, a.Hkv, G, a.L_max,
-                                                             a.p.block_size, bps, nsc, ns, scale_log2, part, a.err);
-        if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
+        e = launch_kernel(decode_split_kernel<128>, dim3(ns, rows), dim3(128), 0, a.stream, true, qp, kp, vp, dkp, dvp,
+                          a.tree_mask, a.kv_len, idx, counts, idx_stride, a.n_draft, a.Hq, a.Hkv, G, a.L_max,
+                          a.p.block_size, bps, nsc, ns, scale_log2, part, a.err);
+        if (e != cudaSuccess) return e;
         prof_mark(a.stream, "attend");
-        decode_combine_kernel<128><<<rows, 128, 0, a.stream>>>(part, counts, bps, nsc, ns, a.n_draft, a.Hq, a.Hkv, G,
-                                                               static_cast<__nv_bfloat16*>(a.o), a.lse);
+        e = launch_kernel(decode_combine_kernel<128>, dim3(rows, (G + 3) / 4), dim3(128), 0, a.stream, true, part,
+                          counts, bps, nsc, ns, a.n_draft, a.Hq, a.Hkv, G, op, a.lse);
     } else {
-        decode_split_kernel<64><<<grid, 128, 0, a.stream>>>(qp, kp, vp, dkp, dvp, a.tree_mask, a.kv_len, idx, counts,
-                                                            idx_stride, a.n_draft, a.Hq, a.Hkv, G, a.L_max,
-                                                            a.p.block_size, bps, nsc, ns, scale_log2, part, a.err);
-        if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
+        e = launch_kernel(decode_split_kernel<64>, dim3(ns, rows), dim3(128), 0, a.stream, true, qp, kp, vp, dkp, dvp,
+                          a.tree_mask, a.kv_len, idx, counts, idx_stride, a.n_draft, a.Hq, a.Hkv, G, a.L_max,
+                          a.p.block_size, bps, nsc, ns, scale_log2, part, a.err);
+        if (e != cudaSuccess) return e;
         prof_mark(a.stream, "attend");
-        decode_combine_kernel<64><<<rows, 128, 0, a.stream>>>(part, counts, bps, nsc, ns, a.n_draft, a.Hq, a.Hkv, G,
-                                                              static_cast<__nv_bfloat16*>(a.o), a.lse);
+        e = launch_kernel(decode_combine_kernel<64>, dim3(rows, (G + 7) / 8), dim3(128), 0, a.stream, true, part,
+                          counts, bps, nsc, ns, a.n_draft, a.Hq, a.Hkv, G, op, a.lse);
     }
     prof_mark(a.stream, "combine");
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace infllmv2

@@ -151,6 +151,105 @@ score_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
     }
 }
 
+
+// Decode-shaped scoring: one query token (G <= 16 heads, one MMA m-tile) per CTA and a chunk of
+// blocks; each warp issues the loads of all its kernel n-tiles before its first MMA, so the
+// whole chunk (about 33 KB) is in flight at once and the scan runs at memory speed.
+template <int D, int NPW>
+__global__ void __launch_bounds__(128)
+score_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kern,
+                    const int* __restrict__ kv_len, int Tq, int Hq, int Hkv, int G, int L_max, int M_max,
+                    int nblk_max, int tree, Params p, int blocks_per_cta, int kmax,
+                    float* __restrict__ S, int* __restrict__ err) {
+    extern __shared__ float ks[];  // [kmax] max over heads per kernel of the chunk
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, cq = lane & 3;
+    const int t = blockIdx.y;
+    const int bg = blockIdx.z;
+    const int b = bg / Hkv, g = bg % Hkv;
+    const int bs = p.block_size, c = p.kernel_size, s = p.kernel_stride;
+    pdl_trigger();
+    const int L = kv_len[b];
+    const bool bad_len = tree ? (L < 1 || L > L_max) : (L < Tq || L > L_max);
+    if (bad_len || kernels_in(L, c, s) > M_max) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && t == 0) raise_error(err, kDevErrIndex);
+        return;
+    }
+    if (L < p.dense_len) return;
+    const int pos = tree ? L - 1 : L - Tq + t;
+    const int bt = pos / bs;
+    const int blk0 = blockIdx.x * blocks_per_cta;
+    if (blk0 > bt) return;
+    const int blk1 = min(blk0 + blocks_per_cta, bt + 1);
+    const int jlo = first_kernel_of_block(blk0, bs, c, s);
+    const int jhi = min(last_kernel_of_block(blk1 - 1, bs, s), kernels_in(pos + 1, c, s) - 1);
+    const int nj = jhi - jlo + 1;
+    const int n_tiles = nj > 0 ? (nj + 7) / 8 : 0;
+
+    // ---- kernel rows: all of this warp's n-tiles, issued up front
+    const __nv_bfloat16* kbase = kern + static_cast<size_t>(bg) * M_max * D + 8 * cq;
+    uint4 w[NPW][D / 32];
+#pragma unroll
+    for (int u = 0; u < NPW; ++u) {
+        const int nt = warp * NPW + u;
+        const int jrow = min(jlo + nt * 8 + gq, jhi);
+        const bool live = nt < n_tiles;
+        const __nv_bfloat16* krow = kbase + static_cast<size_t>(live ? jrow : jlo) * D;
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) w[u][i] = live ? ldg_v4_stream(krow + 32 * i) : make_uint4(0, 0, 0, 0);
+    }
+    // ---- Q fragments (rows = heads; rows >= G are zero)
+    uint32_t a[D / 16][4];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int r = gq + 8 * half;
+        const bool ok = r < G;
+        const __nv_bfloat16* qrow = q + ((static_cast<size_t>(b) * Tq + t) * Hq + g * G + (ok ? r : 0)) * D;
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+            const uint4 v = ok ? ldg_v4(qrow + 32 * i + 8 * cq) : make_uint4(0, 0, 0, 0);
+            a[2 * i][half] = v.x;
+            a[2 * i][2 + half] = v.y;
+            a[2 * i + 1][half] = v.z;
+            a[2 * i + 1][2 + half] = v.w;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < NPW; ++u) {
+        const int nt = warp * NPW + u;
+        if (nt >= n_tiles) break;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+            mma_16816(acc, a[2 * i], w[u][i].x, w[u][i].y);
+            mma_16816(acc, a[2 * i + 1], w[u][i].z, w[u][i].w);
+        }
+        const int j0 = jlo + nt * 8 + 2 * cq;
+        // rows past G are padding: keep them out of the head max
+        if (gq >= G) acc[0] = acc[1] = -INFINITY;
+        if (gq + 8 >= G) acc[2] = acc[3] = -INFINITY;
+        float v0 = fmaxf(acc[0], acc[2]), v1 = fmaxf(acc[1], acc[3]);
+#pragma unroll
+        for (int m = 4; m < 32; m <<= 1) {
+            v0 = fmaxf(v0, __shfl_xor_sync(0xffffffffu, v0, m));
+            v1 = fmaxf(v1, __shfl_xor_sync(0xffffffffu, v1, m));
+        }
+        if (gq == 0) {
+            // every kernel up to jhi ends at or before pos, so all are visible
+            if (j0 <= jhi) ks[j0 - jlo] = v0;
+            if (j0 + 1 <= jhi) ks[j0 + 1 - jlo] = v1;
+        }
+    }
+    __syncthreads();
+    for (int blk = blk0 + threadIdx.x; blk < blk1; blk += 128) {
+        const int ja = max(first_kernel_of_block(blk, bs, c, s), jlo);
+        const int jz = min(last_kernel_of_block(blk, bs, s), jhi);
+        float m = -INFINITY;
+        for (int jj = ja; jj <= jz; ++jj) m = fmaxf(m, ks[jj - jlo]);
+        S[(static_cast<size_t>(bg) * Tq + t) * nblk_max + blk] = m;
+    }
+}
+
 __device__ __forceinline__ bool is_forced(int blk, int bt, const Params& p) {
     return blk < p.n_init || blk > bt - p.n_local;
 }
@@ -159,19 +258,28 @@ __device__ __forceinline__ uint64_t cand_key(float s, int blk) {
     return (static_cast<uint64_t>(ordered_key(s)) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(blk));
 }
 
-template <int NT>
+// Top-k selection, one CTA per (b, g, t) row.  Each thread keeps up to PER candidate keys in
+// registers (blocks tid, tid+NT, ...); rows longer than NT*PER re-read the scores each pass.
+// The radix select starts at the first bit where the candidates' keys differ (found with an
+// AND/OR reduction), uses 8-bit digits, and counts digits with warp-aggregated shared atomics
+// (lanes holding the same digit add once), so scores crowded into a few exponents cost no
+// atomic contention.
+template <int NT, int PER>
 __global__ void __launch_bounds__(NT)
 topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq, int Hkv,
             int nblk_max, int L_max, int tree, Params p, int* __restrict__ idx,
             int* __restrict__ counts, int S_max, int* __restrict__ err) {
     constexpr int NW = NT / 32;
     __shared__ unsigned hist[256];
+    __shared__ unsigned long long s_and[NW], s_or[NW];
     __shared__ int s_digit, s_above, s_cnt;
     __shared__ int s_warp[NW];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int row = blockIdx.x;
     const int t = row % Tq;
     const int b = row / (Tq * Hkv);
+    pdl_wait();
+    pdl_trigger();
     const int L = kv_len[b];
     int* out = idx + static_cast<size_t>(row) * S_max;
     const bool bad_len = tree ? (L < 1 || L > L_max) : (L < Tq || L > L_max);
@@ -192,21 +300,75 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq,
     const int n_forced = a_init + (n - max(lo_local, a_init));
     const int nc = n - n_forced;
     const bool take_all = L < p.dense_len || nc <= p.topk;
+    const bool take_none = !take_all && p.topk == 0;  // only the forced blocks
+    const bool in_regs = n <= NT * PER;
+
+    uint64_t key[PER];
+    bool live[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int blk = tid + u * NT;
+        live[u] = !take_all && !take_none && in_regs && blk < n && !is_forced(blk, bt, p);
+        key[u] = live[u] ? cand_key(__ldcg(srow + blk), blk) : 0ull;
+    }
+    auto get_key = [&](int blk, bool& ok) -> uint64_t {
+        ok = blk < n && !is_forced(blk, bt, p);
+        return ok ? cand_key(__ldcg(srow + blk), blk) : 0ull;
+    };
 
     uint64_t prefix = 0, mask = 0;
-    if (!take_all) {
+    if (!take_all && !take_none) {
+        // common leading bits of all candidate keys
+        uint64_t k_and = ~0ull, k_or = 0ull;
+        if (in_regs) {
+#pragma unroll
+            for (int u = 0; u < PER; ++u)
+                if (live[u]) { k_and &= key[u]; k_or |= key[u]; }
+        } else {
+            for (int blk = tid; blk < n; blk += NT) {
+                bool ok;
+                const uint64_t kk = get_key(blk, ok);
+                if (ok) { k_and &= kk; k_or |= kk; }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            k_and &= __shfl_xor_sync(0xffffffffu, k_and, off);
+            k_or |= __shfl_xor_sync(0xffffffffu, k_or, off);
+        }
+        if (lane == 0) { s_and[warp] = k_and; s_or[warp] = k_or; }
+        __syncthreads();
+        k_and = ~0ull;
+        k_or = 0ull;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) { k_and &= s_and[w]; k_or |= s_or[w]; }
+        const uint64_t diff = k_and ^ k_or;  // non-zero: keys are unique and nc > topk >= 1
+        const int top = 63 - __clzll(diff);  // highest bit where candidates differ
+        mask = top >= 63 ? 0ull : (~0ull << (top + 1));
+        prefix = k_and & mask;
         int rem = p.topk;
-        for (int shift = 56; shift >= 0; shift -= 8) {
+        for (int shift = max(top - 7, 0);; shift = max(shift - 8, 0)) {
+            const int width = min(8, top + 1 - shift);  // first pass may be narrower than 8 bits
             for (int i = tid; i < 256; i += NT) hist[i] = 0;
             __syncthreads();
-            for (int blk = tid; blk < n; blk += NT) {
-                if (is_forced(blk, bt, p)) continue;
-                const uint64_t key = cand_key(srow[blk], blk);
-                if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+            auto count = [&](uint64_t kk, bool ok) {
+                const unsigned dig = static_cast<unsigned>((kk >> shift) & 255u);
+                const bool hit = ok && (kk & mask) == prefix;
+                const unsigned peers = __match_any_sync(0xffffffffu, hit ? dig : 256u + lane);
+                if (hit && lane == __ffs(peers) - 1) atomicAdd(&hist[dig], static_cast<unsigned>(__popc(peers)));
+            };
+            if (in_regs) {
+#pragma unroll
+                for (int u = 0; u < PER; ++u) count(key[u], live[u]);
+            } else {
+                for (int base = 0; base < n; base += NT) {
+                    bool ok;
+                    const uint64_t kk = get_key(base + tid, ok);
+                    count(kk, ok);
+                }
             }
             __syncthreads();
             if (warp == 0) {
-                // lane l holds bins 255-8l .. 248-8l, highest first
                 unsigned cnt[8], tot = 0;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -234,11 +396,12 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq,
                 }
             }
             __syncthreads();
-            const int digit = s_digit;
+            const uint64_t dmask = ((1ull << width) - 1ull) << shift;
             rem -= s_above;
-            prefix |= static_cast<uint64_t>(digit) << shift;
-            mask |= 0xFFull << shift;
-            if (s_cnt == rem) break;  // every key of this digit is needed: threshold found
+            prefix |= static_cast<uint64_t>(s_digit) << shift;
+            mask |= dmask;
+            if (s_cnt == rem || shift == 0) break;  // every key of this digit is needed
+            __syncthreads();
         }
     }
 
@@ -248,10 +411,11 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq,
         const int blk = base + tid;
         bool sel = false;
         if (blk < n) {
-            sel = take_all || is_forced(blk, bt, p) || ((cand_key(srow[blk], blk) & mask) >= prefix);
+            if (take_all || is_forced(blk, bt, p)) sel = true;
+            else if (!take_none) sel = (cand_key(__ldcg(srow + blk), blk) & mask) >= prefix;
         }
         const unsigned ballot = __ballot_sync(0xffffffffu, sel);
-        __syncthreads();  // s_warp of the previous round fully consumed
+        __syncthreads();
         if (lane == 0) s_warp[warp] = __popc(ballot);
         __syncthreads();
         int before = total, round_total = 0;
@@ -290,6 +454,8 @@ size_t select_workspace_bytes(int B, int Tq, int Hkv, int L_max, const Params& p
     return static_cast<size_t>(B) * Hkv * Tq * nblk * sizeof(float);
 }
 
+static int score_kmax(int bpc, const Params& p) { return (bpc * p.block_size + p.kernel_size) / p.kernel_stride + 2; }
+
 template <int D, int WARPS, int MT>
 static cudaError_t launch_score_t(const SelectArgs& a, float* S) {
     const int G = a.Hq / a.Hkv;
@@ -297,7 +463,7 @@ static cudaError_t launch_score_t(const SelectArgs& a, float* S) {
     const Params& p = a.p;
     const int nblk_max = (a.L_max + p.block_size - 1) / p.block_size;
     const int bpc = a.blocks_per_cta;
-    const int kmax = (bpc * p.block_size + p.kernel_size) / p.kernel_stride + 2;
+    const int kmax = score_kmax(bpc, p);
     const size_t smem = static_cast<size_t>(tpc) * kmax * sizeof(float);
     dim3 grid((nblk_max + bpc - 1) / bpc, (a.Tq + tpc - 1) / tpc, a.B * a.Hkv);
     auto kfn = score_kernel<D, WARPS, MT>;
@@ -311,27 +477,55 @@ static cudaError_t launch_score_t(const SelectArgs& a, float* S) {
     return cudaGetLastError();
 }
 
+// Kernel n-tiles per warp of score_decode_kernel for a chunk of bpc blocks.
+constexpr int kDecodeNPW = 5;
+
+template <int D>
+static cudaError_t launch_score_decode_t(const SelectArgs& a, float* S, int bpc) {
+    const int G = a.Hq / a.Hkv;
+    const Params& p = a.p;
+    const int nblk_max = (a.L_max + p.block_size - 1) / p.block_size;
+    const int kmax = score_kmax(bpc, p);
+    dim3 grid((nblk_max + bpc - 1) / bpc, a.Tq, a.B * a.Hkv);
+    return launch_kernel(score_decode_kernel<D, kDecodeNPW>, grid, dim3(128), static_cast<size_t>(kmax) * sizeof(float),
+                         a.stream, false, static_cast<const __nv_bfloat16*>(a.q),
+                         static_cast<const __nv_bfloat16*>(a.kernel_cache), a.kv_len, a.Tq, a.Hq, a.Hkv, G, a.L_max,
+                         a.M_max, nblk_max, a.tree, p, bpc, kmax, S, a.err);
+}
+
 cudaError_t launch_block_select(const SelectArgs& a, float* S) {
     const Params& p = a.p;
     const int G = a.Hq / a.Hkv;
     const int nblk_max = (a.L_max + p.block_size - 1) / p.block_size;
     cudaError_t e;
-    // few queries: all warps of a CTA split one token-tile's kernels; many queries: each warp
-    // owns one m-tile and the CTA's warps share the kernels through L1.
     const bool many = static_cast<long long>(a.Tq) * G >= 64;
-    if (a.d == 128) e = many ? launch_score_t<128, 4, 4>(a, S) : launch_score_t<128, 4, 1>(a, S);
-    else e = many ? launch_score_t<64, 4, 4>(a, S) : launch_score_t<64, 4, 1>(a, S);
+    bool decode_shaped = false;
+    if (!many) {
+        // one token per CTA; the chunk must fit 4 warps x kDecodeNPW n-tiles of 8 kernels
+        int bpc = a.blocks_per_cta;
+        while (bpc > 1 && score_kmax(bpc, p) > 4 * kDecodeNPW * 8) bpc /= 2;
+        if (score_kmax(bpc, p) <= 4 * kDecodeNPW * 8) {
+            decode_shaped = true;
+            e = a.d == 128 ? launch_score_decode_t<128>(a, S, bpc) : launch_score_decode_t<64>(a, S, bpc);
+        }
+    }
+    if (!decode_shaped) {
+        // many queries: each warp owns one m-tile and the CTA's warps share the kernels through L1
+        if (a.d == 128) e = many ? launch_score_t<128, 4, 4>(a, S) : launch_score_t<128, 4, 1>(a, S);
+        else e = many ? launch_score_t<64, 4, 4>(a, S) : launch_score_t<64, 4, 1>(a, S);
+    }
     if (e != cudaSuccess) return e;
     prof_mark(a.stream, "score");
     const int rows = a.B * a.Hkv * a.Tq;
-    if (nblk_max <= 512)
-        topk_kernel<128><<<rows, 128, 0, a.stream>>>(S, a.kv_len, a.Tq, a.Hkv, nblk_max, a.L_max, a.tree, p,
-                                                     a.idx, a.counts, a.S_max, a.err);
+    const bool pdl = decode_shaped;
+    if (nblk_max <= 256)
+        e = launch_kernel(topk_kernel<128, 2>, dim3(rows), dim3(128), 0, a.stream, pdl, S, a.kv_len, a.Tq, a.Hkv,
+                          nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
     else
-        topk_kernel<512><<<rows, 512, 0, a.stream>>>(S, a.kv_len, a.Tq, a.Hkv, nblk_max, a.L_max, a.tree, p,
-                                                     a.idx, a.counts, a.S_max, a.err);
+        e = launch_kernel(topk_kernel<256, 8>, dim3(rows), dim3(256), 0, a.stream, pdl, S, a.kv_len, a.Tq, a.Hkv,
+                          nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
     prof_mark(a.stream, "topk");
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace infllmv2
