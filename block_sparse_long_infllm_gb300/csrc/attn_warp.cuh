@@ -4,7 +4,7 @@
 //
 // Rows are the G heads of one query token (padded to 16).  QK^T and PV run as m16n8k16 warp
 // MMAs with fp32 accumulators; the softmax runs in fp32 in the log2 domain.  Operands come
-// straight from global memory with 128-bit loads, no shared memory:
+// from global memory with 128-bit loads, or from TMA-filled 128-byte-swizzled shared tiles:
 //   * QK^T: the head dimension is permuted the same way for Q and K (the sum over d does
 //     not depend on the order of its terms) so each lane's 16 bytes of a K row feed two
 //     k-steps of its B fragment;
@@ -14,6 +14,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace infllmv2 {
 
@@ -60,55 +61,12 @@ __device__ __forceinline__ void acc_init(WarpAcc<D>& A) {
     A.l[0] = A.l[1] = 0.f;
 }
 
-// Feed 32 keys whose rows are k_rows[kk*D], v_rows[kk*D] (kk = 0..31); bit kk of `valid` says
-// key kk takes part.  Rows of keys that do not take part are never read.
+// Online-softmax update with the scores s (this lane's values of 4 n-tiles x 16 rows x 8 keys,
+// unscaled, keys masked by `valid`) and the V fragments vw of the same 32 keys, then O += P V.
 template <int D>
-__device__ __forceinline__ void attend32(WarpAcc<D>& A, const QFrag<D>& Q, const __nv_bfloat16* k_rows,
-                                         const __nv_bfloat16* v_rows, uint32_t valid, float scale_log2) {
-    const int lane = threadIdx.x & 31;
-    const int g = lane >> 2, c = lane & 3;
-
-    // ---- V rows for the two k-steps (keys 16kk + 2c + {0,1}, 16kk + 8 + 2c + {0,1}); issued first
-    constexpr int VW = D / 16;  // 32-bit words per lane per V row
-    uint32_t vw[2][4][VW];
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int key = 16 * kk + 2 * c + (r & 1) + 8 * (r >> 1);
-            const bool ok = (valid >> key) & 1u;
-            const uint4* src = reinterpret_cast<const uint4*>(v_rows + static_cast<size_t>(key) * D + (D / 8) * g);
-#pragma unroll
-            for (int u = 0; u < VW / 4; ++u) {
-                const uint4 w = ok ? ldg_v4_stream(src + u) : make_uint4(0, 0, 0, 0);
-                vw[kk][r][4 * u + 0] = w.x;
-                vw[kk][r][4 * u + 1] = w.y;
-                vw[kk][r][4 * u + 2] = w.z;
-                vw[kk][r][4 * u + 3] = w.w;
-            }
-        }
-    }
-
-    // ---- S = Q K^T for 4 n-tiles of 8 keys
-    float s[4][4];
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-        const int key = nt * 8 + g;
-        const bool ok = (valid >> key) & 1u;
-        const __nv_bfloat16* src = k_rows + static_cast<size_t>(key) * D + 8 * c;
-        uint4 w[D / 32];
-#pragma unroll
-        for (int i = 0; i < D / 32; ++i) w[i] = ok ? ldg_v4_stream(src + 32 * i) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
-#pragma unroll
-        for (int i = 0; i < D / 32; ++i) {
-            mma_16816(s[nt], Q.a[2 * i], w[i].x, w[i].y);
-            mma_16816(s[nt], Q.a[2 * i + 1], w[i].z, w[i].w);
-        }
-    }
-
-    // ---- online softmax (log2 domain)
+__device__ __forceinline__ void softmax_pv(WarpAcc<D>& A, float (&s)[4][4], const uint32_t (&vw)[2][4][D / 16],
+                                           uint32_t valid, float scale_log2) {
+    const int c = threadIdx.x & 3;
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
@@ -150,8 +108,6 @@ __device__ __forceinline__ void attend32(WarpAcc<D>& A, const QFrag<D>& Q, const
         pa[kk][2 * hi + 0] = pack_bf16x2(pv[0], pv[1]);
         pa[kk][2 * hi + 1] = pack_bf16x2(pv[2], pv[3]);
     }
-
-    // ---- O += P V
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
 #pragma unroll
@@ -161,6 +117,108 @@ __device__ __forceinline__ void attend32(WarpAcc<D>& A, const QFrag<D>& Q, const
             mma_16816(A.o[nt], pa[kk], b0, b1);
         }
     }
+}
+
+// S = Q K^T for 4 n-tiles of 8 keys from per-lane 16-byte K slices kw[nt][i] (head-dim
+// elements 32i + 8c .. +7 of key nt*8 + g).
+template <int D>
+__device__ __forceinline__ void qk_tiles(float (&s)[4][4], const QFrag<D>& Q, const uint4 (&kw)[4][D / 32]) {
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+            mma_16816(s[nt], Q.a[2 * i], kw[nt][i].x, kw[nt][i].y);
+            mma_16816(s[nt], Q.a[2 * i + 1], kw[nt][i].z, kw[nt][i].w);
+        }
+    }
+}
+
+// Feed 32 keys whose rows are k_rows[kk*D], v_rows[kk*D] (kk = 0..31) in global memory; bit kk
+// of `valid` says key kk takes part.  Rows of keys that do not take part are never read.
+template <int D>
+__device__ __forceinline__ void attend32(WarpAcc<D>& A, const QFrag<D>& Q, const __nv_bfloat16* k_rows,
+                                         const __nv_bfloat16* v_rows, uint32_t valid, float scale_log2) {
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    constexpr int VW = D / 16;  // 32-bit words per lane per V row
+    uint32_t vw[2][4][VW];
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int key = 16 * kk + 2 * c + (r & 1) + 8 * (r >> 1);
+            const bool ok = (valid >> key) & 1u;
+            const uint4* src = reinterpret_cast<const uint4*>(v_rows + static_cast<size_t>(key) * D + (D / 8) * g);
+#pragma unroll
+            for (int u = 0; u < VW / 4; ++u) {
+                const uint4 w = ok ? ldg_v4_stream(src + u) : make_uint4(0, 0, 0, 0);
+                vw[kk][r][4 * u + 0] = w.x;
+                vw[kk][r][4 * u + 1] = w.y;
+                vw[kk][r][4 * u + 2] = w.z;
+                vw[kk][r][4 * u + 3] = w.w;
+            }
+        }
+    }
+    uint4 kw[4][D / 32];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+        const int key = nt * 8 + g;
+        const bool ok = (valid >> key) & 1u;
+        const __nv_bfloat16* src = k_rows + static_cast<size_t>(key) * D + 8 * c;
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) kw[nt][i] = ok ? ldg_v4_stream(src + 32 * i) : make_uint4(0, 0, 0, 0);
+    }
+    float s[4][4];
+    qk_tiles<D>(s, Q, kw);
+    softmax_pv<D>(A, s, vw, valid, scale_log2);
+}
+
+// Same for 32 keys starting at row `row0` of K and V tiles in shared memory, each stored as
+// D/64 boxes of `rows` x 128 bytes with the 128-byte swizzle (tma.cuh), 1024-byte aligned.
+// V rows of keys that do not take part read as zero (the cache past kv_len is arbitrary).
+template <int D>
+__device__ __forceinline__ void attend32_smem(WarpAcc<D>& A, const QFrag<D>& Q, uint32_t k_tile, uint32_t v_tile,
+                                              int rows, int row0, uint32_t valid, float scale_log2) {
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const uint32_t box = static_cast<uint32_t>(rows) * 128u;
+    constexpr int VW = D / 16;
+    uint32_t vw[2][4][VW];
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int key = 16 * kk + 2 * c + (r & 1) + 8 * (r >> 1);
+            const bool ok = (valid >> key) & 1u;
+            const int row = row0 + key;
+#pragma unroll
+            for (int u = 0; u < VW / 4; ++u) {
+                // elements (D/8)g + 8u .. +7 of the row: box col/64, chunk (col % 64)/8
+                const int col = (D / 8) * g + 8 * u;
+                const uint32_t addr = v_tile + (col / 64) * box + swz128(row, (col % 64) / 8);
+                const uint4 w = ok ? lds_v4(addr) : make_uint4(0, 0, 0, 0);
+                vw[kk][r][4 * u + 0] = w.x;
+                vw[kk][r][4 * u + 1] = w.y;
+                vw[kk][r][4 * u + 2] = w.z;
+                vw[kk][r][4 * u + 3] = w.w;
+            }
+        }
+    }
+    uint4 kw[4][D / 32];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+        const int row = row0 + nt * 8 + g;
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+            const int col = 32 * i + 8 * c;
+            kw[nt][i] = lds_v4(k_tile + (col / 64) * box + swz128(row, (col % 64) / 8));
+        }
+    }
+    float s[4][4];
+    qk_tiles<D>(s, Q, kw);
+    softmax_pv<D>(A, s, vw, valid, scale_log2);
 }
 
 // Sum the lanes' shares of the row sums (after the last tile).

@@ -1,6 +1,7 @@
 // internal.h -- launch interfaces between the C-ABI layer (api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -55,6 +56,11 @@ struct DecodeArgs {
     int* err;
     cudaStream_t stream;
 };
+
+// 2-D bf16 tensor map over `rows` rows of `inner` elements (row stride inner*2 bytes) with
+// box [box_rows][box_inner] and the 128-byte swizzle; false if the driver refuses.
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                       uint32_t box_rows);
 
 // Stage timing (infllmv2_profile_*): no-ops unless profiling is enabled.
 void prof_begin(cudaStream_t stream);

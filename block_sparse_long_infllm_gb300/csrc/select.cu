@@ -12,12 +12,15 @@
 //   head dimension is permuted identically for Q and the kernels (a dot product does not
 //   depend on the order of its terms), which lets every lane fetch its operands with one
 //   128-bit load per 32 elements straight from global memory, fully coalesced.
-// topk_kernel: one CTA per (b, g, t).  Candidate keys are (ordered score << 32 | ~block id),
-//   unique, so "score descending, lower id first on ties" is plain key order.  A radix
-//   select over 8-bit digits finds the k-th largest key (usually in 2-3 passes), then the
-//   chosen and forced blocks are compacted in ascending id order with warp ballots.
+// score_decode_kernel: the same scores for few queries (decode, trees): one token per CTA,
+//   the chunk's semantic kernels arrive in shared memory by one TMA tensor copy.
+// topk_kernel: one CTA per (b, g, t).  A radix select over the order-preserving 32-bit image
+//   of the fp32 scores finds the k-th largest score; blocks tied with it are taken in
+//   ascending id order, so "score descending, lower id first" holds exactly.  The chosen and
+//   forced blocks are compacted in ascending id order with warp ballots.
 #include "common.cuh"
 #include "internal.h"
+#include "tma.cuh"
 
 namespace infllmv2 {
 
@@ -152,16 +155,26 @@ score_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
 }
 
 
+
+// Rows of the kernel-cache box a decode scoring CTA loads (>= kernels of one chunk).
+constexpr int kScoreBoxRows = 136;
+
 // Decode-shaped scoring: one query token (G <= 16 heads, one MMA m-tile) per CTA and a chunk of
-// blocks; each warp issues the loads of all its kernel n-tiles before its first MMA, so the
-// whole chunk (about 33 KB) is in flight at once and the scan runs at memory speed.
-template <int D, int NPW>
+// blocks.  Thread 0 issues one TMA tensor copy per 64 head-dim columns of the chunk's kernel
+// rows (<= 136 x 256 B) into 128-byte-swizzled shared memory, so every CTA's whole chunk is in
+// flight at once; warps then read their B fragments from shared memory without bank conflicts.
+template <int D>
 __global__ void __launch_bounds__(128)
-score_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kern,
+score_decode_kernel(const __grid_constant__ CUtensorMap tm_kern, const __nv_bfloat16* __restrict__ q,
                     const int* __restrict__ kv_len, int Tq, int Hq, int Hkv, int G, int L_max, int M_max,
-                    int nblk_max, int tree, Params p, int blocks_per_cta, int kmax,
-                    float* __restrict__ S, int* __restrict__ err) {
-    extern __shared__ float ks[];  // [kmax] max over heads per kernel of the chunk
+                    int nblk_max, int tree, Params p, int blocks_per_cta, float* __restrict__ S,
+                    int* __restrict__ err) {
+    constexpr int kBox = kScoreBoxRows * 128;  // bytes of one 64-column box
+    extern __shared__ unsigned char smem_dyn[];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    float* ks = reinterpret_cast<float*>(base + (D / 64) * kBox);  // [kScoreBoxRows] head max per kernel
+    uint64_t* bar = reinterpret_cast<uint64_t*>(ks + kScoreBoxRows);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, cq = lane & 3;
     const int t = blockIdx.y;
@@ -185,18 +198,15 @@ score_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
     const int jhi = min(last_kernel_of_block(blk1 - 1, bs, s), kernels_in(pos + 1, c, s) - 1);
     const int nj = jhi - jlo + 1;
     const int n_tiles = nj > 0 ? (nj + 7) / 8 : 0;
-
-    // ---- kernel rows: all of this warp's n-tiles, issued up front
-    const __nv_bfloat16* kbase = kern + static_cast<size_t>(bg) * M_max * D + 8 * cq;
-    uint4 w[NPW][D / 32];
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        if (n_tiles > 0) {
+            mbar_arrive_expect_tx(bar, (D / 64) * kBox);
 #pragma unroll
-    for (int u = 0; u < NPW; ++u) {
-        const int nt = warp * NPW + u;
-        const int jrow = min(jlo + nt * 8 + gq, jhi);
-        const bool live = nt < n_tiles;
-        const __nv_bfloat16* krow = kbase + static_cast<size_t>(live ? jrow : jlo) * D;
-#pragma unroll
-        for (int i = 0; i < D / 32; ++i) w[u][i] = live ? ldg_v4_stream(krow + 32 * i) : make_uint4(0, 0, 0, 0);
+            for (int sub = 0; sub < D / 64; ++sub)
+                tma_load_2d(base + sub * kBox, &tm_kern, 64 * sub, bg * M_max + jlo, bar);
+        }
     }
     // ---- Q fragments (rows = heads; rows >= G are zero)
     uint32_t a[D / 16][4];
@@ -214,15 +224,19 @@ score_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
             a[2 * i + 1][2 + half] = v.w;
         }
     }
-#pragma unroll
-    for (int u = 0; u < NPW; ++u) {
-        const int nt = warp * NPW + u;
-        if (nt >= n_tiles) break;
+    __syncthreads();  // barrier initialised before anyone waits on it
+    bool ok = n_tiles == 0 || mbar_wait(bar, 0);
+    if (!ok && lane == 0) raise_error(err, kDevErrTimeout);
+    const uint32_t kb = smem_u32(base);
+    for (int nt = warp; ok && nt < n_tiles; nt += 4) {
+        const int row = nt * 8 + gq;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) {
-            mma_16816(acc, a[2 * i], w[u][i].x, w[u][i].y);
-            mma_16816(acc, a[2 * i + 1], w[u][i].z, w[u][i].w);
+            const int col = 32 * i + 8 * cq;
+            const uint4 w = lds_v4(kb + (col / 64) * kBox + swz128(row, (col % 64) / 8));
+            mma_16816(acc, a[2 * i], w.x, w.y);
+            mma_16816(acc, a[2 * i + 1], w.z, w.w);
         }
         const int j0 = jlo + nt * 8 + 2 * cq;
         // rows past G are padding: keep them out of the head max
@@ -241,6 +255,10 @@ score_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
         }
     }
     __syncthreads();
+    if (!ok) {
+        if (threadIdx.x == 0) mbar_wait(bar, 0);  // let a late copy land before the CTA exits
+        return;
+    }
     for (int blk = blk0 + threadIdx.x; blk < blk1; blk += 128) {
         const int ja = max(first_kernel_of_block(blk, bs, c, s), jlo);
         const int jz = min(last_kernel_of_block(blk, bs, s), jhi);
@@ -254,26 +272,22 @@ __device__ __forceinline__ bool is_forced(int blk, int bt, const Params& p) {
     return blk < p.n_init || blk > bt - p.n_local;
 }
 
-__device__ __forceinline__ uint64_t cand_key(float s, int blk) {
-    return (static_cast<uint64_t>(ordered_key(s)) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(blk));
-}
-
-// Top-k selection, one CTA per (b, g, t) row.  Each thread keeps up to PER candidate keys in
-// registers (blocks tid, tid+NT, ...); rows longer than NT*PER re-read the scores each pass.
-// The radix select starts at the first bit where the candidates' keys differ (found with an
-// AND/OR reduction), uses 8-bit digits, and counts digits with warp-aggregated shared atomics
-// (lanes holding the same digit add once), so scores crowded into a few exponents cost no
-// atomic contention.
-template <int NT, int PER>
+// Top-k selection, one CTA per (b, g, t) row.  The row's candidate keys (the order-preserving
+// 32-bit image of each non-forced block's score) are staged in shared memory.  The radix select
+// starts at the first bit where candidate keys differ (an AND/OR reduction), uses 8-bit digits,
+// and counts digits with warp-aggregated shared atomics (lanes with the same digit add once).
+// It ends with the k-th largest key T, the number `above` of keys > T, and `rem` = k - above of
+// the keys equal to T still to take: those go to the lowest block ids.
+template <int NT>
 __global__ void __launch_bounds__(NT)
-topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq, int Hkv,
-            int nblk_max, int L_max, int tree, Params p, int* __restrict__ idx,
-            int* __restrict__ counts, int S_max, int* __restrict__ err) {
+topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq, int Hkv, int nblk_max, int L_max,
+            int tree, Params p, int* __restrict__ idx, int* __restrict__ counts, int S_max, int* __restrict__ err) {
     constexpr int NW = NT / 32;
+    extern __shared__ uint32_t s_key[];  // [n] candidate keys (forced blocks: unused)
     __shared__ unsigned hist[256];
-    __shared__ unsigned long long s_and[NW], s_or[NW];
+    __shared__ uint32_t s_and[NW], s_or[NW];
     __shared__ int s_digit, s_above, s_cnt;
-    __shared__ int s_warp[NW];
+    __shared__ int s_w1[NW], s_w2[NW];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int row = blockIdx.x;
     const int t = row % Tq;
@@ -301,127 +315,133 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq,
     const int nc = n - n_forced;
     const bool take_all = L < p.dense_len || nc <= p.topk;
     const bool take_none = !take_all && p.topk == 0;  // only the forced blocks
-    const bool in_regs = n <= NT * PER;
+    const bool select = !take_all && !take_none;
 
-    uint64_t key[PER];
-    bool live[PER];
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-        const int blk = tid + u * NT;
-        live[u] = !take_all && !take_none && in_regs && blk < n && !is_forced(blk, bt, p);
-        key[u] = live[u] ? cand_key(__ldcg(srow + blk), blk) : 0ull;
-    }
-    auto get_key = [&](int blk, bool& ok) -> uint64_t {
-        ok = blk < n && !is_forced(blk, bt, p);
-        return ok ? cand_key(__ldcg(srow + blk), blk) : 0ull;
-    };
-
-    uint64_t prefix = 0, mask = 0;
-    if (!take_all && !take_none) {
-        // common leading bits of all candidate keys
-        uint64_t k_and = ~0ull, k_or = 0ull;
-        if (in_regs) {
-#pragma unroll
-            for (int u = 0; u < PER; ++u)
-                if (live[u]) { k_and &= key[u]; k_or |= key[u]; }
-        } else {
-            for (int blk = tid; blk < n; blk += NT) {
-                bool ok;
-                const uint64_t kk = get_key(blk, ok);
-                if (ok) { k_and &= kk; k_or |= kk; }
-            }
+    uint32_t T = 0, mask = 0;
+    int rem = 0;
+    if (select) {
+        uint32_t k_and = ~0u, k_or = 0u;
+        for (int blk = tid; blk < n; blk += NT) {
+            if (is_forced(blk, bt, p)) continue;
+            const uint32_t kk = ordered_key(__ldcg(srow + blk));
+            s_key[blk] = kk;
+            k_and &= kk;
+            k_or |= kk;
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             k_and &= __shfl_xor_sync(0xffffffffu, k_and, off);
             k_or |= __shfl_xor_sync(0xffffffffu, k_or, off);
         }
-        if (lane == 0) { s_and[warp] = k_and; s_or[warp] = k_or; }
+        if (lane == 0) {
+            s_and[warp] = k_and;
+            s_or[warp] = k_or;
+        }
         __syncthreads();
-        k_and = ~0ull;
-        k_or = 0ull;
+        k_and = ~0u;
+        k_or = 0u;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) { k_and &= s_and[w]; k_or |= s_or[w]; }
-        const uint64_t diff = k_and ^ k_or;  // non-zero: keys are unique and nc > topk >= 1
-        const int top = 63 - __clzll(diff);  // highest bit where candidates differ
-        mask = top >= 63 ? 0ull : (~0ull << (top + 1));
-        prefix = k_and & mask;
-        int rem = p.topk;
-        for (int shift = max(top - 7, 0);; shift = max(shift - 8, 0)) {
-            const int width = min(8, top + 1 - shift);  // first pass may be narrower than 8 bits
-            for (int i = tid; i < 256; i += NT) hist[i] = 0;
-            __syncthreads();
-            auto count = [&](uint64_t kk, bool ok) {
-                const unsigned dig = static_cast<unsigned>((kk >> shift) & 255u);
-                const bool hit = ok && (kk & mask) == prefix;
-                const unsigned peers = __match_any_sync(0xffffffffu, hit ? dig : 256u + lane);
-                if (hit && lane == __ffs(peers) - 1) atomicAdd(&hist[dig], static_cast<unsigned>(__popc(peers)));
-            };
-            if (in_regs) {
-#pragma unroll
-                for (int u = 0; u < PER; ++u) count(key[u], live[u]);
-            } else {
+        for (int w = 0; w < NW; ++w) {
+            k_and &= s_and[w];
+            k_or |= s_or[w];
+        }
+        const uint32_t diff = k_and ^ k_or;
+        rem = p.topk;
+        if (diff == 0) {  // every candidate has the same score
+            T = k_and;
+            mask = ~0u;
+        } else {
+            const int top = 31 - __clz(diff);  // highest bit where candidates differ
+            mask = top >= 31 ? 0u : (~0u << (top + 1));
+            T = k_and & mask;
+            for (int shift = max(top - 7, 0);; shift = max(shift - 8, 0)) {
+                const int width = min(8, top + 1 - shift);
+                for (int i = tid; i < 256; i += NT) hist[i] = 0;
+                __syncthreads();
                 for (int base = 0; base < n; base += NT) {
-                    bool ok;
-                    const uint64_t kk = get_key(base + tid, ok);
-                    count(kk, ok);
+                    const int blk = base + tid;
+                    const bool cand = blk < n && !is_forced(blk, bt, p);
+                    const uint32_t kk = cand ? s_key[blk] : 0u;
+                    const bool hit = cand && (kk & mask) == T;
+                    const unsigned dig = (kk >> shift) & 255u;
+                    const unsigned peers = __match_any_sync(0xffffffffu, hit ? dig : 256u + lane);
+                    if (hit && lane == __ffs(peers) - 1) atomicAdd(&hist[dig], static_cast<unsigned>(__popc(peers)));
                 }
-            }
-            __syncthreads();
-            if (warp == 0) {
-                unsigned cnt[8], tot = 0;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    cnt[e] = hist[255 - (lane * 8 + e)];
-                    tot += cnt[e];
-                }
-                unsigned incl = tot;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const unsigned v = __shfl_up_sync(0xffffffffu, incl, off);
-                    if (lane >= off) incl += v;
-                }
-                unsigned above = incl - tot;
-                if (above < static_cast<unsigned>(rem) && static_cast<unsigned>(rem) <= incl) {
+                __syncthreads();
+                if (warp == 0) {
+                    // lane l holds bins 255-8l .. 248-8l, highest first
+                    unsigned cnt[8], tot = 0;
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        if (above + cnt[e] >= static_cast<unsigned>(rem)) {
-                            s_digit = 255 - (lane * 8 + e);
-                            s_above = static_cast<int>(above);
-                            s_cnt = static_cast<int>(cnt[e]);
-                            break;
+                        cnt[e] = hist[255 - (lane * 8 + e)];
+                        tot += cnt[e];
+                    }
+                    unsigned incl = tot;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const unsigned v = __shfl_up_sync(0xffffffffu, incl, off);
+                        if (lane >= off) incl += v;
+                    }
+                    unsigned above = incl - tot;
+                    if (above < static_cast<unsigned>(rem) && static_cast<unsigned>(rem) <= incl) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            if (above + cnt[e] >= static_cast<unsigned>(rem)) {
+                                s_digit = 255 - (lane * 8 + e);
+                                s_above = static_cast<int>(above);
+                                s_cnt = static_cast<int>(cnt[e]);
+                                break;
+                            }
+                            above += cnt[e];
                         }
-                        above += cnt[e];
                     }
                 }
+                __syncthreads();
+                rem -= s_above;
+                T |= static_cast<uint32_t>(s_digit) << shift;
+                mask |= ((1u << width) - 1u) << shift;
+                const bool done = s_cnt == rem || shift == 0;
+                __syncthreads();
+                if (done) break;
             }
-            __syncthreads();
-            const uint64_t dmask = ((1ull << width) - 1ull) << shift;
-            rem -= s_above;
-            prefix |= static_cast<uint64_t>(s_digit) << shift;
-            mask |= dmask;
-            if (s_cnt == rem || shift == 0) break;  // every key of this digit is needed
-            __syncthreads();
+            if (mask != ~0u) rem = 1 << 30;  // the whole digit group is taken: no tie to break
         }
     }
 
-    // ---- compaction in ascending block order
-    int total = 0;
+    // ---- compaction in ascending block order; keys equal to T (under mask) are taken while
+    // fewer than `rem` of them have been taken
+    int total = 0, tied = 0;
     for (int base = 0; base < n; base += NT) {
         const int blk = base + tid;
-        bool sel = false;
+        bool sel = false, tie = false;
         if (blk < n) {
-            if (take_all || is_forced(blk, bt, p)) sel = true;
-            else if (!take_none) sel = (cand_key(__ldcg(srow + blk), blk) & mask) >= prefix;
+            if (take_all || is_forced(blk, bt, p)) {
+                sel = true;
+            } else if (select) {
+                const uint32_t km = s_key[blk] & mask;
+                sel = km > T;
+                tie = km == T;
+            }
         }
-        const unsigned ballot = __ballot_sync(0xffffffffu, sel);
+        const unsigned tie_ballot = __ballot_sync(0xffffffffu, tie);
         __syncthreads();
-        if (lane == 0) s_warp[warp] = __popc(ballot);
+        if (lane == 0) s_w2[warp] = __popc(tie_ballot);
+        __syncthreads();
+        int tie_before = tied, tie_round = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            if (w < warp) tie_before += s_w2[w];
+            tie_round += s_w2[w];
+        }
+        if (tie && tie_before + __popc(tie_ballot & ((1u << lane) - 1u)) < rem) sel = true;
+        tied += tie_round;
+        const unsigned ballot = __ballot_sync(0xffffffffu, sel);
+        if (lane == 0) s_w1[warp] = __popc(ballot);
         __syncthreads();
         int before = total, round_total = 0;
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
-            const int v = s_warp[w];
+            const int v = s_w1[w];
             if (w < warp) before += v;
             round_total += v;
         }
@@ -477,34 +497,35 @@ static cudaError_t launch_score_t(const SelectArgs& a, float* S) {
     return cudaGetLastError();
 }
 
-// Kernel n-tiles per warp of score_decode_kernel for a chunk of bpc blocks.
-constexpr int kDecodeNPW = 5;
-
 template <int D>
 static cudaError_t launch_score_decode_t(const SelectArgs& a, float* S, int bpc) {
     const int G = a.Hq / a.Hkv;
     const Params& p = a.p;
     const int nblk_max = (a.L_max + p.block_size - 1) / p.block_size;
-    const int kmax = score_kmax(bpc, p);
+    CUtensorMap tm;
+    const uint64_t rows = static_cast<uint64_t>(a.B) * a.Hkv * a.M_max;
+    if (!make_tmap_bf16_2d(&tm, a.kernel_cache, D, rows, 64, kScoreBoxRows)) return cudaErrorInvalidValue;
+    const int smem = (D / 64) * kScoreBoxRows * 128 + kScoreBoxRows * 4 + 8 + 1024;
+    auto kfn = score_decode_kernel<D>;
+    if (cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); e != cudaSuccess)
+        return e;
     dim3 grid((nblk_max + bpc - 1) / bpc, a.Tq, a.B * a.Hkv);
-    return launch_kernel(score_decode_kernel<D, kDecodeNPW>, grid, dim3(128), static_cast<size_t>(kmax) * sizeof(float),
-                         a.stream, false, static_cast<const __nv_bfloat16*>(a.q),
-                         static_cast<const __nv_bfloat16*>(a.kernel_cache), a.kv_len, a.Tq, a.Hq, a.Hkv, G, a.L_max,
-                         a.M_max, nblk_max, a.tree, p, bpc, kmax, S, a.err);
+    return launch_kernel(kfn, grid, dim3(128), smem, a.stream, false, tm, static_cast<const __nv_bfloat16*>(a.q),
+                         a.kv_len, a.Tq, a.Hq, a.Hkv, G, a.L_max, a.M_max, nblk_max, a.tree, p, bpc, S, a.err);
 }
 
 cudaError_t launch_block_select(const SelectArgs& a, float* S) {
     const Params& p = a.p;
     const int G = a.Hq / a.Hkv;
     const int nblk_max = (a.L_max + p.block_size - 1) / p.block_size;
-    cudaError_t e;
+    cudaError_t e = cudaSuccess;
     const bool many = static_cast<long long>(a.Tq) * G >= 64;
     bool decode_shaped = false;
-    if (!many) {
-        // one token per CTA; the chunk must fit 4 warps x kDecodeNPW n-tiles of 8 kernels
+    if (!many && a.M_max > 0) {
+        // one token per CTA; the chunk's kernels must fit the TMA box
         int bpc = a.blocks_per_cta;
-        while (bpc > 1 && score_kmax(bpc, p) > 4 * kDecodeNPW * 8) bpc /= 2;
-        if (score_kmax(bpc, p) <= 4 * kDecodeNPW * 8) {
+        while (bpc > 1 && score_kmax(bpc, p) > kScoreBoxRows) bpc /= 2;
+        if (score_kmax(bpc, p) <= kScoreBoxRows) {
             decode_shaped = true;
             e = a.d == 128 ? launch_score_decode_t<128>(a, S, bpc) : launch_score_decode_t<64>(a, S, bpc);
         }
@@ -517,13 +538,20 @@ cudaError_t launch_block_select(const SelectArgs& a, float* S) {
     if (e != cudaSuccess) return e;
     prof_mark(a.stream, "score");
     const int rows = a.B * a.Hkv * a.Tq;
-    const bool pdl = decode_shaped;
-    if (nblk_max <= 256)
-        e = launch_kernel(topk_kernel<128, 2>, dim3(rows), dim3(128), 0, a.stream, pdl, S, a.kv_len, a.Tq, a.Hkv,
-                          nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
+    const size_t smem = static_cast<size_t>(nblk_max) * sizeof(uint32_t);
+    if (smem > 48 * 1024) {
+        auto kfn = nblk_max <= 512 ? topk_kernel<128> : topk_kernel<256>;
+        if (cudaError_t e2 = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  static_cast<int>(smem));
+            e2 != cudaSuccess)
+            return e2;
+    }
+    if (nblk_max <= 512)
+        e = launch_kernel(topk_kernel<128>, dim3(rows), dim3(128), smem, a.stream, decode_shaped, S, a.kv_len, a.Tq,
+                          a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
     else
-        e = launch_kernel(topk_kernel<256, 8>, dim3(rows), dim3(256), 0, a.stream, pdl, S, a.kv_len, a.Tq, a.Hkv,
-                          nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
+        e = launch_kernel(topk_kernel<256>, dim3(rows), dim3(256), smem, a.stream, decode_shaped, S, a.kv_len, a.Tq,
+                          a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
     prof_mark(a.stream, "topk");
     return e;
 }
