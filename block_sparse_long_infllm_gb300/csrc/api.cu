@@ -17,6 +17,7 @@ namespace {
 constexpr int kVersion = 100;  // 0.1.0
 constexpr int kMaxDevices = 64;
 constexpr int kMaxLen = 1 << 28;
+constexpr int kMaxBlocks = 1024 * 32;  // blocks per sequence the top-k kernel holds in registers
 
 // Device error word: bits of infllmv2::kDevErr*, set by kernels, read and cleared by
 // infllmv2_sync_status.
@@ -84,7 +85,7 @@ DecodeWs decode_ws(int B, int n_draft, int Hkv, int d, int L_max, const Params& 
     DecodeWs w{};
     const int S_cap = infllmv2::selection_capacity(p, L_max);
     int bps, nsc, ns;
-    infllmv2::decode_split_shape(S_cap, p.block_size, true, &bps, &nsc, &ns);
+    infllmv2::decode_split_shape(p, L_max, true, &bps, &nsc, &ns);
     const size_t rows = static_cast<size_t>(B) * Hkv * n_draft;
     w.scores = 0;
     w.idx = align256(w.scores + rows * n_blocks(L_max, p.block_size) * sizeof(float));
@@ -256,6 +257,7 @@ int infllmv2_block_select(const void* q, const void* kernel_cache, const int32_t
     if (B == 0 || Tq == 0) return INFLLMV2_OK;
     if (Tq > L_max) return INFLLMV2_ERR_INVALID_ARG;
     if (S_max < infllmv2::selection_capacity(p, L_max)) return INFLLMV2_ERR_INVALID_ARG;
+    if (n_blocks(L_max, p.block_size) > kMaxBlocks) return INFLLMV2_ERR_UNSUPPORTED;
     if (!q || !kernel_cache || !kv_len || !idx || !counts) return INFLLMV2_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(kernel_cache) || !aligned16(kv_len) || !aligned16(idx) || !aligned16(counts))
         return INFLLMV2_ERR_INVALID_ARG;
@@ -318,6 +320,7 @@ int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache, con
         !aligned16(kv_len) || !aligned16(o))
         return INFLLMV2_ERR_INVALID_ARG;
     if (lse != nullptr && !aligned16(lse)) return INFLLMV2_ERR_INVALID_ARG;
+    if (n_blocks(L_max, p.block_size) > kMaxBlocks) return INFLLMV2_ERR_UNSUPPORTED;
     const int S_cap = infllmv2::selection_capacity(p, L_max);
     if ((idx_out == nullptr) != (counts_out == nullptr)) return INFLLMV2_ERR_INVALID_ARG;
     if (idx_out != nullptr && (S_max < S_cap || !aligned16(idx_out) || !aligned16(counts_out)))
@@ -338,7 +341,7 @@ int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache, con
     infllmv2::DecodeArgs da{q, k_cache, v_cache, kv_len, draft_k, draft_v, tree_mask, B, n_draft, Hq, Hkv, d, L_max,
                             o, lse, p, err, st};
     return cuda_status(
-        infllmv2::launch_decode_attention(da, idx, counts, stride, S_cap, reinterpret_cast<float*>(ws + w.part)));
+        infllmv2::launch_decode_attention(da, idx, counts, stride, reinterpret_cast<float*>(ws + w.part)));
 }
 
 }  // extern "C"

@@ -78,44 +78,58 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     WarpAcc<D> A;
     acc_init(A);
     if (cache_split) {
-        if (threadIdx.x == 0) {
-            const int* list = idx + static_cast<size_t>(sel_row) * idx_stride;
-            const int bt = (L - 1) / BS;
+        // this CTA takes chunks sp, sp + n_split_cache, ... of BPS selected blocks (more than one
+        // only for rows below dense_len, whose selection can exceed the sparse capacity)
+        const int* list = idx + static_cast<size_t>(sel_row) * idx_stride;
+        const int bt = (L - 1) / BS;
+        uint32_t phase = 0;
+        for (int ch = sp; ch * BPS < cnt; ch += n_split_cache, phase ^= 1u) {
+            if (threadIdx.x == 0) {
 #pragma unroll
-            for (int k = 0; k < BPS; ++k) {
-                const int at = sp * BPS + k;
-                int blk = at < cnt ? list[at] : -1;
-                if (at < cnt && (blk < 0 || blk > bt)) {
-                    raise_error(err, kDevErrIndex);
-                    blk = -1;
-                }
-                s_blk[k] = blk;
-                if (blk >= 0) {
-                    const int row = (b * Hkv + g) * L_max + blk * BS;
-                    mbar_arrive_expect_tx(&bars[k], 2 * kTile);
+                for (int k = 0; k < BPS; ++k) {
+                    const int at = ch * BPS + k;
+                    int blk = at < cnt ? list[at] : -1;
+                    if (at < cnt && (blk < 0 || blk > bt)) {
+                        raise_error(err, kDevErrIndex);
+                        blk = -1;
+                    }
+                    s_blk[k] = blk;
+                    if (blk >= 0) {
+                        const int row = (b * Hkv + g) * L_max + blk * BS;
+                        mbar_arrive_expect_tx(&bars[k], 2 * kTile);
 #pragma unroll
-                    for (int sub = 0; sub < D / 64; ++sub) {
-                        tma_load_2d(base + (2 * k) * kTile + sub * BS * 128, &tm_k, 64 * sub, row, &bars[k]);
-                        tma_load_2d(base + (2 * k + 1) * kTile + sub * BS * 128, &tm_v, 64 * sub, row, &bars[k]);
+                        for (int sub = 0; sub < D / 64; ++sub) {
+                            tma_load_2d(base + (2 * k) * kTile + sub * BS * 128, &tm_k, 64 * sub, row, &bars[k]);
+                            tma_load_2d(base + (2 * k + 1) * kTile + sub * BS * 128, &tm_v, 64 * sub, row, &bars[k]);
+                        }
+                    } else {
+                        mbar_arrive(&bars[k]);  // keep every slot's phase in step
                     }
                 }
             }
-        }
-        __syncthreads();
-        for (int tile = warp; tile < BPS * kTilesPerBlock; tile += 4) {
-            const int k = tile / kTilesPerBlock;
-            const int blk = s_blk[k];
-            if (blk < 0) continue;
-            const int r0 = (tile % kTilesPerBlock) * 32;
-            const int n_ok = L - (blk * BS + r0);
-            if (n_ok <= 0) continue;
-            const uint32_t valid = n_ok >= 32 ? 0xffffffffu : ((1u << n_ok) - 1u);
-            if (!mbar_wait(&bars[k], 0)) {
-                if (lane == 0) raise_error(err, kDevErrTimeout);
-                continue;
+            __syncthreads();
+            for (int tile = warp; tile < BPS * kTilesPerBlock; tile += 4) {
+                const int k = tile / kTilesPerBlock;
+                const int blk = s_blk[k];
+                if (blk < 0) continue;
+                const int r0 = (tile % kTilesPerBlock) * 32;
+                const int n_ok = L - (blk * BS + r0);
+                if (n_ok <= 0) continue;
+                const uint32_t valid = n_ok >= 32 ? 0xffffffffu : ((1u << n_ok) - 1u);
+                if (!mbar_wait(&bars[k], phase)) {
+                    if (lane == 0) raise_error(err, kDevErrTimeout);
+                    continue;
+                }
+                attend32_smem<D>(A, Q, smem_u32(base + (2 * k) * kTile), smem_u32(base + (2 * k + 1) * kTile), BS,
+                                 r0, valid, scale_log2);
             }
-            attend32_smem<D>(A, Q, smem_u32(base + (2 * k) * kTile), smem_u32(base + (2 * k + 1) * kTile), BS, r0,
-                             valid, scale_log2);
+            // every copy of this chunk has landed and been read before the tiles are refilled
+            if (threadIdx.x == 0) {
+#pragma unroll
+                for (int k = 0; k < BPS; ++k)
+                    if (!mbar_wait(&bars[k], phase)) raise_error(err, kDevErrTimeout);
+            }
+            __syncthreads();
         }
     } else if (sp >= n_split_cache && tree_mask != nullptr && len_ok) {
         const int j0 = warp * 32;
@@ -131,14 +145,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         raise_error(err, kDevErrIndex);
     }
     acc_finish_rowsum(A);
-
-    // every copy has landed before the tiles are reused for the merge
-    if (cache_split && threadIdx.x == 0) {
-#pragma unroll
-        for (int k = 0; k < BPS; ++k)
-            if (s_blk[k] >= 0 && !mbar_wait(&bars[k], 0)) raise_error(err, kDevErrTimeout);
-    }
-    __syncthreads();
+    __syncthreads();  // the tiles are reused for the merge
 
     // ---- merge the four warps (reusing the tile memory)
     float* sm_m = reinterpret_cast<float*>(base);
@@ -249,11 +256,16 @@ size_t decode_partial_bytes(int B, int n_draft, int Hkv, int d, int n_split) {
     return static_cast<size_t>(B) * n_draft * Hkv * n_split * per * sizeof(float);
 }
 
-void decode_split_shape(int S_cap, int bs, bool tree, int* blocks_per_split, int* n_split_cache, int* n_split) {
-    // 128 keys per split (one 32-key tile per warp): two 64-token blocks or one 128-token block.
-    const int bps = bs >= 128 ? 1 : 128 / bs;
+void decode_split_shape(const Params& p, int L_max, bool tree, int* blocks_per_split, int* n_split_cache,
+                        int* n_split) {
+    // 128 keys per chunk (one 32-key tile per warp): two 64-token blocks or one 128-token block;
+    // one CTA per chunk of a sparse row's selection (top-k + forced); longer (dense) selections
+    // loop over several chunks per CTA.
+    const int bps = p.block_size >= 128 ? 1 : 128 / p.block_size;
+    const int nblk = (L_max + p.block_size - 1) / p.block_size;
+    const int sparse_cap = max(1, min(p.topk + p.n_init + p.n_local, nblk));
     *blocks_per_split = bps;
-    *n_split_cache = (S_cap + bps - 1) / bps;
+    *n_split_cache = (sparse_cap + bps - 1) / bps;
     *n_split = *n_split_cache + (tree ? 1 : 0);
 }
 
@@ -274,9 +286,9 @@ static cudaError_t launch_split_t(const DecodeArgs& a, const CUtensorMap& tk, co
 }
 
 cudaError_t launch_decode_attention(const DecodeArgs& a, const int* idx, const int* counts, int idx_stride,
-                                    int S_cap, float* part) {
+                                    float* part) {
     int bps, nsc, ns;
-    decode_split_shape(S_cap, a.p.block_size, a.tree_mask != nullptr, &bps, &nsc, &ns);
+    decode_split_shape(a.p, a.L_max, a.tree_mask != nullptr, &bps, &nsc, &ns);
     const int G = a.Hq / a.Hkv;
     const int rows = a.B * a.n_draft * a.Hkv;
     const int bs = a.p.block_size;

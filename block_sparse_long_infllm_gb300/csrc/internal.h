@@ -76,10 +76,10 @@ cudaError_t launch_block_select(const SelectArgs& a, float* S);
 
 cudaError_t launch_prefill_attention(const PrefillArgs& a);
 
-void decode_split_shape(int S_cap, int bs, bool tree, int* blocks_per_split, int* n_split_cache,
+void decode_split_shape(const Params& p, int L_max, bool tree, int* blocks_per_split, int* n_split_cache,
                         int* n_split);
 size_t decode_partial_bytes(int B, int n_draft, int Hkv, int d, int n_split);
 cudaError_t launch_decode_attention(const DecodeArgs& a, const int* idx, const int* counts, int idx_stride,
-                                    int S_cap, float* part);
+                                    float* part);
 
 }  // namespace infllmv2

@@ -272,22 +272,23 @@ __device__ __forceinline__ bool is_forced(int blk, int bt, const Params& p) {
     return blk < p.n_init || blk > bt - p.n_local;
 }
 
-// Top-k selection, one CTA per (b, g, t) row.  The row's candidate keys (the order-preserving
-// 32-bit image of each non-forced block's score) are staged in shared memory.  The radix select
-// starts at the first bit where candidate keys differ (an AND/OR reduction), uses 8-bit digits,
-// and counts digits with warp-aggregated shared atomics (lanes with the same digit add once).
-// It ends with the k-th largest key T, the number `above` of keys > T, and `rem` = k - above of
-// the keys equal to T still to take: those go to the lowest block ids.
-template <int NT>
+// Top-k selection, one CTA per (b, g, t) row.  Thread t owns the contiguous blocks
+// [t*PER, t*PER + PER) and keeps their candidate keys (the order-preserving 32-bit image of each
+// non-forced block's score) in registers.  A radix select starts at the first bit where the
+// candidate keys differ (an AND/OR reduction), uses 8-bit digits and double-buffered histograms
+// counted with warp-aggregated shared atomics (lanes with the same digit add once), and ends
+// with the k-th largest key T, the keys above it, and `rem` keys equal to T still to take --
+// those go to the lowest block ids.  One block-wide scan of (chosen, tied) counts then places
+// every chosen block in ascending order.
+template <int NT, int PER>
 __global__ void __launch_bounds__(NT)
 topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq, int Hkv, int nblk_max, int L_max,
             int tree, Params p, int* __restrict__ idx, int* __restrict__ counts, int S_max, int* __restrict__ err) {
     constexpr int NW = NT / 32;
-    extern __shared__ uint32_t s_key[];  // [n] candidate keys (forced blocks: unused)
-    __shared__ unsigned hist[256];
+    __shared__ unsigned hist[2][256];
     __shared__ uint32_t s_and[NW], s_or[NW];
     __shared__ int s_digit, s_above, s_cnt;
-    __shared__ int s_w1[NW], s_w2[NW];
+    __shared__ int s_wsel[NW], s_wtie[NW];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int row = blockIdx.x;
     const int t = row % Tq;
@@ -316,18 +317,27 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq,
     const bool take_all = L < p.dense_len || nc <= p.topk;
     const bool take_none = !take_all && p.topk == 0;  // only the forced blocks
     const bool select = !take_all && !take_none;
+    const int blk_base = tid * PER;
+
+    uint32_t key[PER];
+    bool cand[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int blk = blk_base + u;
+        cand[u] = select && blk < n && !is_forced(blk, bt, p);
+        key[u] = cand[u] ? ordered_key(__ldcg(srow + blk)) : 0u;
+    }
 
     uint32_t T = 0, mask = 0;
     int rem = 0;
     if (select) {
         uint32_t k_and = ~0u, k_or = 0u;
-        for (int blk = tid; blk < n; blk += NT) {
-            if (is_forced(blk, bt, p)) continue;
-            const uint32_t kk = ordered_key(__ldcg(srow + blk));
-            s_key[blk] = kk;
-            k_and &= kk;
-            k_or |= kk;
-        }
+#pragma unroll
+        for (int u = 0; u < PER; ++u)
+            if (cand[u]) {
+                k_and &= key[u];
+                k_or |= key[u];
+            }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             k_and &= __shfl_xor_sync(0xffffffffu, k_and, off);
@@ -337,6 +347,7 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq,
             s_and[warp] = k_and;
             s_or[warp] = k_or;
         }
+        for (int i = tid; i < 256; i += NT) hist[0][i] = 0;
         __syncthreads();
         k_and = ~0u;
         k_or = 0u;
@@ -354,18 +365,17 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq,
             const int top = 31 - __clz(diff);  // highest bit where candidates differ
             mask = top >= 31 ? 0u : (~0u << (top + 1));
             T = k_and & mask;
+            int buf = 0;
             for (int shift = max(top - 7, 0);; shift = max(shift - 8, 0)) {
                 const int width = min(8, top + 1 - shift);
-                for (int i = tid; i < 256; i += NT) hist[i] = 0;
-                __syncthreads();
-                for (int base = 0; base < n; base += NT) {
-                    const int blk = base + tid;
-                    const bool cand = blk < n && !is_forced(blk, bt, p);
-                    const uint32_t kk = cand ? s_key[blk] : 0u;
-                    const bool hit = cand && (kk & mask) == T;
-                    const unsigned dig = (kk >> shift) & 255u;
+                unsigned* h = hist[buf];
+                for (int i = tid; i < 256; i += NT) hist[buf ^ 1][i] = 0;  // next pass's histogram
+#pragma unroll
+                for (int u = 0; u < PER; ++u) {
+                    const bool hit = cand[u] && (key[u] & mask) == T;
+                    const unsigned dig = (key[u] >> shift) & 255u;
                     const unsigned peers = __match_any_sync(0xffffffffu, hit ? dig : 256u + lane);
-                    if (hit && lane == __ffs(peers) - 1) atomicAdd(&hist[dig], static_cast<unsigned>(__popc(peers)));
+                    if (hit && lane == __ffs(peers) - 1) atomicAdd(&h[dig], static_cast<unsigned>(__popc(peers)));
                 }
                 __syncthreads();
                 if (warp == 0) {
@@ -373,7 +383,7 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq,
                     unsigned cnt[8], tot = 0;
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        cnt[e] = hist[255 - (lane * 8 + e)];
+                        cnt[e] = h[255 - (lane * 8 + e)];
                         tot += cnt[e];
                     }
                     unsigned incl = tot;
@@ -400,57 +410,77 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq,
                 rem -= s_above;
                 T |= static_cast<uint32_t>(s_digit) << shift;
                 mask |= ((1u << width) - 1u) << shift;
-                const bool done = s_cnt == rem || shift == 0;
-                __syncthreads();
-                if (done) break;
+                if (s_cnt == rem || shift == 0) break;  // uniform: every thread read the same values
+                buf ^= 1;
             }
             if (mask != ~0u) rem = 1 << 30;  // the whole digit group is taken: no tie to break
         }
     }
 
-    // ---- compaction in ascending block order; keys equal to T (under mask) are taken while
-    // fewer than `rem` of them have been taken
-    int total = 0, tied = 0;
-    for (int base = 0; base < n; base += NT) {
-        const int blk = base + tid;
-        bool sel = false, tie = false;
-        if (blk < n) {
-            if (take_all || is_forced(blk, bt, p)) {
+    // ---- chosen = forced, or key above T, or one of the first `rem` keys equal to T
+    int n_sel = 0, n_tie = 0;
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int blk = blk_base + u;
+        if (blk >= n) continue;
+        if (take_all || is_forced(blk, bt, p)) {
+            ++n_sel;
+        } else if (cand[u]) {
+            const uint32_t km = key[u] & mask;
+            n_sel += km > T;
+            n_tie += km == T;
+        }
+    }
+    // block-wide exclusive scans of the two counts
+    int sel_incl = n_sel, tie_incl = n_tie;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, sel_incl, off);
+        const int c = __shfl_up_sync(0xffffffffu, tie_incl, off);
+        if (lane >= off) {
+            sel_incl += a;
+            tie_incl += c;
+        }
+    }
+    if (lane == 31) {
+        s_wsel[warp] = sel_incl;
+        s_wtie[warp] = tie_incl;
+    }
+    __syncthreads();
+    int sel_before = sel_incl - n_sel, tie_before = tie_incl - n_tie, sel_total = 0, tie_total = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        if (w < warp) {
+            sel_before += s_wsel[w];
+            tie_before += s_wtie[w];
+        }
+        sel_total += s_wsel[w];
+        tie_total += s_wtie[w];
+    }
+    const int ties_taken = min(tie_total, rem);
+    // ties taken before this thread shift every later position
+    int pos_out = sel_before + min(tie_before, rem);
+    int tie_rank = tie_before;
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int blk = blk_base + u;
+        if (blk >= n) continue;
+        bool sel = take_all || is_forced(blk, bt, p);
+        if (!sel && cand[u]) {
+            const uint32_t km = key[u] & mask;
+            if (km > T) {
                 sel = true;
-            } else if (select) {
-                const uint32_t km = s_key[blk] & mask;
-                sel = km > T;
-                tie = km == T;
+            } else if (km == T) {
+                sel = tie_rank < rem;
+                ++tie_rank;
             }
         }
-        const unsigned tie_ballot = __ballot_sync(0xffffffffu, tie);
-        __syncthreads();
-        if (lane == 0) s_w2[warp] = __popc(tie_ballot);
-        __syncthreads();
-        int tie_before = tied, tie_round = 0;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            if (w < warp) tie_before += s_w2[w];
-            tie_round += s_w2[w];
-        }
-        if (tie && tie_before + __popc(tie_ballot & ((1u << lane) - 1u)) < rem) sel = true;
-        tied += tie_round;
-        const unsigned ballot = __ballot_sync(0xffffffffu, sel);
-        if (lane == 0) s_w1[warp] = __popc(ballot);
-        __syncthreads();
-        int before = total, round_total = 0;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            const int v = s_w1[w];
-            if (w < warp) before += v;
-            round_total += v;
-        }
         if (sel) {
-            const int pos_out = before + __popc(ballot & ((1u << lane) - 1u));
             if (pos_out < S_max) out[pos_out] = blk;
+            ++pos_out;
         }
-        total += round_total;
     }
+    const int total = sel_total + ties_taken;
     for (int i = total + tid; i < S_max; i += NT) out[i] = -1;
     if (tid == 0) {
         counts[row] = min(total, S_max);
@@ -538,20 +568,15 @@ cudaError_t launch_block_select(const SelectArgs& a, float* S) {
     if (e != cudaSuccess) return e;
     prof_mark(a.stream, "score");
     const int rows = a.B * a.Hkv * a.Tq;
-    const size_t smem = static_cast<size_t>(nblk_max) * sizeof(uint32_t);
-    if (smem > 48 * 1024) {
-        auto kfn = nblk_max <= 512 ? topk_kernel<128> : topk_kernel<256>;
-        if (cudaError_t e2 = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  static_cast<int>(smem));
-            e2 != cudaSuccess)
-            return e2;
-    }
-    if (nblk_max <= 512)
-        e = launch_kernel(topk_kernel<128>, dim3(rows), dim3(128), smem, a.stream, decode_shaped, S, a.kv_len, a.Tq,
+    if (nblk_max <= 128 * 4)
+        e = launch_kernel(topk_kernel<128, 4>, dim3(rows), dim3(128), 0, a.stream, decode_shaped, S, a.kv_len, a.Tq,
+                          a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
+    else if (nblk_max <= 256 * 16)
+        e = launch_kernel(topk_kernel<256, 16>, dim3(rows), dim3(256), 0, a.stream, decode_shaped, S, a.kv_len, a.Tq,
                           a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
     else
-        e = launch_kernel(topk_kernel<256>, dim3(rows), dim3(256), smem, a.stream, decode_shaped, S, a.kv_len, a.Tq,
-                          a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
+        e = launch_kernel(topk_kernel<1024, 32>, dim3(rows), dim3(1024), 0, a.stream, decode_shaped, S, a.kv_len,
+                          a.Tq, a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
     prof_mark(a.stream, "topk");
     return e;
 }
