@@ -274,20 +274,19 @@ __device__ __forceinline__ bool is_forced(int blk, int bt, const Params& p) {
 
 // Top-k selection, one CTA per (b, g, t) row.  Thread t owns the contiguous blocks
 // [t*PER, t*PER + PER) and keeps their candidate keys (the order-preserving 32-bit image of each
-// non-forced block's score) in registers.  A radix select starts at the first bit where the
-// candidate keys differ (an AND/OR reduction), uses 8-bit digits and double-buffered histograms
-// counted with warp-aggregated shared atomics (lanes with the same digit add once), and ends
-// with the k-th largest key T, the keys above it, and `rem` keys equal to T still to take --
-// those go to the lowest block ids.  One block-wide scan of (chosen, tied) counts then places
-// every chosen block in ascending order.
+// non-forced block's score) in registers.  The k-th largest key T is found bit by bit from the
+// first bit where candidate keys differ: for each bit, the number of keys >= (T | bit) is one
+// per-thread count, one warp reduction and one barrier; the search stops as soon as exactly k
+// keys clear the threshold.  Keys above T are taken, and of the keys equal to T (exact ties)
+// the `rem` with the lowest block ids.  One block-wide scan of (chosen, tied) counts then
+// places every chosen block in ascending order.
 template <int NT, int PER>
 __global__ void __launch_bounds__(NT)
 topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq, int Hkv, int nblk_max, int L_max,
             int tree, Params p, int* __restrict__ idx, int* __restrict__ counts, int S_max, int* __restrict__ err) {
     constexpr int NW = NT / 32;
-    __shared__ unsigned hist[2][256];
     __shared__ uint32_t s_and[NW], s_or[NW];
-    __shared__ int s_digit, s_above, s_cnt;
+    __shared__ int s_cnt[2][NW];
     __shared__ int s_wsel[NW], s_wtie[NW];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int row = blockIdx.x;
@@ -328,8 +327,9 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq,
         key[u] = cand[u] ? ordered_key(__ldcg(srow + blk)) : 0u;
     }
 
-    uint32_t T = 0, mask = 0;
-    int rem = 0;
+    // threshold: keys >= T are taken (all of them when tie_limit is not hit)
+    uint32_t T = 0;
+    int rem = 1 << 30;  // how many keys equal to T to take (the rest of T's ties are left out)
     if (select) {
         uint32_t k_and = ~0u, k_or = 0u;
 #pragma unroll
@@ -347,7 +347,6 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq,
             s_and[warp] = k_and;
             s_or[warp] = k_or;
         }
-        for (int i = tid; i < 256; i += NT) hist[0][i] = 0;
         __syncthreads();
         k_and = ~0u;
         k_or = 0u;
@@ -357,65 +356,43 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq,
             k_or |= s_or[w];
         }
         const uint32_t diff = k_and ^ k_or;
-        rem = p.topk;
-        if (diff == 0) {  // every candidate has the same score
-            T = k_and;
-            mask = ~0u;
-        } else {
-            const int top = 31 - __clz(diff);  // highest bit where candidates differ
-            mask = top >= 31 ? 0u : (~0u << (top + 1));
-            T = k_and & mask;
-            int buf = 0;
-            for (int shift = max(top - 7, 0);; shift = max(shift - 8, 0)) {
-                const int width = min(8, top + 1 - shift);
-                unsigned* h = hist[buf];
-                for (int i = tid; i < 256; i += NT) hist[buf ^ 1][i] = 0;  // next pass's histogram
+        const int k = p.topk;
+        int top = diff == 0 ? -1 : 31 - __clz(diff);
+        T = top >= 31 ? 0u : (k_and & (~0u << (top + 1)));  // bits above `top` are common to all
+        bool exact = false;
+        int buf = 0;
+        for (int bit = top; bit >= 0; --bit, buf ^= 1) {
+            const uint32_t trial = T | (1u << bit);
+            int c = 0;
 #pragma unroll
-                for (int u = 0; u < PER; ++u) {
-                    const bool hit = cand[u] && (key[u] & mask) == T;
-                    const unsigned dig = (key[u] >> shift) & 255u;
-                    const unsigned peers = __match_any_sync(0xffffffffu, hit ? dig : 256u + lane);
-                    if (hit && lane == __ffs(peers) - 1) atomicAdd(&h[dig], static_cast<unsigned>(__popc(peers)));
-                }
-                __syncthreads();
-                if (warp == 0) {
-                    // lane l holds bins 255-8l .. 248-8l, highest first
-                    unsigned cnt[8], tot = 0;
+            for (int u = 0; u < PER; ++u) c += (cand[u] && key[u] >= trial) ? 1 : 0;
+            c = __reduce_add_sync(0xffffffffu, c);
+            if (lane == 0) s_cnt[buf][warp] = c;
+            __syncthreads();
+            int total = 0;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        cnt[e] = h[255 - (lane * 8 + e)];
-                        tot += cnt[e];
-                    }
-                    unsigned incl = tot;
-#pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const unsigned v = __shfl_up_sync(0xffffffffu, incl, off);
-                        if (lane >= off) incl += v;
-                    }
-                    unsigned above = incl - tot;
-                    if (above < static_cast<unsigned>(rem) && static_cast<unsigned>(rem) <= incl) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            if (above + cnt[e] >= static_cast<unsigned>(rem)) {
-                                s_digit = 255 - (lane * 8 + e);
-                                s_above = static_cast<int>(above);
-                                s_cnt = static_cast<int>(cnt[e]);
-                                break;
-                            }
-                            above += cnt[e];
-                        }
-                    }
-                }
-                __syncthreads();
-                rem -= s_above;
-                T |= static_cast<uint32_t>(s_digit) << shift;
-                mask |= ((1u << width) - 1u) << shift;
-                if (s_cnt == rem || shift == 0) break;  // uniform: every thread read the same values
-                buf ^= 1;
+            for (int w = 0; w < NW; ++w) total += s_cnt[buf][w];
+            if (total >= k) T = trial;  // the k-th largest key has this bit set
+            if (total == k) {          // exactly k keys clear `trial`: no ties to break
+                exact = true;
+                break;
             }
-            if (mask != ~0u) rem = 1 << 30;  // the whole digit group is taken: no tie to break
+        }
+        if (!exact) {
+            // T is the k-th largest key itself; take the keys above it and enough of its ties
+            int c = 0;
+#pragma unroll
+            for (int u = 0; u < PER; ++u) c += (cand[u] && key[u] > T) ? 1 : 0;
+            c = __reduce_add_sync(0xffffffffu, c);
+            if (lane == 0) s_cnt[buf][warp] = c;
+            __syncthreads();
+            int above = 0;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) above += s_cnt[buf][w];
+            rem = k - above;
         }
     }
+    const uint32_t mask = ~0u;
 
     // ---- chosen = forced, or key above T, or one of the first `rem` keys equal to T
     int n_sel = 0, n_tie = 0;
@@ -571,8 +548,11 @@ cudaError_t launch_block_select(const SelectArgs& a, float* S) {
     if (nblk_max <= 128 * 4)
         e = launch_kernel(topk_kernel<128, 4>, dim3(rows), dim3(128), 0, a.stream, decode_shaped, S, a.kv_len, a.Tq,
                           a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
-    else if (nblk_max <= 256 * 16)
-        e = launch_kernel(topk_kernel<256, 16>, dim3(rows), dim3(256), 0, a.stream, decode_shaped, S, a.kv_len, a.Tq,
+    else if (nblk_max <= 256 * 8)
+        e = launch_kernel(topk_kernel<256, 8>, dim3(rows), dim3(256), 0, a.stream, decode_shaped, S, a.kv_len, a.Tq,
+                          a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
+    else if (nblk_max <= 512 * 16)
+        e = launch_kernel(topk_kernel<512, 16>, dim3(rows), dim3(512), 0, a.stream, decode_shaped, S, a.kv_len, a.Tq,
                           a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
     else
         e = launch_kernel(topk_kernel<1024, 32>, dim3(rows), dim3(1024), 0, a.stream, decode_shaped, S, a.kv_len,
