@@ -75,6 +75,8 @@ size_t select_workspace_bytes(int B, int Tq, int Hkv, int L_max, const Params& p
 cudaError_t launch_block_select(const SelectArgs& a, float* S);
 
 cudaError_t launch_prefill_attention(const PrefillArgs& a);
+bool tc_prefill_supported(const PrefillArgs& a);
+cudaError_t launch_prefill_tc(const PrefillArgs& a);
 
 void decode_split_shape(const Params& p, int L_max, bool tree, int* blocks_per_split, int* n_split_cache,
                         int* n_split);

@@ -82,6 +82,12 @@ prefill_warp_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
 }
 
 cudaError_t launch_prefill_attention(const PrefillArgs& a) {
+    if (tc_prefill_supported(a)) {
+        // tensor-core path; shapes it cannot hold in shared memory fall through to the warp path
+        const cudaError_t e = launch_prefill_tc(a);
+        if (e != cudaErrorInvalidValue) return e;
+        (void)cudaGetLastError();
+    }
     const int G = a.Hq / a.Hkv;
     const float scale_log2 = a.p.scale * 1.4426950408889634f;
     dim3 grid((a.Tq + 3) / 4, a.B * a.Hkv);

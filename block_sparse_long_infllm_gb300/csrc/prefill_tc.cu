@@ -1,0 +1,430 @@
+// prefill_tc.cu -- block-sparse causal attention for a prefill chunk on the 5th-generation tensor
+// cores ("MiniCPM4: 如何在手机电脑上高效运行大语言模型", section 1.1 "InfLLM v2": attention on the
+// selected blocks only; "CPM.cu：端侧大模型推理的 CUDA 加速引擎", section 4: chunked prefill).
+//
+// One CTA owns a tile of 8 query tokens x the 16 query heads of one KV head: 128 rows, one
+// TMEM lane each.  The tile walks the union of its tokens' selected blocks (a token's heads
+// share one selection); a row whose token did not select a block masks it out.
+//   * Producer warp (warp 4, one lane): TMA loads of Q (once) and of each block's K and V into
+//     two-stage rings of 128-byte-swizzled shared tiles, and the tcgen05 MMAs: S = Q K^T into
+//     one of two TMEM buffers (M=128, N=block_size, K=d), and O += P V with P read from TMEM
+//     (A operand) and V from shared memory (MN-major B).
+//   * Softmax warps (warps 0-3, thread = row): S row from TMEM; mask (selection, causality);
+//     online max/sum in fp32, log2 domain; the running max is raised only when it grows by more
+//     than 8 (a factor 256), and only then is O rescaled in TMEM; P goes back to TMEM as bf16
+//     over the S buffer it came from.
+// The tensor core computes S of block j+1 while the softmax of block j runs.  Every wait is a
+// bounded mbarrier wait: one that runs out sets the device error word and an abort flag that
+// ends every loop; the producer drains what it issued and the TMEM is freed before exit.
+#include <algorithm>
+
+#include "internal.h"
+#include "umma.cuh"
+
+namespace infllmv2 {
+
+constexpr int kTcTokens = 8;   // tokens per tile: 8 x 16 heads = 128 rows
+constexpr int kTcRows = 128;
+constexpr int kTcThreads = 160;
+
+template <int D, int BS>
+struct TcSmem {
+    static constexpr int kQ = D * kTcRows * 2;     // Q tile
+    static constexpr int kKV = D * BS * 2;         // one K (or V) block
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kQ;               // 2 stages
+    static constexpr int kVOff = kQ + 2 * kKV;     // 2 stages
+    static constexpr int kBarOff = kQ + 4 * kKV;   // q, k[2], v[2], s[2], o, p[2]  (10 x 8 B)
+    static constexpr int kMiscOff = kBarOff + 128; // tmem base, abort flag, union size
+    static constexpr int kUnionOff = kMiscOff + 64;
+    static int bytes(int max_union, int nwords) { return kUnionOff + 8 * max_union + 8 * nwords + 1024; }
+};
+
+template <int D, int BS>
+__global__ void __launch_bounds__(kTcThreads, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const int* __restrict__ idx,
+                  const int* __restrict__ counts, int S_max, const int* __restrict__ kv_len, int Tq, int Hq, int Hkv,
+                  int L_max, int max_union, float scale_log2, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                  int* __restrict__ err) {
+    using SM = TcSmem<D, BS>;
+    constexpr int G = 16;
+    constexpr uint32_t kIdescS = idesc_bf16_f32(kTcRows, BS, 0, 0);
+    constexpr uint32_t kIdescO = idesc_bf16_f32(kTcRows, D, 0, 1);
+    constexpr uint32_t kTmemCols = (2 * BS + D) <= 256 ? 256u : 512u;
+    extern __shared__ unsigned char smem_dyn[];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    uint64_t* bar_q = reinterpret_cast<uint64_t*>(base + SM::kBarOff);
+    uint64_t* bar_k = bar_q + 1;  // [2] K block landed
+    uint64_t* bar_v = bar_q + 3;  // [2] V block landed
+    uint64_t* bar_s = bar_q + 5;  // [2] S = Q K^T done
+    uint64_t* bar_o = bar_q + 7;  //     O += P V done
+    uint64_t* bar_p = bar_q + 8;  // [2] P written by all 128 softmax threads
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(base + SM::kMiscOff);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(base + SM::kMiscOff + 4);
+    int* s_U = reinterpret_cast<int*>(base + SM::kMiscOff + 8);
+    int* ublk = reinterpret_cast<int*>(base + SM::kUnionOff);          // [max_union] union blocks, ascending
+    uint32_t* umask = reinterpret_cast<uint32_t*>(ublk + max_union);   // [max_union] tokens that chose each
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.y / Hkv, g = blockIdx.y % Hkv;
+    const int t0 = blockIdx.x * kTcTokens;
+    const int Lb = kv_len[b];
+    if (Lb < Tq || Lb > L_max) {
+        if (tid == 0) raise_error(err, kDevErrIndex);
+        return;
+    }
+    const int n_tok = min(kTcTokens, Tq - t0);
+    const int bt_max = (Lb - Tq + t0 + n_tok - 1) / BS;
+    const int nwords = bt_max / 32 + 1;
+    uint32_t* bitmap = umask + max_union;                           // [nwords]
+    int* wpre = reinterpret_cast<int*>(bitmap + nwords);            // [nwords] exclusive popcount prefix
+
+    if (tid == 0) {
+        mbar_init(bar_q, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_k[i], 1);
+            mbar_init(&bar_v[i], 1);
+            mbar_init(&bar_s[i], 1);
+            mbar_init(&bar_p[i], 128);
+        }
+        mbar_init(bar_o, 1);
+        fence_mbar_init();
+        *s_abort = 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(s_tmem, kTmemCols);
+        tmem_relinquish();
+    }
+
+    // ---- union of the tile's selections: bitmap over blocks, then ranks by prefix popcounts
+    for (int w = tid; w < nwords; w += kTcThreads) bitmap[w] = 0;
+    for (int u = tid; u < max_union; u += kTcThreads) umask[u] = 0;
+    __syncthreads();
+    const int* cnt_row = counts != nullptr ? counts + (static_cast<size_t>(b) * Hkv + g) * Tq + t0 : nullptr;
+    const int* idx_row = idx != nullptr ? idx + ((static_cast<size_t>(b) * Hkv + g) * Tq + t0) * S_max : nullptr;
+    const int per_tok = idx != nullptr ? S_max : bt_max + 1;
+    auto entry = [&](int e, int& tk) -> int {  // block id of entry e (token tk), or -1
+        tk = e / per_tok;
+        const int r = e % per_tok;
+        const int bt = (Lb - Tq + t0 + tk) / BS;
+        if (idx == nullptr) return r <= bt ? r : -1;
+        const int cnt = min(max(cnt_row[tk], 0), S_max);
+        if (r >= cnt) return -1;
+        const int blk = idx_row[static_cast<size_t>(tk) * S_max + r];
+        return (blk < 0 || blk > bt) ? -2 : blk;
+    };
+    for (int e = tid; e < n_tok * per_tok; e += kTcThreads) {
+        int tk;
+        const int blk = entry(e, tk);
+        if (blk == -2) raise_error(err, kDevErrIndex);
+        if (blk >= 0) atomicOr(&bitmap[blk >> 5], 1u << (blk & 31));
+    }
+    if (idx != nullptr && tid < n_tok) {
+        const int cnt = cnt_row[tid];
+        if (cnt < 0 || cnt > S_max) raise_error(err, kDevErrIndex);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int run = 0;
+        for (int w0 = 0; w0 < nwords; w0 += 32) {
+            const int w = w0 + lane;
+            const int c = w < nwords ? __popc(bitmap[w]) : 0;
+            int incl = c;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
+            }
+            if (w < nwords) wpre[w] = run + incl - c;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) *s_U = run;
+    }
+    __syncthreads();
+    for (int e = tid; e < n_tok * per_tok; e += kTcThreads) {
+        int tk;
+        const int blk = entry(e, tk);
+        if (blk < 0) continue;
+        const int rank = wpre[blk >> 5] + __popc(bitmap[blk >> 5] & ((1u << (blk & 31)) - 1u));
+        if (rank < max_union) {
+            ublk[rank] = blk;
+            atomicOr(&umask[rank], 1u << tk);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const int U = min(*s_U, max_union);
+    const uint32_t tmem = *s_tmem;
+    const uint32_t tS0 = tmem, tS1 = tmem + BS, tO = tmem + 2 * BS;
+
+    if (warp == 4) {
+        // ======================= producer: TMA + MMA issue (one lane)
+        if (lane == 0 && U > 0) {
+            const uint32_t sQ = smem_u32(base + SM::kQOff);
+            const int kv_row0 = (b * Hkv + g) * L_max;
+            int k_issued[2] = {0, 0}, v_issued[2] = {0, 0};  // loads issued per stage
+            int s_issued = 0, o_issued = 0;                  // MMA groups committed
+            auto load = [&](int j, bool is_v) {
+                const int st = j & 1;
+                uint64_t* bar = is_v ? &bar_v[st] : &bar_k[st];
+                unsigned char* dst = base + (is_v ? SM::kVOff : SM::kKOff) + st * SM::kKV;
+                mbar_arrive_expect_tx(bar, SM::kKV);
+#pragma unroll
+                for (int sub = 0; sub < D / 64; ++sub)
+                    tma_load_2d(dst + sub * BS * 128, is_v ? &tm_v : &tm_k, 64 * sub, kv_row0 + ublk[j] * BS, bar);
+                (is_v ? v_issued : k_issued)[st] += 1;
+            };
+            auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+                if (*s_abort) return false;
+                if (mbar_wait(bar, parity)) return true;
+                raise_error(err, kDevErrTimeout);
+                *s_abort = 1;
+                return false;
+            };
+            auto issue_s = [&](int j) {
+                const uint32_t kb = smem_u32(base + SM::kKOff + (j & 1) * SM::kKV);
+                const uint32_t dS = (j & 1) ? tS1 : tS0;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t qo = (kk / 4) * (kTcRows * 128) + (kk % 4) * 32;
+                    const uint32_t ko = (kk / 4) * (BS * 128) + (kk % 4) * 32;
+                    mma_ss(dS, sw128_desc(sQ + qo, 16, 1024), sw128_desc(kb + ko, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar_s[j & 1]);
+                ++s_issued;
+            };
+            auto issue_pv = [&](int j) {
+                const uint32_t vb = smem_u32(base + SM::kVOff + (j & 1) * SM::kKV);
+                const uint32_t aP = (j & 1) ? tS1 : tS0;
+#pragma unroll
+                for (int kk = 0; kk < BS / 16; ++kk) {
+                    // B = V (keys x d, d contiguous): 16 keys per step = 2 groups of 8 rows; the
+                    // 64-column halves of d are BS*128 bytes apart
+                    const uint64_t bdesc = sw128_desc(vb + kk * 16 * 128, BS * 128, 1024);
+                    mma_ts(tO, aP + kk * 8, bdesc, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(bar_o);
+                ++o_issued;
+            };
+            // Q: one 16-row box per token (its 16 heads) and 64-column half
+            mbar_arrive_expect_tx(bar_q, SM::kQ);
+            for (int tk = 0; tk < kTcTokens; ++tk) {
+                const int t = min(t0 + tk, Tq - 1);
+                const int qrow = (b * Tq + t) * Hq + g * G;
+#pragma unroll
+                for (int sub = 0; sub < D / 64; ++sub)
+                    tma_load_2d(base + SM::kQOff + sub * (kTcRows * 128) + tk * (G * 128), &tm_q, 64 * sub, qrow, bar_q);
+            }
+            load(0, false);
+            load(0, true);
+            if (U > 1) {
+                load(1, false);
+                load(1, true);
+            }
+            bool ok = wait(bar_q, 0) && wait(&bar_k[0], 0);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+            }
+            for (int j = 0; ok && j < U; ++j) {
+                if (j + 1 < U) {
+                    // S(j+1) overwrites the buffer of P(j-1): PV(j-1) must be done; that also frees V stage (j+1)&1
+                    if (j >= 1) {
+                        if (!(ok = wait(bar_o, (j - 1) & 1))) break;
+                        load(j + 1, true);
+                    }
+                    if (!(ok = wait(&bar_k[(j + 1) & 1], ((j + 1) >> 1) & 1))) break;
+                    tc_fence_after();
+                    issue_s(j + 1);
+                }
+                if (j + 2 < U) {  // K stage j&1 is free once S(j) is done
+                    if (!(ok = wait(&bar_s[j & 1], (j >> 1) & 1))) break;
+                    load(j + 2, false);
+                }
+                if (!(ok = wait(&bar_p[j & 1], (j >> 1) & 1))) break;
+                if (!(ok = wait(&bar_v[j & 1], (j >> 1) & 1))) break;
+                tc_fence_after();
+                issue_pv(j);
+            }
+            // drain: every copy and MMA issued has completed before TMEM and shared memory go away
+            const long long drain = kWaitBudgetCycles / 8;
+            for (int st = 0; st < 2; ++st) {
+                if (k_issued[st] > 0) mbar_wait(&bar_k[st], (k_issued[st] - 1) & 1, drain);
+                if (v_issued[st] > 0) mbar_wait(&bar_v[st], (v_issued[st] - 1) & 1, drain);
+            }
+            if (s_issued > 0) mbar_wait(&bar_s[(s_issued - 1) & 1], ((s_issued - 1) >> 1) & 1, drain);
+            if (o_issued > 0) mbar_wait(bar_o, (o_issued - 1) & 1, drain);
+        }
+    } else {
+        // ======================= softmax warps: thread tid owns row tid = (token tid/16, head tid%16)
+        const int r = tid;
+        const int tk = r / G;
+        const bool live = tk < n_tok;
+        const int pos = Lb - Tq + t0 + tk;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < U; ++j) {
+            // warp-uniform: the TMEM loads and stores below are warp-collective
+            const bool waited = !*s_abort && mbar_wait(&bar_s[j & 1], (j >> 1) & 1);
+            if (!__all_sync(0xffffffffu, waited)) {
+                if (!*s_abort && lane == 0) raise_error(err, kDevErrTimeout);
+                *s_abort = 1;
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
+            const int blk = ublk[j];
+            const bool chose = live && ((umask[j] >> tk) & 1u);
+            // valid keys of this row: x = blk*BS + c <= pos
+            const int n_valid = chose ? min(BS, pos - blk * BS + 1) : 0;
+            float sv[BS];
+#pragma unroll
+            for (int c0 = 0; c0 < BS; c0 += 32) {
+                uint32_t rr[32];
+                tmem_ld32(tS + c0, rr);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) sv[c0 + e] = __uint_as_float(rr[e]);
+            }
+            float mb = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < BS; ++c) {
+                sv[c] = c < n_valid ? sv[c] * scale_log2 : -INFINITY;
+                mb = fmaxf(mb, sv[c]);
+            }
+            // raise the running max only when it grows by more than 8 (then rescale O)
+            bool rescale = false;
+            float factor = 1.f;
+            if (mb > m_run + 8.f) {
+                if (m_run != -INFINITY) {
+                    rescale = true;
+                    factor = fast_exp2(m_run - mb);
+                    l_run *= factor;
+                }
+                m_run = mb;
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+                // O must hold PV(j-1) before it is rescaled
+                if (j >= 1 && !mbar_wait(bar_o, (j - 1) & 1)) {
+                    raise_error(err, kDevErrTimeout);
+                    *s_abort = 1;
+                }
+                __syncwarp();
+                tc_fence_after();
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t rr[32];
+                    tmem_ld32(tO + lane_off + c0, rr);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * factor);
+                    tmem_st32(tO + lane_off + c0, rr);
+                }
+                tmem_st_wait();
+            }
+            const float ref = m_run == -INFINITY ? 0.f : m_run;
+#pragma unroll
+            for (int c0 = 0; c0 < BS; c0 += 64) {
+                uint32_t pw[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float p0 = fast_exp2(sv[c0 + 2 * e] - ref);
+                    const float p1 = fast_exp2(sv[c0 + 2 * e + 1] - ref);
+                    l_run += p0 + p1;
+                    pw[e] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tS + c0 / 2, pw);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bar_p[j & 1]);
+        }
+        // ---- epilogue: O / l -> bf16, lse
+        const bool go = __all_sync(0xffffffffu, ok && U > 0 && !*s_abort);
+        if (U == 0 && live) {  // nothing selected: zero output
+            const int h = g * G + (r % G);
+            __nv_bfloat16* dst = o + ((static_cast<size_t>(b) * Tq + t0 + tk) * Hq + h) * D;
+            for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
+            if (lse != nullptr) lse[(static_cast<size_t>(b) * Hq + h) * Tq + t0 + tk] = -INFINITY;
+        }
+        if (go) {
+            const bool done = mbar_wait(bar_o, (U - 1) & 1);
+            if (!__all_sync(0xffffffffu, done)) {
+                if (lane == 0) raise_error(err, kDevErrTimeout);
+                *s_abort = 1;
+            } else {
+                tc_fence_after();
+                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                const int t = t0 + tk;
+                const int h = g * G + (r % G);
+                __nv_bfloat16* dst = o + ((static_cast<size_t>(b) * Tq + (live ? t : 0)) * Hq + h) * D;
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t rr[32];
+                    tmem_ld32(tO + lane_off + c0, rr);
+                    tmem_ld_wait();
+                    if (live) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            w[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * inv, __uint_as_float(rr[2 * e + 1]) * inv);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            reinterpret_cast<uint4*>(dst + c0)[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                    }
+                }
+                if (live && lse != nullptr)
+                    lse[(static_cast<size_t>(b) * Hq + h) * Tq + t] =
+                        l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+bool tc_prefill_supported(const PrefillArgs& a) {
+    const int G = a.Hq / a.Hkv;
+    return G == 16 && (a.d == 64 || a.d == 128) && (a.p.block_size == 64 || a.p.block_size == 128);
+}
+
+template <int D, int BS>
+static cudaError_t launch_tc_t(const PrefillArgs& a) {
+    using SM = TcSmem<D, BS>;
+    const int nblk = (a.L_max + BS - 1) / BS;
+    const int per_tok = a.idx != nullptr ? a.S_max : nblk;
+    const int max_union = std::min(kTcTokens * per_tok, nblk);
+    const int nwords = nblk / 32 + 1;
+    const int smem = SM::bytes(max_union, nwords);
+    if (smem > 227 * 1024) return cudaErrorInvalidValue;
+    CUtensorMap tq, tk, tv;
+    const uint64_t q_rows = static_cast<uint64_t>(a.B) * a.Tq * a.Hq;
+    const uint64_t kv_rows = static_cast<uint64_t>(a.B) * a.Hkv * a.L_max;
+    if (!make_tmap_bf16_2d(&tq, a.q, D, q_rows, 64, 16) || !make_tmap_bf16_2d(&tk, a.k_cache, D, kv_rows, 64, BS) ||
+        !make_tmap_bf16_2d(&tv, a.v_cache, D, kv_rows, 64, BS))
+        return cudaErrorInvalidValue;
+    auto kfn = prefill_tc_kernel<D, BS>;
+    if (cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); e != cudaSuccess)
+        return e;
+    dim3 grid((a.Tq + kTcTokens - 1) / kTcTokens, a.B * a.Hkv);
+    const float scale_log2 = a.p.scale * 1.4426950408889634f;
+    return launch_kernel(kfn, grid, dim3(kTcThreads), smem, a.stream, false, tq, tk, tv, a.idx, a.counts, a.S_max,
+                         a.kv_len, a.Tq, a.Hq, a.Hkv, a.L_max, max_union, scale_log2,
+                         static_cast<__nv_bfloat16*>(a.o), a.lse, a.err);
+}
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a) {
+    if (a.d == 128) return a.p.block_size == 128 ? launch_tc_t<128, 128>(a) : launch_tc_t<128, 64>(a);
+    return a.p.block_size == 128 ? launch_tc_t<64, 128>(a) : launch_tc_t<64, 64>(a);
+}
+
+}  // namespace infllmv2

@@ -154,3 +154,38 @@ def test_bad_arguments_raise(cuda_lib):
     with pytest.raises(L.InfLLMv2Error) as e:
         L.kernel_pool(k, kern[:, :, :3].contiguous(), 0, w.L, w.params())
     assert e.value.status == L.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bs,d", [(128, 128), (64, 128), (64, 64), (128, 64)])
+def test_prefill_group16_tensor_core_path(cuda_lib, bs, d):
+    # 16 heads per KV head take the tcgen05 path; 203 queries leave a ragged last tile of 8,
+    # two sequences of different lengths, selection wider than one tile's union
+    w = synth.WORKLOADS["chunked_prefill_32k"].scaled(B=2, L=2500, Tq=203, Hq=32, Hkv=2, d=d, block_size=bs,
+                                                       topk=4, n_local=2, dense_len=0, seed=3800 + bs + d)
+    inp = synth.make_inputs(w)
+    inp["kv_len"] = np.array([2500, 1311], dtype=np.int32)
+    p = w.params()
+    g = run_gpu(w, inp, pool_split=0, params=p)
+    kern_ref, _ = oracle.kernel_pool(inp["k_cache"], inp["kv_len"], 32, 16, n_kernels(w))
+    S = oracle.block_scores(inp["q"], kern_ref, inp["kv_len"], w.Hkv, p)
+    oidx, ocnt, kth, _ = oracle.select(S, inp["kv_len"], w.Tq, p, S_max=g["S_cap"])
+    gidx, gcnt = g["idx"].cpu().numpy(), g["counts"].cpu().numpy()
+    assert compare_selection(gidx, gcnt, oidx, ocnt, S, kth)[3] == 0
+    o_ref, lse_ref = oracle.attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["kv_len"], gidx, gcnt, p)
+    check_output(bf16_to_f64(g["o"]), o_ref)
+    assert np.max(np.abs(g["lse"].cpu().numpy() - lse_ref)) < 2e-3
+
+
+def test_prefill_group16_dense_without_selection(cuda_lib):
+    torch = pytest.importorskip("torch")
+    L = lib()
+    w = synth.WORKLOADS["chunked_prefill_32k"].scaled(L=1000, Tq=77, Hq=16, Hkv=1, d=128, block_size=64,
+                                                       seed=3900)
+    inp = synth.make_inputs(w)
+    q, k, v, kv = (to_dev(inp[x]) for x in ("q", "k_cache", "v_cache", "kv_len"))
+    o = torch.empty_like(q)
+    L.sparse_attn_fwd(q, k, v, None, None, kv, o, w.params())
+    torch.cuda.synchronize()
+    assert L.sync_status() == 0
+    o_ref, _ = oracle.attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["kv_len"], None, None, w.params())
+    check_output(bf16_to_f64(o), o_ref)
