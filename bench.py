@@ -482,7 +482,7 @@ def run_prefill(args) -> dict:
             "stages_ms": {kk: round(vv, 4) for kk, vv in stage_ms.items()},
             "algorithmic_gflop": {"attention": fl_attn / 1e9, "score": fl_score / 1e9},
             "keys_per_query": attended / (w.Tq * w.Hq),
-            "roofline": {"bound": "tensor", "kernel": "prefill_warp_kernel", "achieved": round(att_tf, 2),
+            "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": round(att_tf, 2),
                          "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(att_tf / pk["bf16_tflops"], 4),
                          "traffic": None},
             "step_tflops": round(step_tf, 2), "step_frac": round(step_tf / pk["bf16_tflops"], 4),

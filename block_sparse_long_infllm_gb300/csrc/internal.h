@@ -73,6 +73,8 @@ cudaError_t launch_kernel_pool(const void* k_cache, void* kernel_cache, int B, i
 int selection_capacity(const Params& p, int L_max);
 size_t select_workspace_bytes(int B, int Tq, int Hkv, int L_max, const Params& p);
 cudaError_t launch_block_select(const SelectArgs& a, float* S);
+bool score_tc_supported(const SelectArgs& a);
+cudaError_t launch_score_tc(const SelectArgs& a, float* S);
 
 cudaError_t launch_prefill_attention(const PrefillArgs& a);
 bool tc_prefill_supported(const PrefillArgs& a);

@@ -1,9 +1,9 @@
 // kernel_pool.cu -- semantic-kernel pooling ("MiniCPM4: 如何在手机电脑上高效运行大语言模型",
 // section 1.1 "InfLLM v2": overlapping semantic kernels of 32 tokens with stride 16).
 //
-// kernel[j] = bf16_rne(mean of K rows [j*s, j*s + c)).  Each thread owns one kernel and one
-// 8-element slice of the head dimension and reads its c rows with 128-bit loads, so a warp
-// covers two kernels' full rows with coalesced 256-byte segments.  The sum is carried in
+// kernel[j] = bf16_rne(mean of K rows [j*s, j*s + c)).  Four lanes own one kernel and one
+// 8-element slice of the head dimension and read its c rows with 128-bit loads (a warp covers
+// two kernels' slices of 64 bytes per row, coalesced into 32-byte sectors).  The sum is carried in
 // fp64: the sum of up to 2^20 bf16 values whose magnitudes span less than 2^40 is exact in
 // a 53-bit significand, so the result is the exact mean rounded once (the same value any
 // summation order gives).  The work is negligible next to scoring (one read of each new
@@ -36,6 +36,9 @@ __device__ __forceinline__ uint16_t f64_to_bf16_rne(double x) {
     return static_cast<uint16_t>((sign << 15) | (static_cast<unsigned>(e) << 7) | m7);
 }
 
+// Four adjacent lanes share one (kernel, 8-element slice): lane q sums rows q, q+4, q+8, ... of
+// the kernel's c rows with independent 128-bit loads, and the four exact fp64 partial sums are
+// added with shuffles (exact, so the order does not matter).
 template <int D>
 __global__ void __launch_bounds__(256) kernel_pool_kernel(const __nv_bfloat16* __restrict__ k,
                                                           __nv_bfloat16* __restrict__ kern,
@@ -43,24 +46,35 @@ __global__ void __launch_bounds__(256) kernel_pool_kernel(const __nv_bfloat16* _
                                                           int n_new, int c, int s) {
     constexpr int kChunks = D / 8;
     const int bg = blockIdx.y;
-    const int tid = blockIdx.x * blockDim.x + threadIdx.x;
-    if (tid >= n_new * kChunks) return;
-    const int j = j_first + tid / kChunks;
-    const int ch = tid % kChunks;
+    const int gid = blockIdx.x * blockDim.x + threadIdx.x;
+    const int q4 = gid & 3;
+    const int item = gid >> 2;
+    const bool live = item < n_new * kChunks;
+    const int j = j_first + (live ? item / kChunks : 0);
+    const int ch = item % kChunks;
     const uint4* src =
         reinterpret_cast<const uint4*>(k + (static_cast<size_t>(bg) * L_max + static_cast<size_t>(j) * s) * D) + ch;
     double acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.0;
-    for (int i = 0; i < c; ++i) {
-        const uint4 v = ldg_v4(src + static_cast<size_t>(i) * kChunks);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if (live) {
+#pragma unroll 8
+        for (int i = q4; i < c; i += 4) {
+            const uint4 v = ldg_v4(src + static_cast<size_t>(i) * kChunks);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            acc[2 * e] += static_cast<double>(bf16_lo(w[e]));
-            acc[2 * e + 1] += static_cast<double>(bf16_hi(w[e]));
+            for (int e = 0; e < 4; ++e) {
+                acc[2 * e] += static_cast<double>(bf16_lo(w[e]));
+                acc[2 * e + 1] += static_cast<double>(bf16_hi(w[e]));
+            }
         }
     }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 1);
+        acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 2);
+    }
+    if (!live || q4 != 0) return;
     const double cd = static_cast<double>(c);
     uint32_t out[4];
 #pragma unroll
@@ -78,7 +92,7 @@ cudaError_t launch_kernel_pool(const void* k_cache, void* kernel_cache, int B, i
                                cudaStream_t stream) {
     if (n_new <= 0) return cudaSuccess;
     const int threads = 256;
-    const int per_bg = n_new * (d / 8);
+    const int per_bg = 4 * n_new * (d / 8);
     dim3 grid((per_bg + threads - 1) / threads, B * Hkv);
     const auto* kp = static_cast<const __nv_bfloat16*>(k_cache);
     auto* op = static_cast<__nv_bfloat16*>(kernel_cache);

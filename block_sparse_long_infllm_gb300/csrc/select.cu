@@ -537,7 +537,11 @@ cudaError_t launch_block_select(const SelectArgs& a, float* S) {
             e = a.d == 128 ? launch_score_decode_t<128>(a, S, bpc) : launch_score_decode_t<64>(a, S, bpc);
         }
     }
-    if (!decode_shaped) {
+    if (!decode_shaped && many && score_tc_supported(a)) {
+        // many queries, 16 heads per KV head: the tensor-core GEMM scorer
+        e = launch_score_tc(a, S);
+        if (e == cudaSuccess) decode_shaped = false;
+    } else if (!decode_shaped) {
         // many queries: each warp owns one m-tile and the CTA's warps share the kernels through L1
         if (a.d == 128) e = many ? launch_score_t<128, 4, 4>(a, S) : launch_score_t<128, 4, 1>(a, S);
         else e = many ? launch_score_t<64, 4, 4>(a, S) : launch_score_t<64, 4, 1>(a, S);
