@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="profiling aid: run only the chunked-prefill part (no headline value)")
     return ap.parse_args()
 
 
@@ -591,7 +593,7 @@ def main():
     torch.cuda.set_device(local)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
-    out, _ = run_decode(args, world, rank)
+    out = {"metric": METRIC, "profiling_only": True} if args.no_decode else run_decode(args, world, rank)[0]
     if not args.no_prefill:
         out["prefill"] = run_prefill(args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
