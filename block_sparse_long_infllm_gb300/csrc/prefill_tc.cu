@@ -9,10 +9,12 @@
 //     two-stage rings of 128-byte-swizzled shared tiles, and the tcgen05 MMAs: S = Q K^T into
 //     one of two TMEM buffers (M=128, N=block_size, K=d), and O += P V with P read from TMEM
 //     (A operand) and V from shared memory (MN-major B).
-//   * Softmax warps (warps 0-3, thread = row): S row from TMEM; mask (selection, causality);
-//     online max/sum in fp32, log2 domain; the running max is raised only when it grows by more
-//     than 8 (a factor 256), and only then is O rescaled in TMEM; P goes back to TMEM as bf16
-//     over the S buffer it came from.
+//   * Softmax warps (warps 0-3, thread = row): S row from TMEM; causal mask on the query's own
+//     block; online max/sum in fp32; the running max is raised only when it grows by more than
+//     2^8, and only then is O rescaled in TMEM; P goes back to TMEM as bf16 over the S buffer.
+//     Rows of tokens that did not choose a block skip it altogether: the PV MMA leaves their O
+//     lanes untouched (disable-output-lane mask), so the union tile costs softmax work only
+//     where a token really attends.
 // The tensor core computes S of block j+1 while the softmax of block j runs.  Every wait is a
 // bounded mbarrier wait: one that runs out sets the device error word and an abort flag that
 // ends every loop; the producer drains what it issued and the TMEM is freed before exit.
@@ -199,12 +201,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             auto issue_pv = [&](int j) {
                 const uint32_t vb = smem_u32(base + SM::kVOff + (j & 1) * SM::kKV);
                 const uint32_t aP = (j & 1) ? tS1 : tS0;
+                // rows (lanes) of tokens that did not choose block j keep their O: token tk owns
+                // lanes 16tk .. 16tk+15, i.e. half (tk & 1) of mask word tk / 2
+                uint32_t dm[4];
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const uint32_t m = umask[j];
+                    dm[w] = (((m >> (2 * w)) & 1u) ? 0u : 0x0000FFFFu) | (((m >> (2 * w + 1)) & 1u) ? 0u : 0xFFFF0000u);
+                }
 #pragma unroll
                 for (int kk = 0; kk < BS / 16; ++kk) {
                     // B = V (keys x d, d contiguous): 16 keys per step = 2 groups of 8 rows; the
                     // 64-column halves of d are BS*128 bytes apart
                     const uint64_t bdesc = sw128_desc(vb + kk * 16 * 128, BS * 128, 1024);
-                    mma_ts(tO, aP + kk * 8, bdesc, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts_masked(tO, aP + kk * 8, bdesc, kIdescO, dm[0], dm[1], dm[2], dm[3]);
                 }
                 mma_commit(bar_o);
                 ++o_issued;
@@ -265,7 +275,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const bool live = tk < n_tok;
         const int pos = Lb - Tq + t0 + tk;
         const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-        float m_run = -INFINITY, l_run = 0.f;
+        // O starts at zero (every PV accumulates; rows that skip a block keep their O)
+        {
+            uint32_t z[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) z[e] = 0u;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) tmem_st32(tO + lane_off + c0, z);
+            tmem_st_wait();
+        }
+        float m_run = -INFINITY;  // running max of the raw scores q.k (unscaled)
+        float l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < U; ++j) {
             // warp-uniform: the TMEM loads and stores below are warp-collective
@@ -276,71 +296,78 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 ok = false;
                 break;
             }
-            tc_fence_after();
-            const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
-            const int blk = ublk[j];
             const bool chose = live && ((umask[j] >> tk) & 1u);
-            // valid keys of this row: x = blk*BS + c <= pos
-            const int n_valid = chose ? min(BS, pos - blk * BS + 1) : 0;
-            float sv[BS];
-#pragma unroll
-            for (int c0 = 0; c0 < BS; c0 += 32) {
-                uint32_t rr[32];
-                tmem_ld32(tS + c0, rr);
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) sv[c0 + e] = __uint_as_float(rr[e]);
-            }
-            float mb = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < BS; ++c) {
-                sv[c] = c < n_valid ? sv[c] * scale_log2 : -INFINITY;
-                mb = fmaxf(mb, sv[c]);
-            }
-            // raise the running max only when it grows by more than 8 (then rescale O)
-            bool rescale = false;
-            float factor = 1.f;
-            if (mb > m_run + 8.f) {
-                if (m_run != -INFINITY) {
-                    rescale = true;
-                    factor = fast_exp2(m_run - mb);
-                    l_run *= factor;
-                }
-                m_run = mb;
-            }
-            if (__any_sync(0xffffffffu, rescale)) {
-                // O must hold PV(j-1) before it is rescaled
-                if (j >= 1 && !mbar_wait(bar_o, (j - 1) & 1)) {
-                    raise_error(err, kDevErrTimeout);
-                    *s_abort = 1;
-                }
-                __syncwarp();
+            if (__any_sync(0xffffffffu, chose)) {
                 tc_fence_after();
+                const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
+                const int blk = ublk[j];
+                // valid keys of this row: x = blk*BS + c <= pos (only the query's own block is partial)
+                const int n_valid = chose ? min(BS, pos - blk * BS + 1) : 0;
+                float sv[BS];
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
+                for (int c0 = 0; c0 < BS; c0 += 32) {
                     uint32_t rr[32];
-                    tmem_ld32(tO + lane_off + c0, rr);
-                    tmem_ld_wait();
+                    tmem_ld32(tS + c0, rr);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * factor);
-                    tmem_st32(tO + lane_off + c0, rr);
+                    for (int e = 0; e < 32; ++e) sv[c0 + e] = __uint_as_float(rr[e]);
                 }
+                tmem_ld_wait();
+                if (n_valid < BS) {
+#pragma unroll
+                    for (int c = 0; c < BS; ++c) sv[c] = c < n_valid ? sv[c] : -INFINITY;
+                }
+                float mb = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < BS; c += 2) mb = fmaxf(mb, fmaxf(sv[c], sv[c + 1]));
+                // raise the running max only when it grows by more than 8 in the log2 domain
+                bool rescale = false;
+                float factor = 1.f;
+                if (chose && (mb - m_run) * scale_log2 > 8.f) {
+                    if (m_run != -INFINITY) {
+                        rescale = true;
+                        factor = fast_exp2((m_run - mb) * scale_log2);
+                        l_run *= factor;
+                    }
+                    m_run = mb;
+                }
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // O must hold PV(j-1) before it is rescaled
+                    if (j >= 1 && !mbar_wait(bar_o, (j - 1) & 1)) {
+                        raise_error(err, kDevErrTimeout);
+                        *s_abort = 1;
+                    }
+                    __syncwarp();
+                    tc_fence_after();
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t rr[32];
+                        tmem_ld32(tO + lane_off + c0, rr);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * factor);
+                        tmem_st32(tO + lane_off + c0, rr);
+                    }
+                    tmem_st_wait();
+                }
+                // p = 2^((s - m) * scale_log2) as one FFMA and one EX2
+                const float neg = m_run == -INFINITY ? 0.f : -m_run * scale_log2;
+                float lsum0 = 0.f, lsum1 = 0.f;
+#pragma unroll
+                for (int c0 = 0; c0 < BS; c0 += 64) {
+                    uint32_t pw[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float p0 = fast_exp2(fmaf(sv[c0 + 2 * e], scale_log2, neg));
+                        const float p1 = fast_exp2(fmaf(sv[c0 + 2 * e + 1], scale_log2, neg));
+                        lsum0 += p0;
+                        lsum1 += p1;
+                        pw[e] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32(tS + c0 / 2, pw);
+                }
+                if (chose) l_run += lsum0 + lsum1;
                 tmem_st_wait();
             }
-            const float ref = m_run == -INFINITY ? 0.f : m_run;
-#pragma unroll
-            for (int c0 = 0; c0 < BS; c0 += 64) {
-                uint32_t pw[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float p0 = fast_exp2(sv[c0 + 2 * e] - ref);
-                    const float p1 = fast_exp2(sv[c0 + 2 * e + 1] - ref);
-                    l_run += p0 + p1;
-                    pw[e] = pack_bf16x2(p0, p1);
-                }
-                tmem_st32(tS + c0 / 2, pw);
-            }
-            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bar_p[j & 1]);
         }
@@ -380,7 +407,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
                 if (live && lse != nullptr)
                     lse[(static_cast<size_t>(b) * Hq + h) * Tq + t] =
-                        l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+                        l_run > 0.f ? (m_run * scale_log2 + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
             }
         }
     }
