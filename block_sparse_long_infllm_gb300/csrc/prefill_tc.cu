@@ -304,14 +304,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 // valid keys of this row: x = blk*BS + c <= pos (only the query's own block is partial)
                 const int n_valid = chose ? min(BS, pos - blk * BS + 1) : 0;
                 float sv[BS];
+                {
+                    // all loads in flight, then one wait; registers are read only after it
+                    uint32_t rr[BS / 32][32];
 #pragma unroll
-                for (int c0 = 0; c0 < BS; c0 += 32) {
-                    uint32_t rr[32];
-                    tmem_ld32(tS + c0, rr);
+                    for (int q = 0; q < BS / 32; ++q) tmem_ld32(tS + 32 * q, rr[q]);
+                    tmem_ld_wait(rr[0]);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) sv[c0 + e] = __uint_as_float(rr[e]);
+                    for (int q = 1; q < BS / 32; ++q) reg_fence(rr[q]);
+#pragma unroll
+                    for (int q = 0; q < BS / 32; ++q)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) sv[32 * q + e] = __uint_as_float(rr[q][e]);
                 }
-                tmem_ld_wait();
                 if (n_valid < BS) {
 #pragma unroll
                     for (int c = 0; c < BS; ++c) sv[c] = c < n_valid ? sv[c] : -INFINITY;
@@ -342,7 +347,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t rr[32];
                         tmem_ld32(tO + lane_off + c0, rr);
-                        tmem_ld_wait();
+                        tmem_ld_wait(rr);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * factor);
                         tmem_st32(tO + lane_off + c0, rr);
@@ -394,7 +399,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t rr[32];
                     tmem_ld32(tO + lane_off + c0, rr);
-                    tmem_ld_wait();
+                    tmem_ld_wait(rr);
                     if (live) {
                         uint32_t w[16];
 #pragma unroll

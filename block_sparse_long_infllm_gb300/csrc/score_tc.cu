@@ -187,7 +187,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int tp = 0; tp < kScTokens; tp += 2) {
                 uint32_t rr[32];
                 tmem_ld32(tmem + st * kScN + lane_off + tp * G, rr);
-                tmem_ld_wait();
+                tmem_ld_wait(rr);
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     float m = __uint_as_float(rr[16 * u]);
