@@ -12,9 +12,9 @@
 //   * Softmax warps (warps 0-3, thread = row): S row from TMEM; causal mask on the query's own
 //     block; online max/sum in fp32; the running max is raised only when it grows by more than
 //     2^8, and only then is O rescaled in TMEM; P goes back to TMEM as bf16 over the S buffer.
-//     Rows of tokens that did not choose a block skip it altogether: the PV MMA leaves their O
-//     lanes untouched (disable-output-lane mask), so the union tile costs softmax work only
-//     where a token really attends.
+//     Rows of tokens that did not choose a block get zero P rows; a warp none of whose rows
+//     chose the block only stores those zeros, so the union tile costs softmax work only where
+//     a token really attends.
 // The tensor core computes S of block j+1 while the softmax of block j runs.  Every wait is a
 // bounded mbarrier wait: one that runs out sets the device error word and an abort flag that
 // ends every loop; the producer drains what it issued and the TMEM is freed before exit.
@@ -201,20 +201,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             auto issue_pv = [&](int j) {
                 const uint32_t vb = smem_u32(base + SM::kVOff + (j & 1) * SM::kKV);
                 const uint32_t aP = (j & 1) ? tS1 : tS0;
-                // rows (lanes) of tokens that did not choose block j keep their O: token tk owns
-                // lanes 16tk .. 16tk+15, i.e. half (tk & 1) of mask word tk / 2
-                uint32_t dm[4];
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const uint32_t m = umask[j];
-                    dm[w] = (((m >> (2 * w)) & 1u) ? 0u : 0x0000FFFFu) | (((m >> (2 * w + 1)) & 1u) ? 0u : 0xFFFF0000u);
-                }
 #pragma unroll
                 for (int kk = 0; kk < BS / 16; ++kk) {
                     // B = V (keys x d, d contiguous): 16 keys per step = 2 groups of 8 rows; the
                     // 64-column halves of d are BS*128 bytes apart
                     const uint64_t bdesc = sw128_desc(vb + kk * 16 * 128, BS * 128, 1024);
-                    mma_ts_masked(tO, aP + kk * 8, bdesc, kIdescO, dm[0], dm[1], dm[2], dm[3]);
+                    mma_ts(tO, aP + kk * 8, bdesc, kIdescO, 1u);
                 }
                 mma_commit(bar_o);
                 ++o_issued;
@@ -371,6 +363,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     tmem_st32(tS + c0 / 2, pw);
                 }
                 if (chose) l_run += lsum0 + lsum1;
+                tmem_st_wait();
+            } else {
+                // no row of this warp chose the block: its P rows are zero (nothing else to do)
+                uint32_t z[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) z[e] = 0u;
+                const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
+#pragma unroll
+                for (int c0 = 0; c0 < BS; c0 += 64) tmem_st32(tS + c0 / 2, z);
                 tmem_st_wait();
             }
             tc_fence_before();
