@@ -206,7 +206,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     // B = V (keys x d, d contiguous): 16 keys per step = 2 groups of 8 rows; the
                     // 64-column halves of d are BS*128 bytes apart
                     const uint64_t bdesc = sw128_desc(vb + kk * 16 * 128, BS * 128, 1024);
-                    mma_ts(tO, aP + kk * 8, bdesc, kIdescO, 1u);
+                    mma_ts(tO, aP + kk * 8, bdesc, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(bar_o);
                 ++o_issued;
@@ -267,15 +267,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const bool live = tk < n_tok;
         const int pos = Lb - Tq + t0 + tk;
         const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-        // O starts at zero (every PV accumulates; rows that skip a block keep their O)
-        {
-            uint32_t z[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) z[e] = 0u;
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) tmem_st32(tO + lane_off + c0, z);
-            tmem_st_wait();
-        }
         float m_run = -INFINITY;  // running max of the raw scores q.k (unscaled)
         float l_run = 0.f;
         bool ok = true;
@@ -289,25 +280,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 break;
             }
             const bool chose = live && ((umask[j] >> tk) & 1u);
+            // S(j) is complete: order every TMEM access below (loads, and the P stores of both
+            // branches, which overwrite S) after the MMA that wrote it
+            tc_fence_after();
             if (__any_sync(0xffffffffu, chose)) {
-                tc_fence_after();
                 const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
                 const int blk = ublk[j];
                 // valid keys of this row: x = blk*BS + c <= pos (only the query's own block is partial)
                 const int n_valid = chose ? min(BS, pos - blk * BS + 1) : 0;
                 float sv[BS];
-                {
-                    // all loads in flight, then one wait; registers are read only after it
-                    uint32_t rr[BS / 32][32];
 #pragma unroll
-                    for (int q = 0; q < BS / 32; ++q) tmem_ld32(tS + 32 * q, rr[q]);
-                    tmem_ld_wait(rr[0]);
+                for (int c0 = 0; c0 < BS; c0 += 32) {
+                    uint32_t rr[32];
+                    tmem_ld32(tS + c0, rr);
+                    tmem_ld_wait(rr);
 #pragma unroll
-                    for (int q = 1; q < BS / 32; ++q) reg_fence(rr[q]);
-#pragma unroll
-                    for (int q = 0; q < BS / 32; ++q)
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) sv[32 * q + e] = __uint_as_float(rr[q][e]);
+                    for (int e = 0; e < 32; ++e) sv[c0 + e] = __uint_as_float(rr[e]);
                 }
                 if (n_valid < BS) {
 #pragma unroll
@@ -366,10 +354,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tmem_st_wait();
             } else {
                 // no row of this warp chose the block: its P rows are zero (nothing else to do)
+                const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
                 uint32_t z[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) z[e] = 0u;
-                const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
 #pragma unroll
                 for (int c0 = 0; c0 < BS; c0 += 64) tmem_st32(tS + c0 / 2, z);
                 tmem_st_wait();
@@ -386,7 +374,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (lse != nullptr) lse[(static_cast<size_t>(b) * Hq + h) * Tq + t0 + tk] = -INFINITY;
         }
         if (go) {
-            const bool done = mbar_wait(bar_o, (U - 1) & 1);
+            // A warp that skipped the last blocks may get here while PV(U-2) is still pending (only
+            // PV(U-3) is sure to be done), and a parity wait is only exact one phase ahead: wait
+            // for PV(U-2) first, then PV(U-1).
+            bool done = U < 2 || mbar_wait(bar_o, (U - 2) & 1);
+            done = done && mbar_wait(bar_o, (U - 1) & 1);
             if (!__all_sync(0xffffffffu, done)) {
                 if (lane == 0) raise_error(err, kDevErrTimeout);
                 *s_abort = 1;
