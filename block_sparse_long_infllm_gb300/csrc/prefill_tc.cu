@@ -5,13 +5,14 @@
 // One CTA owns a tile of 8 query tokens x the 16 query heads of one KV head: 128 rows, one
 // TMEM lane each.  The tile walks the union of its tokens' selected blocks (a token's heads
 // share one selection); a row whose token did not select a block masks it out.
-//   * Producer warp (warp 4, one lane): TMA loads of Q (once) and of each block's K and V into
+//   * Producer warp (warp 8, one lane): TMA loads of Q (once) and of each block's K and V into
 //     two-stage rings of 128-byte-swizzled shared tiles, and the tcgen05 MMAs: S = Q K^T into
 //     one of two TMEM buffers (M=128, N=block_size, K=d), and O += P V with P read from TMEM
 //     (A operand) and V from shared memory (MN-major B).
-//   * Softmax warps (warps 0-3, thread = row): S row from TMEM; causal mask on the query's own
-//     block; online max/sum in fp32; the running max is raised only when it grows by more than
-//     2^8, and only then is O rescaled in TMEM; P goes back to TMEM as bf16 over the S buffer.
+//   * Softmax warps (warps 0-7; two warps per row, each with half of the key columns): S from
+//     TMEM; causal mask on the query's own block; online max/sum in fp32 (the pair combines its
+//     row maxima through shared memory); the running max is raised only when it grows by more
+//     than 2^8, and only then is O rescaled in TMEM; P goes back to TMEM as bf16 over S.
 //     Rows of tokens that did not choose a block get zero P rows; a warp none of whose rows
 //     chose the block only stores those zeros, so the union tile costs softmax work only where
 //     a token really attends.
@@ -27,7 +28,7 @@ namespace infllmv2 {
 
 constexpr int kTcTokens = 8;   // tokens per tile: 8 x 16 heads = 128 rows
 constexpr int kTcRows = 128;
-constexpr int kTcThreads = 160;
+constexpr int kTcThreads = 288;  // 8 softmax warps (two per TMEM lane quarter) + 1 producer warp
 
 template <int D, int BS>
 struct TcSmem {
@@ -38,9 +39,26 @@ struct TcSmem {
     static constexpr int kVOff = kQ + 2 * kKV;     // 2 stages
     static constexpr int kBarOff = kQ + 4 * kKV;   // q, k[2], v[2], s[2], o, p[2]  (10 x 8 B)
     static constexpr int kMiscOff = kBarOff + 128; // tmem base, abort flag, union size
-    static constexpr int kUnionOff = kMiscOff + 64;
-    static int bytes(int max_union, int nwords) { return kUnionOff + 8 * max_union + 8 * nwords + 1024; }
+    static constexpr int kPairOff = kBarOff + 128 + 64;  // [2][128] partial maxima, [2][128] partial sums
+    static constexpr int kUnionOff2 = kPairOff + 4 * 128 * 4;
+    static int bytes(int max_union, int nwords) { return kUnionOff2 + 8 * max_union + 8 * nwords + 1024; }
 };
+
+// AND of `v` over the 64 threads of named barrier `id` (also synchronises them).
+__device__ __forceinline__ bool pair_all(int id, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n"
+        " .reg .pred p, q;\n"
+        " setp.ne.u32 q, %1, 0;\n"
+        " bar.red.and.pred p, %2, 64, q;\n"
+        " selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id)
+        : "memory");
+    return r != 0;
+}
 
 template <int D, int BS>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -62,11 +80,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint64_t* bar_v = bar_q + 3;  // [2] V block landed
     uint64_t* bar_s = bar_q + 5;  // [2] S = Q K^T done
     uint64_t* bar_o = bar_q + 7;  //     O += P V done
-    uint64_t* bar_p = bar_q + 8;  // [2] P written by all 128 softmax threads
+    uint64_t* bar_p = bar_q + 8;  // [2] P written by all 256 softmax threads
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(base + SM::kMiscOff);
     volatile int* s_abort = reinterpret_cast<volatile int*>(base + SM::kMiscOff + 4);
     int* s_U = reinterpret_cast<int*>(base + SM::kMiscOff + 8);
-    int* ublk = reinterpret_cast<int*>(base + SM::kUnionOff);          // [max_union] union blocks, ascending
+    int* ublk = reinterpret_cast<int*>(base + SM::kUnionOff2);          // [max_union] union blocks, ascending
     uint32_t* umask = reinterpret_cast<uint32_t*>(ublk + max_union);   // [max_union] tokens that chose each
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -89,7 +107,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mbar_init(&bar_k[i], 1);
             mbar_init(&bar_v[i], 1);
             mbar_init(&bar_s[i], 1);
-            mbar_init(&bar_p[i], 128);
+            mbar_init(&bar_p[i], 256);
         }
         mbar_init(bar_o, 1);
         fence_mbar_init();
@@ -162,7 +180,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t tmem = *s_tmem;
     const uint32_t tS0 = tmem, tS1 = tmem + BS, tO = tmem + 2 * BS;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ======================= producer: TMA + MMA issue (one lane)
         if (lane == 0 && U > 0) {
             const uint32_t sQ = smem_u32(base + SM::kQOff);
@@ -261,49 +279,61 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (o_issued > 0) mbar_wait(bar_o, (o_issued - 1) & 1, drain);
         }
     } else {
-        // ======================= softmax warps: thread tid owns row tid = (token tid/16, head tid%16)
-        const int r = tid;
+        // ======================= softmax warps: warp w owns TMEM lanes 32*(w%4) .. +31 (rows r =
+        // (token r/16, head r%16)) and half h = w/4 of the key columns and of the output columns;
+        // the two warps of a lane quarter exchange partial row maxima through shared memory.
+        constexpr int HB = BS / 2;  // key columns per half
+        constexpr int HD = D / 2;   // output columns per half
+        float* pmax = reinterpret_cast<float*>(base + SM::kPairOff);  // [2][128]
+        float* psum = pmax + 2 * 128;                                  // [2][128]
+        const int h = warp / 4;
+        const int r = 32 * (warp % 4) + lane;
+        const int pair_bar = 1 + (warp % 4);  // named barrier of warps w and w+4 (64 threads)
         const int tk = r / G;
         const bool live = tk < n_tok;
         const int pos = Lb - Tq + t0 + tk;
-        const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-        float m_run = -INFINITY;  // running max of the raw scores q.k (unscaled)
-        float l_run = 0.f;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
+        float m_run = -INFINITY;  // running max of the raw scores q.k (unscaled), same in both halves
+        float l_run = 0.f;        // this half's share of the row sum
         bool ok = true;
         for (int j = 0; j < U; ++j) {
             // warp-uniform: the TMEM loads and stores below are warp-collective
             const bool waited = !*s_abort && mbar_wait(&bar_s[j & 1], (j >> 1) & 1);
-            if (!__all_sync(0xffffffffu, waited)) {
+            // pair-uniform (both warps of the lane quarter meet at their named barrier below)
+            if (!pair_all(pair_bar, waited)) {
                 if (!*s_abort && lane == 0) raise_error(err, kDevErrTimeout);
                 *s_abort = 1;
                 ok = false;
                 break;
             }
             const bool chose = live && ((umask[j] >> tk) & 1u);
-            // S(j) is complete: order every TMEM access below (loads, and the P stores of both
-            // branches, which overwrite S) after the MMA that wrote it
+            // S(j) is complete: order every TMEM access below after the MMA that wrote it
             tc_fence_after();
+            const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
+            // both warps of the pair see the same tokens, so they take the same branch
             if (__any_sync(0xffffffffu, chose)) {
-                const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
                 const int blk = ublk[j];
                 // valid keys of this row: x = blk*BS + c <= pos (only the query's own block is partial)
-                const int n_valid = chose ? min(BS, pos - blk * BS + 1) : 0;
-                float sv[BS];
+                const int n_valid = chose ? min(BS, pos - blk * BS + 1) - h * HB : 0;
+                float sv[HB];
 #pragma unroll
-                for (int c0 = 0; c0 < BS; c0 += 32) {
+                for (int c0 = 0; c0 < HB; c0 += 32) {
                     uint32_t rr[32];
-                    tmem_ld32(tS + c0, rr);
+                    tmem_ld32(tS + h * HB + c0, rr);
                     tmem_ld_wait(rr);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) sv[c0 + e] = __uint_as_float(rr[e]);
                 }
-                if (n_valid < BS) {
+                if (n_valid < HB) {
 #pragma unroll
-                    for (int c = 0; c < BS; ++c) sv[c] = c < n_valid ? sv[c] : -INFINITY;
+                    for (int c = 0; c < HB; ++c) sv[c] = c < n_valid ? sv[c] : -INFINITY;
                 }
-                float mb = -INFINITY;
+                float mh = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < BS; c += 2) mb = fmaxf(mb, fmaxf(sv[c], sv[c + 1]));
+                for (int c = 0; c < HB; c += 2) mh = fmaxf(mh, fmaxf(sv[c], sv[c + 1]));
+                pmax[h * 128 + r] = mh;
+                asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+                const float mb = fmaxf(mh, pmax[(1 - h) * 128 + r]);
                 // raise the running max only when it grows by more than 8 in the log2 domain
                 bool rescale = false;
                 float factor = 1.f;
@@ -316,7 +346,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     m_run = mb;
                 }
                 if (__any_sync(0xffffffffu, rescale)) {
-                    // O must hold PV(j-1) before it is rescaled
+                    // O must hold PV(j-1) before it is rescaled (PV(j-2) is known to be done)
                     if (j >= 1 && !mbar_wait(bar_o, (j - 1) & 1)) {
                         raise_error(err, kDevErrTimeout);
                         *s_abort = 1;
@@ -324,54 +354,76 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     __syncwarp();
                     tc_fence_after();
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
+                    for (int c0 = 0; c0 < HD; c0 += 32) {
                         uint32_t rr[32];
-                        tmem_ld32(tO + lane_off + c0, rr);
+                        tmem_ld32(tO + lane_off + h * HD + c0, rr);
                         tmem_ld_wait(rr);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * factor);
-                        tmem_st32(tO + lane_off + c0, rr);
+                        tmem_st32(tO + lane_off + h * HD + c0, rr);
                     }
                     tmem_st_wait();
                 }
                 // p = 2^((s - m) * scale_log2) as one FFMA and one EX2
                 const float neg = m_run == -INFINITY ? 0.f : -m_run * scale_log2;
                 float lsum0 = 0.f, lsum1 = 0.f;
+                if constexpr (HB >= 64) {
 #pragma unroll
-                for (int c0 = 0; c0 < BS; c0 += 64) {
-                    uint32_t pw[32];
+                    for (int c0 = 0; c0 < HB; c0 += 64) {
+                        uint32_t pw[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float p0 = fast_exp2(fmaf(sv[c0 + 2 * e], scale_log2, neg));
-                        const float p1 = fast_exp2(fmaf(sv[c0 + 2 * e + 1], scale_log2, neg));
+                        for (int e = 0; e < 32; ++e) {
+                            const float p0 = fast_exp2(fmaf(sv[c0 + 2 * e], scale_log2, neg));
+                            const float p1 = fast_exp2(fmaf(sv[c0 + 2 * e + 1], scale_log2, neg));
+                            lsum0 += p0;
+                            lsum1 += p1;
+                            pw[e] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st32(tS + (h * HB + c0) / 2, pw);
+                    }
+                } else {
+                    uint32_t pw[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = fast_exp2(fmaf(sv[2 * e], scale_log2, neg));
+                        const float p1 = fast_exp2(fmaf(sv[2 * e + 1], scale_log2, neg));
                         lsum0 += p0;
                         lsum1 += p1;
                         pw[e] = pack_bf16x2(p0, p1);
                     }
-                    tmem_st32(tS + c0 / 2, pw);
+                    tmem_st16(tS + h * HB / 2, pw);
                 }
                 if (chose) l_run += lsum0 + lsum1;
                 tmem_st_wait();
             } else {
-                // no row of this warp chose the block: its P rows are zero (nothing else to do)
-                const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
-                uint32_t z[32];
+                // no row of this warp chose the block: its P columns are zero (nothing else to do)
+                if constexpr (HB >= 64) {
+                    uint32_t z[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) z[e] = 0u;
+                    for (int e = 0; e < 32; ++e) z[e] = 0u;
 #pragma unroll
-                for (int c0 = 0; c0 < BS; c0 += 64) tmem_st32(tS + c0 / 2, z);
+                    for (int c0 = 0; c0 < HB; c0 += 64) tmem_st32(tS + (h * HB + c0) / 2, z);
+                } else {
+                    uint32_t z[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) z[e] = 0u;
+                    tmem_st16(tS + h * HB / 2, z);
+                }
                 tmem_st_wait();
             }
             tc_fence_before();
             mbar_arrive(&bar_p[j & 1]);
         }
         // ---- epilogue: O / l -> bf16, lse
+        psum[h * 128 + r] = l_run;
+        asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+        const float l_row = l_run + psum[(1 - h) * 128 + r];
         const bool go = __all_sync(0xffffffffu, ok && U > 0 && !*s_abort);
+        const int hq = g * G + (r % G);
         if (U == 0 && live) {  // nothing selected: zero output
-            const int h = g * G + (r % G);
-            __nv_bfloat16* dst = o + ((static_cast<size_t>(b) * Tq + t0 + tk) * Hq + h) * D;
-            for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
-            if (lse != nullptr) lse[(static_cast<size_t>(b) * Hq + h) * Tq + t0 + tk] = -INFINITY;
+            __nv_bfloat16* dst = o + ((static_cast<size_t>(b) * Tq + t0 + tk) * Hq + hq) * D + h * HD;
+            for (int c = 0; c < HD; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
+            if (lse != nullptr && h == 0) lse[(static_cast<size_t>(b) * Hq + hq) * Tq + t0 + tk] = -INFINITY;
         }
         if (go) {
             // A warp that skipped the last blocks may get here while PV(U-2) is still pending (only
@@ -384,14 +436,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 *s_abort = 1;
             } else {
                 tc_fence_after();
-                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
                 const int t = t0 + tk;
-                const int h = g * G + (r % G);
-                __nv_bfloat16* dst = o + ((static_cast<size_t>(b) * Tq + (live ? t : 0)) * Hq + h) * D;
+                __nv_bfloat16* dst = o + ((static_cast<size_t>(b) * Tq + (live ? t : 0)) * Hq + hq) * D + h * HD;
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
+                for (int c0 = 0; c0 < HD; c0 += 32) {
                     uint32_t rr[32];
-                    tmem_ld32(tO + lane_off + c0, rr);
+                    tmem_ld32(tO + lane_off + h * HD + c0, rr);
                     tmem_ld_wait(rr);
                     if (live) {
                         uint32_t w[16];
@@ -403,9 +454,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                             reinterpret_cast<uint4*>(dst + c0)[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
                     }
                 }
-                if (live && lse != nullptr)
-                    lse[(static_cast<size_t>(b) * Hq + h) * Tq + t] =
-                        l_run > 0.f ? (m_run * scale_log2 + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+                if (live && lse != nullptr && h == 0)
+                    lse[(static_cast<size_t>(b) * Hq + hq) * Tq + t] =
+                        l_row > 0.f ? (m_run * scale_log2 + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
             }
         }
     }
