@@ -6,7 +6,7 @@
 // TMEM lane each.  The tile walks the union of its tokens' selected blocks (a token's heads
 // share one selection); a row whose token did not select a block masks it out.
 //   * Producer warp (warp 8, one lane): TMA loads of Q (once) and of each block's K and V into
-//     two-stage rings of 128-byte-swizzled shared tiles, and the tcgen05 MMAs: S = Q K^T into
+//     three-stage (K) and two-stage (V) rings of 128-byte-swizzled shared tiles, and the tcgen05 MMAs: S = Q K^T into
 //     one of two TMEM buffers (M=128, N=block_size, K=d), and O += P V with P read from TMEM
 //     (A operand) and V from shared memory (MN-major B).
 //   * Softmax warps (warps 0-7; two warps per row, each with half of the key columns): S from
@@ -28,6 +28,7 @@ namespace infllmv2 {
 
 constexpr int kTcTokens = 8;   // tokens per tile: 8 x 16 heads = 128 rows
 constexpr int kTcRows = 128;
+constexpr int kTcKStages = 3;  // K tiles in flight: a block's K is requested as soon as S two blocks back is done
 constexpr int kTcThreads = 288;  // 8 softmax warps (two per TMEM lane quarter) + 1 producer warp
 
 template <int D, int BS>
@@ -35,9 +36,9 @@ struct TcSmem {
     static constexpr int kQ = D * kTcRows * 2;     // Q tile
     static constexpr int kKV = D * BS * 2;         // one K (or V) block
     static constexpr int kQOff = 0;
-    static constexpr int kKOff = kQ;               // 2 stages
-    static constexpr int kVOff = kQ + 2 * kKV;     // 2 stages
-    static constexpr int kBarOff = kQ + 4 * kKV;   // q, k[2], v[2], s[2], o, p[2]  (10 x 8 B)
+    static constexpr int kKOff = kQ;                    // kTcKStages stages
+    static constexpr int kVOff = kQ + kTcKStages * kKV;  // 2 stages
+    static constexpr int kBarOff = kVOff + 2 * kKV;      // q, k[3], v[2], s[2], o, p[2]  (11 x 8 B)
     static constexpr int kMiscOff = kBarOff + 128; // tmem base, abort flag, union size
     static constexpr int kPairOff = kBarOff + 128 + 64;  // [2][128] partial maxima, [2][128] partial sums
     static constexpr int kUnionOff2 = kPairOff + 4 * 128 * 4;
@@ -76,11 +77,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
     uint64_t* bar_q = reinterpret_cast<uint64_t*>(base + SM::kBarOff);
-    uint64_t* bar_k = bar_q + 1;  // [2] K block landed
-    uint64_t* bar_v = bar_q + 3;  // [2] V block landed
-    uint64_t* bar_s = bar_q + 5;  // [2] S = Q K^T done
-    uint64_t* bar_o = bar_q + 7;  //     O += P V done
-    uint64_t* bar_p = bar_q + 8;  // [2] P written by all 256 softmax threads
+    uint64_t* bar_k = bar_q + 1;  // [3] K block landed
+    uint64_t* bar_v = bar_q + 4;  // [2] V block landed
+    uint64_t* bar_s = bar_q + 6;  // [2] S = Q K^T done
+    uint64_t* bar_o = bar_q + 8;  //     O += P V done
+    uint64_t* bar_p = bar_q + 9;  // [2] P written by all 256 softmax threads
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(base + SM::kMiscOff);
     volatile int* s_abort = reinterpret_cast<volatile int*>(base + SM::kMiscOff + 4);
     int* s_U = reinterpret_cast<int*>(base + SM::kMiscOff + 8);
@@ -103,8 +104,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
     if (tid == 0) {
         mbar_init(bar_q, 1);
+        for (int i = 0; i < kTcKStages; ++i) mbar_init(&bar_k[i], 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar_k[i], 1);
             mbar_init(&bar_v[i], 1);
             mbar_init(&bar_s[i], 1);
             mbar_init(&bar_p[i], 256);
@@ -185,10 +186,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (lane == 0 && U > 0) {
             const uint32_t sQ = smem_u32(base + SM::kQOff);
             const int kv_row0 = (b * Hkv + g) * L_max;
-            int k_issued[2] = {0, 0}, v_issued[2] = {0, 0};  // loads issued per stage
+            int k_issued[kTcKStages] = {}, v_issued[2] = {0, 0};  // loads issued per stage
             int s_issued = 0, o_issued = 0;                  // MMA groups committed
             auto load = [&](int j, bool is_v) {
-                const int st = j & 1;
+                const int st = is_v ? (j & 1) : (j % kTcKStages);
                 uint64_t* bar = is_v ? &bar_v[st] : &bar_k[st];
                 unsigned char* dst = base + (is_v ? SM::kVOff : SM::kKOff) + st * SM::kKV;
                 mbar_arrive_expect_tx(bar, SM::kKV);
@@ -205,7 +206,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 return false;
             };
             auto issue_s = [&](int j) {
-                const uint32_t kb = smem_u32(base + SM::kKOff + (j & 1) * SM::kKV);
+                const uint32_t kb = smem_u32(base + SM::kKOff + (j % kTcKStages) * SM::kKV);
                 const uint32_t dS = (j & 1) ? tS1 : tS0;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -238,31 +239,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 for (int sub = 0; sub < D / 64; ++sub)
                     tma_load_2d(base + SM::kQOff + sub * (kTcRows * 128) + tk * (G * 128), &tm_q, 64 * sub, qrow, bar_q);
             }
-            load(0, false);
+            for (int j = 0; j < kTcKStages && j < U; ++j) load(j, false);
             load(0, true);
-            if (U > 1) {
-                load(1, false);
-                load(1, true);
-            }
+            if (U > 1) load(1, true);
             bool ok = wait(bar_q, 0) && wait(&bar_k[0], 0);
             if (ok) {
                 tc_fence_after();
                 issue_s(0);
             }
             for (int j = 0; ok && j < U; ++j) {
+                if (j + kTcKStages < U) {  // K stage of block j is free once S(j) is done
+                    if (!(ok = wait(&bar_s[j & 1], (j >> 1) & 1))) break;
+                    load(j + kTcKStages, false);
+                }
                 if (j + 1 < U) {
                     // S(j+1) overwrites the buffer of P(j-1): PV(j-1) must be done; that also frees V stage (j+1)&1
                     if (j >= 1) {
                         if (!(ok = wait(bar_o, (j - 1) & 1))) break;
                         load(j + 1, true);
                     }
-                    if (!(ok = wait(&bar_k[(j + 1) & 1], ((j + 1) >> 1) & 1))) break;
+                    const int ks = (j + 1) % kTcKStages;
+                    if (!(ok = wait(&bar_k[ks], ((j + 1) / kTcKStages) & 1))) break;
                     tc_fence_after();
                     issue_s(j + 1);
-                }
-                if (j + 2 < U) {  // K stage j&1 is free once S(j) is done
-                    if (!(ok = wait(&bar_s[j & 1], (j >> 1) & 1))) break;
-                    load(j + 2, false);
                 }
                 if (!(ok = wait(&bar_p[j & 1], (j >> 1) & 1))) break;
                 if (!(ok = wait(&bar_v[j & 1], (j >> 1) & 1))) break;
@@ -271,10 +270,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             // drain: every copy and MMA issued has completed before TMEM and shared memory go away
             const long long drain = kWaitBudgetCycles / 8;
-            for (int st = 0; st < 2; ++st) {
+            for (int st = 0; st < kTcKStages; ++st)
                 if (k_issued[st] > 0) mbar_wait(&bar_k[st], (k_issued[st] - 1) & 1, drain);
+            for (int st = 0; st < 2; ++st)
                 if (v_issued[st] > 0) mbar_wait(&bar_v[st], (v_issued[st] - 1) & 1, drain);
-            }
             if (s_issued > 0) mbar_wait(&bar_s[(s_issued - 1) & 1], ((s_issued - 1) >> 1) & 1, drain);
             if (o_issued > 0) mbar_wait(bar_o, (o_issued - 1) & 1, drain);
         }
