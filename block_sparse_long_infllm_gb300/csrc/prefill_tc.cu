@@ -5,10 +5,13 @@
 // One CTA owns a tile of 8 query tokens x the 16 query heads of one KV head: 128 rows, one
 // TMEM lane each.  The tile walks the union of its tokens' selected blocks (a token's heads
 // share one selection); a row whose token did not select a block masks it out.
-//   * Producer warp (warp 8, one lane): TMA loads of Q (once) and of each block's K and V into
-//     three-stage (K) and two-stage (V) rings of 128-byte-swizzled shared tiles, and the tcgen05 MMAs: S = Q K^T into
-//     one of two TMEM buffers (M=128, N=block_size, K=d), and O += P V with P read from TMEM
-//     (A operand) and V from shared memory (MN-major B).
+//   * Load warp (warp 9, one lane): TMA loads of Q (once) and of each block's K and V into
+//     three-stage (K) and two-stage (V) rings of 128-byte-swizzled shared tiles; a stage is
+//     reloaded once the MMA that read it has completed.
+//   * MMA warp (warp 8, one lane): the tcgen05 MMAs, S = Q K^T into one of three TMEM buffers
+//     (M=128, N=block_size, K=d), and O += P V with P read from TMEM (A operand) and V from
+//     shared memory (MN-major B).  An MMA issue holds the issuing thread for about the MMA's
+//     own duration, so this thread does nothing else.
 //   * Softmax warps (warps 0-7; two warps per row, each with half of the key columns): S from
 //     TMEM; causal mask on the query's own block; online max/sum in fp32 (the pair combines its
 //     row maxima through shared memory); the running max is raised only when it grows by more
@@ -16,9 +19,11 @@
 //     Rows of tokens that did not choose a block get zero P rows; a warp none of whose rows
 //     chose the block only stores those zeros, so the union tile costs softmax work only where
 //     a token really attends.
-// The tensor core computes S of block j+1 while the softmax of block j runs.  Every wait is a
+// With three S buffers, S of blocks j+1 and j+2 can be computed (and PV of block j-1 finish)
+// while the softmax of block j runs, so the softmax warps find the next S ready.  Every wait is a
 // bounded mbarrier wait: one that runs out sets the device error word and an abort flag that
-// ends every loop; the producer drains what it issued and the TMEM is freed before exit.
+// ends every loop; the load and MMA warps drain what they issued and the TMEM is freed before
+// exit.
 #include <algorithm>
 
 #include "internal.h"
@@ -28,8 +33,8 @@ namespace infllmv2 {
 
 constexpr int kTcTokens = 8;   // tokens per tile: 8 x 16 heads = 128 rows
 constexpr int kTcRows = 128;
-constexpr int kTcKStages = 3;  // K tiles in flight: a block's K is requested as soon as S two blocks back is done
-constexpr int kTcThreads = 288;  // 8 softmax warps (two per TMEM lane quarter) + 1 producer warp
+constexpr int kTcKStages = 3;  // K tiles in flight; stage j % 3 also names the TMEM S buffer of block j
+constexpr int kTcThreads = 320;  // 8 softmax warps (two per TMEM lane quarter), MMA warp, load warp
 
 template <int D, int BS>
 struct TcSmem {
@@ -38,7 +43,7 @@ struct TcSmem {
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQ;                    // kTcKStages stages
     static constexpr int kVOff = kQ + kTcKStages * kKV;  // 2 stages
-    static constexpr int kBarOff = kVOff + 2 * kKV;      // q, k[3], v[2], s[2], o, p[2]  (11 x 8 B)
+    static constexpr int kBarOff = kVOff + 2 * kKV;      // q, k[3], v[2], s[3], o[2], p[2], fin  (14 x 8 B)
     static constexpr int kMiscOff = kBarOff + 128; // tmem base, abort flag, union size
     static constexpr int kPairOff = kBarOff + 128 + 64;  // [2][128] partial maxima, [2][128] partial sums
     static constexpr int kUnionOff2 = kPairOff + 4 * 128 * 4;
@@ -61,6 +66,22 @@ __device__ __forceinline__ bool pair_all(int id, bool v) {
     return r != 0;
 }
 
+// Bounded wait of the load and MMA threads: gives up when another thread has raised the abort
+// flag, or sets it (and the device error word) when the budget runs out.
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitBudgetCycles) {
+            raise_error(err, kDevErrTimeout);
+            *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
 template <int D, int BS>
 __global__ void __launch_bounds__(kTcThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -72,16 +93,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     constexpr int G = 16;
     constexpr uint32_t kIdescS = idesc_bf16_f32(kTcRows, BS, 0, 0);
     constexpr uint32_t kIdescO = idesc_bf16_f32(kTcRows, D, 0, 1);
-    constexpr uint32_t kTmemCols = (2 * BS + D) <= 256 ? 256u : 512u;
+    constexpr uint32_t kTmemCols = (3 * BS + D) <= 256 ? 256u : 512u;
+    static_assert(3 * BS + D <= 512, "three S buffers and O must fit the 512 TMEM columns");
     extern __shared__ unsigned char smem_dyn[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
     uint64_t* bar_q = reinterpret_cast<uint64_t*>(base + SM::kBarOff);
     uint64_t* bar_k = bar_q + 1;  // [3] K block landed
     uint64_t* bar_v = bar_q + 4;  // [2] V block landed
-    uint64_t* bar_s = bar_q + 6;  // [2] S = Q K^T done
-    uint64_t* bar_o = bar_q + 8;  //     O += P V done
-    uint64_t* bar_p = bar_q + 9;  // [2] P written by all 256 softmax threads
+    uint64_t* bar_s = bar_q + 6;    // [3] S = Q K^T done (buffer j % 3)
+    uint64_t* bar_o = bar_q + 9;    // [2] O += P V done (block j on j & 1)
+    uint64_t* bar_p = bar_q + 11;   // [2] P written by all 256 softmax threads
+    uint64_t* bar_fin = bar_q + 13; //     every MMA issued has completed
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(base + SM::kMiscOff);
     volatile int* s_abort = reinterpret_cast<volatile int*>(base + SM::kMiscOff + 4);
     int* s_U = reinterpret_cast<int*>(base + SM::kMiscOff + 8);
@@ -104,13 +127,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
     if (tid == 0) {
         mbar_init(bar_q, 1);
-        for (int i = 0; i < kTcKStages; ++i) mbar_init(&bar_k[i], 1);
+        for (int i = 0; i < kTcKStages; ++i) {
+            mbar_init(&bar_k[i], 1);
+            mbar_init(&bar_s[i], 1);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_v[i], 1);
-            mbar_init(&bar_s[i], 1);
+            mbar_init(&bar_o[i], 1);
             mbar_init(&bar_p[i], 256);
         }
-        mbar_init(bar_o, 1);
+        mbar_init(bar_fin, 1);
         fence_mbar_init();
         *s_abort = 0;
     }
@@ -179,15 +205,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tc_fence_after();
     const int U = min(*s_U, max_union);
     const uint32_t tmem = *s_tmem;
-    const uint32_t tS0 = tmem, tS1 = tmem + BS, tO = tmem + 2 * BS;
+    const uint32_t tO = tmem + 3 * BS;  // S buffers at tmem + i * BS, i = 0, 1, 2
 
-    if (warp == 8) {
-        // ======================= producer: TMA + MMA issue (one lane)
+    if (warp == 9) {
+        // ======================= load warp: TMA (one lane)
         if (lane == 0 && U > 0) {
-            const uint32_t sQ = smem_u32(base + SM::kQOff);
             const int kv_row0 = (b * Hkv + g) * L_max;
             int k_issued[kTcKStages] = {}, v_issued[2] = {0, 0};  // loads issued per stage
-            int s_issued = 0, o_issued = 0;                  // MMA groups committed
             auto load = [&](int j, bool is_v) {
                 const int st = is_v ? (j & 1) : (j % kTcKStages);
                 uint64_t* bar = is_v ? &bar_v[st] : &bar_k[st];
@@ -198,38 +222,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     tma_load_2d(dst + sub * BS * 128, is_v ? &tm_v : &tm_k, 64 * sub, kv_row0 + ublk[j] * BS, bar);
                 (is_v ? v_issued : k_issued)[st] += 1;
             };
-            auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-                if (*s_abort) return false;
-                if (mbar_wait(bar, parity)) return true;
-                raise_error(err, kDevErrTimeout);
-                *s_abort = 1;
-                return false;
-            };
-            auto issue_s = [&](int j) {
-                const uint32_t kb = smem_u32(base + SM::kKOff + (j % kTcKStages) * SM::kKV);
-                const uint32_t dS = (j & 1) ? tS1 : tS0;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t qo = (kk / 4) * (kTcRows * 128) + (kk % 4) * 32;
-                    const uint32_t ko = (kk / 4) * (BS * 128) + (kk % 4) * 32;
-                    mma_ss(dS, sw128_desc(sQ + qo, 16, 1024), sw128_desc(kb + ko, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&bar_s[j & 1]);
-                ++s_issued;
-            };
-            auto issue_pv = [&](int j) {
-                const uint32_t vb = smem_u32(base + SM::kVOff + (j & 1) * SM::kKV);
-                const uint32_t aP = (j & 1) ? tS1 : tS0;
-#pragma unroll
-                for (int kk = 0; kk < BS / 16; ++kk) {
-                    // B = V (keys x d, d contiguous): 16 keys per step = 2 groups of 8 rows; the
-                    // 64-column halves of d are BS*128 bytes apart
-                    const uint64_t bdesc = sw128_desc(vb + kk * 16 * 128, BS * 128, 1024);
-                    mma_ts(tO, aP + kk * 8, bdesc, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(bar_o);
-                ++o_issued;
-            };
             // Q: one 16-row box per token (its 16 heads) and 64-column half
             mbar_arrive_expect_tx(bar_q, SM::kQ);
             for (int tk = 0; tk < kTcTokens; ++tk) {
@@ -239,43 +231,83 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 for (int sub = 0; sub < D / 64; ++sub)
                     tma_load_2d(base + SM::kQOff + sub * (kTcRows * 128) + tk * (G * 128), &tm_q, 64 * sub, qrow, bar_q);
             }
-            for (int j = 0; j < kTcKStages && j < U; ++j) load(j, false);
-            load(0, true);
-            if (U > 1) load(1, true);
-            bool ok = wait(bar_q, 0) && wait(&bar_k[0], 0);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0);
-            }
-            for (int j = 0; ok && j < U; ++j) {
-                if (j + kTcKStages < U) {  // K stage of block j is free once S(j) is done
-                    if (!(ok = wait(&bar_s[j & 1], (j >> 1) & 1))) break;
-                    load(j + kTcKStages, false);
+            // the MMA thread consumes K(0), K(1), then per block j: V(j), K(j+2)
+            for (int j = 0; j < 2 && j < U; ++j) load(j, false);
+            for (int i = 0; i < U; ++i) {
+                if (i + 2 < U) {  // K stage (i+2) % 3 held K(i-1): free once S(i-1) is done
+                    if (i >= 1 && !tc_wait(&bar_s[(i - 1) % kTcKStages], ((i - 1) / kTcKStages) & 1, s_abort, err))
+                        break;
+                    load(i + 2, false);
                 }
-                if (j + 1 < U) {
-                    // S(j+1) overwrites the buffer of P(j-1): PV(j-1) must be done; that also frees V stage (j+1)&1
-                    if (j >= 1) {
-                        if (!(ok = wait(bar_o, (j - 1) & 1))) break;
-                        load(j + 1, true);
-                    }
-                    const int ks = (j + 1) % kTcKStages;
-                    if (!(ok = wait(&bar_k[ks], ((j + 1) / kTcKStages) & 1))) break;
-                    tc_fence_after();
-                    issue_s(j + 1);
-                }
-                if (!(ok = wait(&bar_p[j & 1], (j >> 1) & 1))) break;
-                if (!(ok = wait(&bar_v[j & 1], (j >> 1) & 1))) break;
-                tc_fence_after();
-                issue_pv(j);
+                // V stage i & 1 held V(i-2): free once PV(i-2) is done
+                if (i >= 2 && !tc_wait(&bar_o[(i - 2) & 1], ((i - 2) >> 1) & 1, s_abort, err)) break;
+                load(i, true);
             }
-            // drain: every copy and MMA issued has completed before TMEM and shared memory go away
+            // drain: every copy issued has landed before shared memory goes away (only the last
+            // load of a stage can be pending: each earlier one was consumed by a completed MMA)
             const long long drain = kWaitBudgetCycles / 8;
             for (int st = 0; st < kTcKStages; ++st)
                 if (k_issued[st] > 0) mbar_wait(&bar_k[st], (k_issued[st] - 1) & 1, drain);
             for (int st = 0; st < 2; ++st)
                 if (v_issued[st] > 0) mbar_wait(&bar_v[st], (v_issued[st] - 1) & 1, drain);
-            if (s_issued > 0) mbar_wait(&bar_s[(s_issued - 1) & 1], ((s_issued - 1) >> 1) & 1, drain);
-            if (o_issued > 0) mbar_wait(bar_o, (o_issued - 1) & 1, drain);
+        }
+    } else if (warp == 8) {
+        // ======================= MMA warp: tcgen05 issue (one lane)
+        if (lane == 0 && U > 0) {
+            const uint32_t sQ = smem_u32(base + SM::kQOff);
+            bool mma_issued = false;
+            auto wait = [&](uint64_t* bar, uint32_t parity) -> bool { return tc_wait(bar, parity, s_abort, err); };
+            // S(j) into TMEM buffer j % 3 from K stage j % 3
+            auto issue_s = [&](int j) {
+                const int st = j % kTcKStages;
+                const uint32_t kb = smem_u32(base + SM::kKOff + st * SM::kKV);
+                const uint32_t dS = tmem + st * BS;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t qo = (kk / 4) * (kTcRows * 128) + (kk % 4) * 32;
+                    const uint32_t ko = (kk / 4) * (BS * 128) + (kk % 4) * 32;
+                    mma_ss(dS, sw128_desc(sQ + qo, 16, 1024), sw128_desc(kb + ko, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar_s[st]);
+                mma_issued = true;
+            };
+            auto issue_pv = [&](int j) {
+                const uint32_t vb = smem_u32(base + SM::kVOff + (j & 1) * SM::kKV);
+                const uint32_t aP = tmem + (j % kTcKStages) * BS;
+#pragma unroll
+                for (int kk = 0; kk < BS / 16; ++kk) {
+                    // B = V (keys x d, d contiguous): 16 keys per step = 2 groups of 8 rows; the
+                    // 64-column halves of d are BS*128 bytes apart
+                    const uint64_t bdesc = sw128_desc(vb + kk * 16 * 128, BS * 128, 1024);
+                    mma_ts(tO, aP + kk * 8, bdesc, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&bar_o[j & 1]);
+            };
+            bool ok = wait(bar_q, 0);
+            for (int j = 0; ok && j < 2 && j < U; ++j) {
+                if (!(ok = wait(&bar_k[j], 0))) break;
+                tc_fence_after();
+                issue_s(j);
+            }
+            // Iteration j: PV(j) once P(j) is written, then S(j+2) into the buffer PV(j-1) has
+            // released.  All parity waits below are at most one phase ahead of their barrier.
+            for (int j = 0; ok && j < U; ++j) {
+                if (!(ok = wait(&bar_p[j & 1], (j >> 1) & 1))) break;
+                if (!(ok = wait(&bar_v[j & 1], (j >> 1) & 1))) break;
+                tc_fence_after();
+                issue_pv(j);
+                if (j + 2 < U) {
+                    if (j >= 1 && !(ok = wait(&bar_o[(j - 1) & 1], ((j - 1) >> 1) & 1))) break;
+                    const int ks = (j + 2) % kTcKStages;
+                    if (!(ok = wait(&bar_k[ks], ((j + 2) / kTcKStages) & 1))) break;
+                    tc_fence_after();
+                    issue_s(j + 2);
+                }
+            }
+            if (mma_issued) {  // one commit covers every MMA this thread issued
+                mma_commit(bar_fin);
+                mbar_wait(bar_fin, 0, kWaitBudgetCycles / 8);
+            }
         }
     } else {
         // ======================= softmax warps: warp w owns TMEM lanes 32*(w%4) .. +31 (rows r =
@@ -295,9 +327,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         float m_run = -INFINITY;  // running max of the raw scores q.k (unscaled), same in both halves
         float l_run = 0.f;        // this half's share of the row sum
         bool ok = true;
+        int sb = 0;               // S buffer of block j: j % 3, completed phase parity (j / 3) & 1
+        uint32_t sph = 0;
         for (int j = 0; j < U; ++j) {
             // warp-uniform: the TMEM loads and stores below are warp-collective
-            const bool waited = !*s_abort && mbar_wait(&bar_s[j & 1], (j >> 1) & 1);
+            const bool waited = !*s_abort && mbar_wait(&bar_s[sb], sph);
             // pair-uniform (both warps of the lane quarter meet at their named barrier below)
             if (!pair_all(pair_bar, waited)) {
                 if (!*s_abort && lane == 0) raise_error(err, kDevErrTimeout);
@@ -308,7 +342,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const bool chose = live && ((umask[j] >> tk) & 1u);
             // S(j) is complete: order every TMEM access below after the MMA that wrote it
             tc_fence_after();
-            const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
+            const uint32_t tS = tmem + sb * BS + lane_off;
             // both warps of the pair see the same tokens, so they take the same branch
             if (__any_sync(0xffffffffu, chose)) {
                 const int blk = ublk[j];
@@ -345,8 +379,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     m_run = mb;
                 }
                 if (__any_sync(0xffffffffu, rescale)) {
-                    // O must hold PV(j-1) before it is rescaled (PV(j-2) is known to be done)
-                    if (j >= 1 && !mbar_wait(bar_o, (j - 1) & 1)) {
+                    // O must hold PV(j-1) before it is rescaled (S(j) was issued after PV(j-3)
+                    // completed, so the parity wait is exact; PV(j-1) done implies PV(j-2) done)
+                    if (j >= 1 && !mbar_wait(&bar_o[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
                         raise_error(err, kDevErrTimeout);
                         *s_abort = 1;
                     }
@@ -412,6 +447,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             tc_fence_before();
             mbar_arrive(&bar_p[j & 1]);
+            if (++sb == kTcKStages) {
+                sb = 0;
+                sph ^= 1u;
+            }
         }
         // ---- epilogue: O / l -> bf16, lse
         psum[h * 128 + r] = l_run;
@@ -425,11 +464,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (lse != nullptr && h == 0) lse[(static_cast<size_t>(b) * Hq + hq) * Tq + t0 + tk] = -INFINITY;
         }
         if (go) {
-            // A warp that skipped the last blocks may get here while PV(U-2) is still pending (only
-            // PV(U-3) is sure to be done), and a parity wait is only exact one phase ahead: wait
-            // for PV(U-2) first, then PV(U-1).
-            bool done = U < 2 || mbar_wait(bar_o, (U - 2) & 1);
-            done = done && mbar_wait(bar_o, (U - 1) & 1);
+            // S(U-1) was committed after PV(U-3), so only PV(U-2) and PV(U-1) can be pending, one
+            // phase each on their barriers.
+            bool done = U < 2 || mbar_wait(&bar_o[(U - 2) & 1], ((U - 2) >> 1) & 1);
+            done = done && mbar_wait(&bar_o[(U - 1) & 1], ((U - 1) >> 1) & 1);
             if (!__all_sync(0xffffffffu, done)) {
                 if (lane == 0) raise_error(err, kDevErrTimeout);
                 *s_abort = 1;

@@ -189,3 +189,22 @@ def test_prefill_group16_dense_without_selection(cuda_lib):
     assert L.sync_status() == 0
     o_ref, _ = oracle.attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["kv_len"], None, None, w.params())
     check_output(bf16_to_f64(o), o_ref)
+
+
+@pytest.mark.parametrize("bs", [128, 64])
+def test_prefill_group16_short_unions(cuda_lib, bs):
+    # a chunk that starts an empty cache: tiles see unions of 1, 2, 3 ... blocks, the shortest
+    # pipelines of the tensor-core path (fewer blocks than S buffers and K stages)
+    w = synth.WORKLOADS["chunked_prefill_32k"].scaled(B=1, L=300, Tq=300, Hq=16, Hkv=1, d=128, block_size=bs,
+                                                       topk=2, n_init=1, n_local=1, dense_len=0, seed=3950 + bs)
+    inp = synth.make_inputs(w)
+    p = w.params()
+    g = run_gpu(w, inp, pool_split=0, params=p)
+    kern_ref, _ = oracle.kernel_pool(inp["k_cache"], inp["kv_len"], 32, 16, n_kernels(w))
+    S = oracle.block_scores(inp["q"], kern_ref, inp["kv_len"], w.Hkv, p)
+    oidx, ocnt, kth, _ = oracle.select(S, inp["kv_len"], w.Tq, p, S_max=g["S_cap"])
+    gidx, gcnt = g["idx"].cpu().numpy(), g["counts"].cpu().numpy()
+    assert compare_selection(gidx, gcnt, oidx, ocnt, S, kth)[3] == 0
+    o_ref, lse_ref = oracle.attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["kv_len"], gidx, gcnt, p)
+    check_output(bf16_to_f64(g["o"]), o_ref)
+    assert np.max(np.abs(g["lse"].cpu().numpy() - lse_ref)) < 2e-3
