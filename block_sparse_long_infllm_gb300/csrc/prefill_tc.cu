@@ -8,10 +8,11 @@
 //   * Load warp (warp 9, one lane): TMA loads of Q (once) and of each block's K and V into
 //     three-stage (K) and two-stage (V) rings of 128-byte-swizzled shared tiles; a stage is
 //     reloaded once the MMA that read it has completed.
-//   * MMA warp (warp 8, one lane): the tcgen05 MMAs, S = Q K^T into one of three TMEM buffers
-//     (M=128, N=block_size, K=d), and O += P V with P read from TMEM (A operand) and V from
-//     shared memory (MN-major B).  An MMA issue holds the issuing thread for about the MMA's
-//     own duration, so this thread does nothing else.
+//   * Two MMA warps (one lane each) issue the tcgen05 MMAs: warp 8 S = Q K^T into one of three
+//     TMEM buffers (M=128, N=block_size, K=d), warp 10 O += P V with P read from TMEM (A operand)
+//     and V from shared memory (MN-major B).  An MMA issue holds the issuing thread for about
+//     the MMA's own duration; with two issuers, one thread's barrier waits overlap the other's
+//     MMAs and the tensor core is not left idle while a wait resolves.
 //   * Softmax warps (warps 0-7; two warps per row, each with half of the key columns): S from
 //     TMEM; causal mask on the query's own block; online max/sum in fp32 (the pair combines its
 //     row maxima through shared memory); the running max is raised only when it grows by more
@@ -34,7 +35,7 @@ namespace infllmv2 {
 constexpr int kTcTokens = 8;   // tokens per tile: 8 x 16 heads = 128 rows
 constexpr int kTcRows = 128;
 constexpr int kTcKStages = 3;  // K tiles in flight; stage j % 3 also names the TMEM S buffer of block j
-constexpr int kTcThreads = 320;  // 8 softmax warps (two per TMEM lane quarter), MMA warp, load warp
+constexpr int kTcThreads = 352;  // 8 softmax warps (two per TMEM lane quarter), S-MMA, load, PV-MMA warps
 
 template <int D, int BS>
 struct TcSmem {
@@ -43,9 +44,9 @@ struct TcSmem {
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQ;                    // kTcKStages stages
     static constexpr int kVOff = kQ + kTcKStages * kKV;  // 2 stages
-    static constexpr int kBarOff = kVOff + 2 * kKV;      // q, k[3], v[2], s[3], o[2], p[2], fin  (14 x 8 B)
-    static constexpr int kMiscOff = kBarOff + 128; // tmem base, abort flag, union size
-    static constexpr int kPairOff = kBarOff + 128 + 64;  // [2][128] partial maxima, [2][128] partial sums
+    static constexpr int kBarOff = kVOff + 2 * kKV;      // q, k[3], v[2], s[3], o[3], p[3], fin[2]  (17 x 8 B)
+    static constexpr int kMiscOff = kBarOff + 256; // tmem base, abort flag, union size
+    static constexpr int kPairOff = kBarOff + 256 + 64;  // [2][128] partial maxima, [2][128] partial sums
     static constexpr int kUnionOff2 = kPairOff + 4 * 128 * 4;
     static int bytes(int max_union, int nwords) { return kUnionOff2 + 8 * max_union + 8 * nwords + 1024; }
 };
@@ -101,10 +102,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint64_t* bar_q = reinterpret_cast<uint64_t*>(base + SM::kBarOff);
     uint64_t* bar_k = bar_q + 1;  // [3] K block landed
     uint64_t* bar_v = bar_q + 4;  // [2] V block landed
-    uint64_t* bar_s = bar_q + 6;    // [3] S = Q K^T done (buffer j % 3)
-    uint64_t* bar_o = bar_q + 9;    // [2] O += P V done (block j on j & 1)
-    uint64_t* bar_p = bar_q + 11;   // [2] P written by all 256 softmax threads
-    uint64_t* bar_fin = bar_q + 13; //     every MMA issued has completed
+    // Rings indexed by block j: K, S, O and P on j % 3 (completed phase parity (j / 3) & 1), V on
+    // j & 1.  Each next completion of a barrier needs a step that its waiter has not yet allowed,
+    // so no parity wait below can fall two phases behind.
+    uint64_t* bar_s = bar_q + 6;    // [3] S(j) = Q K^T done
+    uint64_t* bar_o = bar_q + 9;    // [3] O += P(j) V(j) done
+    uint64_t* bar_p = bar_q + 12;   // [3] P(j) written by all 256 softmax threads
+    uint64_t* bar_fin = bar_q + 15; // [2] every MMA of the S / PV issuer has completed
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(base + SM::kMiscOff);
     volatile int* s_abort = reinterpret_cast<volatile int*>(base + SM::kMiscOff + 4);
     int* s_U = reinterpret_cast<int*>(base + SM::kMiscOff + 8);
@@ -130,13 +134,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int i = 0; i < kTcKStages; ++i) {
             mbar_init(&bar_k[i], 1);
             mbar_init(&bar_s[i], 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar_v[i], 1);
             mbar_init(&bar_o[i], 1);
             mbar_init(&bar_p[i], 256);
         }
-        mbar_init(bar_fin, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_v[i], 1);
+            mbar_init(&bar_fin[i], 1);
+        }
         fence_mbar_init();
         *s_abort = 0;
     }
@@ -231,17 +235,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 for (int sub = 0; sub < D / 64; ++sub)
                     tma_load_2d(base + SM::kQOff + sub * (kTcRows * 128) + tk * (G * 128), &tm_q, 64 * sub, qrow, bar_q);
             }
-            // the MMA thread consumes K(0), K(1), then per block j: V(j), K(j+2)
-            for (int j = 0; j < 2 && j < U; ++j) load(j, false);
+            for (int j = 0; j < kTcKStages && j < U; ++j) load(j, false);
             for (int i = 0; i < U; ++i) {
-                if (i + 2 < U) {  // K stage (i+2) % 3 held K(i-1): free once S(i-1) is done
-                    if (i >= 1 && !tc_wait(&bar_s[(i - 1) % kTcKStages], ((i - 1) / kTcKStages) & 1, s_abort, err))
-                        break;
-                    load(i + 2, false);
-                }
                 // V stage i & 1 held V(i-2): free once PV(i-2) is done
-                if (i >= 2 && !tc_wait(&bar_o[(i - 2) & 1], ((i - 2) >> 1) & 1, s_abort, err)) break;
+                if (i >= 2 && !tc_wait(&bar_o[(i - 2) % kTcKStages], ((i - 2) / kTcKStages) & 1, s_abort, err)) break;
                 load(i, true);
+                // K stage i % 3 held K(i): free once S(i) is done
+                if (i + kTcKStages < U) {
+                    if (!tc_wait(&bar_s[i % kTcKStages], (i / kTcKStages) & 1, s_abort, err)) break;
+                    load(i + kTcKStages, false);
+                }
             }
             // drain: every copy issued has landed before shared memory goes away (only the last
             // load of a stage can be pending: each earlier one was consumed by a completed MMA)
@@ -252,14 +255,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (v_issued[st] > 0) mbar_wait(&bar_v[st], (v_issued[st] - 1) & 1, drain);
         }
     } else if (warp == 8) {
-        // ======================= MMA warp: tcgen05 issue (one lane)
+        // ======================= S issuer (one lane): S(j) into TMEM buffer j % 3 from K stage j % 3
         if (lane == 0 && U > 0) {
             const uint32_t sQ = smem_u32(base + SM::kQOff);
-            bool mma_issued = false;
-            auto wait = [&](uint64_t* bar, uint32_t parity) -> bool { return tc_wait(bar, parity, s_abort, err); };
-            // S(j) into TMEM buffer j % 3 from K stage j % 3
-            auto issue_s = [&](int j) {
+            bool issued = false;
+            bool ok = tc_wait(bar_q, 0, s_abort, err);
+            for (int j = 0; ok && j < U; ++j) {
                 const int st = j % kTcKStages;
+                // buffer j % 3 held P(j-3): free once PV(j-3) is done
+                if (j >= kTcKStages && !(ok = tc_wait(&bar_o[st], ((j - kTcKStages) / kTcKStages) & 1, s_abort, err)))
+                    break;
+                if (!(ok = tc_wait(&bar_k[st], (j / kTcKStages) & 1, s_abort, err))) break;
+                tc_fence_after();
                 const uint32_t kb = smem_u32(base + SM::kKOff + st * SM::kKV);
                 const uint32_t dS = tmem + st * BS;
 #pragma unroll
@@ -269,11 +276,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     mma_ss(dS, sw128_desc(sQ + qo, 16, 1024), sw128_desc(kb + ko, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&bar_s[st]);
-                mma_issued = true;
-            };
-            auto issue_pv = [&](int j) {
+                issued = true;
+            }
+            if (issued) {  // one commit covers every MMA this thread issued
+                mma_commit(&bar_fin[0]);
+                mbar_wait(&bar_fin[0], 0, kWaitBudgetCycles / 8);
+            }
+        }
+    } else if (warp == 10) {
+        // ======================= PV issuer (one lane): O += P(j) V(j), P in TMEM buffer j % 3
+        if (lane == 0 && U > 0) {
+            bool issued = false;
+            bool ok = true;
+            for (int j = 0; ok && j < U; ++j) {
+                const int st = j % kTcKStages;
+                if (!(ok = tc_wait(&bar_p[st], (j / kTcKStages) & 1, s_abort, err))) break;
+                if (!(ok = tc_wait(&bar_v[j & 1], (j >> 1) & 1, s_abort, err))) break;
+                tc_fence_after();
                 const uint32_t vb = smem_u32(base + SM::kVOff + (j & 1) * SM::kKV);
-                const uint32_t aP = tmem + (j % kTcKStages) * BS;
+                const uint32_t aP = tmem + st * BS;
 #pragma unroll
                 for (int kk = 0; kk < BS / 16; ++kk) {
                     // B = V (keys x d, d contiguous): 16 keys per step = 2 groups of 8 rows; the
@@ -281,32 +302,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     const uint64_t bdesc = sw128_desc(vb + kk * 16 * 128, BS * 128, 1024);
                     mma_ts(tO, aP + kk * 8, bdesc, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(&bar_o[j & 1]);
-            };
-            bool ok = wait(bar_q, 0);
-            for (int j = 0; ok && j < 2 && j < U; ++j) {
-                if (!(ok = wait(&bar_k[j], 0))) break;
-                tc_fence_after();
-                issue_s(j);
+                mma_commit(&bar_o[st]);
+                issued = true;
             }
-            // Iteration j: PV(j) once P(j) is written, then S(j+2) into the buffer PV(j-1) has
-            // released.  All parity waits below are at most one phase ahead of their barrier.
-            for (int j = 0; ok && j < U; ++j) {
-                if (!(ok = wait(&bar_p[j & 1], (j >> 1) & 1))) break;
-                if (!(ok = wait(&bar_v[j & 1], (j >> 1) & 1))) break;
-                tc_fence_after();
-                issue_pv(j);
-                if (j + 2 < U) {
-                    if (j >= 1 && !(ok = wait(&bar_o[(j - 1) & 1], ((j - 1) >> 1) & 1))) break;
-                    const int ks = (j + 2) % kTcKStages;
-                    if (!(ok = wait(&bar_k[ks], ((j + 2) / kTcKStages) & 1))) break;
-                    tc_fence_after();
-                    issue_s(j + 2);
-                }
-            }
-            if (mma_issued) {  // one commit covers every MMA this thread issued
-                mma_commit(bar_fin);
-                mbar_wait(bar_fin, 0, kWaitBudgetCycles / 8);
+            if (issued) {
+                mma_commit(&bar_fin[1]);
+                mbar_wait(&bar_fin[1], 0, kWaitBudgetCycles / 8);
             }
         }
     } else {
@@ -379,9 +380,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     m_run = mb;
                 }
                 if (__any_sync(0xffffffffu, rescale)) {
-                    // O must hold PV(j-1) before it is rescaled (S(j) was issued after PV(j-3)
-                    // completed, so the parity wait is exact; PV(j-1) done implies PV(j-2) done)
-                    if (j >= 1 && !mbar_wait(&bar_o[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
+                    // O must hold PV(j-1) before it is rescaled (PV(j-1) done implies PV(j-2) done:
+                    // one issuer, one accumulator)
+                    if (j >= 1 && !mbar_wait(&bar_o[(j - 1) % kTcKStages], ((j - 1) / kTcKStages) & 1)) {
                         raise_error(err, kDevErrTimeout);
                         *s_abort = 1;
                     }
@@ -446,7 +447,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tmem_st_wait();
             }
             tc_fence_before();
-            mbar_arrive(&bar_p[j & 1]);
+            mbar_arrive(&bar_p[sb]);
             if (++sb == kTcKStages) {
                 sb = 0;
                 sph ^= 1u;
@@ -464,10 +465,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (lse != nullptr && h == 0) lse[(static_cast<size_t>(b) * Hq + hq) * Tq + t0 + tk] = -INFINITY;
         }
         if (go) {
-            // S(U-1) was committed after PV(U-3), so only PV(U-2) and PV(U-1) can be pending, one
-            // phase each on their barriers.
-            bool done = U < 2 || mbar_wait(&bar_o[(U - 2) & 1], ((U - 2) >> 1) & 1);
-            done = done && mbar_wait(&bar_o[(U - 1) & 1], ((U - 1) >> 1) & 1);
+            // PV(U-1) done implies every earlier PV done; S(U-1) was issued after PV(U-4)
+            // completed, so the barrier of PV(U-1) is at most one phase behind.
+            const bool done = mbar_wait(&bar_o[(U - 1) % kTcKStages], ((U - 1) / kTcKStages) & 1);
             if (!__all_sync(0xffffffffu, done)) {
                 if (lane == 0) raise_error(err, kDevErrTimeout);
                 *s_abort = 1;
