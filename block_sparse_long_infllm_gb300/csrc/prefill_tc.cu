@@ -67,6 +67,34 @@ __device__ __forceinline__ bool pair_all(int id, bool v) {
     return r != 0;
 }
 
+// Three-input maximum and paired fp32 arithmetic (one instruction for two lanes of data).
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(__float_as_uint(lo)), "r"(__float_as_uint(hi)));
+    return d;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t v, float& lo, float& hi) {
+    uint32_t a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(a), "=r"(b) : "l"(v));
+    lo = __uint_as_float(a);
+    hi = __uint_as_float(b);
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // Bounded wait of the load and MMA threads: gives up when another thread has raised the abort
 // flag, or sets it (and the device error word) when the budget runs out.
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
@@ -330,41 +358,60 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         bool ok = true;
         int sb = 0;               // S buffer of block j: j % 3, completed phase parity (j / 3) & 1
         uint32_t sph = 0;
-        for (int j = 0; j < U; ++j) {
-            // warp-uniform: the TMEM loads and stores below are warp-collective
-            const bool waited = !*s_abort && mbar_wait(&bar_s[sb], sph);
-            // pair-uniform (both warps of the lane quarter meet at their named barrier below)
+        // S(j) is loaded from TMEM one step ahead: the load of block j+1 is issued before this
+        // warp waits for its P(j) stores, so the two latencies overlap.  Both warps of a pair
+        // see the same tokens, so they take the same branches and meet at the same barriers.
+        uint32_t ra[32], rb[32];
+        auto chooses = [&](int jj) -> bool {  // warp-uniform: does any row of this warp attend block jj?
+            return __any_sync(0xffffffffu, live && ((umask[jj] >> tk) & 1u));
+        };
+        auto load_s = [&](int sbuf) {
+            const uint32_t tS = tmem + sbuf * BS + lane_off + h * HB;
+            tmem_ld32(tS, ra);
+            if constexpr (HB == 64) tmem_ld32(tS + 32, rb);
+        };
+        if (U > 0) {
+            const bool waited = !*s_abort && mbar_wait(&bar_s[0], 0);
             if (!pair_all(pair_bar, waited)) {
                 if (!*s_abort && lane == 0) raise_error(err, kDevErrTimeout);
                 *s_abort = 1;
                 ok = false;
-                break;
+            } else if (chooses(0)) {
+                tc_fence_after();
+                load_s(0);
             }
+        }
+        for (int j = 0; ok && j < U; ++j) {
             const bool chose = live && ((umask[j] >> tk) & 1u);
-            // S(j) is complete: order every TMEM access below after the MMA that wrote it
-            tc_fence_after();
             const uint32_t tS = tmem + sb * BS + lane_off;
-            // both warps of the pair see the same tokens, so they take the same branch
+            const int sb1 = sb + 1 == kTcKStages ? 0 : sb + 1;
+            const uint32_t sph1 = sb1 == 0 ? sph ^ 1u : sph;
             if (__any_sync(0xffffffffu, chose)) {
-                const int blk = ublk[j];
-                // valid keys of this row: x = blk*BS + c <= pos (only the query's own block is partial)
-                const int n_valid = chose ? min(BS, pos - blk * BS + 1) - h * HB : 0;
-                float sv[HB];
+                // S(j) of this half, in place in the load registers (column c in ra / rb)
+                tmem_ld_wait(ra);
+                if constexpr (HB == 64) reg_fence(rb);
+                auto sv = [&](int c) -> float { return __uint_as_float(c < 32 ? ra[c] : rb[c - 32]); };
+                // valid keys of a row that chose the block: x = blk*BS + c <= pos (only the
+                // query's own block is partial); rows that did not choose it get p = 0 below
+                const int n_valid = min(BS, pos - ublk[j] * BS + 1) - h * HB;
+                if (__any_sync(0xffffffffu, chose && n_valid < HB)) {
 #pragma unroll
-                for (int c0 = 0; c0 < HB; c0 += 32) {
-                    uint32_t rr[32];
-                    tmem_ld32(tS + h * HB + c0, rr);
-                    tmem_ld_wait(rr);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) sv[c0 + e] = __uint_as_float(rr[e]);
+                    for (int c = 0; c < HB; ++c) {
+                        uint32_t& x = c < 32 ? ra[c] : rb[c - 32];
+                        x = c < n_valid ? x : __float_as_uint(-INFINITY);
+                    }
                 }
-                if (n_valid < HB) {
+                // row maximum of this half: eight independent chains of three-input maxima
+                float mc[8];
 #pragma unroll
-                    for (int c = 0; c < HB; ++c) sv[c] = c < n_valid ? sv[c] : -INFINITY;
-                }
-                float mh = -INFINITY;
+                for (int k = 0; k < 8; ++k) mc[k] = sv(k);
 #pragma unroll
-                for (int c = 0; c < HB; c += 2) mh = fmaxf(mh, fmaxf(sv[c], sv[c + 1]));
+                for (int c = 8; c + 16 <= HB; c += 16)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mc[k] = fmax3f(mc[k], sv(c + k), sv(c + 8 + k));
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mc[k] = fmaxf(mc[k], sv(HB - 8 + k));
+                const float mh = fmax3f(fmax3f(mc[0], mc[1], mc[2]), fmax3f(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
                 pmax[h * 128 + r] = mh;
                 asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
                 const float mb = fmaxf(mh, pmax[(1 - h) * 128 + r]);
@@ -399,59 +446,65 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     }
                     tmem_st_wait();
                 }
-                // p = 2^((s - m) * scale_log2) as one FFMA and one EX2
-                const float neg = m_run == -INFINITY ? 0.f : -m_run * scale_log2;
-                float lsum0 = 0.f, lsum1 = 0.f;
-                if constexpr (HB >= 64) {
+                // p = 2^((s - m) * scale_log2): one paired FFMA per two columns, one EX2 each
+                // (-inf offset for rows that did not choose the block: p = 0); the row sum runs
+                // in four paired accumulators (eight independent chains)
+                const float neg = !chose ? -INFINITY : (m_run == -INFINITY ? 0.f : -m_run * scale_log2);
+                const uint64_t sc2 = f32x2(scale_log2, scale_log2), ng2 = f32x2(neg, neg);
+                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-                    for (int c0 = 0; c0 < HB; c0 += 64) {
-                        uint32_t pw[32];
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const float p0 = fast_exp2(fmaf(sv[c0 + 2 * e], scale_log2, neg));
-                            const float p1 = fast_exp2(fmaf(sv[c0 + 2 * e + 1], scale_log2, neg));
-                            lsum0 += p0;
-                            lsum1 += p1;
-                            pw[e] = pack_bf16x2(p0, p1);
-                        }
-                        tmem_st32(tS + (h * HB + c0) / 2, pw);
-                    }
-                } else {
+                for (int c0 = 0; c0 < HB; c0 += 32) {  // 32 columns -> 16 packed P words per store
                     uint32_t pw[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        const float p0 = fast_exp2(fmaf(sv[2 * e], scale_log2, neg));
-                        const float p1 = fast_exp2(fmaf(sv[2 * e + 1], scale_log2, neg));
-                        lsum0 += p0;
-                        lsum1 += p1;
+                        float x0, x1;
+                        f32x2_split(ffma2(f32x2(sv(c0 + 2 * e), sv(c0 + 2 * e + 1)), sc2, ng2), x0, x1);
+                        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                        acc[e & 3] = fadd2(acc[e & 3], f32x2(p0, p1));
                         pw[e] = pack_bf16x2(p0, p1);
                     }
-                    tmem_st16(tS + h * HB / 2, pw);
+                    tmem_st16(tS + (h * HB + c0) / 2, pw);
                 }
-                if (chose) l_run += lsum0 + lsum1;
-                tmem_st_wait();
+                if (chose) {
+                    float a0, a1, b0, b1;
+                    f32x2_split(fadd2(acc[0], acc[1]), a0, a1);
+                    f32x2_split(fadd2(acc[2], acc[3]), b0, b1);
+                    l_run += (a0 + b0) + (a1 + b1);
+                }
             } else {
                 // no row of this warp chose the block: its P columns are zero (nothing else to do)
-                if constexpr (HB >= 64) {
-                    uint32_t z[32];
+                uint32_t z[16];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) z[e] = 0u;
+                for (int e = 0; e < 16; ++e) z[e] = 0u;
 #pragma unroll
-                    for (int c0 = 0; c0 < HB; c0 += 64) tmem_st32(tS + (h * HB + c0) / 2, z);
-                } else {
-                    uint32_t z[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) z[e] = 0u;
-                    tmem_st16(tS + h * HB / 2, z);
-                }
-                tmem_st_wait();
+                for (int c0 = 0; c0 < HB; c0 += 32) tmem_st16(tS + (h * HB + c0) / 2, z);
             }
+            // S(j+1): if it is already complete, start its load before the wait for the P stores
+            const bool more = j + 1 < U;
+            const bool next = more && chooses(j + 1);
+            const bool ready = more && mbar_test_wait(&bar_s[sb1], sph1);
+            if (ready && next) {
+                tc_fence_after();
+                load_s(sb1);
+            }
+            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bar_p[sb]);
-            if (++sb == kTcKStages) {
-                sb = 0;
-                sph ^= 1u;
+            if (more) {
+                const bool waited = ready || (!*s_abort && mbar_wait(&bar_s[sb1], sph1));
+                if (!pair_all(pair_bar, waited)) {
+                    if (!*s_abort && lane == 0) raise_error(err, kDevErrTimeout);
+                    *s_abort = 1;
+                    ok = false;
+                    break;
+                }
+                if (!ready && next) {
+                    tc_fence_after();
+                    load_s(sb1);
+                }
             }
+            sb = sb1;
+            sph = sph1;
         }
         // ---- epilogue: O / l -> bf16, lse
         psum[h * 128 + r] = l_run;
