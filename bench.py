@@ -338,10 +338,18 @@ def run_decode(args, world, rank):
 
     alg = decode_algorithmic_bytes(d)
     pk = peaks()
-    dom = max(("score", "attend"), key=lambda s: stage_ms.get(s, 0.0))
-    achieved = alg[dom] / (stage_ms[dom] * 1e-3) / 1e9
-    kernel_names = {"score": "score_decode_kernel", "attend": "decode_split_kernel"}
-    sha = source_sha("select.cu" if dom == "score" else "decode.cu", "attn_warp.cuh", "common.cuh", "tma.cuh")
+    fused = "fused" in stage_ms
+    if fused:  # one cooperative kernel per step: scores, selection, attention and merge
+        dom = "fused"
+        achieved = alg["total"] / (stage_ms[dom] * 1e-3) / 1e9
+        alg = dict(alg, fused=alg["total"])
+        src = "decode_cluster.cu"
+    else:
+        dom = max(("score", "attend"), key=lambda s: stage_ms.get(s, 0.0))
+        achieved = alg[dom] / (stage_ms[dom] * 1e-3) / 1e9
+        src = "select.cu" if dom == "score" else "decode.cu"
+    kernel_names = {"score": "score_decode_kernel", "attend": "decode_split_kernel", "fused": "decode_cluster_kernel"}
+    sha = source_sha(src, "attn_warp.cuh", "common.cuh", "tma.cuh")
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": ncu_traffic(kernel_names[dom], sha),
                 "kernel": kernel_names[dom], "algorithmic_bytes": alg[dom], "peak_source": pk["source"],
@@ -358,9 +366,10 @@ def run_decode(args, world, rank):
                        "parallelism": f"replicas x{world}",
                        "l2": f"inputs larger than L2: {R} replicas of Q, K/V and kernel caches cycled step by step "
                              f"({R} x {alg['total'] / 1e6:.1f} MB touched per cycle)",
-                       "launch": f"CUDA graph of {R} steps, replayed; kernels chained with programmatic dependent launch",
+                       "launch": (f"CUDA graph of {R} steps, replayed; one cluster kernel per step (one 16-CTA cluster per row)" if fused else
+                                  f"CUDA graph of {R} steps, replayed; kernels chained with programmatic dependent launch"),
                        "kernel_cache": "resident (pooled before timing)"},
-               roofline=roofline, clocks=clk, gpu_launches=4 * K, device_status=status)
+               roofline=roofline, clocks=clk, gpu_launches=(1 if fused else 4) * K, device_status=status)
     out["value"] = world * w.B * w.Tq * K / (total_ms * 1e-3)
     out["step"] = {"algorithmic_bytes": alg["total"], "kernel_cache_bytes": alg["kernel_cache"],
                    "selected_kv_bytes": alg["selected_kv"], "achieved_gbs": round(step_alg_gbs, 1),

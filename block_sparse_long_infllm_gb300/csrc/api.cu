@@ -334,12 +334,20 @@ int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache, con
     int* counts = counts_out != nullptr ? counts_out : reinterpret_cast<int*>(ws + w.counts);
     const int stride = idx_out != nullptr ? S_max : S_cap;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    infllmv2::SelectArgs sa{q, kernel_cache, kv_len, B, n_draft, Hq, Hkv, d, L_max, M_max, tree ? 1 : 0, idx, counts,
-                            stride, blocks_per_score_cta(p), p, err, st};
-    prof_begin(st);
-    if (int rc = cuda_status(infllmv2::launch_block_select(sa, reinterpret_cast<float*>(ws + w.scores)))) return rc;
     infllmv2::DecodeArgs da{q, k_cache, v_cache, kv_len, draft_k, draft_v, tree_mask, B, n_draft, Hq, Hkv, d, L_max,
                             o, lse, p, err, st};
+    prof_begin(st);
+    if (infllmv2::decode_cluster_supported(da, M_max)) {
+        const cudaError_t e = infllmv2::launch_decode_cluster(da, kernel_cache, M_max, idx_out, S_max, counts_out);
+        if (e != cudaErrorNotSupported) {
+            prof_mark(st, "fused");
+            return cuda_status(e);
+        }
+        (void)cudaGetLastError();  // not launched: take the separate kernels
+    }
+    infllmv2::SelectArgs sa{q, kernel_cache, kv_len, B, n_draft, Hq, Hkv, d, L_max, M_max, tree ? 1 : 0, idx, counts,
+                            stride, blocks_per_score_cta(p), p, err, st};
+    if (int rc = cuda_status(infllmv2::launch_block_select(sa, reinterpret_cast<float*>(ws + w.scores)))) return rc;
     return cuda_status(
         infllmv2::launch_decode_attention(da, idx, counts, stride, reinterpret_cast<float*>(ws + w.part)));
 }

@@ -18,6 +18,13 @@
 
 namespace infllmv2 {
 
+// One split's fp32 partial of a decode row: running maxima m[16] (log2 domain), row sums l[16]
+// and unnormalised outputs o[16][D] for the (up to 16) heads of the row.
+template <int D>
+struct PartialLayout {
+    static constexpr int kFloats = 16 + 16 + 16 * D;
+};
+
 template <int D>
 struct QFrag {
     uint32_t a[D / 16][4];

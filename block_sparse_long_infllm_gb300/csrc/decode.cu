@@ -20,11 +20,6 @@
 
 namespace infllmv2 {
 
-template <int D>
-struct PartialLayout {
-    static constexpr int kFloats = 16 + 16 + 16 * D;  // m[16], l[16], o[16][D]
-};
-
 template <int D, int BS, int BPS>
 struct SplitSmem {
     static constexpr int kTile = BS * D * 2;                         // one block of K (or V)

@@ -86,4 +86,12 @@ size_t decode_partial_bytes(int B, int n_draft, int Hkv, int d, int n_split);
 cudaError_t launch_decode_attention(const DecodeArgs& a, const int* idx, const int* counts, int idx_stride,
                                     float* part);
 
+// Single-token decode (no draft tree) with one thread-block cluster per row: scores, selection,
+// attention and merge, every intermediate in shared memory.  cudaErrorNotSupported when the
+// shape or the device is outside what it covers (the caller then runs the separate selection
+// and attention kernels).  idx_out / counts_out may be null.
+bool decode_cluster_supported(const DecodeArgs& a, int M_max);
+cudaError_t launch_decode_cluster(const DecodeArgs& a, const void* kernel_cache, int M_max, int* idx_out,
+                                  int idx_stride, int* counts_out);
+
 }  // namespace infllmv2

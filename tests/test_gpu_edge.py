@@ -208,3 +208,41 @@ def test_prefill_group16_short_unions(cuda_lib, bs):
     o_ref, lse_ref = oracle.attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["kv_len"], gidx, gcnt, p)
     check_output(bf16_to_f64(g["o"]), o_ref)
     assert np.max(np.abs(g["lse"].cpu().numpy() - lse_ref)) < 2e-3
+
+
+@pytest.mark.parametrize("bs", [64, 128])
+def test_decode_tied_scores_take_lowest_blocks(cuda_lib, bs):
+    # every semantic kernel equal (zero): all candidate blocks tie, so the selection is the
+    # forced blocks plus the lowest-numbered candidates, exactly
+    torch = pytest.importorskip("torch")
+    L = lib()
+    w = BASE.scaled(B=2, L=20000, block_size=bs, topk=16, dense_len=0, seed=3960 + bs)
+    inp = synth.make_inputs(w)
+    inp["kv_len"] = np.array([20000, 13001], dtype=np.int32)
+    p = w.params()
+    q, k, v, kv = (to_dev(inp[x]) for x in ("q", "k_cache", "v_cache", "kv_len"))
+    M = max(n_kernels(w), 1)
+    kern = torch.zeros((w.B, w.Hkv, M, w.d), dtype=torch.bfloat16, device="cuda")
+    S_cap = L.selection_capacity(p, w.L_max)
+    idx = torch.empty((w.B, w.Hkv, 1, S_cap), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((w.B, w.Hkv, 1), dtype=torch.int32, device="cuda")
+    ws = torch.empty(L.workspace_size(L.ENTRY_DECODE, w.B, 1, w.Hq, w.Hkv, w.d, w.L_max, p),
+                     dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, 1), dtype=torch.float32, device="cuda")
+    L.decode(q, k, v, kern, kv, o, ws, p, lse=lse, idx_out=idx, counts_out=cnt)
+    torch.cuda.synchronize()
+    assert L.sync_status() == 0
+    kern_ref = np.zeros((w.B, w.Hkv, M, w.d), dtype=np.uint16)
+    S = oracle.block_scores(inp["q"], kern_ref, inp["kv_len"], w.Hkv, p,
+                            nblk_max=(w.L_max - 1) // w.block_size + 1)
+    oidx, ocnt, _, _ = oracle.select(S, inp["kv_len"], 1, p, S_max=S_cap)
+    gidx, gcnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    assert np.array_equal(gcnt, ocnt)
+    for b in range(w.B):
+        for g in range(w.Hkv):
+            n = int(ocnt[b, g, 0])
+            assert sorted(gidx[b, g, 0, :n].tolist()) == sorted(oidx[b, g, 0, :n].tolist())
+    o_ref, lse_ref = oracle.attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["kv_len"], gidx, gcnt, p)
+    check_output(bf16_to_f64(o), o_ref)
+    assert np.max(np.abs(lse.cpu().numpy() - lse_ref)) < 2e-3
