@@ -26,6 +26,7 @@
 
 #include "attn_warp.cuh"
 #include "internal.h"
+#include "umma.cuh"
 
 namespace infllmv2 {
 
@@ -34,6 +35,7 @@ constexpr int kDcKRows = 768;     // kernel rows of one scoring pass (6 TMA boxe
 constexpr int kDcMaxSel = 4096;   // selection capacity covered (the list lives in shared memory)
 constexpr int kDcMaxPer = 16;     // keys per thread in the selection: rows of up to 4096 blocks
 constexpr int kDcCand = 384;      // candidates ranked exactly after the pre-threshold
+constexpr int kDcFastPer = 8;     // strided keys per thread on the fast selection path (<= 2048 blocks)
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -80,11 +82,13 @@ struct ClusterSmem {
     static constexpr int kMerge = (8 * 16 * 2 + 8 * 16 * (D + 4)) * 4;
     static constexpr int kPartial = (32 + 16 * D) * 4;         // m[16], l[16], o[16][D]
     static_assert(kMerge <= kX, "merge scratch fits the tile memory");
-    // offsets from the 1024-aligned base: tiles | keys[nblk_max] | ks | partial | sel[S_cap] | barriers
-    __host__ __device__ static int off_keys() { return kX; }
-    __host__ __device__ static int off_ks(int nblk_max) { return kX + ((4 * nblk_max + 15) & ~15); }
-    __host__ __device__ static int off_p(int nblk_max) { return off_ks(nblk_max) + 4 * kDcKRows; }
-    __host__ __device__ static int off_sel(int nblk_max) { return off_p(nblk_max) + kPartial; }
+    // offsets from the 1024-aligned base: tiles | partial (the Q tile while scoring) | keys[nblk_max]
+    // | ks | sel[S_cap] | barriers
+    static_assert(kPartial >= (D / 64) * 16 * 128, "the Q tile fits the partial");
+    __host__ __device__ static int off_p() { return kX; }
+    __host__ __device__ static int off_keys() { return kX + ((kPartial + 15) & ~15); }
+    __host__ __device__ static int off_ks(int nblk_max) { return off_keys() + ((4 * nblk_max + 15) & ~15); }
+    __host__ __device__ static int off_sel(int nblk_max) { return off_ks(nblk_max) + 4 * kDcKRows; }
     __host__ __device__ static int off_bar(int nblk_max, int S_cap) { return (off_sel(nblk_max) + 4 * S_cap + 15) & ~15; }
     static int bytes(int nblk_max, int S_cap) { return off_bar(nblk_max, S_cap) + 8 * (1 + kPB) + 1024; }
 };
@@ -92,7 +96,8 @@ struct ClusterSmem {
 template <int D, int BS>
 __global__ void __launch_bounds__(kDcThreads, 1)
 decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16* __restrict__ q,
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q,
+                      const __nv_bfloat16* __restrict__ q,
                       const int* __restrict__ kv_len, int Hq, int Hkv, int G, int L_max, int M_max, Params p,
                       ClusterShape sh, int* __restrict__ idx_out, int idx_stride, int* __restrict__ counts_out,
                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse, float scale_log2,
@@ -107,7 +112,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                                                            ~static_cast<uintptr_t>(1023));
     uint32_t* keys = reinterpret_cast<uint32_t*>(base + SM::off_keys());           // [nblk_max], filled by all CTAs
     float* ks = reinterpret_cast<float*>(base + SM::off_ks(sh.nblk_max));           // [kDcKRows]
-    float* part = reinterpret_cast<float*>(base + SM::off_p(sh.nblk_max));          // m, l, o
+    float* part = reinterpret_cast<float*>(base + SM::off_p());                     // m, l, o
     int* sel = reinterpret_cast<int*>(base + SM::off_sel(sh.nblk_max));             // [S_cap]
     uint64_t* bar_a = reinterpret_cast<uint64_t*>(base + SM::off_bar(sh.nblk_max, sh.S_cap));
     uint64_t* bar_b = bar_a + 1;  // [PB]
@@ -115,9 +120,11 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     __shared__ int s_cnt[3][4];
     __shared__ float s_w[32];
     __shared__ float s_f[8][16];  // merge weights of the 8 warps per row
-    __shared__ __align__(16) uint32_t s_mx[kDcThreads];   // per-thread maxima of the candidate keys
     __shared__ unsigned long long s_cv[kDcCand];          // candidates >= tau: key << 32 | ~block
-    __shared__ uint32_t s_tau, s_T;
+    __shared__ int s_rk[kDcCand];                          // their ranks
+    __shared__ uint64_t s_bar_piece[kDcKRows / 128];       // scoring: kernel rows of piece p landed
+    __shared__ uint64_t s_bar_mma[2], s_bar_free[2];       // scoring accumulator buffers: written / read
+    __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, cq = lane & 3;
@@ -131,34 +138,62 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
         prefetch_tmap(&tm_kern);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_q);
         mbar_init(bar_a, 1);
         for (int k = 0; k < PB; ++k) mbar_init(&bar_b[k], 1);
+        for (int k = 0; k < kDcKRows / 128; ++k) mbar_init(&s_bar_piece[k], 1);
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(&s_bar_mma[k], 1);
+            mbar_init(&s_bar_free[k], 128);
+        }
         fence_mbar_init();
     }
+    if (warp == 0) {  // scoring accumulators: 2 x 16 TMEM columns (kernel row x head, fp32)
+        tmem_alloc(&s_tmem, 32);
+        tmem_relinquish();
+    }
     if (tid < 12) (&s_cnt[0][0])[tid] = 0;
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
 
     // ================= 1. scores of this CTA's blocks, pushed as keys to every CTA
+    // Thread 128 (warp 4) issues the TMA copies (Q once, then 128-row pieces of kernel rows) and,
+    // per piece, the tcgen05 MMAs S[kernel row][head] = K_kernel Q^T (M=128, N=16, K=d) into one of
+    // two TMEM buffers; warps 0-3 read each piece back (one kernel row per thread) and keep the
+    // maximum over the G heads.  A piece is scored as soon as it lands.
+    constexpr int kPieces = kDcKRows / 128;
+    constexpr uint32_t kIdesc = idesc_bf16_f32(128, 16, 0, 0);
     const int blkA0 = static_cast<int>(rank) * sh.CB;
     const int blkA1 = min(blkA0 + sh.CB, sh.nblk_max);
-    uint32_t ph_a = 0;
-    auto issue_scoring = [&](int sub0) {
-        // kernel rows of blocks [sub0, sub0 + SC) for the longest cache
+    const bool issuer = tid == 128;
+    const uint32_t sQ = smem_u32(part);
+    uint32_t piece_uses = 0;  // issuer: bit p = phase parity of s_bar_piece[p]
+    int gi = 0;               // scoring MMA groups so far (issuer and readers count alike)
+    auto pass_rows = [&](int sub0, int& jlo, int& jend) {
         const int sub1 = min(sub0 + sh.SC, blkA1);
-        const int jlo = first_kernel_of_block(sub0, BS, c, s);
-        const int jend = min(last_kernel_of_block(sub1 - 1, BS, s), M_max - 1);
-        const int nrows = jend - jlo + 1;
-        if (nrows > 0) {
-            const int pieces = (nrows + 127) / 128;
-            mbar_arrive_expect_tx(bar_a, pieces * (D / 64) * 128 * 128);
+        jlo = first_kernel_of_block(sub0, BS, c, s);
+        jend = min(last_kernel_of_block(sub1 - 1, BS, s), M_max - 1);
+        return jend - jlo + 1;
+    };
+    auto issue_pass = [&](int sub0) {  // kernel rows of blocks [sub0, sub0 + SC) for the longest cache
+        int jlo, jend;
+        const int nrows = pass_rows(sub0, jlo, jend);
+        for (int pc = 0; pc * 128 < nrows; ++pc) {
+            mbar_arrive_expect_tx(&s_bar_piece[pc], (D / 64) * 128 * 128);
             for (int half = 0; half < D / 64; ++half)
-                for (int pc = 0; pc < pieces; ++pc)
-                    tma_load_2d(base + half * (kDcKRows * 128) + pc * (128 * 128), &tm_kern, 64 * half,
-                                row * M_max + jlo + pc * 128, bar_a);
+                tma_load_2d(base + half * (kDcKRows * 128) + pc * (128 * 128), &tm_kern, 64 * half,
+                            row * M_max + jlo + pc * 128, &s_bar_piece[pc]);
         }
     };
-    if (tid == 0 && blkA0 < blkA1) issue_scoring(blkA0);
-    // Q fragments: rows = heads (rows >= G read as zero); kept for the attention
+    if (issuer) {
+        mbar_arrive_expect_tx(bar_a, (D / 64) * 16 * 128);
+        for (int half = 0; half < D / 64; ++half)
+            tma_load_2d(part + half * (16 * 128 / 4), &tm_q, 64 * half, b * Hq + g * G, bar_a);
+        if (blkA0 < blkA1) issue_pass(blkA0);
+    }
+    // Q fragments: rows = heads (rows >= G read as zero), for the attention
     QFrag<D> Q;
     load_q(Q, q + (static_cast<size_t>(b) * Hq + static_cast<size_t>(g) * G) * D, D, G);
     const int L = kv_len[b];
@@ -167,64 +202,69 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     const bool dense = L < p.dense_len;
     auto forced = [&](int blk) { return blk < p.n_init || blk > bt - p.n_local; };
     const uint32_t keys_base = smem_u32(keys);
+    bool q_landed = false;
     for (int sub0 = blkA0; sub0 < blkA1; sub0 += sh.SC) {
+        int jlo, jend;
+        const int nrows = pass_rows(sub0, jlo, jend);
         const int sub1 = min(sub0 + sh.SC, blkA1);
-        const int jlo = first_kernel_of_block(sub0, BS, c, s);
-        const int jend = min(last_kernel_of_block(sub1 - 1, BS, s), M_max - 1);
-        const int nrows = jend - jlo + 1;
         const bool work = len_ok && !dense && sub0 <= bt && nrows > 0;
         const int bz = min(sub1, bt + 1);  // blocks [sub0, bz) are scored
         const int jhi = work ? min(min(last_kernel_of_block(bz - 1, BS, s), kernels_in(L, c, s) - 1), jend) : -1;
-        bool landed = true;
-        if (nrows > 0) {
-            landed = mbar_wait(bar_a, ph_a);
-            ph_a ^= 1u;
-            if (!landed && tid == 0) raise_error(err, kDevErrTimeout);
-        }
-        if (work && landed) {
-            const uint32_t kb = smem_u32(base);
-            const int n_tiles = jhi >= jlo ? (jhi - jlo + 8) / 8 : 0;
-            // four n-tiles of 8 kernels per warp at a time: independent MMA chains
-            for (int nt0 = warp; nt0 < n_tiles; nt0 += 4 * (kDcThreads / 32)) {
-                float acc[4][4];
+        const int nj = work ? jhi - jlo + 1 : 0;  // visible kernel rows of the pass
+        const int n_issued = nrows > 0 ? (nrows + 127) / 128 : 0;
+        const int n_mma = nj > 0 ? (nj + 127) / 128 : 0;
+        if (issuer) {
+            bool ok = true;
+            if (n_mma > 0 && !q_landed) {
+                ok = mbar_wait(bar_a, 0);
+                q_landed = true;
+            }
+            for (int pc = 0; pc < n_issued; ++pc) {
+                // every issued piece must land before its tiles are reused, scored or not
+                const bool landed = mbar_wait(&s_bar_piece[pc], (piece_uses >> pc) & 1u);
+                ok = ok && landed;
+                piece_uses ^= 1u << pc;
+                if (pc >= n_mma) continue;
+                const int buf = (gi + pc) & 1;
+                if (gi + pc >= 2) ok = ok && mbar_wait(&s_bar_free[buf], ((gi + pc - 2) >> 1) & 1);
+                if (ok) {
+                    tc_fence_after();
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[u][e] = 0.f;
-#pragma unroll
-                for (int i = 0; i < D / 32; ++i) {
-                    const int col = 32 * i + 8 * cq;
-                    const uint32_t cb = kb + (col / 64) * (kDcKRows * 128);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int nt = nt0 + u * (kDcThreads / 32);
-                        if (nt < n_tiles) {
-                            const uint4 w = lds_v4(cb + swz128(nt * 8 + gq, (col % 64) / 8));
-                            mma_16816(acc[u], Q.a[2 * i], w.x, w.y);
-                            mma_16816(acc[u], Q.a[2 * i + 1], w.z, w.w);
-                        }
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ko = (kk / 4) * (kDcKRows * 128) + (kk % 4) * 32;
+                        const uint32_t qo = (kk / 4) * (16 * 128) + (kk % 4) * 32;
+                        mma_ss(tmem + 16 * buf, sw128_desc(smem_u32(base) + pc * (128 * 128) + ko, 16, 1024),
+                               sw128_desc(sQ + qo, 16, 1024), kIdesc, kk > 0 ? 1u : 0u);
                     }
                 }
+                mma_commit(&s_bar_mma[buf]);  // also when not issued: the readers' waits stay in step
+            }
+            if (!ok) raise_error(err, kDevErrTimeout);
+        } else if (warp < 4) {
+            for (int pc = 0; pc < n_mma; ++pc) {
+                const int buf = (gi + pc) & 1;
+                const bool got = mbar_wait(&s_bar_mma[buf], ((gi + pc) >> 1) & 1);
+                tc_fence_after();
+                uint32_t v[16];
+                tmem_ld16(tmem + 16 * buf + (static_cast<uint32_t>(32 * warp) << 16), v);
+                tmem_ld_wait16(v);
+                tc_fence_before();
+                mbar_arrive(&s_bar_free[buf]);
+                const int r = pc * 128 + 32 * warp + lane;  // kernel row jlo + r
+                if (got && r < nj) {
+                    float m = -INFINITY;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int nt = nt0 + u * (kDcThreads / 32);
-                    if (nt >= n_tiles) break;
-                    if (gq >= G) acc[u][0] = acc[u][1] = -INFINITY;
-                    if (gq + 8 >= G) acc[u][2] = acc[u][3] = -INFINITY;
-                    float v0 = fmaxf(acc[u][0], acc[u][2]), v1 = fmaxf(acc[u][1], acc[u][3]);
-#pragma unroll
-                    for (int m = 4; m < 32; m <<= 1) {
-                        v0 = fmaxf(v0, __shfl_xor_sync(0xffffffffu, v0, m));
-                        v1 = fmaxf(v1, __shfl_xor_sync(0xffffffffu, v1, m));
-                    }
-                    if (gq == 0) {
-                        const int j0 = nt * 8 + 2 * cq;  // relative to jlo
-                        if (jlo + j0 <= jhi) ks[j0] = v0;
-                        if (jlo + j0 + 1 <= jhi) ks[j0 + 1] = v1;
-                    }
+                    for (int h = 0; h < 16; ++h)
+                        if (h < G) m = fmaxf(m, __uint_as_float(v[h]));
+                    ks[r] = m;
+                } else if (!got && lane == 0) {
+                    raise_error(err, kDevErrTimeout);
                 }
             }
-            __syncthreads();
+        }
+        gi += n_mma;
+        __syncthreads();
+        if (work) {
             // block score = max over its visible kernels; its selection key goes to every CTA
             for (int blk = sub0 + tid; blk < bz; blk += kDcThreads) {
                 const int ja = max(first_kernel_of_block(blk, BS, c, s), jlo);
@@ -237,7 +277,14 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
             }
         }
         __syncthreads();  // tiles and ks free for the next pass
-        if (tid == 0 && sub0 + sh.SC < blkA1) issue_scoring(sub0 + sh.SC);
+        if (issuer && sub0 + sh.SC < blkA1) issue_pass(sub0 + sh.SC);
+    }
+    if (issuer && !q_landed) mbar_wait(bar_a, 0);  // the Q copy has landed before its tile is reused
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 32);
     }
     cluster_sync();
 
@@ -251,112 +298,30 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
         const int nc = n - n_forced;
         const bool take_all = len_ok && (dense || nc <= p.topk);
         const bool select = len_ok && !take_all && p.topk > 0;
-        // thread t holds the keys of blocks [t*per, t*per + per)
         const int nn = max(n, 0);
-        const int per = (nn + kDcThreads - 1) / kDcThreads;
-        const int i0 = min(tid * per, nn), i1 = min(i0 + per, nn);
-        uint32_t kr[kDcMaxPer];
-#pragma unroll
-        for (int u = 0; u < kDcMaxPer; ++u) kr[u] = select && i0 + u < i1 ? keys[i0 + u] : 0u;
-        uint32_t T = 0;
-        int krem = 0;
-        bool searched = false;
-        if (select) {
-            // Pre-threshold tau: the k-th largest of the threads' maxima over the strided keys
-            // t, t + 256, ... (neighbouring blocks have correlated scores, so a stride spreads
-            // each thread over the row).  At least k keys are >= tau, and unless the scores are
-            // heavily tied only a few more; those candidates are ranked exactly (key descending,
-            // block ascending, one 64-bit compare) and the k-th one is T.
+        const int lo_f = max(lo_local, a_init);  // first local block not already an initial one
+        int total = 0;
+        bool done = false;
+        if (select && nn <= kDcFastPer * kDcThreads && p.topk <= kDcThreads) {
+            // Fast path.  tau = the k-th largest of the threads' maxima over the strided keys
+            // t, t + 256, ... (neighbouring blocks have correlated scores: a stride spreads each
+            // thread over the row), found bit by bit from block-wide predicate counts.  At least
+            // k keys are >= tau and, unless the scores are heavily tied, only a few more; those
+            // candidates are ranked exactly (key descending, block ascending, one 64-bit
+            // compare), and the list is the initial blocks, the k best candidates in block order
+            // and the local blocks.
             const int k = p.topk;
-            uint32_t ks_[kDcMaxPer];
+            uint32_t kv[kDcFastPer];
             uint32_t mx = 0u;
 #pragma unroll
-            for (int u = 0; u < kDcMaxPer; ++u) {
+            for (int u = 0; u < kDcFastPer; ++u) {
                 const int i = tid + u * kDcThreads;
-                ks_[u] = i < nn ? keys[i] : 0u;
-                mx = max(mx, ks_[u]);
+                kv[u] = i < nn ? keys[i] : 0u;
+                mx = max(mx, kv[u]);
             }
-            s_mx[tid] = mx;
-            if (tid == 0) s_tau = 0u;
-            __syncthreads();
-            if (k <= kDcThreads && mx != 0u) {
-                int r = 0, e = 0;
-                const uint4* v4 = reinterpret_cast<const uint4*>(s_mx);
-#pragma unroll 8
-                for (int j = 0; j < kDcThreads / 4; ++j) {
-                    const uint4 v = v4[j];
-                    r += (v.x > mx) + (v.y > mx) + (v.z > mx) + (v.w > mx);
-                    e += (v.x == mx) + (v.y == mx) + (v.z == mx) + (v.w == mx);
-                }
-                if (r < k && r + e >= k) s_tau = mx;  // every writer writes the same value
-            }
-            __syncthreads();
-            const uint32_t tau = s_tau;
-            int nc_t = 0;
-            if (tau != 0u)
-#pragma unroll
-                for (int u = 0; u < kDcMaxPer; ++u) nc_t += ks_[u] >= tau ? 1 : 0;
-            int incl = nc_t;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int x = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += x;
-            }
-            if (lane == 31) s_wsum[0][warp] = incl;
-            __syncthreads();
-            int c_before = incl - nc_t, c_total = 0;
-#pragma unroll
-            for (int w = 0; w < kDcThreads / 32; ++w) {
-                if (w < warp) c_before += s_wsum[0][w];
-                c_total += s_wsum[0][w];
-            }
-            if (tau != 0u && c_total <= kDcCand) {
-                // candidate value: key in the high word, complemented block in the low word, so
-                // a larger value is a better block
-#pragma unroll
-                for (int u = 0; u < kDcMaxPer; ++u)
-                    if (tau != 0u && ks_[u] >= tau) {
-                        s_cv[c_before++] = (static_cast<unsigned long long>(ks_[u]) << 32) |
-                                           static_cast<uint32_t>(~(tid + u * kDcThreads));
-                    }
-                __syncthreads();
-                for (int i = tid; i < c_total; i += kDcThreads) {
-                    const unsigned long long vi = s_cv[i];
-                    int rnk = 0;
-#pragma unroll 4
-                    for (int j = 0; j < c_total; ++j) rnk += s_cv[j] > vi ? 1 : 0;
-                    if (rnk == k - 1) s_T = static_cast<uint32_t>(vi >> 32);  // exactly one has rank k - 1
-                }
-                __syncthreads();
-                T = s_T;
-                int above = 0;
-#pragma unroll
-                for (int u = 0; u < kDcMaxPer; ++u) above += kr[u] > T ? 1 : 0;
-                above = __reduce_add_sync(0xffffffffu, above);
-                __syncthreads();  // s_wsum reuse
-                if (lane == 0) s_wsum[1][warp] = above;
-                __syncthreads();
-                int tot = 0;
-#pragma unroll
-                for (int w = 0; w < kDcThreads / 32; ++w) tot += s_wsum[1][w];
-                krem = k - tot;
-                searched = true;
-            }
-            __syncthreads();
-        }
-        if (select && !searched) {
-            uint32_t k_and = ~0u, k_or = 0u;
-#pragma unroll
-            for (int u = 0; u < kDcMaxPer; ++u)
-                if (kr[u] != 0u) {
-                    k_and &= kr[u];
-                    k_or |= kr[u];
-                }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                k_and &= __shfl_xor_sync(0xffffffffu, k_and, off);
-                k_or |= __shfl_xor_sync(0xffffffffu, k_or, off);
-            }
+            const int nz = __syncthreads_count(mx != 0u);
+            uint32_t k_and = __reduce_and_sync(0xffffffffu, mx != 0u ? mx : ~0u);
+            uint32_t k_or = __reduce_or_sync(0xffffffffu, mx);
             if (lane == 0) {
                 s_wsum[0][warp] = static_cast<int>(k_and);
                 s_wsum[1][warp] = static_cast<int>(k_or);
@@ -369,124 +334,223 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                 k_and &= static_cast<uint32_t>(s_wsum[0][w]);
                 k_or |= static_cast<uint32_t>(s_wsum[1][w]);
             }
-            // bits above the highest one where candidate keys differ are common to all; below
-            // it the k-th largest key is decided two bits per round from the counts of keys >=
-            // three trial values (warp reductions, shared atomics, one barrier; the counters of
-            // round r+1, last read in round r-2, are cleared in round r)
-            const uint32_t diff = k_and ^ k_or;
-            int bit = diff == 0u ? -1 : 31 - __clz(diff);
-            T = bit >= 31 ? 0u : (k_and & (~0u << (bit + 1)));
-            const int k = p.topk;
-            int buf = 0;
-            while (bit >= 0) {
-                const int nb = bit >= 1 ? 2 : 1;
-                const int lo = bit - nb + 1;
-                uint32_t tr[3];
-                int cn[3] = {0, 0, 0};
+            if (nz >= k) {
+                const uint32_t diff = k_and ^ k_or;
+                int bit = diff == 0u ? -1 : 31 - __clz(diff);
+                uint32_t tau = bit >= 31 ? 0u : (k_and & (~0u << (bit + 1)));
+                for (; bit >= 0; --bit) {
+                    const uint32_t trial = tau | (1u << bit);
+                    const int cnt = __syncthreads_count(mx >= trial);
+                    if (cnt >= k) tau = trial;
+                    if (cnt == k) break;
+                }
+                int nc_t = 0;
 #pragma unroll
-                for (int u = 0; u < 3; ++u) tr[u] = T | (static_cast<uint32_t>(u + 1) << lo);
+                for (int u = 0; u < kDcFastPer; ++u) nc_t += (kv[u] != 0u && kv[u] >= tau) ? 1 : 0;
+                int incl = nc_t;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int x = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += x;
+                }
+                __syncthreads();  // s_wsum reuse
+                if (lane == 31) s_wsum[0][warp] = incl;
+                __syncthreads();
+                int c_before = incl - nc_t, c_total = 0;
+#pragma unroll
+                for (int w = 0; w < kDcThreads / 32; ++w) {
+                    if (w < warp) c_before += s_wsum[0][w];
+                    c_total += s_wsum[0][w];
+                }
+                if (c_total <= kDcCand) {
+                    // candidate value: key in the high word, complemented block in the low word,
+                    // so that a larger value is a better block
+#pragma unroll
+                    for (int u = 0; u < kDcFastPer; ++u)
+                        if (kv[u] != 0u && kv[u] >= tau)
+                            s_cv[c_before++] = (static_cast<unsigned long long>(kv[u]) << 32) |
+                                               static_cast<uint32_t>(~(tid + u * kDcThreads));
+                    __syncthreads();
+                    for (int i = tid; i < c_total; i += kDcThreads) {
+                        const unsigned long long vi = s_cv[i];
+                        int rnk = 0;
+#pragma unroll 4
+                        for (int j = 0; j < c_total; ++j) rnk += s_cv[j] > vi ? 1 : 0;
+                        s_rk[i] = rnk;
+                    }
+                    __syncthreads();
+                    for (int i = tid; i < c_total; i += kDcThreads) {
+                        if (s_rk[i] >= k) continue;
+                        const uint32_t bi = ~static_cast<uint32_t>(s_cv[i]);
+                        int before = 0;
+#pragma unroll 4
+                        for (int j = 0; j < c_total; ++j)
+                            before += (s_rk[j] < k && ~static_cast<uint32_t>(s_cv[j]) < bi) ? 1 : 0;
+                        sel[a_init + before] = static_cast<int>(bi);
+                    }
+                    for (int i = tid; i < a_init; i += kDcThreads) sel[i] = i;
+                    for (int i = tid; i < nn - lo_f; i += kDcThreads) sel[a_init + k + i] = lo_f + i;
+                    total = a_init + k + (nn - lo_f);
+                    done = true;
+                }
+            }
+            __syncthreads();
+        }
+        if (!done) {
+            // General path: thread t holds the keys of blocks [t*per, t*per + per); the k-th
+            // largest key T is decided two bits per round from block-wide counts; the list is
+            // compacted in block order.
+            const int per = (nn + kDcThreads - 1) / kDcThreads;
+            const int i0 = min(tid * per, nn), i1 = min(i0 + per, nn);
+            uint32_t kr[kDcMaxPer];
+#pragma unroll
+            for (int u = 0; u < kDcMaxPer; ++u) kr[u] = select && i0 + u < i1 ? keys[i0 + u] : 0u;
+            uint32_t T = 0;
+            int krem = 0;
+            if (select) {
+                uint32_t k_and = ~0u, k_or = 0u;
 #pragma unroll
                 for (int u = 0; u < kDcMaxPer; ++u)
+                    if (kr[u] != 0u) {
+                        k_and &= kr[u];
+                        k_or |= kr[u];
+                    }
 #pragma unroll
-                    for (int v = 0; v < 3; ++v) cn[v] += kr[u] >= tr[v] ? 1 : 0;
-#pragma unroll
-                for (int v = 0; v < 3; ++v) cn[v] = __reduce_add_sync(0xffffffffu, cn[v]);
-                if (lane == 0)
-#pragma unroll
-                    for (int v = 0; v < 3; ++v) atomicAdd(&s_cnt[buf][v], cn[v]);
-                if (tid < 3) s_cnt[(buf + 1) % 3][tid] = 0;
+                for (int off = 16; off > 0; off >>= 1) {
+                    k_and &= __shfl_xor_sync(0xffffffffu, k_and, off);
+                    k_or |= __shfl_xor_sync(0xffffffffu, k_or, off);
+                }
+                if (lane == 0) {
+                    s_wsum[0][warp] = static_cast<int>(k_and);
+                    s_wsum[1][warp] = static_cast<int>(k_or);
+                }
                 __syncthreads();
-                int pick = -1;
-                for (int v = (nb == 2 ? 2 : 0); v >= 0; --v)
-                    if (s_cnt[buf][v] >= k) {
-                        pick = v;
-                        break;
-                    }
-                const bool exact = pick >= 0 && s_cnt[buf][pick] == k;
-                if (pick >= 0) T = tr[pick];
-                bit -= nb;
-                buf = (buf + 1) % 3;
-                if (exact) break;  // exactly k keys clear T: no ties to break
-            }
-            // keys above T are taken, and of the keys equal to T the lowest blocks
-            int above = 0;
+                k_and = ~0u;
+                k_or = 0u;
 #pragma unroll
-            for (int u = 0; u < kDcMaxPer; ++u) above += kr[u] > T ? 1 : 0;
-            above = __reduce_add_sync(0xffffffffu, above);
-            if (lane == 0) atomicAdd(&s_cnt[buf][3], above);  // slot 3: zero since the start
+                for (int w = 0; w < kDcThreads / 32; ++w) {
+                    k_and &= static_cast<uint32_t>(s_wsum[0][w]);
+                    k_or |= static_cast<uint32_t>(s_wsum[1][w]);
+                }
+                // bits above the highest one where candidate keys differ are common to all; below
+                // it the k-th largest key is decided two bits per round from the counts of keys >=
+                // three trial values (warp reductions, shared atomics, one barrier; the counters of
+                // round r+1, last read in round r-2, are cleared in round r)
+                const uint32_t diff = k_and ^ k_or;
+                int bit = diff == 0u ? -1 : 31 - __clz(diff);
+                T = bit >= 31 ? 0u : (k_and & (~0u << (bit + 1)));
+                const int k = p.topk;
+                int buf = 0;
+                while (bit >= 0) {
+                    const int nb = bit >= 1 ? 2 : 1;
+                    const int lo = bit - nb + 1;
+                    uint32_t tr[3];
+                    int cn[3] = {0, 0, 0};
+#pragma unroll
+                    for (int u = 0; u < 3; ++u) tr[u] = T | (static_cast<uint32_t>(u + 1) << lo);
+#pragma unroll
+                    for (int u = 0; u < kDcMaxPer; ++u)
+#pragma unroll
+                        for (int v = 0; v < 3; ++v) cn[v] += kr[u] >= tr[v] ? 1 : 0;
+#pragma unroll
+                    for (int v = 0; v < 3; ++v) cn[v] = __reduce_add_sync(0xffffffffu, cn[v]);
+                    if (lane == 0)
+#pragma unroll
+                        for (int v = 0; v < 3; ++v) atomicAdd(&s_cnt[buf][v], cn[v]);
+                    if (tid < 3) s_cnt[(buf + 1) % 3][tid] = 0;
+                    __syncthreads();
+                    int pick = -1;
+                    for (int v = (nb == 2 ? 2 : 0); v >= 0; --v)
+                        if (s_cnt[buf][v] >= k) {
+                            pick = v;
+                            break;
+                        }
+                    const bool exact = pick >= 0 && s_cnt[buf][pick] == k;
+                    if (pick >= 0) T = tr[pick];
+                    bit -= nb;
+                    buf = (buf + 1) % 3;
+                    if (exact) break;  // exactly k keys clear T: no ties to break
+                }
+                // keys above T are taken, and of the keys equal to T the lowest blocks
+                int above = 0;
+#pragma unroll
+                for (int u = 0; u < kDcMaxPer; ++u) above += kr[u] > T ? 1 : 0;
+                above = __reduce_add_sync(0xffffffffu, above);
+                if (lane == 0) atomicAdd(&s_cnt[buf][3], above);  // slot 3: zero since the start
+                __syncthreads();
+                krem = k - s_cnt[buf][3];
+            }
+            // ---- ascending compaction: forced, keys above T, the first krem keys equal to T
+            int n_sel = 0, n_tie = 0;
+            if (len_ok) {
+                if (!select) {
+                    for (int i = i0; i < i1; ++i) n_sel += (take_all || forced(i)) ? 1 : 0;
+                } else {
+#pragma unroll
+                    for (int u = 0; u < kDcMaxPer; ++u) {
+                        if (i0 + u >= i1) break;
+                        if (forced(i0 + u)) {
+                            ++n_sel;
+                        } else {
+                            n_sel += kr[u] > T;
+                            n_tie += kr[u] == T;
+                        }
+                    }
+                }
+            }
+            int sel_incl = n_sel, tie_incl = n_tie;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int x = __shfl_up_sync(0xffffffffu, sel_incl, off);
+                const int y = __shfl_up_sync(0xffffffffu, tie_incl, off);
+                if (lane >= off) {
+                    sel_incl += x;
+                    tie_incl += y;
+                }
+            }
+            __syncthreads();  // s_wsum reuse
+            if (lane == 31) {
+                s_wsum[0][warp] = sel_incl;
+                s_wsum[1][warp] = tie_incl;
+            }
             __syncthreads();
-            krem = k - s_cnt[buf][3];
-        }
-        // ---- ascending compaction: forced, keys above T, the first krem keys equal to T
-        int n_sel = 0, n_tie = 0;
-        if (len_ok) {
-            if (!select) {
-                for (int i = i0; i < i1; ++i) n_sel += (take_all || forced(i)) ? 1 : 0;
-            } else {
+            int sel_before = sel_incl - n_sel, tie_before = tie_incl - n_tie, sel_total = 0, tie_total = 0;
 #pragma unroll
-                for (int u = 0; u < kDcMaxPer; ++u) {
-                    if (i0 + u >= i1) break;
-                    if (forced(i0 + u)) {
-                        ++n_sel;
-                    } else {
-                        n_sel += kr[u] > T;
-                        n_tie += kr[u] == T;
+            for (int w = 0; w < kDcThreads / 32; ++w) {
+                if (w < warp) {
+                    sel_before += s_wsum[0][w];
+                    tie_before += s_wsum[1][w];
+                }
+                sel_total += s_wsum[0][w];
+                tie_total += s_wsum[1][w];
+            }
+            int pos = sel_before + min(tie_before, krem);
+            int tie_rank = tie_before;
+            if (len_ok) {
+                if (!select) {
+                    for (int i = i0; i < i1; ++i)
+                        if (take_all || forced(i)) {
+                            if (pos < sh.S_cap) sel[pos] = i;
+                            ++pos;
+                        }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < kDcMaxPer; ++u) {
+                        if (i0 + u >= i1) break;
+                        bool pick = forced(i0 + u) || kr[u] > T;
+                        if (!pick && kr[u] == T) {
+                            pick = tie_rank < krem;
+                            ++tie_rank;
+                        }
+                        if (pick) {
+                            if (pos < sh.S_cap) sel[pos] = i0 + u;
+                            ++pos;
+                        }
                     }
                 }
             }
+            total = sel_total + min(tie_total, krem);
         }
-        int sel_incl = n_sel, tie_incl = n_tie;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int x = __shfl_up_sync(0xffffffffu, sel_incl, off);
-            const int y = __shfl_up_sync(0xffffffffu, tie_incl, off);
-            if (lane >= off) {
-                sel_incl += x;
-                tie_incl += y;
-            }
-        }
-        __syncthreads();  // s_wsum reuse
-        if (lane == 31) {
-            s_wsum[0][warp] = sel_incl;
-            s_wsum[1][warp] = tie_incl;
-        }
-        __syncthreads();
-        int sel_before = sel_incl - n_sel, tie_before = tie_incl - n_tie, sel_total = 0, tie_total = 0;
-#pragma unroll
-        for (int w = 0; w < kDcThreads / 32; ++w) {
-            if (w < warp) {
-                sel_before += s_wsum[0][w];
-                tie_before += s_wsum[1][w];
-            }
-            sel_total += s_wsum[0][w];
-            tie_total += s_wsum[1][w];
-        }
-        int pos = sel_before + min(tie_before, krem);
-        int tie_rank = tie_before;
-        if (len_ok) {
-            if (!select) {
-                for (int i = i0; i < i1; ++i)
-                    if (take_all || forced(i)) {
-                        if (pos < sh.S_cap) sel[pos] = i;
-                        ++pos;
-                    }
-            } else {
-#pragma unroll
-                for (int u = 0; u < kDcMaxPer; ++u) {
-                    if (i0 + u >= i1) break;
-                    bool pick = forced(i0 + u) || kr[u] > T;
-                    if (!pick && kr[u] == T) {
-                        pick = tie_rank < krem;
-                        ++tie_rank;
-                    }
-                    if (pick) {
-                        if (pos < sh.S_cap) sel[pos] = i0 + u;
-                        ++pos;
-                    }
-                }
-            }
-        }
-        const int total = sel_total + min(tie_total, krem);
         count = min(total, sh.S_cap);
         __syncthreads();  // sel complete
         if (rank == 0) {
@@ -701,16 +765,17 @@ static cudaError_t launch_cluster_t(const DecodeArgs& a, const void* kernel_cach
     sh.CB = (sh.nblk_max + CL - 1) / CL;
     attr[0].val.clusterDim.x = CL;
     cfg.gridDim = dim3(rows * CL);
-    CUtensorMap tkern, tk, tv;
+    CUtensorMap tkern, tk, tv, tq;
     const uint64_t krows = static_cast<uint64_t>(a.B) * a.Hkv * M_max;
     const uint64_t cache_rows = static_cast<uint64_t>(a.B) * a.Hkv * a.L_max;
     if (!make_tmap_bf16_2d(&tkern, kernel_cache, D, krows, 64, 128) ||
         !make_tmap_bf16_2d(&tk, a.k_cache, D, cache_rows, 64, BS) ||
-        !make_tmap_bf16_2d(&tv, a.v_cache, D, cache_rows, 64, BS))
+        !make_tmap_bf16_2d(&tv, a.v_cache, D, cache_rows, 64, BS) ||
+        !make_tmap_bf16_2d(&tq, a.q, D, static_cast<uint64_t>(a.B) * a.Hq, 64, 16))
         return cudaErrorNotSupported;
     const int G = a.Hq / a.Hkv;
     const float scale_log2 = a.p.scale * 1.4426950408889634f;
-    return cudaLaunchKernelEx(&cfg, kfn, tkern, tk, tv, static_cast<const __nv_bfloat16*>(a.q), a.kv_len, a.Hq, a.Hkv,
+    return cudaLaunchKernelEx(&cfg, kfn, tkern, tk, tv, tq, static_cast<const __nv_bfloat16*>(a.q), a.kv_len, a.Hq, a.Hkv,
                               G, a.L_max, M_max, a.p, sh, idx_out, idx_stride, counts_out,
                               static_cast<__nv_bfloat16*>(a.o), a.lse, scale_log2, a.err);
 }
@@ -721,7 +786,8 @@ bool decode_cluster_supported(const DecodeArgs& a, int M_max) {
     if (a.tree_mask != nullptr || a.n_draft != 1) return false;
     if (G < 1 || G > 16 || (a.d != 64 && a.d != 128) || (bs != 64 && bs != 128)) return false;
     // the tensor maps' boxes must fit the tensors
-    if (static_cast<long long>(a.B) * a.Hkv * M_max < 128 || static_cast<long long>(a.B) * a.Hkv * a.L_max < bs)
+    if (static_cast<long long>(a.B) * a.Hkv * M_max < 128 || static_cast<long long>(a.B) * a.Hkv * a.L_max < bs ||
+        static_cast<long long>(a.B) * a.Hq < 16)
         return false;
     return true;
 }
