@@ -495,7 +495,8 @@ def run_prefill(args) -> dict:
             "keys_per_query": attended / (w.Tq * w.Hq),
             "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": round(att_tf, 2),
                          "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(att_tf / pk["bf16_tflops"], 4),
-                         "traffic": None},
+                         "traffic": ncu_traffic("prefill_tc_kernel",
+                                                source_sha("prefill_tc.cu", "umma.cuh", "common.cuh", "tma.cuh"))},
             "step_tflops": round(step_tf, 2), "step_frac": round(step_tf / pk["bf16_tflops"], 4),
             "gpu_launches": 4 * K}
 
