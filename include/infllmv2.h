@@ -192,6 +192,11 @@ int infllmv2_sparse_attn_fwd(const void* q, const void* k_cache, const void* v_c
  * idx_out [B, Hkv, n_draft, S_max] / counts_out [B, Hkv, n_draft] receive the
  * selection when not NULL (S_max is ignored when idx_out is NULL).
  * Requires ws_bytes >= infllmv2_workspace_size(INFLLMV2_ENTRY_DECODE, ...).
+ * Single-token decode runs as one kernel (one thread-block cluster per
+ * (sequence, KV head) row, every intermediate on chip) when the shape allows
+ * (G <= 16, d in {64, 128}, block 64/128, at most 4096 blocks); trees and
+ * other shapes run separate scoring, top-k, split and merge kernels that use
+ * the workspace.  Results are the same either way.
  */
 int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache,
                     const void* kernel_cache, const int32_t* kv_len, const void* draft_k,
