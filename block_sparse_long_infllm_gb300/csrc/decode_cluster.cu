@@ -122,6 +122,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     __shared__ float s_f[8][16];  // merge weights of the 8 warps per row
     __shared__ unsigned long long s_cv[kDcCand];          // candidates >= tau: key << 32 | ~block
     __shared__ int s_rk[kDcCand];                          // their ranks
+    __shared__ int s_pos[kDcCand];                         // positions of the chosen ones
     __shared__ uint64_t s_bar_piece[kDcKRows / 128];       // scoring: kernel rows of piece p landed
     __shared__ uint64_t s_bar_mma[2], s_bar_free[2];       // scoring accumulator buffers: written / read
     __shared__ uint32_t s_tmem;
@@ -370,24 +371,54 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                         if (kv[u] != 0u && kv[u] >= tau)
                             s_cv[c_before++] = (static_cast<unsigned long long>(kv[u]) << 32) |
                                                static_cast<uint32_t>(~(tid + u * kDcThreads));
+                    for (int i = tid; i < c_total; i += kDcThreads) s_rk[i] = 0;
                     __syncthreads();
-                    for (int i = tid; i < c_total; i += kDcThreads) {
-                        const unsigned long long vi = s_cv[i];
-                        int rnk = 0;
-#pragma unroll 4
-                        for (int j = 0; j < c_total; ++j) rnk += s_cv[j] > vi ? 1 : 0;
-                        s_rk[i] = rnk;
+                    // rank of candidate i = number of better candidates; `sp` threads share each
+                    // candidate, each comparing it with one slice of the others
+                    const int sp = max(1, kDcThreads / c_total);
+                    const int seg = (c_total + sp - 1) / sp;
+                    {
+                        const int i = tid / sp, part = tid % sp;
+                        if (i < c_total) {
+                            const unsigned long long vi = s_cv[i];
+                            const int j1 = min(c_total, (part + 1) * seg);
+                            int rnk = 0;
+                            for (int j = part * seg; j < j1; ++j) rnk += s_cv[j] > vi ? 1 : 0;
+                            if (rnk) atomicAdd(&s_rk[i], rnk);
+                        }
+                        for (int i2 = kDcThreads / sp + tid; i2 < c_total; i2 += kDcThreads) {  // c_total > 256
+                            const unsigned long long vi = s_cv[i2];
+                            int rnk = 0;
+                            for (int j = 0; j < c_total; ++j) rnk += s_cv[j] > vi ? 1 : 0;
+                            atomicAdd(&s_rk[i2], rnk);
+                        }
                     }
                     __syncthreads();
-                    for (int i = tid; i < c_total; i += kDcThreads) {
-                        if (s_rk[i] >= k) continue;
-                        const uint32_t bi = ~static_cast<uint32_t>(s_cv[i]);
-                        int before = 0;
-#pragma unroll 4
-                        for (int j = 0; j < c_total; ++j)
-                            before += (s_rk[j] < k && ~static_cast<uint32_t>(s_cv[j]) < bi) ? 1 : 0;
-                        sel[a_init + before] = static_cast<int>(bi);
+                    // position of a chosen candidate = chosen candidates with a lower block
+                    for (int i = tid; i < c_total; i += kDcThreads) s_pos[i] = 0;
+                    __syncthreads();
+                    {
+                        const int i = tid / sp, part = tid % sp;
+                        if (i < c_total && s_rk[i] < k) {
+                            const uint32_t bi = ~static_cast<uint32_t>(s_cv[i]);
+                            const int j1 = min(c_total, (part + 1) * seg);
+                            int before = 0;
+                            for (int j = part * seg; j < j1; ++j)
+                                before += (s_rk[j] < k && ~static_cast<uint32_t>(s_cv[j]) < bi) ? 1 : 0;
+                            if (before) atomicAdd(&s_pos[i], before);
+                        }
+                        for (int i2 = kDcThreads / sp + tid; i2 < c_total; i2 += kDcThreads) {
+                            if (s_rk[i2] >= k) continue;
+                            const uint32_t bi = ~static_cast<uint32_t>(s_cv[i2]);
+                            int before = 0;
+                            for (int j = 0; j < c_total; ++j)
+                                before += (s_rk[j] < k && ~static_cast<uint32_t>(s_cv[j]) < bi) ? 1 : 0;
+                            atomicAdd(&s_pos[i2], before);
+                        }
                     }
+                    __syncthreads();
+                    for (int i = tid; i < c_total; i += kDcThreads)
+                        if (s_rk[i] < k) sel[a_init + s_pos[i]] = static_cast<int>(~static_cast<uint32_t>(s_cv[i]));
                     for (int i = tid; i < a_init; i += kDcThreads) sel[i] = i;
                     for (int i = tid; i < nn - lo_f; i += kDcThreads) sel[a_init + k + i] = lo_f + i;
                     total = a_init + k + (nn - lo_f);
