@@ -10,9 +10,11 @@
 // The per-(token, kernel) maxima go to shared memory, where the block max over the kernels a
 // block overlaps is taken and written to S[b, g, t, block].  Chunks cover whole blocks (31
 // blocks of 64 tokens or 15 of 128), so no block straddles two chunks.
-//   * producer warp (warp 4, one lane): TMA of the Q tile once and of each chunk's kernel rows
+//   * producer warp (warp 8, one lane): TMA of the Q tile once and of each chunk's kernel rows
 //     into two shared stages; one tcgen05 MMA group per chunk into one of two TMEM buffers;
-//   * epilogue warps (warps 0-3): TMEM -> registers -> maxima -> shared -> S.
+//   * epilogue warps (warps 0-7, two per TMEM lane quarter, one half of the 16 tokens each):
+//     TMEM -> registers (all four loads of a thread in flight before one wait) -> maxima ->
+//     shared -> S.
 // Waits are bounded (device error word + abort flag), TMEM is freed before exit.
 #include <algorithm>
 
@@ -24,7 +26,8 @@ namespace infllmv2 {
 constexpr int kScTokens = 16;            // query tokens per CTA: N = 16 x 16 heads = 256
 constexpr int kScN = kScTokens * 16;
 constexpr int kScM = 128;                // kernels per chunk
-constexpr int kScThreads = 160;
+constexpr int kScThreads = 288;  // 8 epilogue warps + the producer warp
+constexpr int kScEpi = 256;      // epilogue threads
 
 template <int D>
 struct ScSmem {
@@ -37,14 +40,14 @@ struct ScSmem {
     static constexpr int kBytes = kBarOff + 128 + 1024;
 };
 
-// AND of `v` over the 128 epilogue threads (named barrier 1; also synchronises them).
+// AND of `v` over the 256 epilogue threads (named barrier 1; also synchronises them).
 __device__ __forceinline__ bool epilogue_all(bool v) {
     uint32_t r;
     asm volatile(
         "{\n"
         " .reg .pred p, q;\n"
         " setp.ne.u32 q, %1, 0;\n"
-        " bar.red.and.pred p, 1, 128, q;\n"
+        " bar.red.and.pred p, 1, 256, q;\n"
         " selp.u32 %0, 1, 0, p;\n"
         "}\n"
         : "=r"(r)
@@ -68,7 +71,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint64_t* bar_q = reinterpret_cast<uint64_t*>(base + SM::kBarOff);
     uint64_t* bar_k = bar_q + 1;     // [2] kernel chunk landed
     uint64_t* bar_acc = bar_q + 3;   // [2] MMA of a chunk done
-    uint64_t* bar_free = bar_q + 5;  // [2] epilogue done with a TMEM buffer (128 arrivals)
+    uint64_t* bar_free = bar_q + 5;  // [2] epilogue done with a TMEM buffer (256 arrivals)
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_q + 8);
     volatile int* s_abort = reinterpret_cast<volatile int*>(bar_q + 9);
 
@@ -93,7 +96,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_k[i], 1);
             mbar_init(&bar_acc[i], 1);
-            mbar_init(&bar_free[i], 128);
+            mbar_init(&bar_free[i], kScEpi);
         }
         fence_mbar_init();
         *s_abort = 0;
@@ -107,7 +110,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ======================= producer
         if (lane == 0) {
             const uint32_t sQ = smem_u32(base + SM::kQOff);
@@ -167,12 +170,15 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (mma_issued > 0) mbar_wait(&bar_acc[(mma_issued - 1) & 1], ((mma_issued - 1) >> 1) & 1, drain);
         }
     } else {
-        // ======================= epilogue: thread tid owns kernel row tid of each chunk
-        const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+        // ======================= epilogue: thread r = 32*(warp%4) + lane owns kernel row r of each
+        // chunk; warps w and w+4 take tokens 0-7 and 8-15 (TMEM columns 128*(w/4) ...)
+        const int r = 32 * (warp % 4) + lane;
+        const int th = warp / 4;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
         for (int ch = 0; ch < n_chunks; ++ch) {
             const int st = ch & 1;
             const bool waited = !*s_abort && mbar_wait(&bar_acc[st], (ch >> 1) & 1);
-            // all four epilogue warps leave together: they meet at the named barrier below
+            // all eight epilogue warps leave together: they meet at the named barrier below
             if (!epilogue_all(waited)) {
                 if (tid == 0 && !*s_abort) raise_error(err, kDevErrTimeout);
                 *s_abort = 1;
@@ -181,29 +187,46 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc_fence_after();
             const int b0 = ch * blocks_per_chunk;
             const int j0 = first_kernel_of_block(b0, bs, c, s);
-            const int j = j0 + tid;
+            const int j = j0 + r;
             const int jend = j * s + c - 1;  // last token of kernel j
-#pragma unroll 2
-            for (int tp = 0; tp < kScTokens; tp += 2) {
-                uint32_t rr[32];
-                tmem_ld32(tmem + st * kScN + lane_off + tp * G, rr);
-                tmem_ld_wait(rr);
+            {
+                uint32_t ra[32], rb[32], rc[32], rd[32];
+                const uint32_t ta = tmem + st * kScN + lane_off + th * 128;
+                tmem_ld32(ta, ra);
+                tmem_ld32(ta + 32, rb);
+                tmem_ld32(ta + 64, rc);
+                tmem_ld32(ta + 96, rd);
+                tmem_ld_wait(ra);
+                reg_fence(rb);
+                reg_fence(rc);
+                reg_fence(rd);
+                auto head_max = [&](const uint32_t (&v)[32], int u) {
+                    float m = __uint_as_float(v[16 * u]);
+#pragma unroll
+                    for (int h = 1; h < G; ++h) m = fmaxf(m, __uint_as_float(v[16 * u + h]));
+                    return m;
+                };
+                float mx[8];
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                    float m = __uint_as_float(rr[16 * u]);
+                    mx[u] = head_max(ra, u);
+                    mx[2 + u] = head_max(rb, u);
+                    mx[4 + u] = head_max(rc, u);
+                    mx[6 + u] = head_max(rd, u);
+                }
 #pragma unroll
-                    for (int h = 1; h < G; ++h) m = fmaxf(m, __uint_as_float(rr[16 * u + h]));
-                    const int tk = tp + u;
+                for (int u = 0; u < 8; ++u) {
+                    const int tk = th * 8 + u;
                     const int pos = Lb - Tq + t0 + tk;
-                    kmax[tk * kScM + tid] = (tk < n_tok && jend <= pos) ? m : -INFINITY;
+                    kmax[tk * kScM + r] = (tk < n_tok && jend <= pos) ? mx[u] : -INFINITY;
                 }
             }
             tc_fence_before();
             mbar_arrive(&bar_free[st]);  // this thread is done with the TMEM buffer
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            asm volatile("bar.sync 1, 256;" ::: "memory");
             // block max over the kernels each block overlaps, for every token of the tile
             const int nb = min(blocks_per_chunk, bt_max + 1 - b0);
-            for (int e = tid; e < n_tok * nb; e += 128) {
+            for (int e = tid; e < n_tok * nb; e += kScEpi) {
                 const int tk = e / nb, blk = b0 + e % nb;
                 const int pos = Lb - Tq + t0 + tk;
                 if (blk > pos / bs) continue;
@@ -213,7 +236,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int jj = ja; jj <= jz; ++jj) m = fmaxf(m, kmax[tk * kScM + jj]);
                 S[(static_cast<size_t>(bg) * Tq + t0 + tk) * nblk_max + blk] = m;
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");  // kmax is rewritten by the next chunk
+            asm volatile("bar.sync 1, 256;" ::: "memory");  // kmax is rewritten by the next chunk
         }
     }
     tc_fence_before();
