@@ -59,7 +59,12 @@ def _load():
             lib.orc_select.argtypes = [p, p, i64, i64, i64, i32, p, p, i64, i64, i64, p, p, p, p]
             lib.orc_attention.argtypes = [p, p, p, p, p, p, p, p, p, i64, i64, i64, i64, i64, i64,
                                           i64, p, ctypes.c_double, p, i64, p, p]
-            for f in (lib.orc_kernel_pool, lib.orc_block_scores, lib.orc_select, lib.orc_attention):
+            lib.orc_attention_f64.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64, i64, i64, p,
+                                              ctypes.c_double, p, p]
+            lib.orc_attention_bwd.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64, i64, i64, p,
+                                              ctypes.c_double, p, p, p, p]
+            for f in (lib.orc_kernel_pool, lib.orc_block_scores, lib.orc_select, lib.orc_attention,
+                      lib.orc_attention_f64, lib.orc_attention_bwd):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -180,6 +185,50 @@ def attention(q, k_cache, v_cache, kv_len, idx, counts, params, t_list=None, dra
                                  Tq, Hq, Hkv, d, L_max, _ptr(_iparams(params)), float(scale),
                                  _ptr(t_list), n_t, _ptr(o), _ptr(lse)), "attention")
     return o, lse
+
+
+def attention_f64(q, k_cache, v_cache, kv_len, idx, counts, params, scale=0.0):
+    """Chunk attention like `attention`, on fp64 inputs (for differentiation).
+    Returns (o float64 [B, Tq, Hq, d], lse float64 [B, Hq, Tq])."""
+    q = _c(q, np.float64)
+    k_cache = _c(k_cache, np.float64)
+    v_cache = _c(v_cache, np.float64)
+    kv_len = _c(kv_len, np.int32)
+    B, Tq, Hq, d = q.shape
+    Hkv, L_max = k_cache.shape[1], k_cache.shape[2]
+    idx = _c(idx, np.int32)
+    counts = _c(counts, np.int32)
+    S_max = 0 if idx is None else idx.shape[-1]
+    o = np.empty((B, Tq, Hq, d), dtype=np.float64)
+    lse = np.empty((B, Hq, Tq), dtype=np.float64)
+    _check(_load().orc_attention_f64(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), _ptr(idx),
+                                     _ptr(counts), S_max, B, Tq, Hq, Hkv, d, L_max,
+                                     _ptr(_iparams(params)), float(scale), _ptr(o), _ptr(lse)),
+           "attention_f64")
+    return o, lse
+
+
+def attention_bwd(q, k_cache, v_cache, kv_len, idx, counts, params, dout, scale=0.0):
+    """Gradients of sum(dout * o) of `attention_f64` with the selection fixed.
+    Returns (dq [B, Tq, Hq, d], dk [B, Hkv, L_max, d], dv [B, Hkv, L_max, d]), float64."""
+    q = _c(q, np.float64)
+    k_cache = _c(k_cache, np.float64)
+    v_cache = _c(v_cache, np.float64)
+    dout = _c(dout, np.float64)
+    kv_len = _c(kv_len, np.int32)
+    B, Tq, Hq, d = q.shape
+    Hkv, L_max = k_cache.shape[1], k_cache.shape[2]
+    idx = _c(idx, np.int32)
+    counts = _c(counts, np.int32)
+    S_max = 0 if idx is None else idx.shape[-1]
+    dq = np.empty_like(q)
+    dk = np.empty_like(k_cache)
+    dv = np.empty_like(v_cache)
+    _check(_load().orc_attention_bwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), _ptr(idx),
+                                     _ptr(counts), S_max, B, Tq, Hq, Hkv, d, L_max,
+                                     _ptr(_iparams(params)), float(scale), _ptr(dout), _ptr(dq),
+                                     _ptr(dk), _ptr(dv)), "attention_bwd")
+    return dq, dk, dv
 
 
 def run(inputs: dict, w, t_list=None, kern=None):

@@ -363,3 +363,154 @@ int orc_attention(const uint16_t* q, const uint16_t* kc, const uint16_t* vc, con
     }
     return err;
 }
+
+/* ---------------------------------------------------------------------------------------------
+ * Backward of the attention step ("MiniCPM4：如何在手机电脑上高效运行大语言模型", section 1.1: InfLLM
+ * v2 is trainable sparse attention; the selection is a discrete choice, so gradients flow through
+ * the attention over the selected keys with the selection held fixed).
+ *
+ * Both functions below take fp64 inputs (q [B,Tq,Hq,d]; caches [B,Hkv,L_max,d]) so that the
+ * backward can be checked against finite differences of the forward; chunk layout only (query t
+ * of a chunk sits at kv_len - Tq + t), no draft tree.  The key set of (b, t, h) is the same as in
+ * orc_attention: tokens x <= pos of the selected blocks (every block from 0 to pos when idx is
+ * NULL).
+ */
+static int64_t gather_keys(int64_t b, int64_t t, int64_t g, int64_t Tq, int64_t Hkv, int64_t L,
+                           int64_t bs, const int32_t* idx, const int32_t* counts, int64_t S_max,
+                           int64_t* keys) {
+    const int64_t pos = L - Tq + t;
+    const int64_t row_id = (b * Hkv + g) * Tq + t;
+    const int64_t nsel = idx ? counts[row_id] : pos / bs + 1;
+    int64_t nk = 0;
+    for (int64_t r = 0; r < nsel; ++r) {
+        const int64_t blk = idx ? idx[row_id * S_max + r] : r;
+        if (blk < 0) return -1;
+        for (int64_t x = blk * bs; x < (blk + 1) * bs; ++x) {
+            if (x >= L || x > pos) break;
+            keys[nk++] = x;
+        }
+    }
+    return nk;
+}
+
+/* o = softmax(scale * q k^T) v over each row's keys, in fp64 (o [B,Tq,Hq,d], lse [B,Hq,Tq]). */
+int orc_attention_f64(const double* q, const double* kc, const double* vc, const int32_t* kv_len,
+                      const int32_t* idx, const int32_t* counts, int64_t S_max, int64_t B, int64_t Tq,
+                      int64_t Hq, int64_t Hkv, int64_t d, int64_t L_max, const int32_t* ip, double scale,
+                      double* o, double* lse) {
+    const int64_t bs = ip[P_BLOCK];
+    if (Hkv <= 0 || Hq % Hkv != 0 || bs <= 0) return ORC_ERR_ARG;
+    const int64_t G = Hq / Hkv;
+    if (scale <= 0.0) scale = 1.0 / sqrt((double)d);
+    int err = ORC_OK;
+#pragma omp parallel for collapse(3) schedule(dynamic)
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t t = 0; t < Tq; ++t)
+            for (int64_t h = 0; h < Hq; ++h) {
+                const int64_t g = h / G, L = kv_len[b];
+                int64_t* keys = (int64_t*)malloc(sizeof(int64_t) * (size_t)(L + 1));
+                double* z = (double*)malloc(sizeof(double) * (size_t)(L + 1));
+                const int64_t nk = gather_keys(b, t, g, Tq, Hkv, L, bs, idx, counts, S_max, keys);
+                if (nk < 0) {
+#pragma omp atomic write
+                    err = ORC_ERR_ARG;
+                }
+                const double* qv = q + ((b * Tq + t) * Hq + h) * d;
+                double zmax = -INFINITY, denom = 0.0;
+                for (int64_t n = 0; n < nk; ++n) {
+                    const double* kv = kc + ((b * Hkv + g) * L_max + keys[n]) * d;
+                    double dot = 0.0;
+                    for (int64_t x = 0; x < d; ++x) dot += qv[x] * kv[x];
+                    z[n] = scale * dot;
+                    if (z[n] > zmax) zmax = z[n];
+                }
+                for (int64_t n = 0; n < nk; ++n) {
+                    z[n] = exp(z[n] - zmax);
+                    denom += z[n];
+                }
+                double* orow = o + ((b * Tq + t) * Hq + h) * d;
+                for (int64_t x = 0; x < d; ++x) {
+                    double acc = 0.0;
+                    for (int64_t n = 0; n < nk; ++n) acc += z[n] * vc[((b * Hkv + g) * L_max + keys[n]) * d + x];
+                    orow[x] = nk > 0 ? acc / denom : 0.0;
+                }
+                if (lse) lse[(b * Hq + h) * Tq + t] = nk > 0 ? zmax + log(denom) : -INFINITY;
+                free(z);
+                free(keys);
+            }
+    return err;
+}
+
+/* Gradients of sum(dout * o) for orc_attention_f64 with the selection fixed.  Per row, with p
+ * the softmax weights and a_n = dout . v_n:
+ *   dv_n += p_n dout;  dz_n = p_n (a_n - sum_m p_m a_m);  dq += scale sum_n dz_n k_n;
+ *   dk_n += scale dz_n q.
+ * dq [B,Tq,Hq,d]; dk, dv [B,Hkv,L_max,d], summed over the heads of a group and over the rows
+ * (rows of one (b, g) run in order, so the sums need no atomics). */
+int orc_attention_bwd(const double* q, const double* kc, const double* vc, const int32_t* kv_len,
+                      const int32_t* idx, const int32_t* counts, int64_t S_max, int64_t B, int64_t Tq,
+                      int64_t Hq, int64_t Hkv, int64_t d, int64_t L_max, const int32_t* ip, double scale,
+                      const double* dout, double* dq, double* dk, double* dv) {
+    const int64_t bs = ip[P_BLOCK];
+    if (Hkv <= 0 || Hq % Hkv != 0 || bs <= 0) return ORC_ERR_ARG;
+    const int64_t G = Hq / Hkv;
+    if (scale <= 0.0) scale = 1.0 / sqrt((double)d);
+    memset(dq, 0, sizeof(double) * (size_t)(B * Tq * Hq * d));
+    memset(dk, 0, sizeof(double) * (size_t)(B * Hkv * L_max * d));
+    memset(dv, 0, sizeof(double) * (size_t)(B * Hkv * L_max * d));
+    int err = ORC_OK;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t g = 0; g < Hkv; ++g) {
+            const int64_t L = kv_len[b];
+            int64_t* keys = (int64_t*)malloc(sizeof(int64_t) * (size_t)(L + 1));
+            double* p = (double*)malloc(sizeof(double) * (size_t)(L + 1));
+            double* a = (double*)malloc(sizeof(double) * (size_t)(L + 1));
+            for (int64_t t = 0; t < Tq; ++t)
+                for (int64_t h = g * G; h < (g + 1) * G; ++h) {
+                    const int64_t nk = gather_keys(b, t, g, Tq, Hkv, L, bs, idx, counts, S_max, keys);
+                    if (nk < 0) {
+#pragma omp atomic write
+                        err = ORC_ERR_ARG;
+                        continue;
+                    }
+                    const double* qv = q + ((b * Tq + t) * Hq + h) * d;
+                    const double* dov = dout + ((b * Tq + t) * Hq + h) * d;
+                    double zmax = -INFINITY, denom = 0.0;
+                    for (int64_t n = 0; n < nk; ++n) {
+                        const double* kv = kc + ((b * Hkv + g) * L_max + keys[n]) * d;
+                        double dot = 0.0;
+                        for (int64_t x = 0; x < d; ++x) dot += qv[x] * kv[x];
+                        p[n] = scale * dot;
+                        if (p[n] > zmax) zmax = p[n];
+                    }
+                    for (int64_t n = 0; n < nk; ++n) {
+                        p[n] = exp(p[n] - zmax);
+                        denom += p[n];
+                    }
+                    double pa = 0.0;
+                    for (int64_t n = 0; n < nk; ++n) {
+                        p[n] /= denom;
+                        const double* vv = vc + ((b * Hkv + g) * L_max + keys[n]) * d;
+                        double dot = 0.0;
+                        for (int64_t x = 0; x < d; ++x) dot += dov[x] * vv[x];
+                        a[n] = dot;
+                        pa += p[n] * dot;
+                    }
+                    double* dqv = dq + ((b * Tq + t) * Hq + h) * d;
+                    for (int64_t n = 0; n < nk; ++n) {
+                        const double dz = p[n] * (a[n] - pa);
+                        const int64_t row = ((b * Hkv + g) * L_max + keys[n]) * d;
+                        for (int64_t x = 0; x < d; ++x) {
+                            dqv[x] += scale * dz * kc[row + x];
+                            dk[row + x] += scale * dz * qv[x];
+                            dv[row + x] += p[n] * dov[x];
+                        }
+                    }
+                }
+            free(a);
+            free(p);
+            free(keys);
+        }
+    return err;
+}
