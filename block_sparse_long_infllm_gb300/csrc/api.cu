@@ -220,6 +220,8 @@ size_t infllmv2_workspace_size(int entry, int B, int Tq, int Hq, int Hkv, int d,
         case INFLLMV2_ENTRY_BLOCK_SELECT: return align256(infllmv2::select_workspace_bytes(B, Tq, Hkv, L_max, p));
         case INFLLMV2_ENTRY_SPARSE_ATTN_FWD: return 0;
         case INFLLMV2_ENTRY_DECODE: return decode_ws(B, Tq, Hkv, d, L_max, p).total;
+        case INFLLMV2_ENTRY_SPARSE_ATTN_BWD:
+            return align256(infllmv2::bwd_workspace_bytes(B, Tq, Hq, Hkv, L_max, p.block_size));
         default: return 0;
     }
 }
@@ -296,6 +298,36 @@ int infllmv2_sparse_attn_fwd(const void* q, const void* k_cache, const void* v_c
     prof_begin(a.stream);
     const cudaError_t e = infllmv2::launch_prefill_attention(a);
     prof_mark(a.stream, "attend");
+    return cuda_status(e);
+}
+
+int infllmv2_sparse_attn_bwd(const void* q, const void* k_cache, const void* v_cache, const void* o,
+                             const float* lse, const void* dout, const int32_t* idx, const int32_t* counts,
+                             int S_max, const int32_t* kv_len, int B, int Tq, int Hq, int Hkv, int d, int L_max,
+                             float* dq, float* dk, float* dv, void* workspace, size_t ws_bytes,
+                             const infllmv2_params* params, void* stream) {
+    Params p;
+    if (int rc = check_params(params, d, &p)) return rc;
+    if (int rc = check_heads(Hq, Hkv, d)) return rc;
+    if (B < 0 || Tq < 0 || L_max <= 0 || L_max > kMaxLen) return INFLLMV2_ERR_INVALID_ARG;
+    if (B == 0 || Tq == 0) return INFLLMV2_OK;
+    if (Tq > L_max) return INFLLMV2_ERR_INVALID_ARG;
+    if (!q || !k_cache || !v_cache || !o || !lse || !dout || !kv_len || !dq || !dk || !dv)
+        return INFLLMV2_ERR_INVALID_ARG;
+    if ((idx == nullptr) != (counts == nullptr)) return INFLLMV2_ERR_INVALID_ARG;
+    if (idx != nullptr && (S_max <= 0 || !aligned16(idx) || !aligned16(counts))) return INFLLMV2_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse) ||
+        !aligned16(dout) || !aligned16(kv_len) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return INFLLMV2_ERR_INVALID_ARG;
+    const size_t need = align256(infllmv2::bwd_workspace_bytes(B, Tq, Hq, Hkv, L_max, p.block_size));
+    if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return INFLLMV2_ERR_WORKSPACE;
+    int* err = device_error_ptr();
+    if (err == nullptr) return INFLLMV2_ERR_CUDA;
+    infllmv2::BwdArgs a{q, k_cache, v_cache, o, dout, lse, idx, counts, S_max, kv_len, B, Tq, Hq, Hkv, d, L_max,
+                        dq, dk, dv, workspace, p, err, static_cast<cudaStream_t>(stream)};
+    prof_begin(a.stream);
+    const cudaError_t e = infllmv2::launch_attention_bwd(a);
+    prof_mark(a.stream, "backward");
     return cuda_status(e);
 }
 

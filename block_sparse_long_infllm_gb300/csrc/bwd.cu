@@ -1,0 +1,446 @@
+// bwd.cu -- gradients of block-sparse attention over a fixed selection (InfLLM v2 is trainable
+// sparse attention: "MiniCPM4：如何在手机电脑上高效运行大语言模型", section 1.1; the selection is a
+// discrete choice, so the gradient flows through the attention over the selected keys).
+//
+// For a row (token t, head h) with softmax weights p over its keys and D = dO . O:
+//   dS = P o (dO V^T - D),  dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
+// Four steps, all on the caller's stream:
+//   1. bwd_rowdot_kernel: D for every (token, head) from the forward's bf16 O and dO.
+//   2. bwd_count / scan / fill kernels: the inverse of the selection, per (sequence, KV head,
+//      block) the chunk tokens that chose it (so dK, dV are summed per key block without
+//      per-element atomics).
+//   3. bwd_dq_kernel: one warp per (token, KV head) = the G query heads of a selection (16 MMA
+//      rows): S = Q K^T and dP = dO V^T recomputed per 32-key tile with m16n8k16 MMAs, P from the
+//      forward's lse, dQ += dS K.
+//   4. bwd_dkdv_kernel: one CTA per (key block, slice of its token list), one warp per 16 keys:
+//      per attending token, S^T = K Q^T and dP^T = V dO^T, then dV += P^T dO and dK += dS^T Q with
+//      the token's Q and dO staged in padded shared memory and read transposed by ldmatrix; the
+//      slices of a block add their sums into fp32 dK, dV (zeroed first).
+// P and dS enter the MMAs as bf16 (the usual flash-attention backward precision); every sum is
+// fp32.
+#include "attn_warp.cuh"
+#include "internal.h"
+
+namespace infllmv2 {
+
+constexpr int kBwdSplit = 128;  // tokens of a block's list per dK/dV CTA
+
+// ---- 1. D = dO . O per (token, head)
+__global__ void bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                                  int rows, int d, float* __restrict__ D) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (warp >= rows) return;
+    const __nv_bfloat16* a = o + static_cast<size_t>(warp) * d;
+    const __nv_bfloat16* b = dout + static_cast<size_t>(warp) * d;
+    float acc = 0.f;
+    for (int x = lane; x < d; x += 32) acc += __bfloat162float(a[x]) * __bfloat162float(b[x]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) D[warp] = acc;
+}
+
+// ---- 2. inverse selection: count, scan, fill
+// Entry (row, r) of the selection: row = (b*Hkv + g)*Tq + t; block idx[row][r] (r < counts[row]),
+// or every block 0..bt when idx is null.
+__device__ __forceinline__ int bwd_entry(const int* idx, const int* counts, int S_max, int row, int r, int bt,
+                                         int nblk, int* err) {
+    if (idx == nullptr) return r <= bt ? r : -1;
+    const int cnt = counts[row];
+    if (cnt < 0 || cnt > S_max || cnt > nblk) {  // (more entries than blocks: duplicates)
+        if (r == 0) raise_error(err, kDevErrIndex);
+        return -1;
+    }
+    if (r >= cnt) return -1;
+    const int blk = idx[static_cast<size_t>(row) * S_max + r];
+    if (blk < 0 || blk > bt) {
+        raise_error(err, kDevErrIndex);
+        return -1;
+    }
+    return blk;
+}
+
+__global__ void bwd_count_kernel(const int* __restrict__ idx, const int* __restrict__ counts, int S_max,
+                                 const int* __restrict__ kv_len, int B, int Tq, int Hkv, int L_max, int bs, int per_row,
+                                 int nblk, int* __restrict__ bcnt, int* __restrict__ err) {
+    const long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int row = static_cast<int>(e / per_row), r = static_cast<int>(e % per_row);
+    if (row >= B * Hkv * Tq) return;
+    const int b = row / (Hkv * Tq);
+    const int L = kv_len[b];
+    if (L < Tq || L > L_max) {
+        if (r == 0 && row % (Hkv * Tq) == 0) raise_error(err, kDevErrIndex);
+        return;
+    }
+    const int t = row % Tq;
+    const int bt = (L - Tq + t) / bs;
+    const int blk = bwd_entry(idx, counts, S_max, row, r, bt, nblk, err);
+    if (blk >= 0) atomicAdd(&bcnt[(row / Tq) * nblk + blk], 1);
+}
+
+// Exclusive scan of one (b, g)'s block counts -> offsets [nblk + 1].
+__global__ void __launch_bounds__(1024) bwd_scan_kernel(const int* __restrict__ bcnt, int nblk, int* __restrict__ boff) {
+    __shared__ int s_warp[32];
+    __shared__ int s_carry;
+    const int bg = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int* c = bcnt + static_cast<size_t>(bg) * nblk;
+    int* out = boff + static_cast<size_t>(bg) * (nblk + 1);
+    if (tid == 0) s_carry = 0;
+    __syncthreads();
+    for (int base = 0; base < nblk; base += 1024) {
+        const int i = base + tid;
+        const int v = i < nblk ? c[i] : 0;
+        int incl = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += x;
+        }
+        if (lane == 31) s_warp[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int w = s_warp[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int x = __shfl_up_sync(0xffffffffu, w, off);
+                if (lane >= off) w += x;
+            }
+            s_warp[lane] = w;  // inclusive over warps
+        }
+        __syncthreads();
+        const int before = s_carry + (warp > 0 ? s_warp[warp - 1] : 0) + incl - v;
+        if (i < nblk) out[i] = before;
+        __syncthreads();
+        if (tid == 1023) s_carry = before + v;
+        __syncthreads();
+    }
+    if (tid == 0) out[nblk] = s_carry;
+}
+
+__global__ void bwd_fill_kernel(const int* __restrict__ idx, const int* __restrict__ counts, int S_max,
+                                const int* __restrict__ kv_len, int B, int Tq, int Hkv, int L_max, int bs, int per_row,
+                                int nblk, const int* __restrict__ boff, int* __restrict__ cursor,
+                                int* __restrict__ list, long long list_stride, int* __restrict__ err) {
+    const long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int row = static_cast<int>(e / per_row), r = static_cast<int>(e % per_row);
+    if (row >= B * Hkv * Tq) return;
+    const int b = row / (Hkv * Tq);
+    const int L = kv_len[b];
+    if (L < Tq || L > L_max) return;
+    const int t = row % Tq;
+    const int bt = (L - Tq + t) / bs;
+    const int blk = bwd_entry(idx, counts, S_max, row, r, bt, nblk, err);
+    if (blk < 0) return;
+    const int bg = row / Tq;
+    const int at = atomicAdd(&cursor[bg * nblk + blk], 1);
+    list[bg * list_stride + boff[static_cast<size_t>(bg) * (nblk + 1) + blk] + at] = t;
+}
+
+// ---- 3. dQ: one warp per (b, t, g)
+template <int D>
+__global__ void __launch_bounds__(128)
+bwd_dq_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_cache,
+              const __nv_bfloat16* __restrict__ v_cache, const __nv_bfloat16* __restrict__ dout,
+              const float* __restrict__ lse, const float* __restrict__ Drow, const int* __restrict__ idx,
+              const int* __restrict__ counts, int S_max, const int* __restrict__ kv_len, int B, int Tq, int Hq,
+              int Hkv, int L_max, int bs, float scale, float* __restrict__ dq, int* __restrict__ err) {
+    const int lane = threadIdx.x & 31;
+    const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (wid >= B * Tq * Hkv) return;
+    const int g = wid % Hkv, t = (wid / Hkv) % Tq, b = wid / (Hkv * Tq);
+    const int G = Hq / Hkv;
+    const int gq = lane >> 2, cq = lane & 3;
+    const int L = kv_len[b];
+    if (L < Tq || L > L_max) return;  // reported by the count kernel
+    const int pos = L - Tq + t;
+    const int bt = pos / bs;
+    const float scale_log2 = scale * 1.4426950408889634f;
+    const size_t qrow = (static_cast<size_t>(b) * Tq + t) * Hq + static_cast<size_t>(g) * G;
+    QFrag<D> Q, dO;
+    load_q(Q, q + qrow * D, D, G);
+    load_q(dO, dout + qrow * D, D, G);
+    float lse2[2], Dr[2];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int h = gq + 8 * half;
+        lse2[half] = h < G ? lse[(static_cast<size_t>(b) * Hq + g * G + h) * Tq + t] * 1.4426950408889634f : INFINITY;
+        Dr[half] = h < G ? Drow[qrow + h] : 0.f;
+    }
+    float acc[D / 8][4];
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+    const int row = (b * Hkv + g) * Tq + t;
+    const int nsel = idx != nullptr ? min(min(max(counts[row], 0), S_max), (L_max + bs - 1) / bs) : bt + 1;
+    const size_t cache0 = static_cast<size_t>(b * Hkv + g) * L_max;
+    constexpr int VW = D / 16;
+    for (int r = 0; r < nsel; ++r) {
+        const int blk = idx != nullptr ? idx[static_cast<size_t>(row) * S_max + r] : r;
+        if (blk < 0 || blk > bt) continue;  // reported by the count kernel
+        for (int r0 = 0; r0 < bs; r0 += 32) {
+            const int x0 = blk * bs + r0;
+            const int n_ok = min(pos, L - 1) - x0 + 1;
+            if (n_ok <= 0) break;
+            const uint32_t valid = n_ok >= 32 ? 0xffffffffu : ((1u << n_ok) - 1u);
+            const __nv_bfloat16* krow = k_cache + (cache0 + x0) * D;
+            const __nv_bfloat16* vrow = v_cache + (cache0 + x0) * D;
+            // K and V rows in the QK^T layout (16 bytes of key nt*8 + gq at 32i + 8cq)
+            uint4 kw[4][D / 32], vq[4][D / 32];
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const int key = nt * 8 + gq;
+                const bool ok = (valid >> key) & 1u;
+#pragma unroll
+                for (int i = 0; i < D / 32; ++i) {
+                    kw[nt][i] = ok ? ldg_v4(krow + static_cast<size_t>(key) * D + 32 * i + 8 * cq) : make_uint4(0, 0, 0, 0);
+                    vq[nt][i] = ok ? ldg_v4(vrow + static_cast<size_t>(key) * D + 32 * i + 8 * cq) : make_uint4(0, 0, 0, 0);
+                }
+            }
+            float s[4][4], dp[4][4];
+            qk_tiles<D>(s, Q, kw);
+            qk_tiles<D>(dp, dO, vq);
+            // dS = P (dP - D) as the A operand of dQ += dS K
+            uint32_t da[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                float v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int key = nt * 8 + 2 * cq + (e & 1);
+                    const float p = ((valid >> key) & 1u) ? fast_exp2(s[nt][e] * scale_log2 - lse2[e >> 1]) : 0.f;
+                    v[e] = p * (dp[nt][e] - Dr[e >> 1]);
+                }
+                const int kk = nt >> 1, hi = nt & 1;
+                da[kk][2 * hi + 0] = pack_bf16x2(v[0], v[1]);
+                da[kk][2 * hi + 1] = pack_bf16x2(v[2], v[3]);
+            }
+            // K rows in the PV layout: lane reads D/8 consecutive elements of its four rows
+            uint32_t kp[2][4][VW];
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr) {
+                    const int key = 16 * kk + 2 * cq + (rr & 1) + 8 * (rr >> 1);
+                    const bool ok = (valid >> key) & 1u;
+                    const uint4* src = reinterpret_cast<const uint4*>(krow + static_cast<size_t>(key) * D + (D / 8) * gq);
+#pragma unroll
+                    for (int u = 0; u < VW / 4; ++u) {
+                        const uint4 w = ok ? ldg_v4(src + u) : make_uint4(0, 0, 0, 0);
+                        kp[kk][rr][4 * u + 0] = w.x;
+                        kp[kk][rr][4 * u + 1] = w.y;
+                        kp[kk][rr][4 * u + 2] = w.z;
+                        kp[kk][rr][4 * u + 3] = w.w;
+                    }
+                }
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+                for (int nt = 0; nt < D / 8; ++nt) {
+                    const uint32_t b0 = pair_halves(kp[kk][0][nt >> 1], kp[kk][1][nt >> 1], nt & 1);
+                    const uint32_t b1 = pair_halves(kp[kk][2][nt >> 1], kp[kk][3][nt >> 1], nt & 1);
+                    mma_16816(acc[nt], da[kk], b0, b1);
+                }
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int h = gq + 8 * (e >> 1);
+            if (h < G) dq[(qrow + h) * D + o_col(D, cq, nt, e)] = acc[nt][e] * scale;
+        }
+}
+
+// ---- 4. dK, dV: one CTA per (key block, slice of its token list), one warp per 16 keys
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                  uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+template <int D, int BS>
+__global__ void __launch_bounds__(BS * 2)
+bwd_dkdv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_cache,
+                const __nv_bfloat16* __restrict__ v_cache, const __nv_bfloat16* __restrict__ dout,
+                const float* __restrict__ lse, const float* __restrict__ Drow, const int* __restrict__ kv_len,
+                int Tq, int Hq, int Hkv, int L_max, int nblk, int max_splits, const int* __restrict__ boff,
+                const int* __restrict__ list, long long list_stride, float scale, float* __restrict__ dk,
+                float* __restrict__ dv) {
+    constexpr int kPad = D + 8;  // bf16 per staged row: 16-byte rows, conflict-free ldmatrix
+    __shared__ __align__(16) __nv_bfloat16 s_q[16][kPad];
+    __shared__ __align__(16) __nv_bfloat16 s_do[16][kPad];
+    __shared__ float s_lse2[16], s_D[16];
+    const int bg = blockIdx.y;
+    const int blk = blockIdx.x / max_splits, split = blockIdx.x % max_splits;
+    const int b = bg / Hkv, g = bg % Hkv;
+    const int G = Hq / Hkv;
+    const int L = kv_len[b];
+    if (L < Tq || L > L_max) return;
+    const int* off = boff + static_cast<size_t>(bg) * (nblk + 1);
+    const int lo = off[blk] + split * kBwdSplit, hi = min(off[blk + 1], lo + kBwdSplit);
+    if (lo >= hi) return;
+    const int* toks = list + bg * list_stride;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gq = lane >> 2, cq = lane & 3;
+    const int key0 = blk * BS + 16 * warp;  // this warp's 16 keys
+    const size_t cache0 = static_cast<size_t>(bg) * L_max;
+    const float scale_log2 = scale * 1.4426950408889634f;
+    // K and V of the warp's keys as A fragments (rows = keys; past the cache: zero, masked below)
+    QFrag<D> KA, VA;
+    {
+        const int nk = max(0, min(16, L - key0));  // rows past the cache read as zero (not loaded)
+        load_q(KA, k_cache + (cache0 + key0) * D, D, nk);
+        load_q(VA, v_cache + (cache0 + key0) * D, D, nk);
+    }
+    float akv[D / 8][4], akk[D / 8][4];
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) akv[nt][e] = akk[nt][e] = 0.f;
+    const uint32_t sq_base = smem_u32(&s_q[0][0]), sdo_base = smem_u32(&s_do[0][0]);
+    for (int it = lo; it < hi; ++it) {
+        const int t = toks[it];
+        const int pos = L - Tq + t;
+        const size_t qrow = (static_cast<size_t>(b) * Tq + t) * Hq + static_cast<size_t>(g) * G;
+        __syncthreads();  // the previous token's rows are no longer read
+        for (int e = tid; e < 16 * (D / 8); e += BS * 2) {
+            const int h = e / (D / 8), c8 = (e % (D / 8)) * 8;
+            uint4 wq = make_uint4(0, 0, 0, 0), wd = make_uint4(0, 0, 0, 0);
+            if (h < G) {
+                wq = ldg_v4(q + (qrow + h) * D + c8);
+                wd = ldg_v4(dout + (qrow + h) * D + c8);
+            }
+            *reinterpret_cast<uint4*>(&s_q[h][c8]) = wq;
+            *reinterpret_cast<uint4*>(&s_do[h][c8]) = wd;
+        }
+        if (tid < 16) {
+            const int h = tid;
+            s_lse2[h] = h < G ? lse[(static_cast<size_t>(b) * Hq + g * G + h) * Tq + t] * 1.4426950408889634f : INFINITY;
+            s_D[h] = h < G ? Drow[qrow + h] : 0.f;
+        }
+        __syncthreads();
+        // S^T = K Q^T, dP^T = V dO^T: rows = keys, columns = heads (two n-tiles of 8)
+        float st[2][4], dpt[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) st[nt][e] = dpt[nt][e] = 0.f;
+            const int h = nt * 8 + gq;
+#pragma unroll
+            for (int i = 0; i < D / 32; ++i) {
+                const uint4 wq = lds_v4(sq_base + (h * kPad + 32 * i + 8 * cq) * 2);
+                const uint4 wd = lds_v4(sdo_base + (h * kPad + 32 * i + 8 * cq) * 2);
+                mma_16816(st[nt], KA.a[2 * i], wq.x, wq.y);
+                mma_16816(st[nt], KA.a[2 * i + 1], wq.z, wq.w);
+                mma_16816(dpt[nt], VA.a[2 * i], wd.x, wd.y);
+                mma_16816(dpt[nt], VA.a[2 * i + 1], wd.z, wd.w);
+            }
+        }
+        // P^T and dS^T (keys past the token or the cache, and padding heads, are zero)
+        uint32_t pa[4], da[4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            float pv[4], dv4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int key = key0 + gq + 8 * (e >> 1);
+                const int h = nt * 8 + 2 * cq + (e & 1);
+                const bool ok = key <= pos && key < L && h < G;
+                const float p = ok ? fast_exp2(st[nt][e] * scale_log2 - s_lse2[h]) : 0.f;
+                pv[e] = p;
+                dv4[e] = p * (dpt[nt][e] - s_D[h]);
+            }
+            pa[2 * nt + 0] = pack_bf16x2(pv[0], pv[1]);
+            pa[2 * nt + 1] = pack_bf16x2(pv[2], pv[3]);
+            da[2 * nt + 0] = pack_bf16x2(dv4[0], dv4[1]);
+            da[2 * nt + 1] = pack_bf16x2(dv4[2], dv4[3]);
+        }
+        // dV += P^T dO, dK += dS^T Q: B = the staged rows read transposed (k = head, n = column)
+        const int mrow = lane & 15, mcol = (lane >> 4) * 8;  // ldmatrix row of lanes 0-15 / 16-31
+#pragma unroll
+        for (int nt = 0; nt < D / 8; nt += 2) {
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4_trans(sdo_base + (mrow * kPad + nt * 8 + mcol) * 2, b0, b1, b2, b3);
+            mma_16816(akv[nt], pa, b0, b1);
+            mma_16816(akv[nt + 1], pa, b2, b3);
+            ldmatrix_x4_trans(sq_base + (mrow * kPad + nt * 8 + mcol) * 2, b0, b1, b2, b3);
+            mma_16816(akk[nt], da, b0, b1);
+            mma_16816(akk[nt + 1], da, b2, b3);
+        }
+    }
+    // sums of this slice into dK, dV (fp32, zeroed before the launch)
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int key = key0 + gq + 8 * (e >> 1);
+            if (key >= L) continue;
+            const int col = nt * 8 + 2 * cq + (e & 1);
+            atomicAdd(&dv[(cache0 + key) * D + col], akv[nt][e]);
+            atomicAdd(&dk[(cache0 + key) * D + col], akk[nt][e] * scale);
+        }
+}
+
+size_t bwd_workspace_bytes(int B, int Tq, int Hq, int Hkv, int L_max, int bs) {
+    const size_t nblk = (L_max + bs - 1) / bs;
+    const size_t rows = static_cast<size_t>(B) * Hkv;
+    auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    return al(static_cast<size_t>(B) * Tq * Hq * 4) + 2 * al(rows * nblk * 4) + al(rows * (nblk + 1) * 4) +
+           al(rows * static_cast<size_t>(Tq) * nblk * 4);
+}
+
+template <int D, int BS>
+static cudaError_t launch_bwd_t(const BwdArgs& a) {
+    const int nblk = (a.L_max + BS - 1) / BS;
+    const size_t rows = static_cast<size_t>(a.B) * a.Hkv;
+    auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    char* ws = static_cast<char*>(a.workspace);
+    float* Dr = reinterpret_cast<float*>(ws);
+    ws += al(static_cast<size_t>(a.B) * a.Tq * a.Hq * 4);
+    int* bcnt = reinterpret_cast<int*>(ws);
+    ws += al(rows * nblk * 4);
+    int* cursor = reinterpret_cast<int*>(ws);
+    ws += al(rows * nblk * 4);
+    int* boff = reinterpret_cast<int*>(ws);
+    ws += al(rows * (nblk + 1) * 4);
+    int* list = reinterpret_cast<int*>(ws);
+    const long long list_stride = static_cast<long long>(a.Tq) * nblk;
+    const float scale = a.p.scale;
+    cudaStream_t st = a.stream;
+    cudaError_t e;
+    if ((e = cudaMemsetAsync(bcnt, 0, 2 * al(rows * nblk * 4), st)) != cudaSuccess) return e;  // counts, cursors
+    const size_t cache = rows * a.L_max * D * sizeof(float);
+    if ((e = cudaMemsetAsync(a.dk, 0, cache, st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(a.dv, 0, cache, st)) != cudaSuccess) return e;
+    const int qrows = a.B * a.Tq * a.Hq;
+    bwd_rowdot_kernel<<<(qrows * 32 + 255) / 256, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(a.o),
+                                                              static_cast<const __nv_bfloat16*>(a.dout), qrows, D, Dr);
+    const int per_row = a.idx != nullptr ? a.S_max : nblk;
+    const long long entries = static_cast<long long>(rows) * a.Tq * per_row;
+    const unsigned eb = static_cast<unsigned>((entries + 255) / 256);
+    bwd_count_kernel<<<eb, 256, 0, st>>>(a.idx, a.counts, a.S_max, a.kv_len, a.B, a.Tq, a.Hkv, a.L_max, BS, per_row,
+                                         nblk, bcnt, a.err);
+    bwd_scan_kernel<<<static_cast<unsigned>(rows), 1024, 0, st>>>(bcnt, nblk, boff);
+    bwd_fill_kernel<<<eb, 256, 0, st>>>(a.idx, a.counts, a.S_max, a.kv_len, a.B, a.Tq, a.Hkv, a.L_max, BS, per_row,
+                                        nblk, boff, cursor, list, list_stride, a.err);
+    const int warps = a.B * a.Tq * a.Hkv;
+    bwd_dq_kernel<D><<<(warps + 3) / 4, 128, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k_cache),
+        static_cast<const __nv_bfloat16*>(a.v_cache), static_cast<const __nv_bfloat16*>(a.dout), a.lse, Dr, a.idx,
+        a.counts, a.S_max, a.kv_len, a.B, a.Tq, a.Hq, a.Hkv, a.L_max, BS, scale, a.dq, a.err);
+    const int max_splits = (a.Tq + kBwdSplit - 1) / kBwdSplit;
+    bwd_dkdv_kernel<D, BS><<<dim3(nblk * max_splits, static_cast<unsigned>(rows)), BS * 2, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k_cache),
+        static_cast<const __nv_bfloat16*>(a.v_cache), static_cast<const __nv_bfloat16*>(a.dout), a.lse, Dr, a.kv_len,
+        a.Tq, a.Hq, a.Hkv, a.L_max, nblk, max_splits, boff, list, list_stride, scale, a.dk, a.dv);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attention_bwd(const BwdArgs& a) {
+    const int bs = a.p.block_size;
+    if (a.d == 128) return bs == 64 ? launch_bwd_t<128, 64>(a) : launch_bwd_t<128, 128>(a);
+    return bs == 64 ? launch_bwd_t<64, 64>(a) : launch_bwd_t<64, 128>(a);
+}
+
+}  // namespace infllmv2

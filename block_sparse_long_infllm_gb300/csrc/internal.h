@@ -57,6 +57,27 @@ struct DecodeArgs {
     cudaStream_t stream;
 };
 
+struct BwdArgs {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const void* o;
+    const void* dout;
+    const float* lse;
+    const int* idx;
+    const int* counts;
+    int S_max;
+    const int* kv_len;
+    int B, Tq, Hq, Hkv, d, L_max;
+    float* dq;
+    float* dk;
+    float* dv;
+    void* workspace;
+    Params p;
+    int* err;
+    cudaStream_t stream;
+};
+
 // 2-D bf16 tensor map over `rows` rows of `inner` elements (row stride inner*2 bytes) with
 // box [box_rows][box_inner] and the 128-byte swizzle; false if the driver refuses.
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
@@ -83,6 +104,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a);
 void decode_split_shape(const Params& p, int L_max, bool tree, int* blocks_per_split, int* n_split_cache,
                         int* n_split);
 size_t decode_partial_bytes(int B, int n_draft, int Hkv, int d, int n_split);
+size_t bwd_workspace_bytes(int B, int Tq, int Hq, int Hkv, int L_max, int bs);
+cudaError_t launch_attention_bwd(const BwdArgs& a);
+
 cudaError_t launch_decode_attention(const DecodeArgs& a, const int* idx, const int* counts, int idx_stride,
                                     float* part);
 

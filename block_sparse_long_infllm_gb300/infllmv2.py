@@ -28,6 +28,7 @@ ERR_NOT_IMPLEMENTED = -7
 ENTRY_BLOCK_SELECT = 1
 ENTRY_SPARSE_ATTN_FWD = 2
 ENTRY_DECODE = 3
+ENTRY_SPARSE_ATTN_BWD = 4
 
 
 class InfLLMv2Error(RuntimeError):
@@ -79,6 +80,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                           pp, p]
     lib.infllmv2_sparse_attn_fwd.argtypes = [p, p, p, p, p, i32, p, i32, i32, i32, i32, i32, i32, p, p,
                                              p, sz, pp, p]
+    lib.infllmv2_sparse_attn_bwd.argtypes = [p, p, p, p, p, p, p, p, i32, p, i32, i32, i32, i32, i32, i32, p, p,
+                                             p, p, sz, pp, p]
     lib.infllmv2_decode.argtypes = [p, p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, p, p, p,
                                     p, i32, p, sz, pp, p]
     lib.infllmv2_decode_noalloc.argtypes = [p, p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, p, p,
@@ -195,6 +198,19 @@ def sparse_attn_fwd(q, k_cache, v_cache, idx, counts, kv_len, o, params, lse=Non
                                            Hkv, d, L_max, _ptr(o), _ptr(lse), _ptr(workspace), ws_bytes,
                                            ctypes.byref(Params.make(params)), _stream(stream)),
            "infllmv2_sparse_attn_fwd")
+
+
+def sparse_attn_bwd(q, k_cache, v_cache, o, lse, dout, idx, counts, kv_len, dq, dk, dv, workspace, params,
+                    stream=None):
+    """Gradients (fp32 dq, dk, dv) of the chunk attention with the selection held fixed."""
+    B, Tq, Hq, d = q.shape
+    Hkv, L_max = k_cache.shape[1], k_cache.shape[2]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().infllmv2_sparse_attn_bwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), _ptr(dout),
+                                           _ptr(idx), _ptr(counts), 0 if idx is None else idx.shape[-1],
+                                           _ptr(kv_len), B, Tq, Hq, Hkv, d, L_max, _ptr(dq), _ptr(dk), _ptr(dv),
+                                           _ptr(workspace), ws_bytes, ctypes.byref(Params.make(params)),
+                                           _stream(stream)), "infllmv2_sparse_attn_bwd")
 
 
 def decode(q, k_cache, v_cache, kernel_cache, kv_len, o, workspace, params, lse=None, draft_k=None,

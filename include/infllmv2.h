@@ -90,7 +90,8 @@ typedef enum infllmv2_status {
 enum {
     INFLLMV2_ENTRY_BLOCK_SELECT = 1,
     INFLLMV2_ENTRY_SPARSE_ATTN_FWD = 2,
-    INFLLMV2_ENTRY_DECODE = 3
+    INFLLMV2_ENTRY_DECODE = 3,
+    INFLLMV2_ENTRY_SPARSE_ATTN_BWD = 4
 };
 
 /* Human-readable text of a status code (static storage, never NULL). */
@@ -174,6 +175,26 @@ int infllmv2_sparse_attn_fwd(const void* q, const void* k_cache, const void* v_c
                              const int32_t* kv_len, int B, int Tq, int Hq, int Hkv, int d,
                              int L_max, void* o, float* lse, void* workspace, size_t ws_bytes,
                              const infllmv2_params* params, void* stream);
+
+/*
+ * Gradients of step 4 for a causal chunk with the selection held fixed (InfLLM
+ * v2 is trainable sparse attention, [MiniCPM4-1.1]; the block choice is
+ * discrete, so the gradient flows through the attention over the selected
+ * keys).  Inputs as for infllmv2_sparse_attn_fwd, plus that call's output o
+ * and lse (required here) and dout [B, Tq, Hq, d] bf16.  With P the weights of
+ * a row and D = dout . o:
+ *   dS = P o (dout v^T - D);  dq = scale dS k;  dk = scale dS^T q;  dv = P^T dout
+ * dq [B, Tq, Hq, d] and dk, dv [B, Hkv, L_max, d] are fp32 and overwritten (dk,
+ * dv are summed over the heads of a group and over the chunk's rows; cache rows
+ * no row attends to get 0).  idx == NULL: dense causal, as in the forward.
+ * Requires ws_bytes >= infllmv2_workspace_size(INFLLMV2_ENTRY_SPARSE_ATTN_BWD, ...).
+ */
+int infllmv2_sparse_attn_bwd(const void* q, const void* k_cache, const void* v_cache, const void* o,
+                             const float* lse, const void* dout, const int32_t* idx,
+                             const int32_t* counts, int S_max, const int32_t* kv_len, int B, int Tq,
+                             int Hq, int Hkv, int d, int L_max, float* dq, float* dk, float* dv,
+                             void* workspace, size_t ws_bytes, const infllmv2_params* params,
+                             void* stream);
 
 /*
  * Steps 2-4 for decoding: selection from the cached kernels, split-KV
