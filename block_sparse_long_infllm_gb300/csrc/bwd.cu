@@ -4,11 +4,15 @@
 //
 // For a row (token t, head h) with softmax weights p over its keys and D = dO . O:
 //   dS = P o (dO V^T - D),  dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
-// Four steps, all on the caller's stream:
-//   1. bwd_rowdot_kernel: D for every (token, head) from the forward's bf16 O and dO.
+// Steps, all on the caller's stream:
+//   1. bwd_rowdot_kernel: D for every (token, head) from the forward's bf16 O and dO (and, beside
+//      it, lse * log2 e in the same row order for the tensor-core kernel).
 //   2. bwd_count / scan / fill kernels: the inverse of the selection, per (sequence, KV head,
 //      block) the chunk tokens that chose it (so dK, dV are summed per key block without
-//      per-element atomics).
+//      per-element atomics); bwd_units_kernel cuts the lists into work units of at most
+//      kBwdUnitTok tokens.
+// With head dim 128, block size 128 and 16 query heads per KV head the gradients come from the
+// tensor-core kernel of bwd_tc.cu; otherwise from two warp-MMA kernels:
 //   3. bwd_dq_kernel: one warp per (token, KV head) = the G query heads of a selection (16 MMA
 //      rows): S = Q K^T and dP = dO V^T recomputed per 32-key tile with m16n8k16 MMAs, P from the
 //      forward's lse, dQ += dS K.
@@ -25,9 +29,10 @@ namespace infllmv2 {
 
 constexpr int kBwdSplit = 128;  // tokens of a block's list per dK/dV CTA
 
-// ---- 1. D = dO . O per (token, head)
+// ---- 1. D = dO . O per (token, head); with `ld`, also (lse * log2 e, D) per row
 __global__ void bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
-                                  int rows, int d, float* __restrict__ D) {
+                                  const float* __restrict__ lse, int rows, int Tq, int Hq, int d, float* __restrict__ D,
+                                  float2* __restrict__ ld) {
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (warp >= rows) return;
     const __nv_bfloat16* a = o + static_cast<size_t>(warp) * d;
@@ -36,7 +41,14 @@ __global__ void bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ o, const __n
     for (int x = lane; x < d; x += 32) acc += __bfloat162float(a[x]) * __bfloat162float(b[x]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) D[warp] = acc;
+    if (lane == 0) {
+        D[warp] = acc;
+        if (ld != nullptr) {
+            const int h = warp % Hq, bt = warp / Hq;  // row (b*Tq + t)*Hq + h; lse is [B][Hq][Tq]
+            const int bb = bt / Tq, t = bt % Tq;
+            ld[warp] = make_float2(lse[(static_cast<size_t>(bb) * Hq + h) * Tq + t] * 1.4426950408889634f, acc);
+        }
+    }
 }
 
 // ---- 2. inverse selection: count, scan, fill
@@ -77,43 +89,69 @@ __global__ void bwd_count_kernel(const int* __restrict__ idx, const int* __restr
     if (blk >= 0) atomicAdd(&bcnt[(row / Tq) * nblk + blk], 1);
 }
 
-// Exclusive scan of one (b, g)'s block counts -> offsets [nblk + 1].
-__global__ void __launch_bounds__(1024) bwd_scan_kernel(const int* __restrict__ bcnt, int nblk, int* __restrict__ boff) {
-    __shared__ int s_warp[32];
-    __shared__ int s_carry;
+// Exclusive scans of one (b, g)'s block counts -> token offsets boff [nblk + 1], and of the units
+// per block (ceil(count / kBwdUnitTok)) -> unit offsets uoff [nblk + 1].
+__global__ void __launch_bounds__(1024) bwd_scan_kernel(const int* __restrict__ bcnt, int nblk, int* __restrict__ boff,
+                                                        int* __restrict__ uoff) {
+    __shared__ int s_warp[2][32];
+    __shared__ int s_carry[2];
     const int bg = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int* c = bcnt + static_cast<size_t>(bg) * nblk;
     int* out = boff + static_cast<size_t>(bg) * (nblk + 1);
-    if (tid == 0) s_carry = 0;
+    int* uout = uoff + static_cast<size_t>(bg) * (nblk + 1);
+    if (tid < 2) s_carry[tid] = 0;
     __syncthreads();
     for (int base = 0; base < nblk; base += 1024) {
         const int i = base + tid;
-        const int v = i < nblk ? c[i] : 0;
-        int incl = v;
+        const int v0 = i < nblk ? c[i] : 0;
+        const int v1 = (v0 + kBwdUnitTok - 1) / kBwdUnitTok;
+        int a0 = v0, a1 = v1;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int x = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += x;
+            const int x0 = __shfl_up_sync(0xffffffffu, a0, off);
+            const int x1 = __shfl_up_sync(0xffffffffu, a1, off);
+            if (lane >= off) {
+                a0 += x0;
+                a1 += x1;
+            }
         }
-        if (lane == 31) s_warp[warp] = incl;
+        if (lane == 31) {
+            s_warp[0][warp] = a0;
+            s_warp[1][warp] = a1;
+        }
         __syncthreads();
         if (warp == 0) {
-            int w = s_warp[lane];
+            int w0 = s_warp[0][lane], w1 = s_warp[1][lane];
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                const int x = __shfl_up_sync(0xffffffffu, w, off);
-                if (lane >= off) w += x;
+                const int x0 = __shfl_up_sync(0xffffffffu, w0, off);
+                const int x1 = __shfl_up_sync(0xffffffffu, w1, off);
+                if (lane >= off) {
+                    w0 += x0;
+                    w1 += x1;
+                }
             }
-            s_warp[lane] = w;  // inclusive over warps
+            s_warp[0][lane] = w0;  // inclusive over warps
+            s_warp[1][lane] = w1;
         }
         __syncthreads();
-        const int before = s_carry + (warp > 0 ? s_warp[warp - 1] : 0) + incl - v;
-        if (i < nblk) out[i] = before;
+        const int before0 = s_carry[0] + (warp > 0 ? s_warp[0][warp - 1] : 0) + a0 - v0;
+        const int before1 = s_carry[1] + (warp > 0 ? s_warp[1][warp - 1] : 0) + a1 - v1;
+        if (i < nblk) {
+            out[i] = before0;
+            uout[i] = before1;
+        }
         __syncthreads();
-        if (tid == 1023) s_carry = before + v;
+        if (tid == 1023) {
+            s_carry[0] = before0 + v0;
+            s_carry[1] = before1 + v1;
+        }
         __syncthreads();
     }
-    if (tid == 0) out[nblk] = s_carry;
+    if (tid == 0) {
+        out[nblk] = s_carry[0];
+        uout[nblk] = s_carry[1];
+    }
 }
 
 __global__ void bwd_fill_kernel(const int* __restrict__ idx, const int* __restrict__ counts, int S_max,
@@ -133,6 +171,21 @@ __global__ void bwd_fill_kernel(const int* __restrict__ idx, const int* __restri
     const int bg = row / Tq;
     const int at = atomicAdd(&cursor[bg * nblk + blk], 1);
     list[bg * list_stride + boff[static_cast<size_t>(bg) * (nblk + 1) + blk] + at] = t;
+}
+
+// Work units {b*Hkv + g, block, first, end}: each block's token list cut into slices of at most
+// kBwdUnitTok tokens, ordered by (b, g), then block.
+__global__ void bwd_units_kernel(const int* __restrict__ boff, const int* __restrict__ uoff, int rows, int nblk,
+                                 int4* __restrict__ units) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= rows * nblk) return;
+    const int bg = e / nblk, blk = e % nblk;
+    int ubase = 0;
+    for (int r = 0; r < bg; ++r) ubase += uoff[static_cast<size_t>(r) * (nblk + 1) + nblk];
+    const int* bo = boff + static_cast<size_t>(bg) * (nblk + 1);
+    const int first = bo[blk], end = bo[blk + 1];
+    int u = ubase + uoff[static_cast<size_t>(bg) * (nblk + 1) + blk];
+    for (int s = first; s < end; s += kBwdUnitTok, ++u) units[u] = make_int4(bg, blk, s, min(s + kBwdUnitTok, end));
 }
 
 // ---- 3. dQ: one warp per (b, t, g)
@@ -382,48 +435,84 @@ bwd_dkdv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         }
 }
 
-size_t bwd_workspace_bytes(int B, int Tq, int Hq, int Hkv, int L_max, int bs) {
-    const size_t nblk = (L_max + bs - 1) / bs;
-    const size_t rows = static_cast<size_t>(B) * Hkv;
+// Workspace: D [B*Tq*Hq] | (lse log2e, D) [B*Tq*Hq] | block counts | cursors | work counter |
+// token offsets | unit offsets | token lists | units; every part 256-byte aligned.
+struct BwdWs {
+    size_t D, ld, bcnt, cursor, counter, boff, uoff, list, units, total;
+    int nblk;
+    long long list_stride;
+};
+
+static BwdWs bwd_ws(int B, int Tq, int Hq, int Hkv, int L_max, int bs) {
     auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-    return al(static_cast<size_t>(B) * Tq * Hq * 4) + 2 * al(rows * nblk * 4) + al(rows * (nblk + 1) * 4) +
-           al(rows * static_cast<size_t>(Tq) * nblk * 4);
+    BwdWs w{};
+    w.nblk = (L_max + bs - 1) / bs;
+    const size_t rows = static_cast<size_t>(B) * Hkv, nblk = static_cast<size_t>(w.nblk);
+    const size_t qrows = static_cast<size_t>(B) * Tq * Hq;
+    w.list_stride = static_cast<long long>(Tq) * w.nblk;
+    const size_t max_units = rows * (static_cast<size_t>(Tq) * nblk / kBwdUnitTok + nblk + 1);
+    size_t o = 0;
+    w.D = o;       o += al(qrows * 4);
+    w.ld = o;      o += al(qrows * 8);
+    w.bcnt = o;    o += al(rows * nblk * 4);
+    w.cursor = o;  o += al(rows * nblk * 4);
+    w.counter = o; o += 256;
+    w.boff = o;    o += al(rows * (nblk + 1) * 4);
+    w.uoff = o;    o += al(rows * (nblk + 1) * 4);
+    w.list = o;    o += al(rows * static_cast<size_t>(Tq) * nblk * 4);
+    w.units = o;   o += al(max_units * 16);
+    w.total = o;
+    return w;
+}
+
+size_t bwd_workspace_bytes(int B, int Tq, int Hq, int Hkv, int L_max, int bs) {
+    return bwd_ws(B, Tq, Hq, Hkv, L_max, bs).total;
 }
 
 template <int D, int BS>
 static cudaError_t launch_bwd_t(const BwdArgs& a) {
-    const int nblk = (a.L_max + BS - 1) / BS;
+    const BwdWs w = bwd_ws(a.B, a.Tq, a.Hq, a.Hkv, a.L_max, BS);
+    const int nblk = w.nblk;
     const size_t rows = static_cast<size_t>(a.B) * a.Hkv;
-    auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
     char* ws = static_cast<char*>(a.workspace);
-    float* Dr = reinterpret_cast<float*>(ws);
-    ws += al(static_cast<size_t>(a.B) * a.Tq * a.Hq * 4);
-    int* bcnt = reinterpret_cast<int*>(ws);
-    ws += al(rows * nblk * 4);
-    int* cursor = reinterpret_cast<int*>(ws);
-    ws += al(rows * nblk * 4);
-    int* boff = reinterpret_cast<int*>(ws);
-    ws += al(rows * (nblk + 1) * 4);
-    int* list = reinterpret_cast<int*>(ws);
-    const long long list_stride = static_cast<long long>(a.Tq) * nblk;
+    float* Dr = reinterpret_cast<float*>(ws + w.D);
+    float2* ld = reinterpret_cast<float2*>(ws + w.ld);
+    int* bcnt = reinterpret_cast<int*>(ws + w.bcnt);
+    int* cursor = reinterpret_cast<int*>(ws + w.cursor);
+    int* counter = reinterpret_cast<int*>(ws + w.counter);
+    int* boff = reinterpret_cast<int*>(ws + w.boff);
+    int* uoff = reinterpret_cast<int*>(ws + w.uoff);
+    int* list = reinterpret_cast<int*>(ws + w.list);
+    int4* units = reinterpret_cast<int4*>(ws + w.units);
+    const long long list_stride = w.list_stride;
+    const bool tc = bwd_tc_supported(a);
     const float scale = a.p.scale;
     cudaStream_t st = a.stream;
     cudaError_t e;
-    if ((e = cudaMemsetAsync(bcnt, 0, 2 * al(rows * nblk * 4), st)) != cudaSuccess) return e;  // counts, cursors
+    if ((e = cudaMemsetAsync(ws + w.bcnt, 0, w.boff - w.bcnt, st)) != cudaSuccess) return e;  // counts, cursors, counter
     const size_t cache = rows * a.L_max * D * sizeof(float);
     if ((e = cudaMemsetAsync(a.dk, 0, cache, st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(a.dv, 0, cache, st)) != cudaSuccess) return e;
     const int qrows = a.B * a.Tq * a.Hq;
+    if (tc && (e = cudaMemsetAsync(a.dq, 0, static_cast<size_t>(qrows) * D * sizeof(float), st)) != cudaSuccess)
+        return e;
     bwd_rowdot_kernel<<<(qrows * 32 + 255) / 256, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(a.o),
-                                                              static_cast<const __nv_bfloat16*>(a.dout), qrows, D, Dr);
+                                                              static_cast<const __nv_bfloat16*>(a.dout), a.lse, qrows,
+                                                              a.Tq, a.Hq, D, Dr, tc ? ld : nullptr);
     const int per_row = a.idx != nullptr ? a.S_max : nblk;
     const long long entries = static_cast<long long>(rows) * a.Tq * per_row;
     const unsigned eb = static_cast<unsigned>((entries + 255) / 256);
     bwd_count_kernel<<<eb, 256, 0, st>>>(a.idx, a.counts, a.S_max, a.kv_len, a.B, a.Tq, a.Hkv, a.L_max, BS, per_row,
                                          nblk, bcnt, a.err);
-    bwd_scan_kernel<<<static_cast<unsigned>(rows), 1024, 0, st>>>(bcnt, nblk, boff);
+    bwd_scan_kernel<<<static_cast<unsigned>(rows), 1024, 0, st>>>(bcnt, nblk, boff, uoff);
     bwd_fill_kernel<<<eb, 256, 0, st>>>(a.idx, a.counts, a.S_max, a.kv_len, a.B, a.Tq, a.Hkv, a.L_max, BS, per_row,
                                         nblk, boff, cursor, list, list_stride, a.err);
+    if (tc) {
+        const int pairs = static_cast<int>(rows) * nblk;
+        bwd_units_kernel<<<(pairs + 255) / 256, 256, 0, st>>>(boff, uoff, static_cast<int>(rows), nblk, units);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        return launch_bwd_tc(a, BwdTcWork{ld, units, uoff, list, list_stride, nblk, counter});
+    }
     const int warps = a.B * a.Tq * a.Hkv;
     bwd_dq_kernel<D><<<(warps + 3) / 4, 128, 0, st>>>(
         static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k_cache),

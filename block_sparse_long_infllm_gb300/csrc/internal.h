@@ -82,6 +82,9 @@ struct BwdArgs {
 // box [box_rows][box_inner] and the 128-byte swizzle; false if the driver refuses.
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
                        uint32_t box_rows);
+// The same over fp32 elements (row stride inner*4 bytes; box_inner*4 must be at most 128).
+bool make_tmap_f32_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                      uint32_t box_rows);
 
 // Stage timing (infllmv2_profile_*): no-ops unless profiling is enabled.
 void prof_begin(cudaStream_t stream);
@@ -106,6 +109,20 @@ void decode_split_shape(const Params& p, int L_max, bool tree, int* blocks_per_s
 size_t decode_partial_bytes(int B, int n_draft, int Hkv, int d, int n_split);
 size_t bwd_workspace_bytes(int B, int Tq, int Hq, int Hkv, int L_max, int bs);
 cudaError_t launch_attention_bwd(const BwdArgs& a);
+// Tensor-core backward (d = 128, block size 128, 16 query heads per KV head) over the work list
+// that launch_attention_bwd builds; see bwd_tc.cu.
+constexpr int kBwdUnitTok = 128;  // tokens of a block's list per backward work unit
+struct BwdTcWork {
+    const float2* ld;     // [B*Tq*Hq] (lse * log2 e, dO . O) per query row
+    const int4* units;    // work units {b*Hkv + g, block, first, end} into the token lists
+    const int* uoff;      // [B*Hkv][nblk + 1] unit offsets per (b, g); [.][nblk] = units of (b, g)
+    const int* list;      // token lists per (b, g, block)
+    long long list_stride;
+    int nblk;
+    int* counter;         // zeroed work counter
+};
+bool bwd_tc_supported(const BwdArgs& a);
+cudaError_t launch_bwd_tc(const BwdArgs& a, const BwdTcWork& w);
 
 cudaError_t launch_decode_attention(const DecodeArgs& a, const int* idx, const int* counts, int idx_stride,
                                     float* part);

@@ -95,22 +95,6 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
     return d;
 }
 
-// Bounded wait of the load and MMA threads: gives up when another thread has raised the abort
-// flag, or sets it (and the device error word) when the budget runs out.
-__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*abort) return false;
-        if (clock64() - t0 > kWaitBudgetCycles) {
-            raise_error(err, kDevErrTimeout);
-            *abort = 1;
-            return false;
-        }
-    }
-    return true;
-}
-
 template <int D, int BS>
 __global__ void __launch_bounds__(kTcThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,

@@ -99,6 +99,32 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // CTAs and acquired here) before its later async-proxy (bulk copy) reads.
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
+// Order this thread's earlier generic-proxy shared-memory writes before later async-proxy reads of
+// them (a bulk copy or reduction out of shared memory, a tcgen05.mma operand).
+__device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// global[dst .. dst + bytes) += shared[src ..] element-wise in fp32, performed by the bulk-copy
+// unit at L2 (addresses 16-byte aligned, bytes a multiple of 16); tracked by the bulk group.
+__device__ __forceinline__ void bulk_reduce_add_f32(void* gdst, const void* ssrc, uint32_t bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
+                 ::"l"(static_cast<uint64_t>(__cvta_generic_to_global(gdst))), "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
+
+// Tiled 2-D reduction shared -> global (element-wise add) through a tensor map; the shared box
+// has the map's layout (here: 128-byte swizzled rows).  Rows outside the tensor are skipped.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* ssrc, int x, int y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(ssrc)), "r"(x), "r"(y)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk group of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until every committed bulk group of this thread has completed (writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -31,18 +31,28 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
-bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-                       uint32_t box_rows) {
+static bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType type, uint64_t elem_bytes, const void* base,
+                         uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint64_t dims[2] = {inner, rows};
-    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint64_t strides[1] = {inner * elem_bytes};
     const cuuint32_t box[2] = {box_inner, box_rows};
     const cuuint32_t estride[2] = {1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                          estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUresult r = fn(map, type, 2, const_cast<void*>(base), dims, strides, box, estride,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                       uint32_t box_rows) {
+    return make_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, rows, box_inner, box_rows);
+}
+
+bool make_tmap_f32_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                      uint32_t box_rows) {
+    return make_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, inner, rows, box_inner, box_rows);
 }
 
 }  // namespace infllmv2

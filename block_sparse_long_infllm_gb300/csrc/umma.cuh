@@ -144,4 +144,20 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Bounded wait of the load and MMA threads: gives up when another thread has raised the abort
+// flag, or sets it (and the device error word) when the budget runs out.
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitBudgetCycles) {
+            raise_error(err, kDevErrTimeout);
+            *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
 }  // namespace infllmv2

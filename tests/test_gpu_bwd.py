@@ -28,7 +28,8 @@ def _check(name, got, ref):
     assert mx <= 1e-2 * scale_max and mean <= 5e-3 * scale_mean, (name, mx, scale_max, mean, scale_mean)
 
 
-def _bwd_case(w, inp, dense=False):
+def _gpu_bwd(w, inp, dense=False):
+    """Forward (selection, o, lse) and backward on the GPU; returns (gpu dict, dq, dk, dv, dout bits)."""
     torch = torch_mod()
     L = lib()
     p = w.params()
@@ -51,6 +52,12 @@ def _bwd_case(w, inp, dense=False):
     L.sparse_attn_bwd(q, k, v, o, lse, dout, idx, cnt, kv, dq, dk, dv, ws, p)
     torch.cuda.synchronize()
     assert L.sync_status() == 0
+    return g, dq, dk, dv, dout_bits
+
+
+def _bwd_case(w, inp, dense=False):
+    p = w.params()
+    g, dq, dk, dv, dout_bits = _gpu_bwd(w, inp, dense)
     gidx = None if dense else g["idx"].cpu().numpy()
     gcnt = None if dense else g["counts"].cpu().numpy()
     rq, rk, rv = oracle.attention_bwd(_bf16_as_f64(inp["q"]), _bf16_as_f64(inp["k_cache"]),
@@ -78,3 +85,43 @@ def test_bwd_group16_ragged_chunk(cuda_lib, bs):
 def test_bwd_dense_causal(cuda_lib):
     w = synth.WORKLOADS["tiny_prefill_2k"].scaled(L=700, Tq=300, seed=4200)
     _bwd_case(w, synth.make_inputs(w), dense=True)
+
+
+def test_bwd_group16_several_units_per_block(cuda_lib):
+    # token lists longer than one 128-token work unit, tiles ending mid-list
+    w = synth.WORKLOADS["chunked_prefill_32k"].scaled(B=1, L=2000, Tq=301, Hq=32, Hkv=2, d=128, block_size=128,
+                                                       topk=4, n_local=2, dense_len=0, seed=4300)
+    _bwd_case(w, synth.make_inputs(w))
+
+
+def test_bwd_group16_dense(cuda_lib):
+    w = synth.WORKLOADS["chunked_prefill_32k"].scaled(B=1, L=700, Tq=300, Hq=16, Hkv=1, d=128, block_size=128,
+                                                       dense_len=0, seed=4400)
+    _bwd_case(w, synth.make_inputs(w), dense=True)
+
+
+def test_bwd_full_chunk_32k_sampled(cuda_lib):
+    """The 32K-context, 4096-query chunk: dq rows of sampled tokens against the oracle run on those
+    tokens alone, and sum_k dV[k] = sum over the group's query rows of dO (softmax rows sum to 1)
+    for every (sequence, KV head) at full size."""
+    w = synth.WORKLOADS["chunked_prefill_32k"]
+    inp = synth.make_inputs(w)
+    p = w.params()
+    g, dq, dk, dv, dout_bits = _gpu_bwd(w, inp)
+    dout = _bf16_as_f64(dout_bits)
+    dv_sum = dv.double().sum(dim=2).cpu().numpy()                  # [B, Hkv, d]
+    G = w.Hq // w.Hkv
+    do_sum = dout.reshape(w.B, w.Tq, w.Hkv, G, w.d).sum(axis=(1, 3))  # [B, Hkv, d]
+    do_abs = np.abs(dout).reshape(w.B, w.Tq, w.Hkv, G, w.d).sum(axis=(1, 3))
+    assert np.all(np.abs(dv_sum - do_sum) <= 4e-3 * do_abs + 1e-3), float(np.abs(dv_sum - do_sum).max())
+    gidx, gcnt = g["idx"].cpu().numpy(), g["counts"].cpu().numpy()
+    q64, k64, v64 = _bf16_as_f64(inp["q"]), _bf16_as_f64(inp["k_cache"]), _bf16_as_f64(inp["v_cache"])
+    dq_gpu = dq.cpu().numpy().astype(np.float64)
+    got, ref = [], []
+    for t in np.random.default_rng(5).choice(w.Tq, 6, replace=False).tolist() + [0, w.Tq - 1]:
+        pos = w.L - w.Tq + t
+        rq, _, _ = oracle.attention_bwd(q64[:, t:t + 1], k64, v64, np.array([pos + 1], dtype=np.int32),
+                                        gidx[:, :, t:t + 1], gcnt[:, :, t:t + 1], p, dout[:, t:t + 1])
+        got.append(dq_gpu[:, t])
+        ref.append(rq[:, 0])
+    _check("dq (sampled tokens)", np.stack(got), np.stack(ref))
