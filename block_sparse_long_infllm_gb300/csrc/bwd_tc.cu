@@ -12,8 +12,9 @@
 //   P^T  = exp2(S^T scale log2e - lse log2e)   bf16, written back over its S^T columns (A operand)
 //   dS^T = P^T o (dP^T - D)          bf16 into shared memory (K-major A of dK, MN-major B of dQ^T)
 //   dV  += P^T dO,  dK += dS^T Q     TMEM accumulators over the unit (128 columns each)
-//   dQ^T = K^T dS^T                  TMEM, 64 columns, head dim on the lanes; staged as fp32 rows in
-//                                    shared memory and added into dq by bulk reductions at L2
+//   dQ^T = K^T dS^T                  TMEM, 64 columns, head dim on the lanes; added into dq from
+//                                    registers by fp32 reductions at L2 (a warp covers 32
+//                                    consecutive head-dim elements of a row: one 128-byte request)
 // At the end of a unit dV and dK (times the softmax scale) are staged as 128-byte-swizzled fp32
 // boxes and added into dk and dv by tiled bulk reductions: the slices of one block may run on
 // different CTAs, and dq collects the partial sums of every block a token selected.
@@ -41,14 +42,13 @@ struct BtSmem {
     static constexpr int kVOff = kKV;
     static constexpr int kRingOff = 2 * kKV;                     // [stage] {Q, dO}
     static constexpr int kDsOff = kRingOff + kBtStages * 2 * kTile;  // dS^T: BS rows x 64 bf16
-    static constexpr int kDqOff = kDsOff + BS * kBtRows * 2;     // dQ staging: fp32 [64][D]
-    static constexpr int kFlushOff = kRingOff;                   // dV, dK staging over ring, dS, dQ staging
-    static constexpr int kLdOff = kDqOff + kBtRows * D * 4;      // [stage][64] (lse log2e, D)
+    static constexpr int kFlushOff = kRingOff;                   // dV, dK staging over ring and dS
+    static constexpr int kLdOff = kFlushOff + 2 * BS * D * 4;    // [stage][64] (lse log2e, D)
     static constexpr int kTokOff = kLdOff + kBtStages * kBtRows * 8;  // the unit's tokens
     static constexpr int kMiscOff = kTokOff + kBwdUnitTok * 4;   // unit {bg, blk, count}, tmem base, abort
     static constexpr int kBarOff = kMiscOff + 64;
     static constexpr int kBytes = kBarOff + 32 * 8 + 1024;       // + alignment slack
-    static_assert(kFlushOff + 2 * BS * D * 4 <= kLdOff, "dV and dK staging must fit below the row data");
+    static_assert(kDsOff + BS * kBtRows * 2 <= kLdOff, "ring and dS^T lie inside the dV, dK staging");
 };
 
 template <int D, int BS>
@@ -239,8 +239,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         issued = true;
                     }
                     if (i + 1 < ntiles) {
-                        // S^T(j+1) into the other buffer (its P^T(j-1) was read by dV(j-1), issued earlier)
+                        // S^T(j+1) into the other buffer, whose P^T(j-1) dV(j-1) has read: the commit
+                        // after dQ^T(j-1) covers it (already complete by now: dP(j) followed it)
                         const int st1 = (j + 1) % kBtStages;
+                        if (j > 0 && !(ok = tc_wait(&bar_free[(j - 1) % kBtStages], ((j - 1) / kBtStages) & 1,
+                                                    s_abort, err)))
+                            break;
                         if (!(ok = tc_wait(&bar_full[st1], ((j + 1) / kBtStages) & 1, s_abort, err))) break;
                         tc_fence_after();
                         qk(tmem + kColS + ((j + 1) & 1) * kBtRows, kb, ring + st1 * 2 * SM::kTile);
@@ -289,7 +293,6 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int r = 32 * q4 + lane;  // key of the block (S, dP, dV, dK) / head-dim row (dQ^T)
         const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
         const float scale_log2 = scale * 1.4426950408889634f;
-        float* stg = reinterpret_cast<float*>(base + SM::kDqOff);
         int j = 0, nstg = 0;
         bool ok = true;
         // One use of the fp32 staging area: the bulk unit has read its previous contents ...
@@ -306,7 +309,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mbar_arrive(bar_stg_full);
             return tid == 0 ? tc_wait(bar_stg_full, nstg & 1, s_abort, err) : true;
         };
-        // dQ^T(jj) (tile ii of the unit) -> fp32 rows -> dq
+        // dQ^T(jj) (tile ii of the unit) -> dq: element (head-dim row r, query row 32h + c)
         auto drain_dq = [&](int jj, int ii, int b, int g, int cnt) -> bool {
             if (!tc_wait(bar_dqf, jj & 1, s_abort, err)) return false;
             tc_fence_after();
@@ -315,20 +318,15 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tmem_ld_wait(v);
             tc_fence_before();
             mbar_arrive(bar_dqe);
-            if (!stage_begin()) return false;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) stg[(32 * h + c) * D + r] = __uint_as_float(v[c]) * scale;
-            const bool fine = stage_end();
-            if (tid == 0 && fine) {
-                for (int k = 0; k < kBtTok && kBtTok * ii + k < cnt; ++k) {
-                    const int t = s_tok[kBtTok * ii + k];
-                    bulk_reduce_add_f32(dq + (static_cast<size_t>(b * Tq + t) * Hq + g * G) * D, stg + k * G * D,
-                                        G * D * 4);
-                }
-                bulk_commit();
+            for (int e = 0; e < 2; ++e) {
+                const int k = kBtTok * ii + 2 * h + e;
+                if (k >= cnt) break;
+                float* dst = dq + (static_cast<size_t>(b * Tq + s_tok[k]) * Hq + g * G) * D + r;
+#pragma unroll
+                for (int c = 0; c < 16; ++c) atomicAdd(dst + c * D, __uint_as_float(v[16 * e + c]) * scale);
             }
-            ++nstg;
-            return fine;
+            return true;
         };
         for (int u = 0; ok; ++u) {
             if (!(ok = tc_wait(bar_kv, u & 1, s_abort, err))) break;
@@ -347,17 +345,24 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     const int k = kBtTok * i + 2 * h + e;
                     pos[e] = k < cnt ? Lb - Tq + s_tok[k] : -1;
                 }
-                const float2* lv = reinterpret_cast<const float2*>(base + SM::kLdOff) + st * kBtRows + 32 * h;
+                // (lse log2e, D) of this half's 32 query rows, two rows per 16-byte broadcast load
+                const float4* lv = reinterpret_cast<const float4*>(base + SM::kLdOff) + (st * kBtRows + 32 * h) / 2;
                 if (!(ok = tc_wait(&bar_s[j & 1], (j >> 1) & 1, s_abort, err))) break;
                 tc_fence_after();
                 const uint32_t tS = tmem + kColS + (j & 1) * kBtRows + 32 * h + lane_off;
                 uint32_t sv[32];
                 tmem_ld32(tS, sv);
                 tmem_ld_wait(sv);
-                float p[32];
+                float p[32], dr[32];
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    p[c] = key <= pos[c >> 4] ? fast_exp2(fmaf(__uint_as_float(sv[c]), scale_log2, -lv[c].x)) : 0.f;
+                for (int e = 0; e < 16; ++e) {
+                    const float4 l2 = lv[e];
+                    const bool live = key <= pos[e >> 3];
+                    p[2 * e] = live ? fast_exp2(fmaf(__uint_as_float(sv[2 * e]), scale_log2, -l2.x)) : 0.f;
+                    p[2 * e + 1] = live ? fast_exp2(fmaf(__uint_as_float(sv[2 * e + 1]), scale_log2, -l2.z)) : 0.f;
+                    dr[2 * e] = l2.y;
+                    dr[2 * e + 1] = l2.w;
+                }
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
@@ -373,8 +378,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 uint32_t dsw[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    dsw[e] = pack_bf16x2(p[2 * e] * (__uint_as_float(dv[2 * e]) - lv[2 * e].y),
-                                         p[2 * e + 1] * (__uint_as_float(dv[2 * e + 1]) - lv[2 * e + 1].y));
+                    dsw[e] = pack_bf16x2(p[2 * e] * (__uint_as_float(dv[2 * e]) - dr[2 * e]),
+                                         p[2 * e + 1] * (__uint_as_float(dv[2 * e + 1]) - dr[2 * e + 1]));
                 // row r of the dS^T tile: 64 bf16 = 8 chunks of 16 bytes, this half's are 4h..4h+3
                 unsigned char* row = base + SM::kDsOff + r * 128;
 #pragma unroll
