@@ -493,6 +493,7 @@ def run_prefill(args) -> dict:
     pk = peaks()
     att_tf = fl_attn / (stage_ms["attend"] * 1e-3) / 1e12
     step_tf = (fl_attn + fl_score) / (ms * 1e-3) / 1e12
+    backward = run_prefill_backward(args, w, p, q, k, v, o, lse, idx, cnt, kv_len, flush, 10.0 * w.d * attended, pk)
     return {"workload": PREFILL, "value": w.Tq / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms, "steps": K,
             "stages_ms": {kk: round(vv, 4) for kk, vv in stage_ms.items()},
             "algorithmic_gflop": {"attention": fl_attn / 1e9, "score": fl_score / 1e9},
@@ -502,7 +503,60 @@ def run_prefill(args) -> dict:
                          "traffic": ncu_traffic("prefill_tc_kernel",
                                                 source_sha("prefill_tc.cu", "umma.cuh", "common.cuh", "tma.cuh"))},
             "step_tflops": round(step_tf, 2), "step_frac": round(step_tf / pk["bf16_tflops"], 4),
-            "gpu_launches": 4 * K}
+            "gpu_launches": 4 * K, "backward": backward}
+
+
+def run_prefill_backward(args, w, p, q, k, v, o, lse, idx, cnt, kv_len, flush, flops: float, pk: dict) -> dict:
+    """dQ, dK, dV of the chunk's attention through its selection (the trainable sparse attention's
+    backward), timed like the forward: L2 flushed before every call, CUDA events on the stream.
+    Algorithmic FLOPs: 10 d per attended (query head, key) -- S and dP recomputed, dV, dK, dQ."""
+    import numpy as np
+    import torch
+
+    from block_sparse_long_infllm_gb300 import infllmv2, synth
+    rng = np.random.default_rng(w.seed + 7)
+    dout = dev_bf16(synth.f32_to_bf16_bits(rng.standard_normal(tuple(q.shape)).astype(np.float32)))
+    dq = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    dk = torch.empty(k.shape, dtype=torch.float32, device="cuda")
+    dv = torch.empty(v.shape, dtype=torch.float32, device="cuda")
+    ws = torch.empty(infllmv2.workspace_size(infllmv2.ENTRY_SPARSE_ATTN_BWD, w.B, w.Tq, w.Hq, w.Hkv, w.d, w.L_max,
+                                             p), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def call():
+        infllmv2.sparse_attn_bwd(q, k, v, o, lse, dout, idx, cnt, kv_len, dq, dk, dv, ws, p)
+
+    for _ in range(3):
+        flush()
+        call()
+    torch.cuda.synchronize()
+    K = args.prefill_steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush()
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    infllmv2.profile_enable(True)
+    stages: dict[str, list[float]] = {}
+    for _ in range(max(3, K // 2)):
+        flush()
+        call()
+        for name, t in infllmv2.profile_read():
+            stages.setdefault(name, []).append(t)
+    infllmv2.profile_enable(False)
+    stage_ms = {kk: statistics.median(vv) for kk, vv in stages.items()}
+    assert infllmv2.sync_status() == 0
+    grad_tf = flops / (stage_ms["bwd_grad"] * 1e-3) / 1e12
+    return {"ms_per_call": ms, "calls": K, "stages_ms": {kk: round(vv, 4) for kk, vv in stage_ms.items()},
+            "algorithmic_gflop": flops / 1e9, "call_tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+            "roofline": {"bound": "tensor", "kernel": "bwd_tc_kernel", "achieved": round(grad_tf, 2),
+                         "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(grad_tf / pk["bf16_tflops"], 4),
+                         "traffic": ncu_traffic("bwd_tc_kernel",
+                                                source_sha("bwd_tc.cu", "umma.cuh", "common.cuh", "tma.cuh"))},
+            "gpu_launches_per_call": 6, "memsets_per_call": 4}
 
 
 # ------------------------------------------------------------------ oracle (CPU) baseline

@@ -325,10 +325,8 @@ int infllmv2_sparse_attn_bwd(const void* q, const void* k_cache, const void* v_c
     if (err == nullptr) return INFLLMV2_ERR_CUDA;
     infllmv2::BwdArgs a{q, k_cache, v_cache, o, dout, lse, idx, counts, S_max, kv_len, B, Tq, Hq, Hkv, d, L_max,
                         dq, dk, dv, workspace, p, err, static_cast<cudaStream_t>(stream)};
-    prof_begin(a.stream);
-    const cudaError_t e = infllmv2::launch_attention_bwd(a);
-    prof_mark(a.stream, "backward");
-    return cuda_status(e);
+    prof_begin(a.stream);  // stages "bwd_prep" (inverse of the selection) and "bwd_grad" (the gradients)
+    return cuda_status(infllmv2::launch_attention_bwd(a));
 }
 
 int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache, const void* kernel_cache,

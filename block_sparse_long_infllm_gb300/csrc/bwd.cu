@@ -29,24 +29,30 @@ namespace infllmv2 {
 
 constexpr int kBwdSplit = 128;  // tokens of a block's list per dK/dV CTA
 
-// ---- 1. D = dO . O per (token, head); with `ld`, also (lse * log2 e, D) per row
+// ---- 1. D = dO . O per (token, head); with `ld`, also (lse * log2 e, D) per row.  d / 8 threads
+// per row, 16 bytes of O and of dO each.
 __global__ void bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                                   const float* __restrict__ lse, int rows, int Tq, int Hq, int d, float* __restrict__ D,
                                   float2* __restrict__ ld) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (warp >= rows) return;
-    const __nv_bfloat16* a = o + static_cast<size_t>(warp) * d;
-    const __nv_bfloat16* b = dout + static_cast<size_t>(warp) * d;
+    const int tpr = d / 8;  // 8 or 16: a power of two dividing the warp
+    const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
+    const int row = gtid / tpr, part = gtid % tpr;
+    const bool live = row < rows;
     float acc = 0.f;
-    for (int x = lane; x < d; x += 32) acc += __bfloat162float(a[x]) * __bfloat162float(b[x]);
+    if (live) {
+        const uint4 a = ldg_v4(o + static_cast<size_t>(row) * d + 8 * part);
+        const uint4 b = ldg_v4(dout + static_cast<size_t>(row) * d + 8 * part);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-        D[warp] = acc;
+        for (int e = 0; e < 4; ++e) acc += bf16_lo(aw[e]) * bf16_lo(bw[e]) + bf16_hi(aw[e]) * bf16_hi(bw[e]);
+    }
+    for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (live && part == 0) {
+        D[row] = acc;
         if (ld != nullptr) {
-            const int h = warp % Hq, bt = warp / Hq;  // row (b*Tq + t)*Hq + h; lse is [B][Hq][Tq]
+            const int h = row % Hq, bt = row / Hq;  // row (b*Tq + t)*Hq + h; lse is [B][Hq][Tq]
             const int bb = bt / Tq, t = bt % Tq;
-            ld[warp] = make_float2(lse[(static_cast<size_t>(bb) * Hq + h) * Tq + t] * 1.4426950408889634f, acc);
+            ld[row] = make_float2(lse[(static_cast<size_t>(bb) * Hq + h) * Tq + t] * 1.4426950408889634f, acc);
         }
     }
 }
@@ -71,22 +77,38 @@ __device__ __forceinline__ int bwd_entry(const int* idx, const int* counts, int 
     return blk;
 }
 
-__global__ void bwd_count_kernel(const int* __restrict__ idx, const int* __restrict__ counts, int S_max,
-                                 const int* __restrict__ kv_len, int B, int Tq, int Hkv, int L_max, int bs, int per_row,
-                                 int nblk, int* __restrict__ bcnt, int* __restrict__ err) {
-    const long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int row = static_cast<int>(e / per_row), r = static_cast<int>(e % per_row);
-    if (row >= B * Hkv * Tq) return;
+// Entry e = r * n_rows + row (rows fastest): a warp sees 32 consecutive tokens at the same
+// selection slot, which mostly name the same few blocks (the selection lists are ascending), so the
+// per-block counters are bumped once per distinct block of the warp.
+__device__ __forceinline__ int bwd_entry_at(const int* idx, const int* counts, int S_max, const int* kv_len, int B,
+                                            int Tq, int Hkv, int L_max, int bs, int per_row, int nblk, long long e,
+                                            int* err, int* row_out) {
+    const int n_rows = B * Hkv * Tq;
+    const int row = static_cast<int>(e % n_rows), r = static_cast<int>(e / n_rows);
+    *row_out = row;
+    if (r >= per_row) return -1;
     const int b = row / (Hkv * Tq);
     const int L = kv_len[b];
     if (L < Tq || L > L_max) {
         if (r == 0 && row % (Hkv * Tq) == 0) raise_error(err, kDevErrIndex);
-        return;
+        return -1;
     }
     const int t = row % Tq;
     const int bt = (L - Tq + t) / bs;
-    const int blk = bwd_entry(idx, counts, S_max, row, r, bt, nblk, err);
-    if (blk >= 0) atomicAdd(&bcnt[(row / Tq) * nblk + blk], 1);
+    return bwd_entry(idx, counts, S_max, row, r, bt, nblk, err);
+}
+
+__global__ void bwd_count_kernel(const int* __restrict__ idx, const int* __restrict__ counts, int S_max,
+                                 const int* __restrict__ kv_len, int B, int Tq, int Hkv, int L_max, int bs, int per_row,
+                                 int nblk, int* __restrict__ bcnt, int* __restrict__ err) {
+    const long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long n = static_cast<long long>(B) * Hkv * Tq * per_row;
+    int row = 0;
+    const int blk = e < n ? bwd_entry_at(idx, counts, S_max, kv_len, B, Tq, Hkv, L_max, bs, per_row, nblk, e, err, &row)
+                          : -1;
+    const int key = blk >= 0 ? (row / Tq) * nblk + blk : -1;
+    const unsigned same = __match_any_sync(0xffffffffu, key);
+    if (key >= 0 && (threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(&bcnt[key], __popc(same));
 }
 
 // Exclusive scans of one (b, g)'s block counts -> token offsets boff [nblk + 1], and of the units
@@ -159,18 +181,19 @@ __global__ void bwd_fill_kernel(const int* __restrict__ idx, const int* __restri
                                 int nblk, const int* __restrict__ boff, int* __restrict__ cursor,
                                 int* __restrict__ list, long long list_stride, int* __restrict__ err) {
     const long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int row = static_cast<int>(e / per_row), r = static_cast<int>(e % per_row);
-    if (row >= B * Hkv * Tq) return;
-    const int b = row / (Hkv * Tq);
-    const int L = kv_len[b];
-    if (L < Tq || L > L_max) return;
-    const int t = row % Tq;
-    const int bt = (L - Tq + t) / bs;
-    const int blk = bwd_entry(idx, counts, S_max, row, r, bt, nblk, err);
-    if (blk < 0) return;
+    const long long n = static_cast<long long>(B) * Hkv * Tq * per_row;
+    int row = 0;
+    const int blk = e < n ? bwd_entry_at(idx, counts, S_max, kv_len, B, Tq, Hkv, L_max, bs, per_row, nblk, e, nullptr,
+                                         &row)
+                          : -1;
     const int bg = row / Tq;
-    const int at = atomicAdd(&cursor[bg * nblk + blk], 1);
-    list[bg * list_stride + boff[static_cast<size_t>(bg) * (nblk + 1) + blk] + at] = t;
+    const int key = blk >= 0 ? bg * nblk + blk : -1;
+    const unsigned same = __match_any_sync(0xffffffffu, key);
+    const int lane = threadIdx.x & 31, leader = __ffs(same) - 1;
+    int at = 0;
+    if (key >= 0 && lane == leader) at = atomicAdd(&cursor[key], __popc(same));
+    at = __shfl_sync(same, at, leader) + __popc(same & ((1u << lane) - 1u));
+    if (key >= 0) list[bg * list_stride + boff[static_cast<size_t>(bg) * (nblk + 1) + blk] + at] = row % Tq;
 }
 
 // Work units {b*Hkv + g, block, first, end}: each block's token list cut into slices of at most
@@ -496,7 +519,7 @@ static cudaError_t launch_bwd_t(const BwdArgs& a) {
     const int qrows = a.B * a.Tq * a.Hq;
     if (tc && (e = cudaMemsetAsync(a.dq, 0, static_cast<size_t>(qrows) * D * sizeof(float), st)) != cudaSuccess)
         return e;
-    bwd_rowdot_kernel<<<(qrows * 32 + 255) / 256, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(a.o),
+    bwd_rowdot_kernel<<<static_cast<unsigned>((static_cast<long long>(qrows) * (D / 8) + 255) / 256), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(a.o),
                                                               static_cast<const __nv_bfloat16*>(a.dout), a.lse, qrows,
                                                               a.Tq, a.Hq, D, Dr, tc ? ld : nullptr);
     const int per_row = a.idx != nullptr ? a.S_max : nblk;
@@ -511,8 +534,12 @@ static cudaError_t launch_bwd_t(const BwdArgs& a) {
         const int pairs = static_cast<int>(rows) * nblk;
         bwd_units_kernel<<<(pairs + 255) / 256, 256, 0, st>>>(boff, uoff, static_cast<int>(rows), nblk, units);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        return launch_bwd_tc(a, BwdTcWork{ld, units, uoff, list, list_stride, nblk, counter});
+        prof_mark(st, "bwd_prep");
+        e = launch_bwd_tc(a, BwdTcWork{ld, units, uoff, list, list_stride, nblk, counter});
+        prof_mark(st, "bwd_grad");
+        return e;
     }
+    prof_mark(st, "bwd_prep");
     const int warps = a.B * a.Tq * a.Hkv;
     bwd_dq_kernel<D><<<(warps + 3) / 4, 128, 0, st>>>(
         static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k_cache),
@@ -523,7 +550,9 @@ static cudaError_t launch_bwd_t(const BwdArgs& a) {
         static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k_cache),
         static_cast<const __nv_bfloat16*>(a.v_cache), static_cast<const __nv_bfloat16*>(a.dout), a.lse, Dr, a.kv_len,
         a.Tq, a.Hq, a.Hkv, a.L_max, nblk, max_splits, boff, list, list_stride, scale, a.dk, a.dv);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    prof_mark(st, "bwd_grad");
+    return e;
 }
 
 cudaError_t launch_attention_bwd(const BwdArgs& a) {

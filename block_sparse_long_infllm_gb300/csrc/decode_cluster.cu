@@ -122,7 +122,8 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     __shared__ float s_f[8][16];  // merge weights of the 8 warps per row
     __shared__ unsigned long long s_cv[kDcCand];          // candidates >= tau: key << 32 | ~block
     __shared__ int s_rk[kDcCand];                          // their ranks
-    __shared__ int s_pos[kDcCand];                         // positions of the chosen ones
+    __shared__ uint32_t s_bits[kDcFastPer * kDcThreads / 32];  // chosen blocks (fast path), one bit each
+    __shared__ int s_wpre[kDcFastPer * kDcThreads / 32];       // chosen blocks below each bitmap word
     __shared__ uint64_t s_bar_piece[kDcKRows / 128];       // scoring: kernel rows of piece p landed
     __shared__ uint64_t s_bar_mma[2], s_bar_free[2];       // scoring accumulator buffers: written / read
     __shared__ uint32_t s_tmem;
@@ -372,6 +373,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                             s_cv[c_before++] = (static_cast<unsigned long long>(kv[u]) << 32) |
                                                static_cast<uint32_t>(~(tid + u * kDcThreads));
                     for (int i = tid; i < c_total; i += kDcThreads) s_rk[i] = 0;
+                    for (int i = tid; i < kDcFastPer * kDcThreads / 32; i += kDcThreads) s_bits[i] = 0u;
                     __syncthreads();
                     // rank of candidate i = number of better candidates; `sp` threads share each
                     // candidate, each comparing it with one slice of the others
@@ -382,8 +384,16 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                         if (i < c_total) {
                             const unsigned long long vi = s_cv[i];
                             const int j1 = min(c_total, (part + 1) * seg);
-                            int rnk = 0;
-                            for (int j = part * seg; j < j1; ++j) rnk += s_cv[j] > vi ? 1 : 0;
+                            int r0 = 0, r1 = 0, r2 = 0, r3 = 0;  // four independent chains of loads
+                            int j = part * seg;
+                            for (; j + 4 <= j1; j += 4) {
+                                r0 += s_cv[j] > vi ? 1 : 0;
+                                r1 += s_cv[j + 1] > vi ? 1 : 0;
+                                r2 += s_cv[j + 2] > vi ? 1 : 0;
+                                r3 += s_cv[j + 3] > vi ? 1 : 0;
+                            }
+                            for (; j < j1; ++j) r0 += s_cv[j] > vi ? 1 : 0;
+                            const int rnk = r0 + r1 + r2 + r3;
                             if (rnk) atomicAdd(&s_rk[i], rnk);
                         }
                         for (int i2 = kDcThreads / sp + tid; i2 < c_total; i2 += kDcThreads) {  // c_total > 256
@@ -394,31 +404,32 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                         }
                     }
                     __syncthreads();
-                    // position of a chosen candidate = chosen candidates with a lower block
-                    for (int i = tid; i < c_total; i += kDcThreads) s_pos[i] = 0;
+                    // position of a chosen candidate = chosen blocks below it: bitmap of the chosen
+                    // blocks, word prefix popcounts (one warp), then one popcount per candidate
+                    for (int i = tid; i < c_total; i += kDcThreads)
+                        if (s_rk[i] < k) {
+                            const uint32_t blk = ~static_cast<uint32_t>(s_cv[i]);
+                            atomicOr(&s_bits[blk >> 5], 1u << (blk & 31));
+                        }
                     __syncthreads();
-                    {
-                        const int i = tid / sp, part = tid % sp;
-                        if (i < c_total && s_rk[i] < k) {
-                            const uint32_t bi = ~static_cast<uint32_t>(s_cv[i]);
-                            const int j1 = min(c_total, (part + 1) * seg);
-                            int before = 0;
-                            for (int j = part * seg; j < j1; ++j)
-                                before += (s_rk[j] < k && ~static_cast<uint32_t>(s_cv[j]) < bi) ? 1 : 0;
-                            if (before) atomicAdd(&s_pos[i], before);
+                    if (warp == 0) {
+                        const int c0 = __popc(s_bits[2 * lane]), c1 = __popc(s_bits[2 * lane + 1]);
+                        int incl = c0 + c1;
+#pragma unroll
+                        for (int off = 1; off < 32; off <<= 1) {
+                            const int x = __shfl_up_sync(0xffffffffu, incl, off);
+                            if (lane >= off) incl += x;
                         }
-                        for (int i2 = kDcThreads / sp + tid; i2 < c_total; i2 += kDcThreads) {
-                            if (s_rk[i2] >= k) continue;
-                            const uint32_t bi = ~static_cast<uint32_t>(s_cv[i2]);
-                            int before = 0;
-                            for (int j = 0; j < c_total; ++j)
-                                before += (s_rk[j] < k && ~static_cast<uint32_t>(s_cv[j]) < bi) ? 1 : 0;
-                            atomicAdd(&s_pos[i2], before);
-                        }
+                        s_wpre[2 * lane] = incl - c0 - c1;
+                        s_wpre[2 * lane + 1] = incl - c1;
                     }
                     __syncthreads();
                     for (int i = tid; i < c_total; i += kDcThreads)
-                        if (s_rk[i] < k) sel[a_init + s_pos[i]] = static_cast<int>(~static_cast<uint32_t>(s_cv[i]));
+                        if (s_rk[i] < k) {
+                            const uint32_t blk = ~static_cast<uint32_t>(s_cv[i]);
+                            sel[a_init + s_wpre[blk >> 5] + __popc(s_bits[blk >> 5] & ((1u << (blk & 31)) - 1u))] =
+                                static_cast<int>(blk);
+                        }
                     for (int i = tid; i < a_init; i += kDcThreads) sel[i] = i;
                     for (int i = tid; i < nn - lo_f; i += kDcThreads) sel[a_init + k + i] = lo_f + i;
                     total = a_init + k + (nn - lo_f);
