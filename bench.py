@@ -559,6 +559,81 @@ def run_prefill_backward(args, w, p, q, k, v, o, lse, idx, cnt, kv_len, flush, f
             "gpu_launches_per_call": 6, "memsets_per_call": 4}
 
 
+# ------------------------------------------------------------------ tree verification (secondary)
+
+def run_tree(args, name: str, **scale) -> dict:
+    """Verification of a draft tree (one call scores, selects and attends for every draft),
+    timed with the L2 flushed before each call.  Algorithmic bytes: the kernel cache once per
+    (sequence, KV head), K and V of the union of the drafts' selected blocks once, the drafts'
+    own K and V."""
+    import numpy as np
+    import torch
+
+    from block_sparse_long_infllm_gb300 import infllmv2, synth
+    w = synth.WORKLOADS[name].scaled(**scale) if scale else synth.WORKLOADS[name]
+    inp = synth.make_inputs(w)
+    p = w.params()
+    q, k, v = dev_bf16(inp["q"]), dev_bf16(inp["k_cache"]), dev_bf16(inp["v_cache"])
+    dk, dvv = dev_bf16(inp["draft_k"]), dev_bf16(inp["draft_v"])
+    mask = torch.from_numpy(np.ascontiguousarray(inp["tree_mask"]).view(np.int64)).cuda()
+    kv_len = torch.from_numpy(inp["kv_len"]).cuda()
+    M = (w.L - w.kernel_size) // w.kernel_stride + 1
+    kern = torch.zeros((w.B, w.Hkv, M, w.d), dtype=torch.bfloat16, device="cuda")
+    infllmv2.kernel_pool(k, kern, 0, w.L, p)
+    S_cap = infllmv2.selection_capacity(p, w.L_max)
+    idx = torch.empty((w.B, w.Hkv, w.Tq, S_cap), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((w.B, w.Hkv, w.Tq), dtype=torch.int32, device="cuda")
+    o = torch.empty_like(q)
+    ws = torch.empty(infllmv2.workspace_size(infllmv2.ENTRY_DECODE, w.B, w.Tq, w.Hq, w.Hkv, w.d, w.L_max, p),
+                     dtype=torch.uint8, device="cuda")
+    flush = Flusher()
+    stream = torch.cuda.current_stream()
+
+    def call():
+        infllmv2.decode(q, k, v, kern, kv_len, o, ws, p, draft_k=dk, draft_v=dvv, tree_mask=mask,
+                        idx_out=idx, counts_out=cnt)
+
+    for _ in range(3):
+        flush()
+        call()
+    torch.cuda.synchronize()
+    K = args.prefill_steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush()
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    infllmv2.profile_enable(True)
+    stages: dict[str, list[float]] = {}
+    for _ in range(max(3, K // 2)):
+        flush()
+        call()
+        for nm, t in infllmv2.profile_read():
+            stages.setdefault(nm, []).append(t)
+    infllmv2.profile_enable(False)
+    assert infllmv2.sync_status() == 0
+    counts, sel = cnt.cpu().numpy(), idx.cpu().numpy()
+    kv_tok = 0
+    for b in range(w.B):
+        for g in range(w.Hkv):
+            union = set()
+            for t in range(w.Tq):
+                union.update(sel[b, g, t, :counts[b, g, t]].tolist())
+            L = int(inp["kv_len"][b])
+            kv_tok += sum(min(w.block_size, L - x * w.block_size) for x in union)
+    alg = (w.B * w.Hkv * M * w.d * 2 + kv_tok * w.d * 4 + 2 * w.B * w.Hkv * w.Tq * w.d * 2
+           + 2 * w.B * w.Tq * w.Hq * w.d * 2)
+    gbs = alg / (ms * 1e-3) / 1e9
+    pk = peaks()
+    return {"workload": name if not scale else f"{name} scaled {scale}", "batch": w.B, "drafts": w.Tq,
+            "ms_per_call": ms, "calls": K, "drafts_per_s": w.B * w.Tq / (ms * 1e-3),
+            "stages_ms": {kk: round(statistics.median(vv), 4) for kk, vv in stages.items()},
+            "algorithmic_bytes": alg, "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4)}
+
+
 # ------------------------------------------------------------------ oracle (CPU) baseline
 
 def oracle_rows(inp, w, kern, rows):
@@ -664,6 +739,8 @@ def main():
     out = {"metric": METRIC, "profiling_only": True} if args.no_decode else run_decode(args, world, rank)[0]
     if not args.no_prefill:
         out["prefill"] = run_prefill(args)
+        out["tree_verify"] = [run_tree(args, "tree_verify_64k"),
+                              run_tree(args, "tree_verify_64k", B=4, Tq=64, seed=1104)]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline()
     if world > 1:
