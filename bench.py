@@ -385,6 +385,65 @@ def run_decode(args, world, rank):
     return out, d
 
 
+def run_decode_append(args, d) -> dict:
+    """The whole decode step of a serving loop through infllmv2_decode_step: append the new
+    token's K and V (and pool the semantic kernel it completes) and decode, in the CUDA graph,
+    replicas cycled as in the headline.  The appended token is the cache's last row, which completes a kernel: every step
+    pays the pooling (the worst case; a kernel completes every 16 tokens)."""
+    import numpy as np
+    import torch
+
+    from block_sparse_long_infllm_gb300 import infllmv2, synth
+    w = d["w"]
+    R = len(d["rep"])
+    rng = np.random.default_rng(w.seed + 11)
+    news = [(dev_bf16(synth.f32_to_bf16_bits(rng.standard_normal((w.B, w.Hkv, w.d)).astype(np.float32))),
+             dev_bf16(synth.f32_to_bf16_bits(rng.standard_normal((w.B, w.Hkv, w.d)).astype(np.float32))))
+            for _ in range(R)]
+
+    def step(r):
+        rep = d["rep"][r % R]
+        kn, vn = news[r % R]
+        infllmv2.decode_step(rep["q"], kn, vn, rep["k"], rep["v"], rep["kern"], d["kv_len"], d["o"], d["ws"], d["p"],
+                             lse=d["lse"], idx_out=d["idx"], counts_out=d["counts"])
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for r in range(R):
+            step(r)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for r in range(R):
+            step(r)
+    g.replay()
+    torch.cuda.synchronize()
+    K = max(R, (min(args.steps, 2000) // R) * R)
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K // R):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / K
+    infllmv2.profile_enable(True)
+    names = set()
+    for r in range(8):
+        step(r)
+        names.update(nm for nm, _ in infllmv2.profile_read())
+    infllmv2.profile_enable(False)
+    assert infllmv2.sync_status() == 0
+    fused = names == {"fused"}
+    return {"ms_per_step": ms, "steps": K, "value": w.B * w.Tq / (ms * 1e-3), "unit": UNIT,
+            "gpu_launches_per_step": 1 if fused else 2,
+            "note": "CUDA graph of infllmv2_decode_step per step (append of the new token's K/V and the kernel it "
+                    "completes, then decode" + (", one cluster kernel" if fused else ", append kernel then decode") +
+                    "); each step pools a kernel (worst case)"}
+
+
 def run_decode_e2e(d, n: int) -> dict:
     """Same step through the public call with host buffers: copy this step's query
     (and lengths) from pinned host memory, decode, read the output back; wall clock."""
@@ -736,7 +795,11 @@ def main():
     torch.cuda.set_device(local)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
-    out = {"metric": METRIC, "profiling_only": True} if args.no_decode else run_decode(args, world, rank)[0]
+    if args.no_decode:
+        out = {"metric": METRIC, "profiling_only": True}
+    else:
+        out, dec = run_decode(args, world, rank)
+        out["decode_step_with_append"] = run_decode_append(args, dec)
     if not args.no_prefill:
         out["prefill"] = run_prefill(args)
         out["tree_verify"] = [run_tree(args, "tree_verify_64k"),

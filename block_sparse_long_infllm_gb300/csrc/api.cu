@@ -249,6 +249,28 @@ int infllmv2_kernel_pool(const void* k_cache, void* kernel_cache, int B, int Hkv
     return cuda_status(e);
 }
 
+int infllmv2_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, void* kernel_cache,
+                    const int32_t* kv_len, int B, int Hkv, int d, int L_max, int M_max, const infllmv2_params* params,
+                    void* stream) {
+    Params p;
+    if (int rc = check_params(params, d, &p)) return rc;
+    if (d != 64 && d != 128) return INFLLMV2_ERR_UNSUPPORTED;
+    if (B < 0 || Hkv <= 0 || L_max <= 0 || L_max > kMaxLen || M_max < 0) return INFLLMV2_ERR_INVALID_ARG;
+    if (B == 0) return INFLLMV2_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !kv_len || (M_max > 0 && !kernel_cache)) return INFLLMV2_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(kv_len) ||
+        (kernel_cache && !aligned16(kernel_cache)))
+        return INFLLMV2_ERR_INVALID_ARG;
+    int* err = device_error_ptr();
+    if (err == nullptr) return INFLLMV2_ERR_CUDA;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    prof_begin(st);
+    const cudaError_t e = infllmv2::launch_append(k_new, v_new, k_cache, v_cache, kernel_cache, kv_len, B, Hkv, L_max,
+                                                  M_max, d, p.kernel_size, p.kernel_stride, err, st);
+    prof_mark(st, "append");
+    return cuda_status(e);
+}
+
 int infllmv2_block_select(const void* q, const void* kernel_cache, const int32_t* kv_len, int B, int Tq, int Hq,
                           int Hkv, int d, int L_max, int M_max, int32_t* idx, int32_t* counts, int S_max,
                           void* workspace, size_t ws_bytes, const infllmv2_params* params, void* stream) {
@@ -327,6 +349,52 @@ int infllmv2_sparse_attn_bwd(const void* q, const void* k_cache, const void* v_c
                         dq, dk, dv, workspace, p, err, static_cast<cudaStream_t>(stream)};
     prof_begin(a.stream);  // stages "bwd_prep" (inverse of the selection) and "bwd_grad" (the gradients)
     return cuda_status(infllmv2::launch_attention_bwd(a));
+}
+
+int infllmv2_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                         void* kernel_cache, const int32_t* kv_len, int B, int Hq, int Hkv, int d, int L_max, int M_max,
+                         void* o, float* lse, int32_t* idx_out, int32_t* counts_out, int S_max, void* workspace,
+                         size_t ws_bytes, const infllmv2_params* params, void* stream) {
+    Params p;
+    if (int rc = check_params(params, d, &p)) return rc;
+    if (int rc = check_heads(Hq, Hkv, d)) return rc;
+    if (B < 0 || L_max <= 0 || L_max > kMaxLen || M_max < 0) return INFLLMV2_ERR_INVALID_ARG;
+    if (B == 0) return INFLLMV2_OK;
+    if (!q || !k_new || !v_new || !k_cache || !v_cache || !kernel_cache || !kv_len || !o) return INFLLMV2_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(kernel_cache) || !aligned16(kv_len) || !aligned16(o) || (lse != nullptr && !aligned16(lse)))
+        return INFLLMV2_ERR_INVALID_ARG;
+    if (n_blocks(L_max, p.block_size) > kMaxBlocks) return INFLLMV2_ERR_UNSUPPORTED;
+    const int S_cap = infllmv2::selection_capacity(p, L_max);
+    if ((idx_out == nullptr) != (counts_out == nullptr)) return INFLLMV2_ERR_INVALID_ARG;
+    if (idx_out != nullptr && (S_max < S_cap || !aligned16(idx_out) || !aligned16(counts_out)))
+        return INFLLMV2_ERR_INVALID_ARG;
+    const DecodeWs w = decode_ws(B, 1, Hkv, d, L_max, p);
+    if (workspace == nullptr || ws_bytes < w.total || !aligned16(workspace)) return INFLLMV2_ERR_WORKSPACE;
+    int* err = device_error_ptr();
+    if (err == nullptr) return INFLLMV2_ERR_CUDA;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    infllmv2::DecodeArgs da{q, k_cache, v_cache, kv_len, nullptr, nullptr, nullptr, B, 1, Hq, Hkv, d, L_max,
+                            o, lse, p, err, st};
+    if (M_max > 0 && infllmv2::decode_cluster_can_append(p) && infllmv2::decode_cluster_supported(da, M_max)) {
+        da.k_new = k_new;
+        da.v_new = v_new;
+        da.k_w = k_cache;
+        da.v_w = v_cache;
+        da.kern_w = kernel_cache;
+        prof_begin(st);
+        const cudaError_t e = infllmv2::launch_decode_cluster(da, kernel_cache, M_max, idx_out, S_max, counts_out);
+        if (e != cudaErrorNotSupported) {
+            prof_mark(st, "fused");
+            return cuda_status(e);
+        }
+        (void)cudaGetLastError();  // not launched: append, then decode
+    }
+    if (int rc = cuda_status(infllmv2::launch_append(k_new, v_new, k_cache, v_cache, kernel_cache, kv_len, B, Hkv, L_max,
+                                                     M_max, d, p.kernel_size, p.kernel_stride, err, st)))
+        return rc;
+    return infllmv2_decode(q, k_cache, v_cache, kernel_cache, kv_len, nullptr, nullptr, nullptr, B, 1, Hq, Hkv, d, L_max,
+                           M_max, o, lse, idx_out, counts_out, S_max, workspace, ws_bytes, params, stream);
 }
 
 int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache, const void* kernel_cache,

@@ -26,6 +26,7 @@
 
 #include "attn_warp.cuh"
 #include "internal.h"
+#include "pool.cuh"
 #include "umma.cuh"
 
 namespace infllmv2 {
@@ -93,7 +94,7 @@ struct ClusterSmem {
     static int bytes(int nblk_max, int S_cap) { return off_bar(nblk_max, S_cap) + 8 * (1 + kPB) + 1024; }
 };
 
-template <int D, int BS>
+template <int D, int BS, bool kAppend>
 __global__ void __launch_bounds__(kDcThreads, 1)
 decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q,
@@ -101,7 +102,9 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                       const int* __restrict__ kv_len, int Hq, int Hkv, int G, int L_max, int M_max, Params p,
                       ClusterShape sh, int* __restrict__ idx_out, int idx_stride, int* __restrict__ counts_out,
                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse, float scale_log2,
-                      int* __restrict__ err) {
+                      int* __restrict__ err, const __nv_bfloat16* __restrict__ k_new,
+                      const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* k_w, __nv_bfloat16* v_w,
+                      __nv_bfloat16* kern_w) {
     using SM = ClusterSmem<D, BS>;
     constexpr int PB = SM::kPB;
     constexpr int kTile = SM::kTile;
@@ -203,6 +206,35 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     const int bt = len_ok ? (L - 1) / BS : -1;
     const bool dense = L < p.dense_len;
     auto forced = [&](int blk) { return blk < p.n_init || blk > bt - p.n_local; };
+    // Decode-step append (the kAppend instance): CTA 0 writes this row's new K and V into cache row L-1
+    // (the attention below reads them after the first cluster barrier), and warp 5 of every CTA
+    // pools its share of the 8-element slices of the kernel the new token completes, for the steps
+    // to come.  This step's scores never need that kernel: it overlaps only the query's own block
+    // and the one before, both local (forced) blocks under the condition the host checks.
+    if constexpr (kAppend) {
+      if (len_ok) {
+        const int pn = L - 1;
+        const uint4* kn = reinterpret_cast<const uint4*>(k_new + static_cast<size_t>(row) * D);
+        if (rank == 0 && warp == 6 && lane < D / 8) {
+            const size_t wr = (static_cast<size_t>(row) * L_max + pn) * D;
+            reinterpret_cast<uint4*>(k_w + wr)[lane] = ldg_v4(kn + lane);
+            reinterpret_cast<uint4*>(v_w + wr)[lane] =
+                ldg_v4(reinterpret_cast<const uint4*>(v_new + static_cast<size_t>(row) * D) + lane);
+        }
+        if (warp == 5 && L >= c && (L - c) % s == 0) {
+            const int jn = (L - c) / s, r0 = jn * s;  // jn < M_max: len_ok
+            const uint4* kr = reinterpret_cast<const uint4*>(k_w + (static_cast<size_t>(row) * L_max + r0) * D);
+            for (int sl0 = 2 * static_cast<int>(rank); sl0 < D / 8; sl0 += 2 * ncta) {
+                const int sl = sl0 + (lane >> 4);
+                const bool live = sl < D / 8;
+                const uint4 sub = live ? ldg_v4(kn + sl) : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 mean = exact_mean_slice(kr + (live ? sl : 0), D / 8, live ? c : 0, lane & 15, pn - r0, sub);
+                if (live && (lane & 15) == 0)
+                    reinterpret_cast<uint4*>(kern_w + (static_cast<size_t>(row) * M_max + jn) * D)[sl] = mean;
+            }
+        }
+      }
+    }
     const uint32_t keys_base = smem_u32(keys);
     bool q_landed = false;
     for (int sub0 = blkA0; sub0 < blkA1; sub0 += sh.SC) {
@@ -608,6 +640,10 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     // ================= 3. attention over the selected blocks rank, rank + CL, ...
     WarpAcc<D> A;
     acc_init(A);
+    // an appended K/V row (generic stores of CTA 0, released and acquired by the cluster barrier)
+    // is read below by this thread's bulk copies
+    if constexpr (kAppend)
+        if (tid == 0) fence_proxy_async_global();
     {
         const int mine = count > static_cast<int>(rank) ? (count - static_cast<int>(rank) + ncta - 1) / ncta : 0;
         uint32_t ph_b = 0;
@@ -763,7 +799,7 @@ static cudaError_t launch_cluster_t(const DecodeArgs& a, const void* kernel_cach
     sh.S_cap = selection_capacity(a.p, a.L_max);
     if (sh.S_cap > kDcMaxSel) return cudaErrorNotSupported;
     const int smem = SM::bytes(sh.nblk_max, sh.S_cap);
-    auto kfn = decode_cluster_kernel<D, BS>;
+    auto kfn = a.k_new != nullptr ? decode_cluster_kernel<D, BS, true> : decode_cluster_kernel<D, BS, false>;
     cudaFuncAttributes fa{};
     if (cudaError_t e = cudaFuncGetAttributes(&fa, kfn); e != cudaSuccess) return e;
     if (smem + static_cast<int>(fa.sharedSizeBytes) > 227 * 1024) return cudaErrorNotSupported;
@@ -819,7 +855,10 @@ static cudaError_t launch_cluster_t(const DecodeArgs& a, const void* kernel_cach
     const float scale_log2 = a.p.scale * 1.4426950408889634f;
     return cudaLaunchKernelEx(&cfg, kfn, tkern, tk, tv, tq, static_cast<const __nv_bfloat16*>(a.q), a.kv_len, a.Hq, a.Hkv,
                               G, a.L_max, M_max, a.p, sh, idx_out, idx_stride, counts_out,
-                              static_cast<__nv_bfloat16*>(a.o), a.lse, scale_log2, a.err);
+                              static_cast<__nv_bfloat16*>(a.o), a.lse, scale_log2, a.err,
+                              static_cast<const __nv_bfloat16*>(a.k_new), static_cast<const __nv_bfloat16*>(a.v_new),
+                              static_cast<__nv_bfloat16*>(a.k_w), static_cast<__nv_bfloat16*>(a.v_w),
+                              static_cast<__nv_bfloat16*>(a.kern_w));
 }
 
 bool decode_cluster_supported(const DecodeArgs& a, int M_max) {
@@ -832,6 +871,12 @@ bool decode_cluster_supported(const DecodeArgs& a, int M_max) {
         static_cast<long long>(a.B) * a.Hq < 16)
         return false;
     return true;
+}
+
+bool decode_cluster_can_append(const Params& p) {
+    // a kernel of c tokens ending at the query spans at most ceil((c-1)/bs) + 1 blocks back from it
+    const int span = (p.kernel_size - 1 + p.block_size - 1) / p.block_size + 1;
+    return p.n_local >= span;
 }
 
 cudaError_t launch_decode_cluster(const DecodeArgs& a, const void* kernel_cache, int M_max, int* idx_out,

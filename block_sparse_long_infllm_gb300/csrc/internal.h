@@ -55,6 +55,13 @@ struct DecodeArgs {
     Params p;
     int* err;
     cudaStream_t stream;
+    // decode-step append (cluster path): the new token's K and V per (sequence, KV head), written
+    // with the kernel it completes into the caches below; null = plain decode
+    const void* k_new = nullptr;
+    const void* v_new = nullptr;
+    void* k_w = nullptr;
+    void* v_w = nullptr;
+    void* kern_w = nullptr;
 };
 
 struct BwdArgs {
@@ -90,6 +97,9 @@ bool make_tmap_f32_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64
 void prof_begin(cudaStream_t stream);
 void prof_mark(cudaStream_t stream, const char* stage);
 
+cudaError_t launch_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, void* kernel_cache,
+                          const int* kv_len, int B, int Hkv, int L_max, int M_max, int d, int c, int s, int* err,
+                          cudaStream_t stream);
 cudaError_t launch_kernel_pool(const void* k_cache, void* kernel_cache, int B, int Hkv, int L_max,
                                int M_max, int d, int j_first, int n_new, int c, int s,
                                cudaStream_t stream);
@@ -132,6 +142,9 @@ cudaError_t launch_decode_attention(const DecodeArgs& a, const int* idx, const i
 // shape or the device is outside what it covers (the caller then runs the separate selection
 // and attention kernels).  idx_out / counts_out may be null.
 bool decode_cluster_supported(const DecodeArgs& a, int M_max);
+// Whether the cluster kernel may append in the same launch: the kernel a new token completes must
+// overlap only blocks that are always local (forced), so that this step's scores never need it.
+bool decode_cluster_can_append(const Params& p);
 cudaError_t launch_decode_cluster(const DecodeArgs& a, const void* kernel_cache, int M_max, int* idx_out,
                                   int idx_stride, int* counts_out);
 

@@ -76,6 +76,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.infllmv2_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, pp]
     lib.infllmv2_workspace_size.restype = sz
     lib.infllmv2_kernel_pool.argtypes = [p, p, i32, i32, i32, i32, i32, i32, i32, pp, p]
+    lib.infllmv2_append.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, pp, p]
+    lib.infllmv2_decode_step.argtypes = [p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, p, p, p, p, i32, p, sz,
+                                         pp, p]
     lib.infllmv2_block_select.argtypes = [p, p, p, i32, i32, i32, i32, i32, i32, i32, p, p, i32, p, sz,
                                           pp, p]
     lib.infllmv2_sparse_attn_fwd.argtypes = [p, p, p, p, p, i32, p, i32, i32, i32, i32, i32, i32, p, p,
@@ -93,8 +96,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.infllmv2_profile_stage_name.restype = ctypes.c_char_p
     for name in ("infllmv2_version", "infllmv2_sync_status", "infllmv2_selection_capacity",
                  "infllmv2_profile_enable", "infllmv2_profile_read",
-                 "infllmv2_kernel_pool", "infllmv2_block_select", "infllmv2_sparse_attn_fwd",
-                 "infllmv2_decode"):
+                 "infllmv2_kernel_pool", "infllmv2_append", "infllmv2_block_select", "infllmv2_sparse_attn_fwd",
+                 "infllmv2_decode", "infllmv2_decode_step"):
         getattr(lib, name).restype = ctypes.c_int
     if path == LIB_PATH:
         _lib = lib
@@ -185,6 +188,29 @@ def block_select(q, kernel_cache, kv_len, idx, counts, workspace, params, L_max:
                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
                                         ctypes.byref(Params.make(params)), _stream(stream)),
            "infllmv2_block_select")
+
+
+def append(k_new, v_new, k_cache, v_cache, kernel_cache, kv_len, params, stream=None):
+    """Write each row's new token (position kv_len - 1) into the caches and pool the kernel it completes."""
+    B, Hkv, L_max, d = k_cache.shape
+    M_max = 0 if kernel_cache is None else kernel_cache.shape[2]
+    _check(load().infllmv2_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(kernel_cache),
+                                  _ptr(kv_len), B, Hkv, d, L_max, M_max, ctypes.byref(Params.make(params)),
+                                  _stream(stream)), "infllmv2_append")
+
+
+def decode_step(q, k_new, v_new, k_cache, v_cache, kernel_cache, kv_len, o, workspace, params, lse=None,
+                idx_out=None, counts_out=None, stream=None):
+    """Append each row's new token (and the kernel it completes), then decode q over the caches."""
+    B, _, Hq, d = q.shape
+    Hkv, L_max = k_cache.shape[1], k_cache.shape[2]
+    M_max = kernel_cache.shape[2]
+    S_max = 0 if idx_out is None else idx_out.shape[-1]
+    _check(load().infllmv2_decode_step(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                       _ptr(kernel_cache), _ptr(kv_len), B, Hq, Hkv, d, L_max, M_max, _ptr(o),
+                                       _ptr(lse), _ptr(idx_out), _ptr(counts_out), S_max, _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       ctypes.byref(Params.make(params)), _stream(stream)), "infllmv2_decode_step")
 
 
 def sparse_attn_fwd(q, k_cache, v_cache, idx, counts, kv_len, o, params, lse=None, workspace=None,

@@ -140,6 +140,27 @@ int infllmv2_kernel_pool(const void* k_cache, void* kernel_cache, int B, int Hkv
                          const infllmv2_params* params, void* stream);
 
 /*
+ * Decode-step append (the per-token cache update of [CPM.cu] section 4, static
+ * preallocated caches, together with step 1's pooling; one launch, so a CUDA
+ * graph of infllmv2_append + infllmv2_decode is one whole decode step).
+ * For every sequence b and KV head g, with p = kv_len[b] - 1 (kv_len counts the
+ * new token):
+ *   k_cache[b,g,p,:] = k_new[b,g,:];  v_cache[b,g,p,:] = v_new[b,g,:]
+ * and, if the new token is the last token of semantic kernel
+ *   j = (kv_len[b] - kernel_size) / kernel_stride   (kv_len[b] >= kernel_size and
+ *   kv_len[b] - kernel_size divisible by kernel_stride),
+ * kernel_cache[b,g,j,:] is computed exactly as infllmv2_kernel_pool does.
+ *   k_new, v_new  [B, Hkv, d] bf16, read only.
+ *   kv_len        [B] device int32, per sequence (read on the device).
+ * kernel_cache may be NULL only when M_max == 0.  Device errors (kv_len[b] < 1 or
+ * > L_max, a kernel index >= M_max) set the error word; that row is skipped.
+ * Cache rows other than p and kernels other than j are untouched.
+ */
+int infllmv2_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                    void* kernel_cache, const int32_t* kv_len, int B, int Hkv, int d,
+                    int L_max, int M_max, const infllmv2_params* params, void* stream);
+
+/*
  * Steps 2-3, block scores and top-k selection for a causal chunk
  * ([MiniCPM4-1.1] dynamic block selection and local retention;
  * [MiniCPM4.0-sparse] dense switch).  Query t of sequence b sits at position
@@ -225,6 +246,25 @@ int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache,
                     int Hkv, int d, int L_max, int M_max, void* o, float* lse, int32_t* idx_out,
                     int32_t* counts_out, int S_max, void* workspace, size_t ws_bytes,
                     const infllmv2_params* params, void* stream);
+
+/*
+ * One whole single-token decode step: infllmv2_append (the new token's K and V
+ * into row kv_len[b]-1 of the caches, and the semantic kernel it completes),
+ * then infllmv2_decode of q over the updated caches ([CPM.cu] section 4: the
+ * per-token cache update and attention of a CUDA-graph decode step).  kv_len
+ * counts the new token.  Arguments as for those two calls (k_new, v_new
+ * [B, Hkv, d] bf16; caches writable; M_max >= 1).  When the kernel the new
+ * token completes can only overlap the query's forced local blocks
+ * (n_local_blocks >= ceil((kernel_size-1)/block_size) + 1) and the
+ * single-kernel decode covers the shape, both happen in that one launch: this
+ * step's scores never use the new kernel, so it is pooled alongside.  Otherwise
+ * the append kernel runs first.  Results are the same either way.
+ */
+int infllmv2_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                         void* v_cache, void* kernel_cache, const int32_t* kv_len, int B, int Hq,
+                         int Hkv, int d, int L_max, int M_max, void* o, float* lse,
+                         int32_t* idx_out, int32_t* counts_out, int S_max, void* workspace,
+                         size_t ws_bytes, const infllmv2_params* params, void* stream);
 
 /*
  * Allocation-free decode.  The paper has no counterpart: this entry point is

@@ -10,8 +10,8 @@ from block_sparse_long_infllm_gb300 import infllmv2
 
 def test_exports_every_declared_function(built_lib):
     names = infllmv2.declared_functions()
-    assert {"infllmv2_kernel_pool", "infllmv2_block_select", "infllmv2_sparse_attn_fwd",
-            "infllmv2_decode"} <= set(names)
+    assert {"infllmv2_kernel_pool", "infllmv2_append", "infllmv2_block_select", "infllmv2_sparse_attn_fwd",
+            "infllmv2_decode", "infllmv2_sparse_attn_bwd"} <= set(names)
     for n in names:
         assert hasattr(built_lib, n), n
 
@@ -98,6 +98,13 @@ def test_bad_shapes_rejected_on_host(built_lib):
         infllmv2.ERR_INVALID_ARG
     assert lib.infllmv2_kernel_pool(fake, fake, 1, 2, 4096, 100, 128, 0, 4096, _params(), None) == \
         infllmv2.ERR_INVALID_ARG
+    # append: d outside {64, 128}; a missing kernel cache while kernels exist; misaligned K
+    assert lib.infllmv2_append(fake, fake, fake, fake, fake, fake, 1, 2, 96, 4096, 255, _params(), None) == \
+        infllmv2.ERR_UNSUPPORTED
+    assert lib.infllmv2_append(fake, fake, fake, fake, None, fake, 1, 2, 128, 4096, 255, _params(), None) == \
+        infllmv2.ERR_INVALID_ARG
+    assert lib.infllmv2_append(odd, fake, fake, fake, fake, fake, 1, 2, 128, 4096, 255, _params(), None) == \
+        infllmv2.ERR_INVALID_ARG
 
 
 def test_empty_calls_are_noops(built_lib):
@@ -105,3 +112,4 @@ def test_empty_calls_are_noops(built_lib):
     assert built_lib.infllmv2_sparse_attn_fwd(fake, fake, fake, None, None, 0, fake, 0, 8, 32, 2, 128, 4096,
                                               fake, None, None, 0, _params(), None) == 0
     assert built_lib.infllmv2_kernel_pool(fake, fake, 1, 2, 4096, 255, 128, 100, 100, _params(), None) == 0
+    assert built_lib.infllmv2_append(fake, fake, fake, fake, fake, fake, 0, 2, 128, 4096, 255, _params(), None) == 0
