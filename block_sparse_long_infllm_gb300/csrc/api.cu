@@ -249,6 +249,84 @@ int infllmv2_kernel_pool(const void* k_cache, void* kernel_cache, int B, int Hkv
     return cuda_status(e);
 }
 
+int infllmv2_kernel_pool_varlen(const void* k_cache, void* kernel_cache, const int32_t* kv_len, const int32_t* cu_q,
+                                int B, int Hkv, int L_max, int M_max, int d, int Tq_max,
+                                const infllmv2_params* params, void* stream) {
+    Params p;
+    if (int rc = check_params(params, d, &p)) return rc;
+    if (d != 64 && d != 128) return INFLLMV2_ERR_UNSUPPORTED;
+    if (B < 0 || Hkv <= 0 || L_max <= 0 || L_max > kMaxLen || M_max < 0 || Tq_max < 0 || Tq_max > L_max)
+        return INFLLMV2_ERR_INVALID_ARG;
+    if (B == 0 || Tq_max == 0 || M_max == 0) return INFLLMV2_OK;
+    if (!k_cache || !kernel_cache || !kv_len || !cu_q || !aligned16(k_cache) || !aligned16(kernel_cache) ||
+        !aligned16(kv_len))
+        return INFLLMV2_ERR_INVALID_ARG;
+    int* err = device_error_ptr();
+    if (err == nullptr) return INFLLMV2_ERR_CUDA;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    prof_begin(st);
+    const cudaError_t e = infllmv2::launch_kernel_pool_seq(k_cache, kernel_cache, kv_len,
+                                                           infllmv2::SeqMap{cu_q, Tq_max, 0}, B, Hkv, L_max, M_max, d,
+                                                           p.kernel_size, p.kernel_stride, err, st);
+    prof_mark(st, "pool");
+    return cuda_status(e);
+}
+
+int infllmv2_block_select_varlen(const void* q, const void* kernel_cache, const int32_t* kv_len, const int32_t* cu_q,
+                                 int B, int Tq_max, int total_q, int Hq, int Hkv, int d, int L_max, int M_max,
+                                 int32_t* idx, int32_t* counts, int S_max, void* workspace, size_t ws_bytes,
+                                 const infllmv2_params* params, void* stream) {
+    Params p;
+    if (int rc = check_params(params, d, &p)) return rc;
+    if (int rc = check_heads(Hq, Hkv, d)) return rc;
+    if (B < 0 || Tq_max < 0 || total_q < 0 || L_max <= 0 || L_max > kMaxLen || M_max < 0) return INFLLMV2_ERR_INVALID_ARG;
+    if (B == 0 || Tq_max == 0 || total_q == 0) return INFLLMV2_OK;
+    if (Tq_max > L_max || Tq_max > total_q) return INFLLMV2_ERR_INVALID_ARG;
+    if (S_max < infllmv2::selection_capacity(p, L_max)) return INFLLMV2_ERR_INVALID_ARG;
+    if (n_blocks(L_max, p.block_size) > kMaxBlocks) return INFLLMV2_ERR_UNSUPPORTED;
+    if (!q || !kernel_cache || !kv_len || !cu_q || !idx || !counts) return INFLLMV2_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kernel_cache) || !aligned16(kv_len) || !aligned16(idx) || !aligned16(counts))
+        return INFLLMV2_ERR_INVALID_ARG;
+    const size_t need = align256(infllmv2::select_workspace_bytes(1, total_q, Hkv, L_max, p));
+    if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return INFLLMV2_ERR_WORKSPACE;
+    int* err = device_error_ptr();
+    if (err == nullptr) return INFLLMV2_ERR_CUDA;
+    infllmv2::SelectArgs a{q, kernel_cache, kv_len, B, Tq_max, Hq, Hkv, d, L_max, M_max, 0, idx, counts, S_max,
+                           blocks_per_score_cta(p), p, err, static_cast<cudaStream_t>(stream)};
+    a.cu_q = cu_q;
+    a.total_q = total_q;
+    prof_begin(a.stream);
+    return cuda_status(infllmv2::launch_block_select(a, static_cast<float*>(workspace)));
+}
+
+int infllmv2_sparse_attn_fwd_varlen(const void* q, const void* k_cache, const void* v_cache, const int32_t* idx,
+                                    const int32_t* counts, int S_max, const int32_t* kv_len, const int32_t* cu_q,
+                                    int B, int Tq_max, int total_q, int Hq, int Hkv, int d, int L_max, void* o,
+                                    float* lse, const infllmv2_params* params, void* stream) {
+    Params p;
+    if (int rc = check_params(params, d, &p)) return rc;
+    if (int rc = check_heads(Hq, Hkv, d)) return rc;
+    if (B < 0 || Tq_max < 0 || total_q < 0 || L_max <= 0 || L_max > kMaxLen) return INFLLMV2_ERR_INVALID_ARG;
+    if (B == 0 || Tq_max == 0 || total_q == 0) return INFLLMV2_OK;
+    if (Tq_max > L_max || Tq_max > total_q) return INFLLMV2_ERR_INVALID_ARG;
+    if (!q || !k_cache || !v_cache || !kv_len || !cu_q || !o) return INFLLMV2_ERR_INVALID_ARG;
+    if ((idx == nullptr) != (counts == nullptr)) return INFLLMV2_ERR_INVALID_ARG;
+    if (idx != nullptr && (S_max <= 0 || !aligned16(idx) || !aligned16(counts))) return INFLLMV2_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(kv_len))
+        return INFLLMV2_ERR_INVALID_ARG;
+    if (lse != nullptr && !aligned16(lse)) return INFLLMV2_ERR_INVALID_ARG;
+    int* err = device_error_ptr();
+    if (err == nullptr) return INFLLMV2_ERR_CUDA;
+    infllmv2::PrefillArgs a{q, k_cache, v_cache, idx, counts, S_max, kv_len, B, Tq_max, Hq, Hkv, d, L_max,
+                            o, lse, p, err, static_cast<cudaStream_t>(stream)};
+    a.cu_q = cu_q;
+    a.total_q = total_q;
+    prof_begin(a.stream);
+    const cudaError_t e = infllmv2::launch_prefill_attention(a);
+    prof_mark(a.stream, "attend");
+    return cuda_status(e);
+}
+
 int infllmv2_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, void* kernel_cache,
                     const int32_t* kv_len, int B, int Hkv, int d, int L_max, int M_max, const infllmv2_params* params,
                     void* stream) {

@@ -31,6 +31,46 @@ __host__ __device__ __forceinline__ int floor_div(int a, int b) {
     return a >= 0 ? a / b : -((-a + b - 1) / b);
 }
 
+// Query layout of a prefill call ("CPM.cu：端侧大模型推理的 CUDA 加速引擎", section 4: chunked
+// prefill, here for many sequences in one launch).  Fixed chunks (cu == nullptr): sequence b's Tq
+// queries are token rows b*Tq .. b*Tq + Tq - 1.  Packed variable-length chunks: sequence b's queries
+// are token rows cu[b] .. cu[b+1] - 1 of `total`.  q and o are [token row, head]; selection-shaped
+// arrays (idx, counts, scores) are [B, Hkv, Tq] fixed or [Hkv, total] packed; lse is [B, Hq, Tq]
+// fixed or [Hq, total] packed.  A sequence's queries are the last len(b) tokens of its cache.
+struct SeqMap {
+    const int* cu;  // [B + 1] device offsets, or nullptr
+    int Tq;         // fixed chunk length, or the longest packed chunk
+    int total;      // token rows: B*Tq, or cu[B]
+    __device__ __forceinline__ int tok0(int b) const { return cu != nullptr ? cu[b] : b * Tq; }
+    __device__ __forceinline__ int len(int b) const { return cu != nullptr ? cu[b + 1] - cu[b] : Tq; }
+    __device__ __forceinline__ size_t sel(int b, int g, int Hkv, int t) const {
+        return cu != nullptr ? static_cast<size_t>(g) * total + cu[b] + t
+                             : (static_cast<size_t>(b) * Hkv + g) * Tq + t;
+    }
+    __device__ __forceinline__ size_t lse(int b, int h, int Hq, int t) const {
+        return cu != nullptr ? static_cast<size_t>(h) * total + cu[b] + t
+                             : (static_cast<size_t>(b) * Hq + h) * Tq + t;
+    }
+    // inverse of sel(): selection row r -> (b, g, t)
+    __device__ __forceinline__ void row_of(long long r, int B, int Hkv, int* b, int* g, int* t) const {
+        if (cu == nullptr) {
+            *t = static_cast<int>(r % Tq);
+            *g = static_cast<int>((r / Tq) % Hkv);
+            *b = static_cast<int>(r / (static_cast<long long>(Tq) * Hkv));
+            return;
+        }
+        *g = static_cast<int>(r / total);
+        const int tok = static_cast<int>(r % total);
+        int lo = 0, hi = B;  // the last b with cu[b] <= tok
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (cu[mid] <= tok) lo = mid; else hi = mid;
+        }
+        *b = lo;
+        *t = tok - cu[lo];
+    }
+};
+
 // Number of complete semantic kernels among the first L tokens.
 __host__ __device__ __forceinline__ int kernels_in(int L, int c, int s) {
     return L < c ? 0 : (L - c) / s + 1;

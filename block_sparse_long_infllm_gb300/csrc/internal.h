@@ -23,6 +23,9 @@ struct SelectArgs {
     Params p;
     int* err;
     cudaStream_t stream;
+    const int* cu_q = nullptr;  // packed variable-length chunks (SeqMap); Tq is then the longest
+    int total_q = 0;            // token rows when packed
+    SeqMap seqmap() const { return SeqMap{cu_q, Tq, cu_q != nullptr ? total_q : B * Tq}; }
 };
 
 struct PrefillArgs {
@@ -39,6 +42,9 @@ struct PrefillArgs {
     Params p;
     int* err;
     cudaStream_t stream;
+    const int* cu_q = nullptr;  // packed variable-length chunks (SeqMap); Tq is then the longest
+    int total_q = 0;            // token rows when packed
+    SeqMap seqmap() const { return SeqMap{cu_q, Tq, cu_q != nullptr ? total_q : B * Tq}; }
 };
 
 struct DecodeArgs {
@@ -100,6 +106,9 @@ void prof_mark(cudaStream_t stream, const char* stage);
 cudaError_t launch_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, void* kernel_cache,
                           const int* kv_len, int B, int Hkv, int L_max, int M_max, int d, int c, int s, int* err,
                           cudaStream_t stream);
+cudaError_t launch_kernel_pool_seq(const void* k_cache, void* kernel_cache, const int* kv_len, const SeqMap& sm,
+                                   int B, int Hkv, int L_max, int M_max, int d, int c, int s, int* err,
+                                   cudaStream_t stream);
 cudaError_t launch_kernel_pool(const void* k_cache, void* kernel_cache, int B, int Hkv, int L_max,
                                int M_max, int d, int j_first, int n_new, int c, int s,
                                cudaStream_t stream);

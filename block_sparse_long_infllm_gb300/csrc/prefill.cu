@@ -15,27 +15,28 @@ template <int D>
 __global__ void __launch_bounds__(128)
 prefill_warp_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
                     const __nv_bfloat16* __restrict__ vc, const int* __restrict__ idx,
-                    const int* __restrict__ counts, int S_max, const int* __restrict__ kv_len, int Tq,
+                    const int* __restrict__ counts, int S_max, const int* __restrict__ kv_len, SeqMap sm,
                     int Hq, int Hkv, int G, int L_max, int bs, float scale_log2,
                     __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int* __restrict__ err) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g8 = lane >> 2, c4 = lane & 3;
     const int t = blockIdx.x * 4 + warp;
     const int b = blockIdx.y / Hkv, g = blockIdx.y % Hkv;
-    if (t >= Tq) return;
+    const int Tq = sm.len(b), tok = sm.tok0(b);
     const int L = kv_len[b];
-    if (L < Tq || L > L_max) {
+    if (Tq < 0 || Tq > sm.Tq || (t < Tq && (L < Tq || L > L_max))) {
         if (lane == 0) raise_error(err, kDevErrIndex);
         return;
     }
+    if (t >= Tq) return;
     const int pos = L - Tq + t;
     const int bt = pos / bs;
     QFrag<D> Q;
-    const size_t q_off = ((static_cast<size_t>(b) * Tq + t) * Hq + static_cast<size_t>(g) * G) * D;
+    const size_t q_off = ((static_cast<size_t>(tok) + t) * Hq + static_cast<size_t>(g) * G) * D;
     load_q(Q, q + q_off, D, G);
     WarpAcc<D> A;
     acc_init(A);
-    const int sel_row = (b * Hkv + g) * Tq + t;
+    const size_t sel_row = sm.sel(b, g, Hkv, t);
     int nsel = idx != nullptr ? counts[sel_row] : bt + 1;
     if (idx != nullptr && (nsel < 0 || nsel > S_max)) {  // a caller-written count outside its idx row
         if (lane == 0) raise_error(err, kDevErrIndex);
@@ -76,7 +77,7 @@ prefill_warp_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
         for (int u = 0; u < D / 32; ++u)
             reinterpret_cast<uint4*>(dst)[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         if (lse != nullptr && c4 == 0)
-            lse[(static_cast<size_t>(b) * Hq + g * G + r) * Tq + t] =
+            lse[sm.lse(b, g * G + r, Hq, t)] =
                 A.l[half] > 0.f ? (A.m[half] + log2f(A.l[half])) * 0.69314718055994530942f : -INFINITY;
     }
 }
@@ -90,17 +91,18 @@ cudaError_t launch_prefill_attention(const PrefillArgs& a) {
     }
     const int G = a.Hq / a.Hkv;
     const float scale_log2 = a.p.scale * 1.4426950408889634f;
+    const SeqMap sm = a.seqmap();
     dim3 grid((a.Tq + 3) / 4, a.B * a.Hkv);
     const auto* qp = static_cast<const __nv_bfloat16*>(a.q);
     const auto* kp = static_cast<const __nv_bfloat16*>(a.k_cache);
     const auto* vp = static_cast<const __nv_bfloat16*>(a.v_cache);
     auto* op = static_cast<__nv_bfloat16*>(a.o);
     if (a.d == 128)
-        prefill_warp_kernel<128><<<grid, 128, 0, a.stream>>>(qp, kp, vp, a.idx, a.counts, a.S_max, a.kv_len, a.Tq,
+        prefill_warp_kernel<128><<<grid, 128, 0, a.stream>>>(qp, kp, vp, a.idx, a.counts, a.S_max, a.kv_len, sm,
                                                              a.Hq, a.Hkv, G, a.L_max, a.p.block_size, scale_log2,
                                                              op, a.lse, a.err);
     else
-        prefill_warp_kernel<64><<<grid, 128, 0, a.stream>>>(qp, kp, vp, a.idx, a.counts, a.S_max, a.kv_len, a.Tq,
+        prefill_warp_kernel<64><<<grid, 128, 0, a.stream>>>(qp, kp, vp, a.idx, a.counts, a.S_max, a.kv_len, sm,
                                                             a.Hq, a.Hkv, G, a.L_max, a.p.block_size, scale_log2,
                                                             op, a.lse, a.err);
     return cudaGetLastError();

@@ -99,7 +99,7 @@ template <int D, int BS>
 __global__ void __launch_bounds__(kTcThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const int* __restrict__ idx,
-                  const int* __restrict__ counts, int S_max, const int* __restrict__ kv_len, int Tq, int Hq, int Hkv,
+                  const int* __restrict__ counts, int S_max, const int* __restrict__ kv_len, SeqMap sm, int Hq, int Hkv,
                   int L_max, int max_union, float scale_log2, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                   int* __restrict__ err) {
     using SM = TcSmem<D, BS>;
@@ -131,10 +131,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int b = blockIdx.y / Hkv, g = blockIdx.y % Hkv;
     const int t0 = blockIdx.x * kTcTokens;
     const int Lb = kv_len[b];
-    if (Lb < Tq || Lb > L_max) {
+    const int Tq = sm.len(b), tok = sm.tok0(b);  // this sequence's chunk: token rows tok .. tok + Tq - 1
+    if (Tq < 0 || Tq > sm.Tq || (t0 < Tq && (Lb < Tq || Lb > L_max))) {
         if (tid == 0) raise_error(err, kDevErrIndex);
         return;
     }
+    if (t0 >= Tq) return;  // packed chunks shorter than the longest
     const int n_tok = min(kTcTokens, Tq - t0);
     const int bt_max = (Lb - Tq + t0 + n_tok - 1) / BS;
     const int nwords = bt_max / 32 + 1;
@@ -165,8 +167,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int w = tid; w < nwords; w += kTcThreads) bitmap[w] = 0;
     for (int u = tid; u < max_union; u += kTcThreads) umask[u] = 0;
     __syncthreads();
-    const int* cnt_row = counts != nullptr ? counts + (static_cast<size_t>(b) * Hkv + g) * Tq + t0 : nullptr;
-    const int* idx_row = idx != nullptr ? idx + ((static_cast<size_t>(b) * Hkv + g) * Tq + t0) * S_max : nullptr;
+    const int* cnt_row = counts != nullptr ? counts + sm.sel(b, g, Hkv, t0) : nullptr;
+    const int* idx_row = idx != nullptr ? idx + sm.sel(b, g, Hkv, t0) * S_max : nullptr;
     const int per_tok = idx != nullptr ? S_max : bt_max + 1;
     auto entry = [&](int e, int& tk) -> int {  // block id of entry e (token tk), or -1
         tk = e / per_tok;
@@ -242,7 +244,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mbar_arrive_expect_tx(bar_q, SM::kQ);
             for (int tk = 0; tk < kTcTokens; ++tk) {
                 const int t = min(t0 + tk, Tq - 1);
-                const int qrow = (b * Tq + t) * Hq + g * G;
+                const int qrow = (tok + t) * Hq + g * G;
 #pragma unroll
                 for (int sub = 0; sub < D / 64; ++sub)
                     tma_load_2d(base + SM::kQOff + sub * (kTcRows * 128) + tk * (G * 128), &tm_q, 64 * sub, qrow, bar_q);
@@ -497,9 +499,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const bool go = __all_sync(0xffffffffu, ok && U > 0 && !*s_abort);
         const int hq = g * G + (r % G);
         if (U == 0 && live) {  // nothing selected: zero output
-            __nv_bfloat16* dst = o + ((static_cast<size_t>(b) * Tq + t0 + tk) * Hq + hq) * D + h * HD;
+            __nv_bfloat16* dst = o + ((static_cast<size_t>(tok) + t0 + tk) * Hq + hq) * D + h * HD;
             for (int c = 0; c < HD; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
-            if (lse != nullptr && h == 0) lse[(static_cast<size_t>(b) * Hq + hq) * Tq + t0 + tk] = -INFINITY;
+            if (lse != nullptr && h == 0) lse[sm.lse(b, hq, Hq, t0 + tk)] = -INFINITY;
         }
         if (go) {
             // PV(U-1) done implies every earlier PV done; S(U-1) was issued after PV(U-4)
@@ -512,7 +514,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tc_fence_after();
                 const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
                 const int t = t0 + tk;
-                __nv_bfloat16* dst = o + ((static_cast<size_t>(b) * Tq + (live ? t : 0)) * Hq + hq) * D + h * HD;
+                __nv_bfloat16* dst = o + ((static_cast<size_t>(tok) + (live ? t : 0)) * Hq + hq) * D + h * HD;
 #pragma unroll
                 for (int c0 = 0; c0 < HD; c0 += 32) {
                     uint32_t rr[32];
@@ -529,7 +531,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     }
                 }
                 if (live && lse != nullptr && h == 0)
-                    lse[(static_cast<size_t>(b) * Hq + hq) * Tq + t] =
+                    lse[sm.lse(b, hq, Hq, t)] =
                         l_row > 0.f ? (m_run * scale_log2 + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
             }
         }
@@ -557,7 +559,8 @@ static cudaError_t launch_tc_t(const PrefillArgs& a) {
     const int smem = SM::bytes(max_union, nwords);
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
     CUtensorMap tq, tk, tv;
-    const uint64_t q_rows = static_cast<uint64_t>(a.B) * a.Tq * a.Hq;
+    const SeqMap sm = a.seqmap();
+    const uint64_t q_rows = static_cast<uint64_t>(sm.total) * a.Hq;
     const uint64_t kv_rows = static_cast<uint64_t>(a.B) * a.Hkv * a.L_max;
     if (!make_tmap_bf16_2d(&tq, a.q, D, q_rows, 64, 16) || !make_tmap_bf16_2d(&tk, a.k_cache, D, kv_rows, 64, BS) ||
         !make_tmap_bf16_2d(&tv, a.v_cache, D, kv_rows, 64, BS))
@@ -568,7 +571,7 @@ static cudaError_t launch_tc_t(const PrefillArgs& a) {
     dim3 grid((a.Tq + kTcTokens - 1) / kTcTokens, a.B * a.Hkv);
     const float scale_log2 = a.p.scale * 1.4426950408889634f;
     return launch_kernel(kfn, grid, dim3(kTcThreads), smem, a.stream, false, tq, tk, tv, a.idx, a.counts, a.S_max,
-                         a.kv_len, a.Tq, a.Hq, a.Hkv, a.L_max, max_union, scale_log2,
+                         a.kv_len, sm, a.Hq, a.Hkv, a.L_max, max_union, scale_log2,
                          static_cast<__nv_bfloat16*>(a.o), a.lse, a.err);
 }
 

@@ -59,7 +59,7 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
 template <int D>
 __global__ void __launch_bounds__(kScThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kern,
-                const int* __restrict__ kv_len, int Tq, int Hq, int Hkv, int L_max, int M_max, int nblk_max, Params p,
+                const int* __restrict__ kv_len, SeqMap sm, int Hq, int Hkv, int L_max, int M_max, int nblk_max, Params p,
                 int blocks_per_chunk, float* __restrict__ S, int* __restrict__ err) {
     using SM = ScSmem<D>;
     constexpr int G = 16;
@@ -81,10 +81,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int t0 = blockIdx.x * kScTokens;
     const int bs = p.block_size, c = p.kernel_size, s = p.kernel_stride;
     const int Lb = kv_len[b];
-    if (Lb < Tq || Lb > L_max || kernels_in(Lb, c, s) > M_max) {
+    const int Tq = sm.len(b), tok = sm.tok0(b);  // this sequence's chunk: token rows tok .. tok + Tq - 1
+    if (Tq < 0 || Tq > sm.Tq || (Tq > 0 && (Lb < Tq || Lb > L_max || kernels_in(Lb, c, s) > M_max))) {
         if (tid == 0 && blockIdx.x == 0) raise_error(err, kDevErrIndex);
         return;
     }
+    if (t0 >= Tq) return;  // packed chunks shorter than the longest
     if (Lb < p.dense_len) return;  // dense sequence: every block is selected, no scores needed
     const int n_tok = min(kScTokens, Tq - t0);
     const int pos_last = Lb - Tq + t0 + n_tok - 1;
@@ -136,7 +138,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_arrive_expect_tx(bar_q, SM::kQ);
             for (int tk = 0; tk < kScTokens; ++tk) {
                 const int t = min(t0 + tk, Tq - 1);
-                const int qrow = (b * Tq + t) * Hq + g * G;
+                const int qrow = (tok + t) * Hq + g * G;
 #pragma unroll
                 for (int sub = 0; sub < D / 64; ++sub)
                     tma_load_2d(base + SM::kQOff + sub * (kScN * 128) + tk * (G * 128), &tm_q, 64 * sub, qrow, bar_q);
@@ -234,7 +236,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const int jz = min(last_kernel_of_block(blk, bs, s) - j0, kScM - 1);
                 float m = -INFINITY;
                 for (int jj = ja; jj <= jz; ++jj) m = fmaxf(m, kmax[tk * kScM + jj]);
-                S[(static_cast<size_t>(bg) * Tq + t0 + tk) * nblk_max + blk] = m;
+                S[sm.sel(b, g, Hkv, t0 + tk) * nblk_max + blk] = m;
             }
             asm volatile("bar.sync 1, 256;" ::: "memory");  // kmax is rewritten by the next chunk
         }
@@ -266,7 +268,8 @@ cudaError_t launch_score_tc(const SelectArgs& a, float* S) {
     const int nb = score_tc_blocks_per_chunk(a.p);
     const int nblk_max = (a.L_max + a.p.block_size - 1) / a.p.block_size;
     CUtensorMap tq, tk;
-    const uint64_t q_rows = static_cast<uint64_t>(a.B) * a.Tq * a.Hq;
+    const SeqMap sm = a.seqmap();
+    const uint64_t q_rows = static_cast<uint64_t>(sm.total) * a.Hq;
     const uint64_t k_rows = static_cast<uint64_t>(a.B) * a.Hkv * a.M_max;
     if (!make_tmap_bf16_2d(&tq, a.q, a.d, q_rows, 64, 16) || !make_tmap_bf16_2d(&tk, a.kernel_cache, a.d, k_rows, 64, kScM))
         return cudaErrorInvalidValue;
@@ -276,14 +279,14 @@ cudaError_t launch_score_tc(const SelectArgs& a, float* S) {
         constexpr int smem = ScSmem<128>::kBytes;
         if (cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); e != cudaSuccess)
             return e;
-        return launch_kernel(kfn, grid, dim3(kScThreads), smem, a.stream, false, tq, tk, a.kv_len, a.Tq, a.Hq, a.Hkv,
+        return launch_kernel(kfn, grid, dim3(kScThreads), smem, a.stream, false, tq, tk, a.kv_len, sm, a.Hq, a.Hkv,
                              a.L_max, a.M_max, nblk_max, a.p, nb, S, a.err);
     }
     auto kfn = score_tc_kernel<64>;
     constexpr int smem = ScSmem<64>::kBytes;
     if (cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); e != cudaSuccess)
         return e;
-    return launch_kernel(kfn, grid, dim3(kScThreads), smem, a.stream, false, tq, tk, a.kv_len, a.Tq, a.Hq, a.Hkv,
+    return launch_kernel(kfn, grid, dim3(kScThreads), smem, a.stream, false, tq, tk, a.kv_len, sm, a.Hq, a.Hkv,
                          a.L_max, a.M_max, nblk_max, a.p, nb, S, a.err);
 }
 

@@ -27,7 +27,7 @@ namespace infllmv2 {
 template <int D, int WARPS, int MT>
 __global__ void __launch_bounds__(WARPS * 32)
 score_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kern,
-             const int* __restrict__ kv_len, int Tq, int Hq, int Hkv, int G, int L_max,
+             const int* __restrict__ kv_len, SeqMap sm, int Hq, int Hkv, int G, int L_max,
              int M_max, int nblk_max, int tree, Params p, int blocks_per_cta, int kmax,
              float* __restrict__ S, int* __restrict__ err) {
     constexpr int NKS = WARPS / MT;  // warps sharing one m-tile split its kernels
@@ -42,13 +42,14 @@ score_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
     const int bs = p.block_size, c = p.kernel_size, s = p.kernel_stride;
 
     const int L = kv_len[b];
-    const bool bad_len = tree ? (L < 1 || L > L_max) : (L < Tq || L > L_max);
-    if (bad_len || kernels_in(L, c, s) > M_max) {
+    const int Tq = sm.len(b), tok = sm.tok0(b);  // this sequence's queries: token rows tok .. tok + Tq - 1
+    const bool bad_len = Tq < 0 || Tq > sm.Tq || (Tq > 0 && (tree ? (L < 1 || L > L_max) : (L < Tq || L > L_max)));
+    if (bad_len || (Tq > 0 && kernels_in(L, c, s) > M_max)) {
         if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(err, kDevErrIndex);
         return;
     }
-    if (L < p.dense_len) return;  // dense sequence: every block is selected, no scores needed
     if (t0 >= Tq) return;
+    if (L < p.dense_len) return;  // dense sequence: every block is selected, no scores needed
     const int t_last = min(t0 + tpc, Tq) - 1;
     const int pos_max = tree ? L - 1 : L - Tq + t_last;
     const int bt_max = pos_max / bs;
@@ -72,7 +73,7 @@ score_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
         tok_r[half] = tl;
         pos_r[half] = tree ? L - 1 : L - Tq + t;
         const bool ok = t < Tq;
-        const __nv_bfloat16* qrow = q + ((static_cast<size_t>(b) * Tq + (ok ? t : 0)) * Hq + g * G + r % G) * D;
+        const __nv_bfloat16* qrow = q + ((static_cast<size_t>(tok) + (ok ? t : 0)) * Hq + g * G + r % G) * D;
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) {
             uint4 w = ok ? ldg_v4(qrow + 32 * i + 8 * cq) : make_uint4(0, 0, 0, 0);
@@ -150,7 +151,7 @@ score_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
         const int jz = min(last_kernel_of_block(blk, bs, s), jhi);
         float m = -INFINITY;
         for (int jj = ja; jj <= jz; ++jj) m = fmaxf(m, ks[tl * kmax + (jj - jlo)]);
-        S[(static_cast<size_t>(bg) * Tq + t) * nblk_max + blk] = m;
+        S[sm.sel(b, g, Hkv, t) * nblk_max + blk] = m;
     }
 }
 
@@ -166,7 +167,7 @@ constexpr int kScoreBoxRows = 136;
 template <int D>
 __global__ void __launch_bounds__(128)
 score_decode_kernel(const __grid_constant__ CUtensorMap tm_kern, const __nv_bfloat16* __restrict__ q,
-                    const int* __restrict__ kv_len, int Tq, int Hq, int Hkv, int G, int L_max, int M_max,
+                    const int* __restrict__ kv_len, SeqMap sm, int Hq, int Hkv, int G, int L_max, int M_max,
                     int nblk_max, int tree, Params p, int blocks_per_cta, float* __restrict__ S,
                     int* __restrict__ err) {
     constexpr int kBox = kScoreBoxRows * 128;  // bytes of one 64-column box
@@ -183,11 +184,13 @@ score_decode_kernel(const __grid_constant__ CUtensorMap tm_kern, const __nv_bflo
     const int bs = p.block_size, c = p.kernel_size, s = p.kernel_stride;
     pdl_trigger();
     const int L = kv_len[b];
-    const bool bad_len = tree ? (L < 1 || L > L_max) : (L < Tq || L > L_max);
-    if (bad_len || kernels_in(L, c, s) > M_max) {
+    const int Tq = sm.len(b), tok = sm.tok0(b);
+    const bool bad_len = Tq < 0 || Tq > sm.Tq || (Tq > 0 && (tree ? (L < 1 || L > L_max) : (L < Tq || L > L_max)));
+    if (bad_len || (Tq > 0 && kernels_in(L, c, s) > M_max)) {
         if (threadIdx.x == 0 && blockIdx.x == 0 && t == 0) raise_error(err, kDevErrIndex);
         return;
     }
+    if (t >= Tq) return;
     if (L < p.dense_len) return;
     const int pos = tree ? L - 1 : L - Tq + t;
     const int bt = pos / bs;
@@ -214,7 +217,7 @@ score_decode_kernel(const __grid_constant__ CUtensorMap tm_kern, const __nv_bflo
     for (int half = 0; half < 2; ++half) {
         const int r = gq + 8 * half;
         const bool ok = r < G;
-        const __nv_bfloat16* qrow = q + ((static_cast<size_t>(b) * Tq + t) * Hq + g * G + (ok ? r : 0)) * D;
+        const __nv_bfloat16* qrow = q + ((static_cast<size_t>(tok) + t) * Hq + g * G + (ok ? r : 0)) * D;
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) {
             const uint4 v = ok ? ldg_v4(qrow + 32 * i + 8 * cq) : make_uint4(0, 0, 0, 0);
@@ -264,7 +267,7 @@ score_decode_kernel(const __grid_constant__ CUtensorMap tm_kern, const __nv_bflo
         const int jz = min(last_kernel_of_block(blk, bs, s), jhi);
         float m = -INFINITY;
         for (int jj = ja; jj <= jz; ++jj) m = fmaxf(m, ks[jj - jlo]);
-        S[(static_cast<size_t>(bg) * Tq + t) * nblk_max + blk] = m;
+        S[sm.sel(b, g, Hkv, t) * nblk_max + blk] = m;
     }
 }
 
@@ -282,21 +285,23 @@ __device__ __forceinline__ bool is_forced(int blk, int bt, const Params& p) {
 // places every chosen block in ascending order.
 template <int NT, int PER>
 __global__ void __launch_bounds__(NT)
-topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, int Tq, int Hkv, int nblk_max, int L_max,
-            int tree, Params p, int* __restrict__ idx, int* __restrict__ counts, int S_max, int* __restrict__ err) {
+topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, SeqMap sm, int B, int Hkv, int nblk_max,
+            int L_max, int tree, Params p, int* __restrict__ idx, int* __restrict__ counts, int S_max,
+            int* __restrict__ err) {
     constexpr int NW = NT / 32;
     __shared__ uint32_t s_and[NW], s_or[NW];
     __shared__ int s_cnt[2][NW];
     __shared__ int s_wsel[NW], s_wtie[NW];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int row = blockIdx.x;
-    const int t = row % Tq;
-    const int b = row / (Tq * Hkv);
+    int b, g_unused, t;
+    sm.row_of(row, B, Hkv, &b, &g_unused, &t);
     pdl_wait();
     pdl_trigger();
     const int L = kv_len[b];
+    const int Tq = sm.len(b);
     int* out = idx + static_cast<size_t>(row) * S_max;
-    const bool bad_len = tree ? (L < 1 || L > L_max) : (L < Tq || L > L_max);
+    const bool bad_len = Tq < 1 || Tq > sm.Tq || (tree ? (L < 1 || L > L_max) : (L < Tq || L > L_max));
     if (bad_len) {
         for (int i = tid; i < S_max; i += NT) out[i] = -1;
         if (tid == 0) {
@@ -500,7 +505,7 @@ static cudaError_t launch_score_t(const SelectArgs& a, float* S) {
     }
     kfn<<<grid, WARPS * 32, smem, a.stream>>>(
         static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.kernel_cache), a.kv_len,
-        a.Tq, a.Hq, a.Hkv, G, a.L_max, a.M_max, nblk_max, a.tree, p, bpc, kmax, S, a.err);
+        a.seqmap(), a.Hq, a.Hkv, G, a.L_max, a.M_max, nblk_max, a.tree, p, bpc, kmax, S, a.err);
     return cudaGetLastError();
 }
 
@@ -518,7 +523,7 @@ static cudaError_t launch_score_decode_t(const SelectArgs& a, float* S, int bpc)
         return e;
     dim3 grid((nblk_max + bpc - 1) / bpc, a.Tq, a.B * a.Hkv);
     return launch_kernel(kfn, grid, dim3(128), smem, a.stream, false, tm, static_cast<const __nv_bfloat16*>(a.q),
-                         a.kv_len, a.Tq, a.Hq, a.Hkv, G, a.L_max, a.M_max, nblk_max, a.tree, p, bpc, S, a.err);
+                         a.kv_len, a.seqmap(), a.Hq, a.Hkv, G, a.L_max, a.M_max, nblk_max, a.tree, p, bpc, S, a.err);
 }
 
 cudaError_t launch_block_select(const SelectArgs& a, float* S) {
@@ -548,19 +553,20 @@ cudaError_t launch_block_select(const SelectArgs& a, float* S) {
     }
     if (e != cudaSuccess) return e;
     prof_mark(a.stream, "score");
-    const int rows = a.B * a.Hkv * a.Tq;
+    const SeqMap sm = a.seqmap();
+    const int rows = a.Hkv * sm.total;
     if (nblk_max <= 128 * 4)
-        e = launch_kernel(topk_kernel<128, 4>, dim3(rows), dim3(128), 0, a.stream, decode_shaped, S, a.kv_len, a.Tq,
-                          a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
+        e = launch_kernel(topk_kernel<128, 4>, dim3(rows), dim3(128), 0, a.stream, decode_shaped, S, a.kv_len, sm,
+                          a.B, a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
     else if (nblk_max <= 256 * 8)
-        e = launch_kernel(topk_kernel<256, 8>, dim3(rows), dim3(256), 0, a.stream, decode_shaped, S, a.kv_len, a.Tq,
-                          a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
+        e = launch_kernel(topk_kernel<256, 8>, dim3(rows), dim3(256), 0, a.stream, decode_shaped, S, a.kv_len, sm,
+                          a.B, a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
     else if (nblk_max <= 512 * 16)
-        e = launch_kernel(topk_kernel<512, 16>, dim3(rows), dim3(512), 0, a.stream, decode_shaped, S, a.kv_len, a.Tq,
-                          a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
+        e = launch_kernel(topk_kernel<512, 16>, dim3(rows), dim3(512), 0, a.stream, decode_shaped, S, a.kv_len, sm,
+                          a.B, a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
     else
         e = launch_kernel(topk_kernel<1024, 32>, dim3(rows), dim3(1024), 0, a.stream, decode_shaped, S, a.kv_len,
-                          a.Tq, a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
+                          sm, a.B, a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
     prof_mark(a.stream, "topk");
     return e;
 }

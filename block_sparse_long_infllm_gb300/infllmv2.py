@@ -77,6 +77,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.infllmv2_workspace_size.restype = sz
     lib.infllmv2_kernel_pool.argtypes = [p, p, i32, i32, i32, i32, i32, i32, i32, pp, p]
     lib.infllmv2_append.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, i32, pp, p]
+    lib.infllmv2_kernel_pool_varlen.argtypes = [p, p, p, p, i32, i32, i32, i32, i32, i32, pp, p]
+    lib.infllmv2_block_select_varlen.argtypes = [p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, p, p, i32, p,
+                                                 sz, pp, p]
+    lib.infllmv2_sparse_attn_fwd_varlen.argtypes = [p, p, p, p, p, i32, p, p, i32, i32, i32, i32, i32, i32, i32, p,
+                                                    p, pp, p]
     lib.infllmv2_decode_step.argtypes = [p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, p, p, p, p, i32, p, sz,
                                          pp, p]
     lib.infllmv2_block_select.argtypes = [p, p, p, i32, i32, i32, i32, i32, i32, i32, p, p, i32, p, sz,
@@ -97,7 +102,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     for name in ("infllmv2_version", "infllmv2_sync_status", "infllmv2_selection_capacity",
                  "infllmv2_profile_enable", "infllmv2_profile_read",
                  "infllmv2_kernel_pool", "infllmv2_append", "infllmv2_block_select", "infllmv2_sparse_attn_fwd",
-                 "infllmv2_decode", "infllmv2_decode_step"):
+                 "infllmv2_decode", "infllmv2_decode_step", "infllmv2_kernel_pool_varlen",
+                 "infllmv2_block_select_varlen", "infllmv2_sparse_attn_fwd_varlen"):
         getattr(lib, name).restype = ctypes.c_int
     if path == LIB_PATH:
         _lib = lib
@@ -211,6 +217,42 @@ def decode_step(q, k_new, v_new, k_cache, v_cache, kernel_cache, kv_len, o, work
                                        _ptr(lse), _ptr(idx_out), _ptr(counts_out), S_max, _ptr(workspace),
                                        workspace.numel() * workspace.element_size(),
                                        ctypes.byref(Params.make(params)), _stream(stream)), "infllmv2_decode_step")
+
+
+def kernel_pool_varlen(k_cache, kernel_cache, kv_len, cu_q, Tq_max: int, params, stream=None):
+    """Pool the kernels completed by each sequence's packed chunk (its last cu_q[b+1]-cu_q[b] tokens)."""
+    B, Hkv, L_max, d = k_cache.shape
+    _check(load().infllmv2_kernel_pool_varlen(_ptr(k_cache), _ptr(kernel_cache), _ptr(kv_len), _ptr(cu_q), B, Hkv,
+                                              L_max, kernel_cache.shape[2], d, int(Tq_max),
+                                              ctypes.byref(Params.make(params)), _stream(stream)),
+           "infllmv2_kernel_pool_varlen")
+
+
+def block_select_varlen(q, kernel_cache, kv_len, cu_q, Tq_max: int, idx, counts, workspace, params, L_max: int,
+                        stream=None):
+    """Selection for packed chunks: q [total_q, Hq, d]; idx [Hkv, total_q, S_max], counts [Hkv, total_q]."""
+    total_q, Hq, d = q.shape
+    B = cu_q.shape[0] - 1
+    Hkv, M_max = kernel_cache.shape[1], kernel_cache.shape[2]
+    _check(load().infllmv2_block_select_varlen(_ptr(q), _ptr(kernel_cache), _ptr(kv_len), _ptr(cu_q), B, int(Tq_max),
+                                               total_q, Hq, Hkv, d, L_max, M_max, _ptr(idx), _ptr(counts),
+                                               idx.shape[-1], _ptr(workspace),
+                                               workspace.numel() * workspace.element_size(),
+                                               ctypes.byref(Params.make(params)), _stream(stream)),
+           "infllmv2_block_select_varlen")
+
+
+def sparse_attn_fwd_varlen(q, k_cache, v_cache, idx, counts, kv_len, cu_q, Tq_max: int, o, params, lse=None,
+                           stream=None):
+    """Attention for packed chunks: q, o [total_q, Hq, d]; lse [Hq, total_q]; idx None = dense causal."""
+    total_q, Hq, d = q.shape
+    B = cu_q.shape[0] - 1
+    Hkv, L_max = k_cache.shape[1], k_cache.shape[2]
+    _check(load().infllmv2_sparse_attn_fwd_varlen(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(idx), _ptr(counts),
+                                                  0 if idx is None else idx.shape[-1], _ptr(kv_len), _ptr(cu_q), B,
+                                                  int(Tq_max), total_q, Hq, Hkv, d, L_max, _ptr(o), _ptr(lse),
+                                                  ctypes.byref(Params.make(params)), _stream(stream)),
+           "infllmv2_sparse_attn_fwd_varlen")
 
 
 def sparse_attn_fwd(q, k_cache, v_cache, idx, counts, kv_len, o, params, lse=None, workspace=None,

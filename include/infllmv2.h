@@ -140,6 +140,43 @@ int infllmv2_kernel_pool(const void* k_cache, void* kernel_cache, int B, int Hkv
                          const infllmv2_params* params, void* stream);
 
 /*
+ * Variable-length batched prefill ([CPM.cu] section 4 chunked prefill, many
+ * sequences with different chunk lengths in one launch).  Sequence b's chunk is
+ * len_b = cu_q[b+1] - cu_q[b] queries: the last len_b tokens of its cache, so
+ * query t sits at position kv_len[b] - len_b + t.  Packed layouts (total_q =
+ * cu_q[B] query rows; cu_q is device int32 [B+1], ascending, cu_q[0] = 0):
+ *   q, o     [total_q, Hq, d]       row cu_q[b] + t
+ *   idx      [Hkv, total_q, S_max]  counts [Hkv, total_q]
+ *   lse      [Hq, total_q]
+ * Tq_max (host) bounds every len_b; total_q (host) is cu_q[B].  A len_b outside
+ * [0, Tq_max] or a kv_len[b] < len_b sets the device error word and skips that
+ * sequence.  Each varlen call computes exactly what its fixed-chunk counterpart
+ * computes for every sequence on its own.
+ *
+ * infllmv2_kernel_pool_varlen: the kernels completed by each sequence's chunk
+ * (step 1, as infllmv2_kernel_pool per sequence).
+ */
+int infllmv2_kernel_pool_varlen(const void* k_cache, void* kernel_cache, const int32_t* kv_len,
+                                const int32_t* cu_q, int B, int Hkv, int L_max, int M_max, int d,
+                                int Tq_max, const infllmv2_params* params, void* stream);
+
+/* Steps 2-3 for packed chunks (as infllmv2_block_select per sequence).  Requires
+ * ws_bytes >= infllmv2_workspace_size(INFLLMV2_ENTRY_BLOCK_SELECT, 1, total_q, ...). */
+int infllmv2_block_select_varlen(const void* q, const void* kernel_cache, const int32_t* kv_len,
+                                 const int32_t* cu_q, int B, int Tq_max, int total_q, int Hq,
+                                 int Hkv, int d, int L_max, int M_max, int32_t* idx,
+                                 int32_t* counts, int S_max, void* workspace, size_t ws_bytes,
+                                 const infllmv2_params* params, void* stream);
+
+/* Step 4 for packed chunks (as infllmv2_sparse_attn_fwd per sequence); idx NULL:
+ * dense causal attention. */
+int infllmv2_sparse_attn_fwd_varlen(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* idx, const int32_t* counts, int S_max,
+                                    const int32_t* kv_len, const int32_t* cu_q, int B, int Tq_max,
+                                    int total_q, int Hq, int Hkv, int d, int L_max, void* o,
+                                    float* lse, const infllmv2_params* params, void* stream);
+
+/*
  * Decode-step append (the per-token cache update of [CPM.cu] section 4, static
  * preallocated caches, together with step 1's pooling; one launch, so a CUDA
  * graph of infllmv2_append + infllmv2_decode is one whole decode step).
