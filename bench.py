@@ -618,6 +618,99 @@ def run_prefill_backward(args, w, p, q, k, v, o, lse, idx, cnt, kv_len, flush, f
             "gpu_launches_per_call": 6, "memsets_per_call": 4}
 
 
+# ------------------------------------------------------------------ variable-length batched prefill (secondary)
+
+VARLEN_LENS = [512, 1024, 2048, 4096, 256, 1536, 768, 3072]          # chunk lengths of 8 sequences
+VARLEN_KV = [8192, 16384, 32768, 24576, 12000, 20000, 30000, 28000]  # their cache lengths after the chunk
+
+
+def run_varlen_prefill(args) -> dict:
+    """One prefill step of 8 sequences with different chunk lengths, packed into one launch per
+    kernel: the chunks' kernels, selection, attention (parameters of the 32K chunked-prefill
+    workload; seeded N(0,1) bf16 inputs).  L2 flushed before each step."""
+    import numpy as np
+    import torch
+
+    from block_sparse_long_infllm_gb300 import infllmv2, synth
+    w = synth.WORKLOADS[PREFILL]
+    p = w.params()
+    B, Hq, Hkv, d, L_max = len(VARLEN_LENS), w.Hq, w.Hkv, w.d, max(VARLEN_KV)
+    cu = np.concatenate([[0], np.cumsum(VARLEN_LENS)]).astype(np.int32)
+    total = int(cu[-1])
+    rng = np.random.default_rng(2024)
+    q = dev_bf16(synth.f32_to_bf16_bits(rng.standard_normal((total, Hq, d), dtype=np.float32)))
+    k = dev_bf16(synth.f32_to_bf16_bits(rng.standard_normal((B, Hkv, L_max, d), dtype=np.float32)))
+    v = dev_bf16(synth.f32_to_bf16_bits(rng.standard_normal((B, Hkv, L_max, d), dtype=np.float32)))
+    kv = torch.tensor(VARLEN_KV, dtype=torch.int32, device="cuda")
+    cu_d = torch.from_numpy(cu).cuda()
+    M = (L_max - w.kernel_size) // w.kernel_stride + 1
+    kern = torch.zeros((B, Hkv, M, d), dtype=torch.bfloat16, device="cuda")
+    infllmv2.kernel_pool(k, kern, 0, L_max, p)   # the cached prefixes' kernels (not timed)
+    S_cap = infllmv2.selection_capacity(p, L_max)
+    idx = torch.empty((Hkv, total, S_cap), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((Hkv, total), dtype=torch.int32, device="cuda")
+    ws = torch.empty(infllmv2.workspace_size(infllmv2.ENTRY_BLOCK_SELECT, 1, total, Hq, Hkv, d, L_max, p),
+                     dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((Hq, total), dtype=torch.float32, device="cuda")
+    Tq_max = max(VARLEN_LENS)
+    flush = Flusher()
+    stream = torch.cuda.current_stream()
+
+    def step(record=None):
+        infllmv2.kernel_pool_varlen(k, kern, kv, cu_d, Tq_max, p)
+        if record is not None:
+            record.append(infllmv2.profile_read())
+        infllmv2.block_select_varlen(q, kern, kv, cu_d, Tq_max, idx, cnt, ws, p, L_max)
+        if record is not None:
+            record.append(infllmv2.profile_read())
+        infllmv2.sparse_attn_fwd_varlen(q, k, v, idx, cnt, kv, cu_d, Tq_max, o, p, lse=lse)
+        if record is not None:
+            record.append(infllmv2.profile_read())
+
+    for _ in range(3):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    K = args.prefill_steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    infllmv2.profile_enable(True)
+    stages: dict[str, list[float]] = {}
+    for _ in range(max(3, K // 2)):
+        flush()
+        rec = []
+        step(rec)
+        for part in rec:
+            for nm, t in part:
+                stages.setdefault(nm, []).append(t)
+    infllmv2.profile_enable(False)
+    assert infllmv2.sync_status() == 0
+    counts, sel = cnt.cpu().numpy(), idx.cpu().numpy()
+    attended = 0
+    G = Hq // Hkv
+    for b in range(B):
+        for t in range(VARLEN_LENS[b]):
+            pos = VARLEN_KV[b] - VARLEN_LENS[b] + t
+            for g in range(Hkv):
+                blks = sel[g, cu[b] + t, :counts[g, cu[b] + t]].astype(np.int64)
+                attended += int(np.minimum(pos + 1 - blks * w.block_size, w.block_size).clip(min=0).sum()) * G
+    stage_ms = {kk: statistics.median(vv) for kk, vv in stages.items()}
+    att_tf = 4.0 * d * attended / (stage_ms["attend"] * 1e-3) / 1e12
+    pk = peaks()
+    return {"sequences": B, "chunk_lengths": VARLEN_LENS, "kv_lengths": VARLEN_KV, "query_tokens": total,
+            "ms_per_step": ms, "steps": K, "value": total / (ms * 1e-3), "unit": UNIT,
+            "stages_ms": {kk: round(vv, 4) for kk, vv in stage_ms.items()},
+            "attention_tflops": round(att_tf, 2), "attention_frac": round(att_tf / pk["bf16_tflops"], 4),
+            "gpu_launches_per_step": 4}
+
+
 # ------------------------------------------------------------------ tree verification (secondary)
 
 def run_tree(args, name: str, **scale) -> dict:
@@ -802,6 +895,7 @@ def main():
         out["decode_step_with_append"] = run_decode_append(args, dec)
     if not args.no_prefill:
         out["prefill"] = run_prefill(args)
+        out["varlen_prefill"] = run_varlen_prefill(args)
         out["tree_verify"] = [run_tree(args, "tree_verify_64k"),
                               run_tree(args, "tree_verify_64k", B=4, Tq=64, seed=1104)]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
