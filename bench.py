@@ -835,6 +835,66 @@ def cpu_baseline(seconds: float = 12.0, prepared=None) -> dict:
                       f"{el:.1f} s; kernel cache precomputed as in the workload"}
 
 
+def secondary_cpu_baselines(out: dict, seconds: float = 3.0) -> None:
+    """The oracle, as it stands, beside each secondary leg, on bounded samples (about `seconds` of
+    host time each): chunked-prefill queries (scores, selection, attention), their gradients (one
+    query at a time, with the selection of the query's own row), and one tree row's drafts."""
+    import numpy as np
+
+    import oracle
+    from block_sparse_long_infllm_gb300 import synth
+    cores = oracle.num_threads()
+    if "prefill" in out:
+        w = synth.WORKLOADS[PREFILL]
+        inp = synth.make_inputs(w)
+        p = w.params()
+        M = oracle.n_kernels(w.L, w.kernel_size, w.kernel_stride)
+        kern, _ = oracle.kernel_pool(inp["k_cache"], inp["kv_len"], w.kernel_size, w.kernel_stride, M)
+        rng = np.random.default_rng(3)
+        n, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < seconds or n == 0:
+            t_list = np.sort(rng.choice(w.Tq, 8, replace=False)).astype(np.int32)
+            oracle.run(inp, w, t_list=t_list, kern=kern)
+            n += 8
+        el = time.perf_counter() - t0
+        out["prefill"]["cpu_baseline"] = {"value": n / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                          "sample": f"{n} random queries of {PREFILL} (all 32 heads), {el:.1f} s; "
+                                                    "kernel cache precomputed"}
+        if "backward" in out["prefill"]:
+            dout = synth.f32_to_bf16_bits(rng.standard_normal((1, 1, w.Hq, w.d)).astype(np.float32))
+            q64 = synth.bf16_bits_to_f32(inp["q"]).astype(np.float64)
+            k64 = synth.bf16_bits_to_f32(inp["k_cache"]).astype(np.float64)
+            v64 = synth.bf16_bits_to_f32(inp["v_cache"]).astype(np.float64)
+            do64 = synth.bf16_bits_to_f32(dout).astype(np.float64)
+            n, t0 = 0, time.perf_counter()
+            while time.perf_counter() - t0 < seconds or n == 0:
+                t = int(rng.integers(w.Tq))
+                pos = w.L - w.Tq + t
+                S = oracle.block_scores(inp["q"][:, t:t + 1], kern, np.array([pos + 1], dtype=np.int32), w.Hkv, p)
+                idx, cnt, _, _ = oracle.select(S, np.array([pos + 1], dtype=np.int32), 1, p)
+                oracle.attention_bwd(q64[:, t:t + 1], k64, v64, np.array([pos + 1], dtype=np.int32), idx, cnt, p, do64)
+                n += 1
+            el = time.perf_counter() - t0
+            out["prefill"]["backward"]["cpu_baseline"] = {
+                "value": n / el, "unit": "query gradients/s", "cores": cores, "kind": "oracle",
+                "sample": f"{n} random queries of {PREFILL}: selection, then dq and the query's dk, dv "
+                          f"contributions (fp64, all 32 heads), {el:.1f} s"}
+    if out.get("tree_verify"):
+        w = synth.WORKLOADS["tree_verify_64k"]
+        inp = synth.make_inputs(w)
+        M = oracle.n_kernels(w.L, w.kernel_size, w.kernel_stride)
+        kern, _ = oracle.kernel_pool(inp["k_cache"], inp["kv_len"], w.kernel_size, w.kernel_stride, M)
+        n, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < seconds or n == 0:
+            oracle.run(inp, w, kern=kern)
+            n += w.Tq
+        el = time.perf_counter() - t0
+        out["tree_verify"][0]["cpu_baseline"] = {
+            "value": n / el, "unit": "drafts/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n // w.Tq} whole verifications of tree_verify_64k ({w.Tq} drafts), {el:.1f} s; "
+                      "kernel cache precomputed"}
+
+
 def run_reference(args, world, rank):
     """The fp64 oracle as the reference arm: each step is one decode row of the
     headline workload with as many of its 16 heads as keep the run within a few minutes."""
@@ -900,6 +960,7 @@ def main():
                               run_tree(args, "tree_verify_64k", B=4, Tq=64, seed=1104)]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline()
+        secondary_cpu_baselines(out)
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
