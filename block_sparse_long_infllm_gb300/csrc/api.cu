@@ -80,13 +80,16 @@ struct DecodeWs {
     size_t scores, idx, counts, part, total;
 };
 
-// Sized for tree verification (one extra split per row) whether or not a mask is passed.
+// Sized for the larger of the tree and the single-token split shapes, whether or not a mask is
+// passed.
 DecodeWs decode_ws(int B, int n_draft, int Hkv, int d, int L_max, const Params& p) {
     DecodeWs w{};
     const int S_cap = infllmv2::selection_capacity(p, L_max);
-    int bps, nsc, ns;
-    infllmv2::decode_split_shape(p, L_max, true, &bps, &nsc, &ns);
     const size_t rows = static_cast<size_t>(B) * Hkv * n_draft;
+    int bps, nsc, ns_tree, ns_single;
+    infllmv2::decode_split_shape(p, L_max, true, static_cast<long long>(rows), &bps, &nsc, &ns_tree);
+    infllmv2::decode_split_shape(p, L_max, false, static_cast<long long>(rows), &bps, &nsc, &ns_single);
+    const int ns = ns_tree > ns_single ? ns_tree : ns_single;
     w.scores = 0;
     w.idx = align256(w.scores + rows * n_blocks(L_max, p.block_size) * sizeof(float));
     w.counts = align256(w.idx + rows * S_cap * sizeof(int));

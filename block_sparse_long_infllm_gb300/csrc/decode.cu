@@ -251,17 +251,22 @@ size_t decode_partial_bytes(int B, int n_draft, int Hkv, int d, int n_split) {
     return static_cast<size_t>(B) * n_draft * Hkv * n_split * per * sizeof(float);
 }
 
-void decode_split_shape(const Params& p, int L_max, bool tree, int* blocks_per_split, int* n_split_cache,
-                        int* n_split) {
+void decode_split_shape(const Params& p, int L_max, bool tree, long long rows, int* blocks_per_split,
+                        int* n_split_cache, int* n_split) {
     // 128 keys per chunk (one 32-key tile per warp): two 64-token blocks or one 128-token block;
     // one CTA per chunk of a sparse row's selection (top-k + forced); longer (dense) selections
-    // loop over several chunks per CTA.
+    // loop over several chunks per CTA.  A tree has a row per draft: with many rows, fewer CTAs per
+    // row (each looping over more chunks) keep the grid near kTreeCtas and cut the partials that
+    // the merge reads back.
+    constexpr long long kTreeCtas = 600;
     const int bps = p.block_size >= 128 ? 1 : 128 / p.block_size;
     const int nblk = (L_max + p.block_size - 1) / p.block_size;
     const int sparse_cap = max(1, min(p.topk + p.n_init + p.n_local, nblk));
+    int nsc = (sparse_cap + bps - 1) / bps;
+    if (tree && rows > 0) nsc = static_cast<int>(max(1ll, min(static_cast<long long>(nsc), kTreeCtas / rows)));
     *blocks_per_split = bps;
-    *n_split_cache = (sparse_cap + bps - 1) / bps;
-    *n_split = *n_split_cache + (tree ? 1 : 0);
+    *n_split_cache = nsc;
+    *n_split = nsc + (tree ? 1 : 0);
 }
 
 template <int D, int BS, int BPS>
@@ -283,7 +288,8 @@ static cudaError_t launch_split_t(const DecodeArgs& a, const CUtensorMap& tk, co
 cudaError_t launch_decode_attention(const DecodeArgs& a, const int* idx, const int* counts, int idx_stride,
                                     float* part) {
     int bps, nsc, ns;
-    decode_split_shape(a.p, a.L_max, a.tree_mask != nullptr, &bps, &nsc, &ns);
+    decode_split_shape(a.p, a.L_max, a.tree_mask != nullptr, static_cast<long long>(a.B) * a.n_draft * a.Hkv, &bps,
+                       &nsc, &ns);
     const int G = a.Hq / a.Hkv;
     const int rows = a.B * a.n_draft * a.Hkv;
     const int bs = a.p.block_size;

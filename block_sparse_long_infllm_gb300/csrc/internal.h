@@ -123,8 +123,8 @@ cudaError_t launch_prefill_attention(const PrefillArgs& a);
 bool tc_prefill_supported(const PrefillArgs& a);
 cudaError_t launch_prefill_tc(const PrefillArgs& a);
 
-void decode_split_shape(const Params& p, int L_max, bool tree, int* blocks_per_split, int* n_split_cache,
-                        int* n_split);
+void decode_split_shape(const Params& p, int L_max, bool tree, long long rows, int* blocks_per_split,
+                        int* n_split_cache, int* n_split);
 size_t decode_partial_bytes(int B, int n_draft, int Hkv, int d, int n_split);
 size_t bwd_workspace_bytes(int B, int Tq, int Hq, int Hkv, int L_max, int bs);
 cudaError_t launch_attention_bwd(const BwdArgs& a);

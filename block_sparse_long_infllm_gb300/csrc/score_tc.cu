@@ -59,7 +59,8 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
 template <int D>
 __global__ void __launch_bounds__(kScThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kern,
-                const int* __restrict__ kv_len, SeqMap sm, int Hq, int Hkv, int L_max, int M_max, int nblk_max, Params p,
+                const int* __restrict__ kv_len, SeqMap sm, int tree, int Hq, int Hkv, int L_max, int M_max, int nblk_max,
+                Params p,
                 int blocks_per_chunk, float* __restrict__ S, int* __restrict__ err) {
     using SM = ScSmem<D>;
     constexpr int G = 16;
@@ -82,16 +83,23 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int bs = p.block_size, c = p.kernel_size, s = p.kernel_stride;
     const int Lb = kv_len[b];
     const int Tq = sm.len(b), tok = sm.tok0(b);  // this sequence's chunk: token rows tok .. tok + Tq - 1
-    if (Tq < 0 || Tq > sm.Tq || (Tq > 0 && (Lb < Tq || Lb > L_max || kernels_in(Lb, c, s) > M_max))) {
+    // query t sits at Lb - Tq + t (a chunk) or, for tree drafts, all at the last cached position Lb - 1
+    const int pos0 = tree ? Lb - 1 : Lb - Tq;  // position of query t is pos0 + (tree ? 0 : t)
+    if (Tq < 0 || Tq > sm.Tq ||
+        (Tq > 0 && (Lb < (tree ? 1 : Tq) || Lb > L_max || kernels_in(Lb, c, s) > M_max))) {
         if (tid == 0 && blockIdx.x == 0) raise_error(err, kDevErrIndex);
         return;
     }
     if (t0 >= Tq) return;  // packed chunks shorter than the longest
     if (Lb < p.dense_len) return;  // dense sequence: every block is selected, no scores needed
     const int n_tok = min(kScTokens, Tq - t0);
-    const int pos_last = Lb - Tq + t0 + n_tok - 1;
+    const int pos_last = tree ? pos0 : pos0 + t0 + n_tok - 1;
     const int bt_max = pos_last / bs;
-    const int n_chunks = bt_max / blocks_per_chunk + 1;
+    // chunks split, split + n_split, ... of the blocks are this CTA's (blockIdx.z = split)
+    const int split = blockIdx.z, n_split = gridDim.z;
+    const int n_chunks_all = bt_max / blocks_per_chunk + 1;
+    const int n_chunks = n_chunks_all > split ? (n_chunks_all - split + n_split - 1) / n_split : 0;
+    if (n_chunks == 0) return;
 
     if (tid == 0) {
         mbar_init(bar_q, 1);
@@ -117,7 +125,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (lane == 0) {
             const uint32_t sQ = smem_u32(base + SM::kQOff);
             int k_issued[2] = {0, 0}, mma_issued = 0;
-            auto chunk_row = [&](int ch) { return first_kernel_of_block(ch * blocks_per_chunk, bs, c, s); };
+            // local chunk k is chunk split + n_split * k of the tile
+            auto chunk_row = [&](int k) { return first_kernel_of_block((split + n_split * k) * blocks_per_chunk, bs, c, s); };
             auto load = [&](int ch) {
                 const int st = ch & 1;
                 mbar_arrive_expect_tx(&bar_k[st], SM::kK);
@@ -187,7 +196,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 break;
             }
             tc_fence_after();
-            const int b0 = ch * blocks_per_chunk;
+            const int b0 = (split + n_split * ch) * blocks_per_chunk;
             const int j0 = first_kernel_of_block(b0, bs, c, s);
             const int j = j0 + r;
             const int jend = j * s + c - 1;  // last token of kernel j
@@ -219,7 +228,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int tk = th * 8 + u;
-                    const int pos = Lb - Tq + t0 + tk;
+                    const int pos = tree ? pos0 : pos0 + t0 + tk;
                     kmax[tk * kScM + r] = (tk < n_tok && jend <= pos) ? mx[u] : -INFINITY;
                 }
             }
@@ -230,7 +239,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int nb = min(blocks_per_chunk, bt_max + 1 - b0);
             for (int e = tid; e < n_tok * nb; e += kScEpi) {
                 const int tk = e / nb, blk = b0 + e % nb;
-                const int pos = Lb - Tq + t0 + tk;
+                const int pos = tree ? pos0 : pos0 + t0 + tk;
                 if (blk > pos / bs) continue;
                 const int ja = first_kernel_of_block(blk, bs, c, s) - j0;
                 const int jz = min(last_kernel_of_block(blk, bs, s) - j0, kScM - 1);
@@ -260,7 +269,7 @@ int score_tc_blocks_per_chunk(const Params& p) {
 }
 
 bool score_tc_supported(const SelectArgs& a) {
-    return a.Hq / a.Hkv == 16 && (a.d == 64 || a.d == 128) && !a.tree && a.M_max > 0 &&
+    return a.Hq / a.Hkv == 16 && (a.d == 64 || a.d == 128) && a.M_max > 0 &&
            score_tc_blocks_per_chunk(a.p) > 0;
 }
 
@@ -273,20 +282,24 @@ cudaError_t launch_score_tc(const SelectArgs& a, float* S) {
     const uint64_t k_rows = static_cast<uint64_t>(a.B) * a.Hkv * a.M_max;
     if (!make_tmap_bf16_2d(&tq, a.q, a.d, q_rows, 64, 16) || !make_tmap_bf16_2d(&tk, a.kernel_cache, a.d, k_rows, 64, kScM))
         return cudaErrorInvalidValue;
-    dim3 grid((a.Tq + kScTokens - 1) / kScTokens, a.B * a.Hkv);
+    // few query tiles (a draft tree, a short chunk): split each tile's chunks of blocks over CTAs
+    const int tiles = ((a.Tq + kScTokens - 1) / kScTokens) * a.B * a.Hkv;
+    const int chunks_max = (nblk_max - 1) / nb + 1;
+    const int n_split = std::max(1, std::min(chunks_max, 300 / std::max(tiles, 1)));
+    dim3 grid((a.Tq + kScTokens - 1) / kScTokens, a.B * a.Hkv, n_split);
     if (a.d == 128) {
         auto kfn = score_tc_kernel<128>;
         constexpr int smem = ScSmem<128>::kBytes;
         if (cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); e != cudaSuccess)
             return e;
-        return launch_kernel(kfn, grid, dim3(kScThreads), smem, a.stream, false, tq, tk, a.kv_len, sm, a.Hq, a.Hkv,
+        return launch_kernel(kfn, grid, dim3(kScThreads), smem, a.stream, false, tq, tk, a.kv_len, sm, a.tree, a.Hq, a.Hkv,
                              a.L_max, a.M_max, nblk_max, a.p, nb, S, a.err);
     }
     auto kfn = score_tc_kernel<64>;
     constexpr int smem = ScSmem<64>::kBytes;
     if (cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); e != cudaSuccess)
         return e;
-    return launch_kernel(kfn, grid, dim3(kScThreads), smem, a.stream, false, tq, tk, a.kv_len, sm, a.Hq, a.Hkv,
+    return launch_kernel(kfn, grid, dim3(kScThreads), smem, a.stream, false, tq, tk, a.kv_len, sm, a.tree, a.Hq, a.Hkv,
                          a.L_max, a.M_max, nblk_max, a.p, nb, S, a.err);
 }
 
