@@ -162,6 +162,10 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
+    // Launched with programmatic stream serialisation: the set-up above may overlap the previous
+    // kernel's tail; nothing the previous kernel may write is read before this wait.
+    pdl_trigger();
+    pdl_wait();
 
     // ================= 1. scores of this CTA's blocks, pushed as keys to every CTA
     // Thread 128 (warp 4) issues the TMA copies (Q once, then 128-row pieces of kernel rows) and,
@@ -812,12 +816,14 @@ static cudaError_t launch_cluster_t(const DecodeArgs& a, const void* kernel_cach
     cfg.blockDim = dim3(kDcThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = a.stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 1;  // (cluster size search without the serialisation attribute)
     // cluster size: the largest whose clusters all fit on the device at once (one wave of rows);
     // if none does, the one that keeps the most SMs busy
     int CL = 0, best_sms = 0, fallback = 0;
@@ -843,6 +849,7 @@ static cudaError_t launch_cluster_t(const DecodeArgs& a, const void* kernel_cach
     sh.CB = (sh.nblk_max + CL - 1) / CL;
     attr[0].val.clusterDim.x = CL;
     cfg.gridDim = dim3(rows * CL);
+    cfg.numAttrs = 2;  // + programmatic stream serialisation: set-up overlaps the previous kernel
     CUtensorMap tkern, tk, tv, tq;
     const uint64_t krows = static_cast<uint64_t>(a.B) * a.Hkv * M_max;
     const uint64_t cache_rows = static_cast<uint64_t>(a.B) * a.Hkv * a.L_max;
