@@ -370,7 +370,7 @@ def run_decode(args, world, rank):
                        "parallelism": f"replicas x{world}",
                        "l2": f"inputs larger than L2: {R} replicas of Q, K/V and kernel caches cycled step by step "
                              f"({R} x {alg['total'] / 1e6:.1f} MB touched per cycle)",
-                       "launch": (f"CUDA graph of {R} steps, replayed; one cluster kernel per step (one 16-CTA cluster per row)" if fused else
+                       "launch": (f"CUDA graph of {R} steps, replayed; one cluster kernel per step (one thread-block cluster per row, the largest size whose clusters all fit the device: 12 CTAs for 8 rows on a GB300)" if fused else
                                   f"CUDA graph of {R} steps, replayed; kernels chained with programmatic dependent launch"),
                        "kernel_cache": "resident (pooled before timing)"},
                roofline=roofline, clocks=clk, gpu_launches=(1 if fused else 4) * K, device_status=status)

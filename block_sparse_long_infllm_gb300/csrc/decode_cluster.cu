@@ -10,24 +10,26 @@
 // CTAs (one per SM) takes the whole row and keeps every intermediate in shared memory:
 //   1. CTA r scores the blocks [r*CB, (r+1)*CB): TMA copies of their kernel rows (issued before
 //      the cache length is read, for the longest cache), warp MMAs q.k for the G heads, max over
-//      the heads, then over the kernels overlapping each block -> its scores in shared memory.
-//   2. Cluster barrier.  Every CTA reads all of the row's scores from its peers' shared memory
-//      and computes the same selection: forced initial and local blocks, and the top-k of the
-//      others by their scores' order-preserving keys (k-th largest key found two bits per round
-//      from block-wide counts; ties go to the lower block), or every block below dense_len.
+//      the heads, then over the kernels overlapping each block -> its order-preserving keys,
+//      which bulk copies put into every peer's shared memory (counted on the peer's barrier).
+//   2. Every CTA computes the same selection from all of the row's keys: forced initial and
+//      local blocks, and the top-k of the others (a threshold from block-wide counts, then an
+//      exact ranking of the few keys above it; ties go to the lower block), or every block below
+//      dense_len.  (The forced blocks' K and V are brought towards L2 at the start; fetching the
+//      candidates' as well, while they are ranked, cost the ranking more than it saved.)
 //   3. CTA r attends to the selected blocks r, r+CL, ...: TMA copies of their K and V, the
 //      warp-MMA online softmax of attn_warp.cuh (32 keys per warp), a merge of the 8 warps into
-//      an fp32 partial (m, l, o) in shared memory.
-//   4. Cluster barrier.  CTA r merges the CL partials of heads r, r+CL, ... from its peers'
-//      shared memory into o (bf16) and lse, and a last barrier keeps every CTA's shared memory
-//      alive until its peers have read it.
+//      an fp32 partial (m, l, o) per head.
+//   4. CTA r merges heads r, r+CL, ...: every CTA copies its partial of a head into the owner's
+//      shared memory (bulk copies, counted on the owner's barrier), and the owner writes o (bf16)
+//      and lse.  Two halves of the cluster barrier order the copies after the peers' set-up and
+//      after their selection (whose memory the partials reuse); there is no barrier at the end.
 // No global memory is written but the outputs, and nothing is carried between launches.
 #include <algorithm>
 
 #include "attn_warp.cuh"
 #include "internal.h"
 #include "pool.cuh"
-#include "umma.cuh"
 
 namespace infllmv2 {
 
@@ -54,18 +56,26 @@ __device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
     return r;
 }
-__device__ __forceinline__ float dsmem_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
+// The cluster barrier in two halves, executed by every thread of every CTA (arrive, then wait, in
+// turn).  The arrive is relaxed: it orders no memory access by itself (a release arrive also waited
+// for this CTA's bulk copies in flight, microseconds here); the barrier initialisations it follows
+// are published by their own fence, and it is only ever used to say that shared memory has been
+// read (values already consumed) or that barriers exist.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// Bring the 128-byte line holding p into L2 (a hint).
+__device__ __forceinline__ void prefetch_l2_line(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
 }
-// All threads of all CTAs of the cluster: earlier shared-memory writes (local or remote) are
-// visible to every CTA after it.
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from this CTA's shared
+// memory to a cluster address (a peer's shared memory); completion is counted in bytes on the
+// barrier at cluster address `bar`, in the destination CTA.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "r"(src), "r"(bytes), "r"(bar)
+                 : "memory");
 }
 
 struct ClusterShape {
@@ -81,25 +91,28 @@ struct ClusterSmem {
     static constexpr int kX = (D / 64) * kDcKRows * 128;      // scoring tiles / K,V tiles / merge scratch
     static constexpr int kPB = kX / (2 * kTile) < 8 ? kX / (2 * kTile) : 8;  // blocks per attention pass
     static constexpr int kMerge = (8 * 16 * 2 + 8 * 16 * (D + 4)) * 4;
-    static constexpr int kPartial = (32 + 16 * D) * 4;         // m[16], l[16], o[16][D]
-    static_assert(kMerge <= kX, "merge scratch fits the tile memory");
-    // offsets from the 1024-aligned base: tiles | partial (the Q tile while scoring) | keys[nblk_max]
-    // | ks | sel[S_cap] | barriers
-    static_assert(kPartial >= (D / 64) * 16 * 128, "the Q tile fits the partial");
-    __host__ __device__ static int off_p() { return kX; }
-    __host__ __device__ static int off_keys() { return kX + ((kPartial + 15) & ~15); }
-    __host__ __device__ static int off_ks(int nblk_max) { return off_keys() + ((4 * nblk_max + 15) & ~15); }
-    __host__ __device__ static int off_sel(int nblk_max) { return off_ks(nblk_max) + 4 * kDcKRows; }
+    static constexpr int kPRow = D + 4;                        // a head's partial: m, l, 2 unused, o[D]
+    static constexpr int kPartial = 16 * kPRow * 4;            // this CTA's partials, after the merge scratch
+    static constexpr int kSlots = 24 * kPRow * 4;              // partials merged here: CL x heads owned <= 24
+    static_assert(kMerge % 16 == 0 && kMerge + kPartial <= kX, "merge scratch and partials fit the tile memory");
+    // offsets from the 1024-aligned base: tiles | keys[nblk_max + 64] and ks[kDcKRows] (while selecting),
+    // then the slots of the partials this CTA merges | sel[S_cap] | barriers
+    __host__ __device__ static int off_keys() { return kX; }
+    __host__ __device__ static int off_ks(int nblk_max) { return kX + ((4 * (nblk_max + 64) + 15) & ~15); }
+    __host__ __device__ static int off_sel(int nblk_max) {
+        const int a = off_ks(nblk_max) + 4 * kDcKRows, b = kX + kSlots;
+        return a > b ? a : b;
+    }
     __host__ __device__ static int off_bar(int nblk_max, int S_cap) { return (off_sel(nblk_max) + 4 * S_cap + 15) & ~15; }
-    static int bytes(int nblk_max, int S_cap) { return off_bar(nblk_max, S_cap) + 8 * (1 + kPB) + 1024; }
+    static int bytes(int nblk_max, int S_cap) { return off_bar(nblk_max, S_cap) + 8 * (kPB + 2) + 1024; }
 };
 
 template <int D, int BS, bool kAppend>
 __global__ void __launch_bounds__(kDcThreads, 1)
 decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q,
-                      const __nv_bfloat16* __restrict__ q,
-                      const int* __restrict__ kv_len, int Hq, int Hkv, int G, int L_max, int M_max, Params p,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* kc,
+                      const __nv_bfloat16* vc, const int* __restrict__ kv_len, int Hq, int Hkv, int G, int L_max, int M_max, Params p,
                       ClusterShape sh, int* __restrict__ idx_out, int idx_stride, int* __restrict__ counts_out,
                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse, float scale_log2,
                       int* __restrict__ err, const __nv_bfloat16* __restrict__ k_new,
@@ -115,21 +128,19 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                                                            ~static_cast<uintptr_t>(1023));
     uint32_t* keys = reinterpret_cast<uint32_t*>(base + SM::off_keys());           // [nblk_max], filled by all CTAs
     float* ks = reinterpret_cast<float*>(base + SM::off_ks(sh.nblk_max));           // [kDcKRows]
-    float* part = reinterpret_cast<float*>(base + SM::off_p());                     // m, l, o
+    float* part = reinterpret_cast<float*>(base + SM::kMerge);                       // [16][kPRow], after attention
     int* sel = reinterpret_cast<int*>(base + SM::off_sel(sh.nblk_max));             // [S_cap]
-    uint64_t* bar_a = reinterpret_cast<uint64_t*>(base + SM::off_bar(sh.nblk_max, sh.S_cap));
-    uint64_t* bar_b = bar_a + 1;  // [PB]
+    uint64_t* bar_b = reinterpret_cast<uint64_t*>(base + SM::off_bar(sh.nblk_max, sh.S_cap));  // [PB]
+    uint64_t* bar_keys = bar_b + PB;      // the peers' keys have landed
+    uint64_t* bar_part = bar_b + PB + 1;  // the partials of the heads merged here have landed
+    constexpr int kPRow = SM::kPRow;
     __shared__ int s_wsum[2][kDcThreads / 32];
     __shared__ int s_cnt[3][4];
-    __shared__ float s_w[32];
-    __shared__ float s_f[8][16];  // merge weights of the 8 warps per row
     __shared__ unsigned long long s_cv[kDcCand];          // candidates >= tau: key << 32 | ~block
     __shared__ int s_rk[kDcCand];                          // their ranks
     __shared__ uint32_t s_bits[kDcFastPer * kDcThreads / 32];  // chosen blocks (fast path), one bit each
     __shared__ int s_wpre[kDcFastPer * kDcThreads / 32];       // chosen blocks below each bitmap word
     __shared__ uint64_t s_bar_piece[kDcKRows / 128];       // scoring: kernel rows of piece p landed
-    __shared__ uint64_t s_bar_mma[2], s_bar_free[2];       // scoring accumulator buffers: written / read
-    __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, cq = lane & 3;
@@ -138,48 +149,43 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     const int row = blockIdx.x / ncta;
     const int b = row / Hkv, g = row % Hkv;
     const int c = p.kernel_size, s = p.kernel_stride;
+    const int nh = static_cast<int>(rank) < G ? (G - 1 - static_cast<int>(rank)) / ncta + 1 : 0;  // heads merged here
+    auto key_bytes = [&](int j) {  // keys CTA j sends: its blocks, rounded up to 16 bytes
+        const int n = max(0, min(sh.nblk_max - j * sh.CB, sh.CB));
+        return static_cast<uint32_t>(((n + 3) & ~3) * 4);
+    };
 
     if (tid == 0) {
         prefetch_tmap(&tm_kern);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
-        prefetch_tmap(&tm_q);
-        mbar_init(bar_a, 1);
         for (int k = 0; k < PB; ++k) mbar_init(&bar_b[k], 1);
         for (int k = 0; k < kDcKRows / 128; ++k) mbar_init(&s_bar_piece[k], 1);
-        for (int k = 0; k < 2; ++k) {
-            mbar_init(&s_bar_mma[k], 1);
-            mbar_init(&s_bar_free[k], 128);
-        }
+        mbar_init(bar_keys, 1);
+        mbar_init(bar_part, 1);
         fence_mbar_init();
-    }
-    if (warp == 0) {  // scoring accumulators: 2 x 16 TMEM columns (kernel row x head, fp32)
-        tmem_alloc(&s_tmem, 32);
-        tmem_relinquish();
+        uint32_t in_keys = 0;
+        for (int j = 0; j < ncta; ++j)
+            if (j != static_cast<int>(rank)) in_keys += key_bytes(j);
+        mbar_arrive_expect_tx(bar_keys, in_keys);
+        mbar_arrive_expect_tx(bar_part, static_cast<uint32_t>(nh * ncta * kPRow * 4));
     }
     if (tid < 12) (&s_cnt[0][0])[tid] = 0;
-    tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = s_tmem;
     // Launched with programmatic stream serialisation: the set-up above may overlap the previous
     // kernel's tail; nothing the previous kernel may write is read before this wait.
     pdl_trigger();
     pdl_wait();
 
     // ================= 1. scores of this CTA's blocks, pushed as keys to every CTA
-    // Thread 128 (warp 4) issues the TMA copies (Q once, then 128-row pieces of kernel rows) and,
-    // per piece, the tcgen05 MMAs S[kernel row][head] = K_kernel Q^T (M=128, N=16, K=d) into one of
-    // two TMEM buffers; warps 0-3 read each piece back (one kernel row per thread) and keep the
-    // maximum over the G heads.  A piece is scored as soon as it lands.
-    constexpr int kPieces = kDcKRows / 128;
-    constexpr uint32_t kIdesc = idesc_bf16_f32(128, 16, 0, 0);
+    // Thread 0 issues the TMA copies of a pass's kernel rows in 128-row pieces; warp w scores the
+    // 32-row tiles w, w + 8, ... of the pass as their pieces land: S[head][kernel row] = Q K^T by
+    // warp MMAs (the Q fragments of the attention below), then the maximum over the G heads.  (With
+    // N = 16 heads a tcgen05 MMA does too little work per issue: one thread issuing the 8 MMAs of a
+    // 128-row piece took longer than the piece took to land.)
     const int blkA0 = static_cast<int>(rank) * sh.CB;
     const int blkA1 = min(blkA0 + sh.CB, sh.nblk_max);
-    const bool issuer = tid == 128;
-    const uint32_t sQ = smem_u32(part);
-    uint32_t piece_uses = 0;  // issuer: bit p = phase parity of s_bar_piece[p]
-    int gi = 0;               // scoring MMA groups so far (issuer and readers count alike)
+    uint32_t piece_uses = 0;  // bit p = phase parity of s_bar_piece[p] (the same in every thread)
     auto pass_rows = [&](int sub0, int& jlo, int& jend) {
         const int sub1 = min(sub0 + sh.SC, blkA1);
         jlo = first_kernel_of_block(sub0, BS, c, s);
@@ -196,12 +202,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                             row * M_max + jlo + pc * 128, &s_bar_piece[pc]);
         }
     };
-    if (issuer) {
-        mbar_arrive_expect_tx(bar_a, (D / 64) * 16 * 128);
-        for (int half = 0; half < D / 64; ++half)
-            tma_load_2d(part + half * (16 * 128 / 4), &tm_q, 64 * half, b * Hq + g * G, bar_a);
-        if (blkA0 < blkA1) issue_pass(blkA0);
-    }
+    if (tid == 0 && blkA0 < blkA1) issue_pass(blkA0);
     // Q fragments: rows = heads (rows >= G read as zero), for the attention
     QFrag<D> Q;
     load_q(Q, q + (static_cast<size_t>(b) * Hq + static_cast<size_t>(g) * G) * D, D, G);
@@ -210,20 +211,38 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     const int bt = len_ok ? (L - 1) / BS : -1;
     const bool dense = L < p.dense_len;
     auto forced = [&](int blk) { return blk < p.n_init || blk > bt - p.n_local; };
-    // Decode-step append (the kAppend instance): CTA 0 writes this row's new K and V into cache row L-1
-    // (the attention below reads them after the first cluster barrier), and warp 5 of every CTA
-    // pools its share of the 8-element slices of the kernel the new token completes, for the steps
-    // to come.  This step's scores never need that kernel: it overlaps only the query's own block
-    // and the one before, both local (forced) blocks under the condition the host checks.
+    // K and V of block blk, brought into L2 ahead of the attention's copies: lines t0, t0 + nt, ...
+    // of its visible rows (K lines first, then V)
+    constexpr int kLines = BS * D * 2 / 128;  // 128-byte lines of one block of K (or V)
+    auto prefetch_block = [&](int blk, int t0, int nt) {
+        const int n_lines = min(BS, L - blk * BS) * (D * 2 / 128);
+        const size_t off = (static_cast<size_t>(row) * L_max + static_cast<size_t>(blk) * BS) * D;
+        const char* kb = reinterpret_cast<const char*>(kc + off);
+        const char* vb = reinterpret_cast<const char*>(vc + off);
+        for (int w = t0; w < 2 * kLines; w += nt) {
+            const int wl = w < kLines ? w : w - kLines;
+            if (wl < n_lines) prefetch_l2_line((w < kLines ? kb : vb) + 128 * wl);
+        }
+    };
+    if (len_ok && warp == kDcThreads / 32 - 1)  // the forced blocks are attended whatever the scores
+        for (int i = 0; i < p.n_init + p.n_local; ++i) {
+            const int blk = i < p.n_init ? i : bt - (i - p.n_init);
+            if (blk >= 0 && blk <= bt && blk % ncta == static_cast<int>(rank)) prefetch_block(blk, lane, 32);
+        }
+    // Decode-step append (the kAppend instance): warp 6 holds this row's new K and V, which the CTA
+    // that attends the last selected block (the query's own) writes into cache row L-1 before its
+    // copies; warp 5 of every CTA pools its share of the 8-element slices of the kernel the new
+    // token completes, for the steps to come.  This step's scores never need that kernel: it
+    // overlaps only the query's own block and the one before, both local (forced) blocks under the
+    // condition the host checks.
+    uint4 k_row = make_uint4(0u, 0u, 0u, 0u), v_row = k_row;
     if constexpr (kAppend) {
       if (len_ok) {
         const int pn = L - 1;
         const uint4* kn = reinterpret_cast<const uint4*>(k_new + static_cast<size_t>(row) * D);
-        if (rank == 0 && warp == 6 && lane < D / 8) {
-            const size_t wr = (static_cast<size_t>(row) * L_max + pn) * D;
-            reinterpret_cast<uint4*>(k_w + wr)[lane] = ldg_v4(kn + lane);
-            reinterpret_cast<uint4*>(v_w + wr)[lane] =
-                ldg_v4(reinterpret_cast<const uint4*>(v_new + static_cast<size_t>(row) * D) + lane);
+        if (warp == 6 && lane < D / 8) {
+            k_row = ldg_v4(kn + lane);
+            v_row = ldg_v4(reinterpret_cast<const uint4*>(v_new + static_cast<size_t>(row) * D) + lane);
         }
         if (warp == 5 && L >= c && (L - c) % s == 0) {
             const int jn = (L - c) / s, r0 = jn * s;  // jn < M_max: len_ok
@@ -239,8 +258,11 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
         }
       }
     }
+    // first half of the cluster barrier: this CTA's barriers are initialised; the peers wait for it
+    // before their first copy into this CTA
+    cluster_arrive_relaxed();
     const uint32_t keys_base = smem_u32(keys);
-    bool q_landed = false;
+    const uint32_t sK = smem_u32(base);
     for (int sub0 = blkA0; sub0 < blkA1; sub0 += sh.SC) {
         int jlo, jend;
         const int nrows = pass_rows(sub0, jlo, jend);
@@ -250,57 +272,42 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
         const int jhi = work ? min(min(last_kernel_of_block(bz - 1, BS, s), kernels_in(L, c, s) - 1), jend) : -1;
         const int nj = work ? jhi - jlo + 1 : 0;  // visible kernel rows of the pass
         const int n_issued = nrows > 0 ? (nrows + 127) / 128 : 0;
-        const int n_mma = nj > 0 ? (nj + 127) / 128 : 0;
-        if (issuer) {
-            bool ok = true;
-            if (n_mma > 0 && !q_landed) {
-                ok = mbar_wait(bar_a, 0);
-                q_landed = true;
+        for (int t = warp; 32 * t < nj; t += kDcThreads / 32) {
+            const int pc = t >> 2;  // the 128-row piece holding the tile
+            if (!__all_sync(0xffffffffu, mbar_wait(&s_bar_piece[pc], (piece_uses >> pc) & 1u))) {
+                if (lane == 0) raise_error(err, kDevErrTimeout);
+                continue;
             }
-            for (int pc = 0; pc < n_issued; ++pc) {
-                // every issued piece must land before its tiles are reused, scored or not
-                const bool landed = mbar_wait(&s_bar_piece[pc], (piece_uses >> pc) & 1u);
-                ok = ok && landed;
-                piece_uses ^= 1u << pc;
-                if (pc >= n_mma) continue;
-                const int buf = (gi + pc) & 1;
-                if (gi + pc >= 2) ok = ok && mbar_wait(&s_bar_free[buf], ((gi + pc - 2) >> 1) & 1);
-                if (ok) {
-                    tc_fence_after();
+            uint4 kw[4][D / 32];
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t ko = (kk / 4) * (kDcKRows * 128) + (kk % 4) * 32;
-                        const uint32_t qo = (kk / 4) * (16 * 128) + (kk % 4) * 32;
-                        mma_ss(tmem + 16 * buf, sw128_desc(smem_u32(base) + pc * (128 * 128) + ko, 16, 1024),
-                               sw128_desc(sQ + qo, 16, 1024), kIdesc, kk > 0 ? 1u : 0u);
-                    }
-                }
-                mma_commit(&s_bar_mma[buf]);  // also when not issued: the readers' waits stay in step
-            }
-            if (!ok) raise_error(err, kDevErrTimeout);
-        } else if (warp < 4) {
-            for (int pc = 0; pc < n_mma; ++pc) {
-                const int buf = (gi + pc) & 1;
-                const bool got = mbar_wait(&s_bar_mma[buf], ((gi + pc) >> 1) & 1);
-                tc_fence_after();
-                uint32_t v[16];
-                tmem_ld16(tmem + 16 * buf + (static_cast<uint32_t>(32 * warp) << 16), v);
-                tmem_ld_wait16(v);
-                tc_fence_before();
-                mbar_arrive(&s_bar_free[buf]);
-                const int r = pc * 128 + 32 * warp + lane;  // kernel row jlo + r
-                if (got && r < nj) {
-                    float m = -INFINITY;
+            for (int nt = 0; nt < 4; ++nt) {
+                const int r = 32 * t + 8 * nt + gq;
 #pragma unroll
-                    for (int h = 0; h < 16; ++h)
-                        if (h < G) m = fmaxf(m, __uint_as_float(v[h]));
-                    ks[r] = m;
-                } else if (!got && lane == 0) {
-                    raise_error(err, kDevErrTimeout);
+                for (int i = 0; i < D / 32; ++i) {
+                    const int col = 32 * i + 8 * cq;
+                    kw[nt][i] = lds_v4(sK + (col / 64) * (kDcKRows * 128) + swz128(r, (col % 64) / 8));
                 }
             }
+            float sc[4][4];
+            qk_tiles<D>(sc, Q, kw);
+            // column 2cq + j of n-tile nt is kernel row 32t + 8nt + 2cq + j; rows gq and gq + 8 are heads
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    float m = fmaxf(gq < G ? sc[nt][j] : -INFINITY, gq + 8 < G ? sc[nt][2 + j] : -INFINITY);
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                    const int r = 32 * t + 8 * nt + 2 * cq + j;
+                    if (gq == 0 && r < nj) ks[r] = m;
+                }
         }
-        gi += n_mma;
+        // every issued piece has landed before its tiles are reused, scored or not
+        if (tid == 0)
+            for (int pc = 0; pc < n_issued; ++pc)
+                if (!mbar_wait(&s_bar_piece[pc], (piece_uses >> pc) & 1u)) raise_error(err, kDevErrTimeout);
+        piece_uses ^= (1u << n_issued) - 1u;
         __syncthreads();
         if (work) {
             // block score = max over its visible kernels; its selection key goes to every CTA
@@ -309,22 +316,27 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                 const int jz = min(last_kernel_of_block(blk, BS, s), jhi);
                 float m = -INFINITY;
                 for (int jj = ja; jj <= jz; ++jj) m = fmaxf(m, ks[jj - jlo]);
-                const uint32_t key = forced(blk) ? 0u : ordered_key(m);  // 0: not a candidate
-                const uint32_t a = keys_base + 4u * blk;
-                for (int j = 0; j < ncta; ++j) dsmem_st_u32(dsmem_addr(a, j), key);
+                keys[blk] = forced(blk) ? 0u : ordered_key(m);  // 0: not a candidate
             }
         }
         __syncthreads();  // tiles and ks free for the next pass
-        if (issuer && sub0 + sh.SC < blkA1) issue_pass(sub0 + sh.SC);
+        if (tid == 0 && sub0 + sh.SC < blkA1) issue_pass(sub0 + sh.SC);
     }
-    if (issuer && !q_landed) mbar_wait(bar_a, 0);  // the Q copy has landed before its tile is reused
-    tc_fence_before();
+    // this CTA's keys -> every peer: bulk copies into the same offsets of the peers' shared memory,
+    // counted on their key barriers; then wait for the peers' keys
+    fence_proxy_async_shared();
     __syncthreads();
-    if (warp == 0) {
-        tc_fence_after();
-        tmem_dealloc(tmem, 32);
+    cluster_wait();
+    if (tid == 0) {
+        const uint32_t nb = key_bytes(static_cast<int>(rank));
+        if (nb > 0)
+            for (int j = 0; j < ncta; ++j)
+                if (j != static_cast<int>(rank))
+                    bulk_copy_to_peer(dsmem_addr(keys_base + 4u * blkA0, j), keys_base + 4u * blkA0, nb,
+                                      dsmem_addr(smem_u32(bar_keys), j));
+        bulk_commit();
     }
-    cluster_sync();
+    if (!mbar_wait(bar_keys, 0) && tid == 0) raise_error(err, kDevErrTimeout);
 
     // ================= 2. the row's selection, computed by every CTA from all the keys
     int count = 0;
@@ -630,6 +642,15 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
             total = sel_total + min(tie_total, krem);
         }
         count = min(total, sh.S_cap);
+        if constexpr (kAppend) {
+            // the new K/V row, by the CTA that attends the last selected block, ahead of its copies
+            if (len_ok && count > 0 && static_cast<int>(rank) == (count - 1) % ncta && warp == 6 && lane < D / 8) {
+                const size_t wr = (static_cast<size_t>(row) * L_max + (L - 1)) * D;
+                reinterpret_cast<uint4*>(k_w + wr)[lane] = k_row;
+                reinterpret_cast<uint4*>(v_w + wr)[lane] = v_row;
+                fence_proxy_async_global();
+            }
+        }
         __syncthreads();  // sel complete
         if (rank == 0) {
             if (tid == 0 && (total > sh.S_cap || !len_ok)) raise_error(err, kDevErrIndex);
@@ -640,14 +661,14 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
             }
         }
     }
+    // second half-barrier: this CTA no longer reads its keys or scores (and its copies of its keys
+    // have been read), whose memory takes the peers' partials after the attention
+    if (tid == 0) bulk_wait_read_all();
+    cluster_arrive_relaxed();
 
     // ================= 3. attention over the selected blocks rank, rank + CL, ...
     WarpAcc<D> A;
     acc_init(A);
-    // an appended K/V row (generic stores of CTA 0, released and acquired by the cluster barrier)
-    // is read below by this thread's bulk copies
-    if constexpr (kAppend)
-        if (tid == 0) fence_proxy_async_global();
     {
         const int mine = count > static_cast<int>(rank) ? (count - static_cast<int>(rank) + ncta - 1) / ncta : 0;
         uint32_t ph_b = 0;
@@ -718,75 +739,81 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                 sm_o[(warp * 16 + gq + 8 * (e >> 1)) * kRowPad + col + (col >> 5)] = A.o[nt][e];
             }
         __syncthreads();
-        if (tid < 16) {  // per row: the warps' weights, the CTA's max and sum
-            const int r = tid;
+        // thread t: row t / 16 (a head), columns 8 (t % 16) .. +7 per pass; each thread forms the
+        // row's warp weights itself
+        constexpr int kCols = 8, kTpr = D / kCols;  // threads per row
+        for (int e0 = tid * kCols; e0 < 16 * D; e0 += kDcThreads * kCols) {
+            const int r = e0 / D, col0 = e0 % D;
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < 8; ++w) M = fmaxf(M, sm_m[w * 16 + r]);
             const float ref = M == -INFINITY ? 0.f : M;
-            float l = 0.f;
+            float f[8], l = 0.f;
 #pragma unroll
             for (int w = 0; w < 8; ++w) {
-                const float f = fast_exp2(sm_m[w * 16 + r] - ref);
-                s_f[w][r] = f;
-                l += sm_l[w * 16 + r] * f;
+                f[w] = fast_exp2(sm_m[w * 16 + r] - ref);
+                l += sm_l[w * 16 + r] * f[w];
             }
-            part[r] = M;
-            part[16 + r] = l;
-        }
-        __syncthreads();
-        for (int e = tid; e < 16 * D; e += kDcThreads) {
-            const int r = e / D, col = e % D;
-            float acc = 0.f;
+            if ((tid % kTpr) == 0) {
+                part[r * kPRow] = M;
+                part[r * kPRow + 1] = l;
+            }
 #pragma unroll
-            for (int w = 0; w < 8; ++w) acc += sm_o[(w * 16 + r) * kRowPad + col + (col >> 5)] * s_f[w][r];
-            part[32 + e] = acc;
+            for (int i = 0; i < kCols; ++i) {
+                const int col = col0 + i;
+                float acc = 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) acc += sm_o[(w * 16 + r) * kRowPad + col + (col >> 5)] * f[w];
+                part[r * kPRow + 4 + col] = acc;
+            }
         }
     }
-    cluster_sync();
-
-    // ================= 4. merge of the CTAs' partials: heads rank, rank + CL, ...
-    const uint32_t p_base = smem_u32(part);
-    for (int h = static_cast<int>(rank); h < G; h += ncta) {
-        if (warp == 0) {
-            // weights of the CTAs for head h
-            float m = -INFINITY, l = 0.f;
-            if (lane < ncta) {
-                m = dsmem_f32(dsmem_addr(p_base + 4u * h, lane));
-                l = dsmem_f32(dsmem_addr(p_base + 4u * (16 + h), lane));
-            }
-            float M = m;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-            const float ref = M == -INFINITY ? 0.f : M;
-            const float f = lane < ncta ? fast_exp2(m - ref) : 0.f;
-            float Ls = l * f;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
-            s_w[lane] = f;
-            if (lane == 0) {
-                s_wsum[0][0] = __float_as_int(M);
-                s_wsum[0][1] = __float_as_int(Ls);
-            }
+    // ================= 4. merge of the CTAs' partials: CTA r merges heads r, r + CL, ...
+    // Every CTA copies its partial of head h into slot (h / CL, its rank) of CTA h % CL, once the
+    // peers are past their selection (their key memory holds the slots).
+    const uint32_t slots = keys_base;  // [nh][CL][kPRow] fp32
+    fence_proxy_async_shared();
+    __syncthreads();
+    cluster_wait();
+    if (tid == 0) {
+        for (int h = 0; h < G; ++h) {
+            const int owner = h % ncta, hl = h / ncta;
+            const uint32_t dst = slots + 4u * static_cast<uint32_t>((hl * ncta + static_cast<int>(rank)) * kPRow);
+            bulk_copy_to_peer(dsmem_addr(dst, owner), smem_u32(part + h * kPRow), kPRow * 4,
+                              dsmem_addr(smem_u32(bar_part), owner));
         }
-        __syncthreads();
-        const float M = __int_as_float(s_wsum[0][0]), Ls = __int_as_float(s_wsum[0][1]);
+        bulk_commit();
+    }
+    if (!mbar_wait(bar_part, 0) && tid == 0) raise_error(err, kDevErrTimeout);
+    const float* sl = reinterpret_cast<const float*>(keys);
+    for (int e = tid; e < nh * D; e += kDcThreads) {
+        const int hl = e / D, d = e % D, h = static_cast<int>(rank) + ncta * hl;
+        const float* ph = sl + hl * ncta * kPRow;
+        float m[16], l[16], v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            m[j] = j < ncta ? ph[j * kPRow] : -INFINITY;
+            l[j] = j < ncta ? ph[j * kPRow + 1] : 0.f;
+            v[j] = j < ncta ? ph[j * kPRow + 4 + d] : 0.f;
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) M = fmaxf(M, m[j]);
+        const float ref = M == -INFINITY ? 0.f : M;
+        float Ls = 0.f, acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float f = j < ncta ? fast_exp2(m[j] - ref) : 0.f;
+            Ls += l[j] * f;
+            acc += v[j] * f;
+        }
         const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-        for (int d = tid; d < D; d += kDcThreads) {
-            float v[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                v[j] = j < ncta ? dsmem_f32(dsmem_addr(p_base + 4u * (32 + h * D + d), j)) : 0.f;
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) acc += v[j] * s_w[j];
-            o[(static_cast<size_t>(b) * Hq + g * G + h) * D + d] = __float2bfloat16_rn(acc * inv);
-        }
-        if (lse != nullptr && tid == 0)
+        o[(static_cast<size_t>(b) * Hq + g * G + h) * D + d] = __float2bfloat16_rn(acc * inv);
+        if (lse != nullptr && d == 0)
             lse[static_cast<size_t>(b) * Hq + g * G + h] = Ls > 0.f ? (M + log2f(Ls)) * 0.69314718055994530942f : -INFINITY;
-        __syncthreads();
     }
-    cluster_sync();  // peers have finished reading this CTA's shared memory
+    // this CTA's copies have read its partials before it exits
+    if (tid == 0) bulk_wait_read_all();
 }
 
 template <int D, int BS>
@@ -845,22 +872,23 @@ static cudaError_t launch_cluster_t(const DecodeArgs& a, const void* kernel_cach
         }
     }
     if (CL == 0) CL = fallback;
-    if (CL == 0) return cudaErrorNotSupported;
-    sh.CB = (sh.nblk_max + CL - 1) / CL;
+    if (CL == 0 || ((16 + CL - 1) / CL) * CL * SM::kPRow * 4 > SM::kSlots) return cudaErrorNotSupported;
+    sh.CB = ((sh.nblk_max + CL - 1) / CL + 3) & ~3;  // a multiple of 4: each CTA's keys are 16-byte copies
     attr[0].val.clusterDim.x = CL;
     cfg.gridDim = dim3(rows * CL);
     cfg.numAttrs = 2;  // + programmatic stream serialisation: set-up overlaps the previous kernel
-    CUtensorMap tkern, tk, tv, tq;
+    CUtensorMap tkern, tk, tv;
     const uint64_t krows = static_cast<uint64_t>(a.B) * a.Hkv * M_max;
     const uint64_t cache_rows = static_cast<uint64_t>(a.B) * a.Hkv * a.L_max;
     if (!make_tmap_bf16_2d(&tkern, kernel_cache, D, krows, 64, 128) ||
         !make_tmap_bf16_2d(&tk, a.k_cache, D, cache_rows, 64, BS) ||
-        !make_tmap_bf16_2d(&tv, a.v_cache, D, cache_rows, 64, BS) ||
-        !make_tmap_bf16_2d(&tq, a.q, D, static_cast<uint64_t>(a.B) * a.Hq, 64, 16))
+        !make_tmap_bf16_2d(&tv, a.v_cache, D, cache_rows, 64, BS))
         return cudaErrorNotSupported;
     const int G = a.Hq / a.Hkv;
     const float scale_log2 = a.p.scale * 1.4426950408889634f;
-    return cudaLaunchKernelEx(&cfg, kfn, tkern, tk, tv, tq, static_cast<const __nv_bfloat16*>(a.q), a.kv_len, a.Hq, a.Hkv,
+    return cudaLaunchKernelEx(&cfg, kfn, tkern, tk, tv, static_cast<const __nv_bfloat16*>(a.q),
+                              static_cast<const __nv_bfloat16*>(a.k_cache), static_cast<const __nv_bfloat16*>(a.v_cache),
+                              a.kv_len, a.Hq, a.Hkv,
                               G, a.L_max, M_max, a.p, sh, idx_out, idx_stride, counts_out,
                               static_cast<__nv_bfloat16*>(a.o), a.lse, scale_log2, a.err,
                               static_cast<const __nv_bfloat16*>(a.k_new), static_cast<const __nv_bfloat16*>(a.v_new),
@@ -874,8 +902,7 @@ bool decode_cluster_supported(const DecodeArgs& a, int M_max) {
     if (a.tree_mask != nullptr || a.n_draft != 1) return false;
     if (G < 1 || G > 16 || (a.d != 64 && a.d != 128) || (bs != 64 && bs != 128)) return false;
     // the tensor maps' boxes must fit the tensors
-    if (static_cast<long long>(a.B) * a.Hkv * M_max < 128 || static_cast<long long>(a.B) * a.Hkv * a.L_max < bs ||
-        static_cast<long long>(a.B) * a.Hq < 16)
+    if (static_cast<long long>(a.B) * a.Hkv * M_max < 128 || static_cast<long long>(a.B) * a.Hkv * a.L_max < bs)
         return false;
     return true;
 }

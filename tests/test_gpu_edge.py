@@ -246,3 +246,27 @@ def test_decode_tied_scores_take_lowest_blocks(cuda_lib, bs):
     o_ref, lse_ref = oracle.attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["kv_len"], gidx, gcnt, p)
     check_output(bf16_to_f64(o), o_ref)
     assert np.max(np.abs(lse.cpu().numpy() - lse_ref)) < 2e-3
+
+
+@pytest.mark.parametrize("decisive", [False, True], ids=["as_written", "decisive"])
+def test_decode_output_without_selection_list(cuda_lib, decisive):
+    # The single-kernel decode may attend to a candidate-ordered list and skip building the
+    # block-ordered selection when the caller does not ask for it: o and lse must be the same
+    # bits with and without idx_out, and match the oracle over the oracle's own selection.
+    import torch
+    w = synth.WORKLOADS["decode_128k_b4"].scaled(B=2, L=65536, seed=3400 + int(decisive))
+    inp = synth.make_inputs(w, decisive=decisive)
+    g, oidx, ocnt = _parity(w, inp)
+    L = lib()
+    p = w.params()
+    o2 = torch.empty_like(g["o"])
+    lse2 = torch.empty_like(g["lse"])
+    ws = torch.empty(L.workspace_size(L.ENTRY_DECODE, w.B, w.Tq, w.Hq, w.Hkv, w.d, w.L_max, p),
+                     dtype=torch.uint8, device="cuda")
+    L.decode(g["q"], g["k"], g["v"], g["kern"], g["kv_len"], o2, ws, p, lse=lse2)
+    torch.cuda.synchronize()
+    assert L.sync_status() == 0
+    assert torch.equal(o2.view(torch.int16), g["o"].view(torch.int16))
+    assert torch.equal(lse2, g["lse"])
+    o_ref, lse_ref = oracle.attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["kv_len"], oidx, ocnt, p)
+    check_output(bf16_to_f64(o2), o_ref)
