@@ -15,8 +15,9 @@
 //   2. Every CTA computes the same selection from all of the row's keys: forced initial and
 //      local blocks, and the top-k of the others (a threshold from block-wide counts, then an
 //      exact ranking of the few keys above it; ties go to the lower block), or every block below
-//      dense_len.  (The forced blocks' K and V are brought towards L2 at the start; fetching the
-//      candidates' as well, while they are ranked, cost the ranking more than it saved.)
+//      dense_len.  The forced blocks' K and V are brought towards L2 at the start, the few
+//      candidates' while they are ranked (bulk prefetches), and before the programmatic wait the
+//      CTA prefetches its q and kernel rows: a prefetch reads no value.
 //   3. CTA r attends to the selected blocks r, r+CL, ...: TMA copies of their K and V, the
 //      warp-MMA online softmax of attn_warp.cuh (32 keys per warp), a merge of the 8 warps into
 //      an fp32 partial (m, l, o) per head.
@@ -65,9 +66,15 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-// Bring the 128-byte line holding p into L2 (a hint).
+// Bring the 128-byte line holding p, or `bytes` from p (16-byte aligned, a multiple of 16) by the
+// bulk-copy unit, into L2.  Hints: no value is read, so they may run ahead of the programmatic
+// wait (L2 stays coherent with the previous kernel's writes).
 __device__ __forceinline__ void prefetch_l2_line(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
 }
 // Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from this CTA's shared
 // memory to a cluster address (a peer's shared memory); completion is counted in bytes on the
@@ -111,7 +118,7 @@ template <int D, int BS, bool kAppend>
 __global__ void __launch_bounds__(kDcThreads, 1)
 decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
-                      const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* kc,
+                      const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* kern_rows, const __nv_bfloat16* kc,
                       const __nv_bfloat16* vc, const int* __restrict__ kv_len, int Hq, int Hkv, int G, int L_max, int M_max, Params p,
                       ClusterShape sh, int* __restrict__ idx_out, int idx_stride, int* __restrict__ counts_out,
                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse, float scale_log2,
@@ -140,6 +147,10 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     __shared__ int s_rk[kDcCand];                          // their ranks
     __shared__ uint32_t s_bits[kDcFastPer * kDcThreads / 32];  // chosen blocks (fast path), one bit each
     __shared__ int s_wpre[kDcFastPer * kDcThreads / 32];       // chosen blocks below each bitmap word
+    __shared__ uint32_t s_mx[kDcThreads];                  // the threads' maxima of their strided keys
+    __shared__ int s_byrank[kDcThreads];                   // chosen candidates' blocks by rank
+    __shared__ uint32_t s_tau[2];                          // threshold, and whether k maxima are nonzero
+    __shared__ int s_nc;                                   // candidates compacted so far
     __shared__ uint64_t s_bar_piece[kDcKRows / 128];       // scoring: kernel rows of piece p landed
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -175,6 +186,22 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     // Launched with programmatic stream serialisation: the set-up above may overlap the previous
     // kernel's tail; nothing the previous kernel may write is read before this wait.
     pdl_trigger();
+    {   // While the previous kernel finishes: this CTA's lines of q and of the cache length, and its
+        // kernel rows of the first scoring pass for the longest cache (bulk prefetches of up to 128
+        // rows, lane p of warp 1 rows 128p ...), towards L2 and into the address translations.
+        const char* qb = reinterpret_cast<const char*>(q + (static_cast<size_t>(b) * Hq + static_cast<size_t>(g) * G) * D);
+        if (tid < (G * D * 2 + 127) / 128) prefetch_l2_line(qb + 128 * tid);
+        if (tid == kDcThreads - 1) prefetch_l2_line(kv_len + b);
+        const int pa0 = static_cast<int>(rank) * sh.CB, pa1 = min(pa0 + sh.CB, sh.nblk_max);
+        if (warp == 1 && pa0 < pa1) {
+            const int j0 = first_kernel_of_block(pa0, BS, c, s);
+            const int j1 = min(last_kernel_of_block(min(pa0 + sh.SC, pa1) - 1, BS, s), M_max - 1);
+            const int r0 = j0 + 128 * lane;
+            if (r0 <= j1)
+                bulk_prefetch_l2(kern_rows + (static_cast<size_t>(row) * M_max + r0) * D,
+                                 static_cast<uint32_t>(min(128, j1 - r0 + 1) * D * 2));
+        }
+    }
     pdl_wait();
 
     // ================= 1. scores of this CTA's blocks, pushed as keys to every CTA
@@ -192,17 +219,21 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
         jend = min(last_kernel_of_block(sub1 - 1, BS, s), M_max - 1);
         return jend - jlo + 1;
     };
-    auto issue_pass = [&](int sub0) {  // kernel rows of blocks [sub0, sub0 + SC) for the longest cache
+    // kernel rows of blocks [sub0, sub0 + SC) for the longest cache: piece p is issued by lane 0 of
+    // warp p (a copy issue holds its thread; one thread issuing all of them delayed the last)
+    static_assert(kDcKRows / 128 <= kDcThreads / 32, "a warp per piece");
+    auto issue_pass = [&](int sub0) {
         int jlo, jend;
         const int nrows = pass_rows(sub0, jlo, jend);
-        for (int pc = 0; pc * 128 < nrows; ++pc) {
+        const int pc = warp;
+        if (lane == 0 && pc * 128 < nrows) {
             mbar_arrive_expect_tx(&s_bar_piece[pc], (D / 64) * 128 * 128);
             for (int half = 0; half < D / 64; ++half)
                 tma_load_2d(base + half * (kDcKRows * 128) + pc * (128 * 128), &tm_kern, 64 * half,
                             row * M_max + jlo + pc * 128, &s_bar_piece[pc]);
         }
     };
-    if (tid == 0 && blkA0 < blkA1) issue_pass(blkA0);
+    if (blkA0 < blkA1) issue_pass(blkA0);
     // Q fragments: rows = heads (rows >= G read as zero), for the attention
     QFrag<D> Q;
     load_q(Q, q + (static_cast<size_t>(b) * Hq + static_cast<size_t>(g) * G) * D, D, G);
@@ -320,26 +351,34 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
             }
         }
         __syncthreads();  // tiles and ks free for the next pass
-        if (tid == 0 && sub0 + sh.SC < blkA1) issue_pass(sub0 + sh.SC);
+        if (sub0 + sh.SC < blkA1) issue_pass(sub0 + sh.SC);
     }
     // this CTA's keys -> every peer: bulk copies into the same offsets of the peers' shared memory,
     // counted on their key barriers; then wait for the peers' keys
     fence_proxy_async_shared();
     __syncthreads();
     cluster_wait();
-    if (tid == 0) {
+    if (warp == 0) {  // lane j copies to peer j
         const uint32_t nb = key_bytes(static_cast<int>(rank));
-        if (nb > 0)
-            for (int j = 0; j < ncta; ++j)
-                if (j != static_cast<int>(rank))
-                    bulk_copy_to_peer(dsmem_addr(keys_base + 4u * blkA0, j), keys_base + 4u * blkA0, nb,
-                                      dsmem_addr(smem_u32(bar_keys), j));
+        if (nb > 0 && lane < ncta && lane != static_cast<int>(rank))
+            bulk_copy_to_peer(dsmem_addr(keys_base + 4u * blkA0, lane), keys_base + 4u * blkA0, nb,
+                              dsmem_addr(smem_u32(bar_keys), lane));
         bulk_commit();
     }
     if (!mbar_wait(bar_keys, 0) && tid == 0) raise_error(err, kDevErrTimeout);
 
     // ================= 2. the row's selection, computed by every CTA from all the keys
     int count = 0;
+    // fast path: the attention's list is init blocks [0, r_ainit) | s_byrank[0, r_k) | local blocks
+    // from r_lof; otherwise sel[] in block order
+    bool by_rank = false;
+    int r_ainit = 0, r_lof = 0, r_k = 0;
+    auto list_blk = [&](int e) {
+        if (!by_rank) return sel[e];
+        if (e < r_ainit) return e;
+        if (e < r_ainit + r_k) return s_byrank[e - r_ainit];
+        return r_lof + (e - r_ainit - r_k);
+    };
     {
         const int n = bt + 1;
         const int a_init = min(p.n_init, max(n, 0));
@@ -355,11 +394,11 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
         if (select && nn <= kDcFastPer * kDcThreads && p.topk <= kDcThreads) {
             // Fast path.  tau = the k-th largest of the threads' maxima over the strided keys
             // t, t + 256, ... (neighbouring blocks have correlated scores: a stride spreads each
-            // thread over the row), found bit by bit from block-wide predicate counts.  At least
-            // k keys are >= tau and, unless the scores are heavily tied, only a few more; those
-            // candidates are ranked exactly (key descending, block ascending, one 64-bit
-            // compare), and the list is the initial blocks, the k best candidates in block order
-            // and the local blocks.
+            // thread over the row), found bit by bit by one warp.  At least k keys are >= tau and,
+            // unless the scores are heavily tied, only a few more; those candidates are ranked
+            // exactly (key descending, block ascending, one 64-bit compare).  The attention takes
+            // the list init blocks | chosen candidates by rank | local blocks; the block-order
+            // list is built only when the caller asks for it.
             const int k = p.topk;
             uint32_t kv[kDcFastPer];
             uint32_t mx = 0u;
@@ -369,31 +408,49 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                 kv[u] = i < nn ? keys[i] : 0u;
                 mx = max(mx, kv[u]);
             }
-            const int nz = __syncthreads_count(mx != 0u);
-            uint32_t k_and = __reduce_and_sync(0xffffffffu, mx != 0u ? mx : ~0u);
-            uint32_t k_or = __reduce_or_sync(0xffffffffu, mx);
-            if (lane == 0) {
-                s_wsum[0][warp] = static_cast<int>(k_and);
-                s_wsum[1][warp] = static_cast<int>(k_or);
+            s_mx[tid] = mx;
+            if (tid == 0) s_nc = 0;
+            __syncthreads();
+            if (warp == 0) {
+                uint32_t m8[kDcThreads / 32];
+                uint32_t nz = 0u, k_and = ~0u, k_or = 0u;
+#pragma unroll
+                for (int j = 0; j < kDcThreads / 32; ++j) {
+                    m8[j] = s_mx[lane + 32 * j];
+                    if (m8[j] != 0u) {
+                        ++nz;
+                        k_and &= m8[j];
+                    }
+                    k_or |= m8[j];
+                }
+                nz = __reduce_add_sync(0xffffffffu, nz);
+                k_and = __reduce_and_sync(0xffffffffu, k_and);
+                k_or = __reduce_or_sync(0xffffffffu, k_or);
+                uint32_t tau = 0u;
+                if (nz >= static_cast<uint32_t>(k)) {
+                    const uint32_t diff = k_and ^ k_or;
+                    int bit = diff == 0u ? -1 : 31 - __clz(diff);
+                    tau = bit >= 31 ? 0u : (k_and & (~0u << (bit + 1)));
+                    for (; bit >= 0; --bit) {
+                        const uint32_t trial = tau | (1u << bit);
+                        uint32_t cnt = 0u;
+#pragma unroll
+                        for (int j = 0; j < kDcThreads / 32; ++j) cnt += m8[j] >= trial ? 1u : 0u;
+                        cnt = __reduce_add_sync(0xffffffffu, cnt);
+                        if (cnt >= static_cast<uint32_t>(k)) tau = trial;
+                        if (cnt == static_cast<uint32_t>(k)) break;
+                    }
+                }
+                if (lane == 0) {
+                    s_tau[0] = tau;
+                    s_tau[1] = nz >= static_cast<uint32_t>(k) ? 1u : 0u;
+                }
             }
             __syncthreads();
-            k_and = ~0u;
-            k_or = 0u;
-#pragma unroll
-            for (int w = 0; w < kDcThreads / 32; ++w) {
-                k_and &= static_cast<uint32_t>(s_wsum[0][w]);
-                k_or |= static_cast<uint32_t>(s_wsum[1][w]);
-            }
-            if (nz >= k) {
-                const uint32_t diff = k_and ^ k_or;
-                int bit = diff == 0u ? -1 : 31 - __clz(diff);
-                uint32_t tau = bit >= 31 ? 0u : (k_and & (~0u << (bit + 1)));
-                for (; bit >= 0; --bit) {
-                    const uint32_t trial = tau | (1u << bit);
-                    const int cnt = __syncthreads_count(mx >= trial);
-                    if (cnt >= k) tau = trial;
-                    if (cnt == k) break;
-                }
+            const uint32_t tau = s_tau[0];
+            if (s_tau[1] != 0u) {
+                // candidates -> s_cv, compacted by one shared counter (warp-aggregated); their order
+                // is arbitrary, their ranks are not
                 int nc_t = 0;
 #pragma unroll
                 for (int u = 0; u < kDcFastPer; ++u) nc_t += (kv[u] != 0u && kv[u] >= tau) ? 1 : 0;
@@ -403,85 +460,98 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                     const int x = __shfl_up_sync(0xffffffffu, incl, off);
                     if (lane >= off) incl += x;
                 }
-                __syncthreads();  // s_wsum reuse
-                if (lane == 31) s_wsum[0][warp] = incl;
-                __syncthreads();
-                int c_before = incl - nc_t, c_total = 0;
+                int wbase = 0;
+                if (lane == 31 && incl > 0) wbase = atomicAdd(&s_nc, incl);
+                int pos = __shfl_sync(0xffffffffu, wbase, 31) + incl - nc_t;
 #pragma unroll
-                for (int w = 0; w < kDcThreads / 32; ++w) {
-                    if (w < warp) c_before += s_wsum[0][w];
-                    c_total += s_wsum[0][w];
+                for (int u = 0; u < kDcFastPer; ++u)
+                    if (kv[u] != 0u && kv[u] >= tau) {
+                        if (pos < kDcCand)
+                            s_cv[pos] = (static_cast<unsigned long long>(kv[u]) << 32) |
+                                        static_cast<uint32_t>(~(tid + u * kDcThreads));
+                        ++pos;
+                    }
+                __syncthreads();
+                const int c_total = s_nc;
+                if (c_total <= k + k / 2 && tid < 2 * ((c_total - static_cast<int>(rank) + ncta - 1) / ncta)) {
+                    // few candidates beyond the k to be chosen: K (even threads) and V of candidates
+                    // rank, rank + CL, ... go towards L2 while they are ranked
+                    const int blk = static_cast<int>(~static_cast<uint32_t>(s_cv[static_cast<int>(rank) + ncta * (tid >> 1)]));
+                    const size_t off = (static_cast<size_t>(row) * L_max + static_cast<size_t>(blk) * BS) * D;
+                    bulk_prefetch_l2((tid & 1) ? vc + off : kc + off, static_cast<uint32_t>(min(BS, L - blk * BS) * D * 2));
                 }
                 if (c_total <= kDcCand) {
-                    // candidate value: key in the high word, complemented block in the low word,
-                    // so that a larger value is a better block
-#pragma unroll
-                    for (int u = 0; u < kDcFastPer; ++u)
-                        if (kv[u] != 0u && kv[u] >= tau)
-                            s_cv[c_before++] = (static_cast<unsigned long long>(kv[u]) << 32) |
-                                               static_cast<uint32_t>(~(tid + u * kDcThreads));
-                    for (int i = tid; i < c_total; i += kDcThreads) s_rk[i] = 0;
-                    for (int i = tid; i < kDcFastPer * kDcThreads / 32; i += kDcThreads) s_bits[i] = 0u;
-                    __syncthreads();
-                    // rank of candidate i = number of better candidates; `sp` threads share each
-                    // candidate, each comparing it with one slice of the others
-                    const int sp = max(1, kDcThreads / c_total);
+                    // rank of candidate i = number of better candidates; sp (a power of two) threads
+                    // of one warp share each candidate and add their counts by shuffles
+                    const int sp = c_total <= kDcThreads / 4 ? 4 : c_total <= kDcThreads / 2 ? 2 : 1;
                     const int seg = (c_total + sp - 1) / sp;
-                    {
-                        const int i = tid / sp, part = tid % sp;
-                        if (i < c_total) {
-                            const unsigned long long vi = s_cv[i];
-                            const int j1 = min(c_total, (part + 1) * seg);
-                            int r0 = 0, r1 = 0, r2 = 0, r3 = 0;  // four independent chains of loads
-                            int j = part * seg;
-                            for (; j + 4 <= j1; j += 4) {
-                                r0 += s_cv[j] > vi ? 1 : 0;
-                                r1 += s_cv[j + 1] > vi ? 1 : 0;
-                                r2 += s_cv[j + 2] > vi ? 1 : 0;
-                                r3 += s_cv[j + 3] > vi ? 1 : 0;
+                    const int i = tid / sp, part = tid % sp;
+                    int rnk = 0;
+                    unsigned long long vi = 0ull;
+                    if (i < c_total) {
+                        vi = s_cv[i];
+                        const int j1 = min(c_total, (part + 1) * seg);
+                        int r0 = 0, r1 = 0, r2 = 0, r3 = 0;  // four independent chains of loads
+                        int j = part * seg;
+                        for (; j + 4 <= j1; j += 4) {
+                            r0 += s_cv[j] > vi ? 1 : 0;
+                            r1 += s_cv[j + 1] > vi ? 1 : 0;
+                            r2 += s_cv[j + 2] > vi ? 1 : 0;
+                            r3 += s_cv[j + 3] > vi ? 1 : 0;
+                        }
+                        for (; j < j1; ++j) r0 += s_cv[j] > vi ? 1 : 0;
+                        rnk = r0 + r1 + r2 + r3;
+                    }
+                    for (int off = 1; off < sp; off <<= 1) rnk += __shfl_xor_sync(0xffffffffu, rnk, off);
+                    if (part == 0 && i < c_total) {
+                        s_rk[i] = rnk;
+                        if (rnk < k) s_byrank[rnk] = static_cast<int>(~static_cast<uint32_t>(vi));
+                    }
+                    for (int i2 = kDcThreads + tid; i2 < c_total; i2 += kDcThreads) {  // c_total > 256
+                        const unsigned long long v2 = s_cv[i2];
+                        int r2 = 0;
+                        for (int j = 0; j < c_total; ++j) r2 += s_cv[j] > v2 ? 1 : 0;
+                        s_rk[i2] = r2;
+                        if (r2 < k) s_byrank[r2] = static_cast<int>(~static_cast<uint32_t>(v2));
+                    }
+                    for (int i3 = tid; i3 < kDcFastPer * kDcThreads / 32; i3 += kDcThreads) s_bits[i3] = 0u;
+                    __syncthreads();
+                    if (idx_out != nullptr) {
+                        // the list in block order: bitmap of the chosen blocks, word prefix popcounts
+                        // (one warp), then one popcount per chosen candidate
+                        for (int i3 = tid; i3 < c_total; i3 += kDcThreads)
+                            if (s_rk[i3] < k) {
+                                const uint32_t blk = ~static_cast<uint32_t>(s_cv[i3]);
+                                atomicOr(&s_bits[blk >> 5], 1u << (blk & 31));
                             }
-                            for (; j < j1; ++j) r0 += s_cv[j] > vi ? 1 : 0;
-                            const int rnk = r0 + r1 + r2 + r3;
-                            if (rnk) atomicAdd(&s_rk[i], rnk);
-                        }
-                        for (int i2 = kDcThreads / sp + tid; i2 < c_total; i2 += kDcThreads) {  // c_total > 256
-                            const unsigned long long vi = s_cv[i2];
-                            int rnk = 0;
-                            for (int j = 0; j < c_total; ++j) rnk += s_cv[j] > vi ? 1 : 0;
-                            atomicAdd(&s_rk[i2], rnk);
-                        }
-                    }
-                    __syncthreads();
-                    // position of a chosen candidate = chosen blocks below it: bitmap of the chosen
-                    // blocks, word prefix popcounts (one warp), then one popcount per candidate
-                    for (int i = tid; i < c_total; i += kDcThreads)
-                        if (s_rk[i] < k) {
-                            const uint32_t blk = ~static_cast<uint32_t>(s_cv[i]);
-                            atomicOr(&s_bits[blk >> 5], 1u << (blk & 31));
-                        }
-                    __syncthreads();
-                    if (warp == 0) {
-                        const int c0 = __popc(s_bits[2 * lane]), c1 = __popc(s_bits[2 * lane + 1]);
-                        int incl = c0 + c1;
+                        __syncthreads();
+                        if (warp == 0) {
+                            const int c0 = __popc(s_bits[2 * lane]), c1 = __popc(s_bits[2 * lane + 1]);
+                            int wi = c0 + c1;
 #pragma unroll
-                        for (int off = 1; off < 32; off <<= 1) {
-                            const int x = __shfl_up_sync(0xffffffffu, incl, off);
-                            if (lane >= off) incl += x;
+                            for (int off = 1; off < 32; off <<= 1) {
+                                const int x = __shfl_up_sync(0xffffffffu, wi, off);
+                                if (lane >= off) wi += x;
+                            }
+                            s_wpre[2 * lane] = wi - c0 - c1;
+                            s_wpre[2 * lane + 1] = wi - c1;
                         }
-                        s_wpre[2 * lane] = incl - c0 - c1;
-                        s_wpre[2 * lane + 1] = incl - c1;
+                        __syncthreads();
+                        for (int i3 = tid; i3 < c_total; i3 += kDcThreads)
+                            if (s_rk[i3] < k) {
+                                const uint32_t blk = ~static_cast<uint32_t>(s_cv[i3]);
+                                sel[a_init + s_wpre[blk >> 5] + __popc(s_bits[blk >> 5] & ((1u << (blk & 31)) - 1u))] =
+                                    static_cast<int>(blk);
+                            }
+                        for (int i3 = tid; i3 < a_init; i3 += kDcThreads) sel[i3] = i3;
+                        for (int i3 = tid; i3 < nn - lo_f; i3 += kDcThreads) sel[a_init + k + i3] = lo_f + i3;
                     }
-                    __syncthreads();
-                    for (int i = tid; i < c_total; i += kDcThreads)
-                        if (s_rk[i] < k) {
-                            const uint32_t blk = ~static_cast<uint32_t>(s_cv[i]);
-                            sel[a_init + s_wpre[blk >> 5] + __popc(s_bits[blk >> 5] & ((1u << (blk & 31)) - 1u))] =
-                                static_cast<int>(blk);
-                        }
-                    for (int i = tid; i < a_init; i += kDcThreads) sel[i] = i;
-                    for (int i = tid; i < nn - lo_f; i += kDcThreads) sel[a_init + k + i] = lo_f + i;
                     total = a_init + k + (nn - lo_f);
                     done = true;
+                    by_rank = true;
+                    r_ainit = a_init;
+                    r_lof = lo_f;
+                    r_k = k;
                 }
             }
             __syncthreads();
@@ -663,7 +733,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     }
     // second half-barrier: this CTA no longer reads its keys or scores (and its copies of its keys
     // have been read), whose memory takes the peers' partials after the attention
-    if (tid == 0) bulk_wait_read_all();
+    if (warp == 0) bulk_wait_read_all();
     cluster_arrive_relaxed();
 
     // ================= 3. attention over the selected blocks rank, rank + CL, ...
@@ -671,24 +741,23 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     acc_init(A);
     {
         const int mine = count > static_cast<int>(rank) ? (count - static_cast<int>(rank) + ncta - 1) / ncta : 0;
+        auto blk_at = [&](int t) { return list_blk(static_cast<int>(rank) + ncta * t); };
         uint32_t ph_b = 0;
         for (int t0 = 0; t0 < mine; t0 += PB) {
-            if (tid == 0) {
+            if (lane == 0 && warp < PB) {  // slot k by warp k
+                const int k = warp;
+                const int t = t0 + k;
+                const int blk = t < mine ? blk_at(t) : -1;
+                if (blk >= 0) {
+                    const int krow = row * L_max + blk * BS;
+                    mbar_arrive_expect_tx(&bar_b[k], 2 * kTile);
 #pragma unroll
-                for (int k = 0; k < PB; ++k) {
-                    const int t = t0 + k;
-                    const int blk = t < mine ? sel[static_cast<int>(rank) + ncta * t] : -1;
-                    if (blk >= 0) {
-                        const int krow = row * L_max + blk * BS;
-                        mbar_arrive_expect_tx(&bar_b[k], 2 * kTile);
-#pragma unroll
-                        for (int sub = 0; sub < D / 64; ++sub) {
-                            tma_load_2d(base + (2 * k) * kTile + sub * BS * 128, &tm_k, 64 * sub, krow, &bar_b[k]);
-                            tma_load_2d(base + (2 * k + 1) * kTile + sub * BS * 128, &tm_v, 64 * sub, krow, &bar_b[k]);
-                        }
-                    } else {
-                        mbar_arrive(&bar_b[k]);  // keep every slot's phase in step
+                    for (int sub = 0; sub < D / 64; ++sub) {
+                        tma_load_2d(base + (2 * k) * kTile + sub * BS * 128, &tm_k, 64 * sub, krow, &bar_b[k]);
+                        tma_load_2d(base + (2 * k + 1) * kTile + sub * BS * 128, &tm_v, 64 * sub, krow, &bar_b[k]);
                     }
+                } else {
+                    mbar_arrive(&bar_b[k]);  // keep every slot's phase in step
                 }
             }
             __syncthreads();
@@ -696,7 +765,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                 const int k = tile / kTilesPerBlock;
                 const int t = t0 + k;
                 if (t >= mine) continue;
-                const int blk = sel[static_cast<int>(rank) + ncta * t];
+                const int blk = blk_at(t);
                 const int r0 = (tile % kTilesPerBlock) * 32;
                 const int n_ok = L - (blk * BS + r0);
                 if (n_ok <= 0) continue;
@@ -775,8 +844,9 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     fence_proxy_async_shared();
     __syncthreads();
     cluster_wait();
-    if (tid == 0) {
-        for (int h = 0; h < G; ++h) {
+    if (warp == 0) {  // lane h copies head h
+        const int h = lane;
+        if (h < G) {
             const int owner = h % ncta, hl = h / ncta;
             const uint32_t dst = slots + 4u * static_cast<uint32_t>((hl * ncta + static_cast<int>(rank)) * kPRow);
             bulk_copy_to_peer(dsmem_addr(dst, owner), smem_u32(part + h * kPRow), kPRow * 4,
@@ -813,7 +883,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
             lse[static_cast<size_t>(b) * Hq + g * G + h] = Ls > 0.f ? (M + log2f(Ls)) * 0.69314718055994530942f : -INFINITY;
     }
     // this CTA's copies have read its partials before it exits
-    if (tid == 0) bulk_wait_read_all();
+    if (warp == 0) bulk_wait_read_all();
 }
 
 template <int D, int BS>
@@ -887,6 +957,7 @@ static cudaError_t launch_cluster_t(const DecodeArgs& a, const void* kernel_cach
     const int G = a.Hq / a.Hkv;
     const float scale_log2 = a.p.scale * 1.4426950408889634f;
     return cudaLaunchKernelEx(&cfg, kfn, tkern, tk, tv, static_cast<const __nv_bfloat16*>(a.q),
+                              static_cast<const __nv_bfloat16*>(kernel_cache),
                               static_cast<const __nv_bfloat16*>(a.k_cache), static_cast<const __nv_bfloat16*>(a.v_cache),
                               a.kv_len, a.Hq, a.Hkv,
                               G, a.L_max, M_max, a.p, sh, idx_out, idx_stride, counts_out,
