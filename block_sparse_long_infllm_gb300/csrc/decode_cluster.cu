@@ -97,7 +97,8 @@ struct ClusterSmem {
     static constexpr int kTile = BS * D * 2;                  // one K (or V) block
     static constexpr int kX = (D / 64) * kDcKRows * 128;      // scoring tiles / K,V tiles / merge scratch
     static constexpr int kPB = kX / (2 * kTile) < 8 ? kX / (2 * kTile) : 8;  // blocks per attention pass
-    static constexpr int kMerge = (8 * 16 * 2 + 8 * 16 * (D + 4)) * 4;
+    static constexpr int kMergeRow = D + D / 8;                // 8-warp merge scratch row: 4 floats of pad per 32
+    static constexpr int kMerge = (8 * 16 * 2 + 8 * 16 * kMergeRow) * 4;
     static constexpr int kPRow = D + 4;                        // a head's partial: m, l, 2 unused, o[D]
     static constexpr int kPartial = 16 * kPRow * 4;            // this CTA's partials, after the merge scratch
     static constexpr int kSlots = 24 * kPRow * 4;              // partials merged here: CL x heads owned <= 24
@@ -129,7 +130,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     constexpr int PB = SM::kPB;
     constexpr int kTile = SM::kTile;
     constexpr int kTilesPerBlock = BS / 32;
-    constexpr int kRowPad = D + 4;
+    constexpr int kMergeRow = SM::kMergeRow;
     extern __shared__ unsigned char smem_dyn[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
@@ -792,20 +793,24 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
         // merge the 8 warps (scratch in the tile memory) into this CTA's partial
         float* sm_m = reinterpret_cast<float*>(base);
         float* sm_l = sm_m + 8 * 16;
-        float* sm_o = sm_l + 8 * 16;  // [8][16][kRowPad]
+        float* sm_o = sm_l + 8 * 16;  // [8][16][kMergeRow]
         if (cq == 0) {
             sm_m[warp * 16 + gq] = A.m[0];
             sm_m[warp * 16 + gq + 8] = A.m[1];
             sm_l[warp * 16 + gq] = A.l[0];
             sm_l[warp * 16 + gq + 8] = A.l[1];
         }
-        // column c of a row is stored at c + c/32: the four lanes of a quad write different banks
+        // column c of a row is stored at c + 4 (c / 32).  A lane's n-tiles nt .. nt + 3 of one
+        // accumulator slot are 4 consecutive columns (the layout of attn_warp.cuh), stored as one
+        // 16-byte word; the 4 lanes of a quad land in different 16-byte bank groups.
+        auto mpad = [](int col) { return col + 4 * (col >> 5); };
 #pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt)
+        for (int e = 0; e < 4; ++e)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int nt = 0; nt < D / 8; nt += 4) {
                 const int col = o_col(D, cq, nt, e);
-                sm_o[(warp * 16 + gq + 8 * (e >> 1)) * kRowPad + col + (col >> 5)] = A.o[nt][e];
+                *reinterpret_cast<float4*>(&sm_o[(warp * 16 + gq + 8 * (e >> 1)) * kMergeRow + mpad(col)]) =
+                    make_float4(A.o[nt][e], A.o[nt + 1][e], A.o[nt + 2][e], A.o[nt + 3][e]);
             }
         __syncthreads();
         // thread t: row t / 16 (a head), columns 8 (t % 16) .. +7 per pass; each thread forms the
@@ -827,14 +832,22 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                 part[r * kPRow] = M;
                 part[r * kPRow + 1] = l;
             }
+            float acc[kCols];
 #pragma unroll
-            for (int i = 0; i < kCols; ++i) {
-                const int col = col0 + i;
-                float acc = 0.f;
+            for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
 #pragma unroll
-                for (int w = 0; w < 8; ++w) acc += sm_o[(w * 16 + r) * kRowPad + col + (col >> 5)] * f[w];
-                part[r * kPRow + 4 + col] = acc;
-            }
+            for (int w = 0; w < 8; ++w)
+#pragma unroll
+                for (int i = 0; i < kCols; i += 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(&sm_o[(w * 16 + r) * kMergeRow + mpad(col0 + i)]);
+                    acc[i] += x.x * f[w];
+                    acc[i + 1] += x.y * f[w];
+                    acc[i + 2] += x.z * f[w];
+                    acc[i + 3] += x.w * f[w];
+                }
+#pragma unroll
+            for (int i = 0; i < kCols; i += 4)
+                *reinterpret_cast<float4*>(&part[r * kPRow + 4 + col0 + i]) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
         }
     }
     // ================= 4. merge of the CTAs' partials: CTA r merges heads r, r + CL, ...
