@@ -211,12 +211,14 @@ def setup_decode(name: str, replicas: int = REPLICAS):
     return d
 
 
-def decode_call(d, r: int = 0, q=None, kv_len=None):
+def decode_call(d, r: int = 0, q=None, kv_len=None, selection: bool = False):
+    """One decode step: o and lse.  With selection=True the step also writes the block lists
+    (idx, counts), which the timed steps do not ask for."""
     from block_sparse_long_infllm_gb300 import infllmv2
     rep = d["rep"][r % len(d["rep"])]
     infllmv2.decode(rep["q"] if q is None else q, rep["k"], rep["v"], rep["kern"],
                     d["kv_len"] if kv_len is None else kv_len, d["o"], d["ws"], d["p"], lse=d["lse"],
-                    idx_out=d["idx"], counts_out=d["counts"])
+                    idx_out=d["idx"] if selection else None, counts_out=d["counts"] if selection else None)
 
 
 def decode_algorithmic_bytes(d) -> dict:
@@ -336,6 +338,8 @@ def run_decode(args, world, rank):
         lat.append(a.elapsed_time(b))
     del flush
 
+    decode_call(d, 0, selection=True)  # the selection the steps make, for the algorithmic bytes
+    torch.cuda.synchronize()
     alg = decode_algorithmic_bytes(d)
     pk = peaks()
     fused = "fused" in stage_ms
@@ -405,7 +409,7 @@ def run_decode_append(args, d) -> dict:
         rep = d["rep"][r % R]
         kn, vn = news[r % R]
         infllmv2.decode_step(rep["q"], kn, vn, rep["k"], rep["v"], rep["kern"], d["kv_len"], d["o"], d["ws"], d["p"],
-                             lse=d["lse"], idx_out=d["idx"], counts_out=d["counts"])
+                             lse=d["lse"])
 
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -445,32 +449,36 @@ def run_decode_append(args, d) -> dict:
 
 
 def run_decode_e2e(d, n: int) -> dict:
-    """Same step through the public call with host buffers: copy this step's query
-    (and lengths) from pinned host memory, decode, read the output back; wall clock."""
+    """Same step through the public host-buffer call (infllmv2_decode_host): each step copies its
+    query and lengths from pinned host memory, decodes, copies o and lse back and waits; wall clock
+    per step, replicas cycled."""
     import torch
+
+    from block_sparse_long_infllm_gb300 import infllmv2
     w = d["w"]
-    q_host = d["rep"][0]["q"].cpu().pin_memory()
+    q_host = d["rep"][0]["q"].view(w.B, w.Hq, w.d).cpu().pin_memory()
     kv_host = d["kv_len"].cpu().pin_memory()
-    o_host = torch.empty(d["o"].shape, dtype=d["o"].dtype).pin_memory()
-    q_dev = torch.empty_like(d["rep"][0]["q"])
+    o_host = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16).pin_memory()
+    lse_host = torch.empty((w.B, w.Hq), dtype=torch.float32).pin_memory()
+    q_dev = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
     kv_dev = torch.empty_like(d["kv_len"])
-    stream = torch.cuda.current_stream()
+    o_dev = torch.empty_like(q_dev)
+    lse_dev = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
     times = []
     for i in range(n + 3):
+        rep = d["rep"][i % len(d["rep"])]
         t0 = time.perf_counter()
-        q_dev.copy_(q_host, non_blocking=True)
-        kv_dev.copy_(kv_host, non_blocking=True)
-        decode_call(d, i, q=q_dev, kv_len=kv_dev)
-        o_host.copy_(d["o"], non_blocking=True)
-        stream.synchronize()
+        infllmv2.decode_host(q_host, kv_host, o_host, q_dev, kv_dev, o_dev, rep["k"], rep["v"], rep["kern"],
+                             d["ws"], d["p"], lse_host=lse_host, lse_dev=lse_dev)
         if i >= 3:
             times.append(time.perf_counter() - t0)
     h2d = q_host.numel() * q_host.element_size() + kv_host.numel() * kv_host.element_size()
-    d2h = o_host.numel() * o_host.element_size()
+    d2h = o_host.numel() * o_host.element_size() + lse_host.numel() * lse_host.element_size()
     return {"value": w.B * w.Tq / statistics.mean(times), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * statistics.mean(times),
-            "note": "wall clock per step (copy in, decode call, copy out, synchronise); replicas cycled; "
-                    "KV and kernel caches resident"}
+            "note": "wall clock per step of infllmv2_decode_host (q and lengths copied in from pinned host "
+                    "memory, one decode launch, o and lse copied out, the device error word read, the "
+                    "stream waited for); replicas cycled; KV and kernel caches resident"}
 
 
 # ------------------------------------------------------------------ prefill (secondary)

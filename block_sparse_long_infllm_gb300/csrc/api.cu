@@ -432,6 +432,63 @@ int infllmv2_sparse_attn_bwd(const void* q, const void* k_cache, const void* v_c
     return cuda_status(infllmv2::launch_attention_bwd(a));
 }
 
+static int decode_impl(bool launch, const void* q, const void* k_cache, const void* v_cache, const void* kernel_cache,
+                       const int32_t* kv_len, const void* draft_k, const void* draft_v, const uint64_t* tree_mask,
+                       int B, int n_draft, int Hq, int Hkv, int d, int L_max, int M_max, void* o, float* lse,
+                       int32_t* idx_out, int32_t* counts_out, int S_max, void* workspace, size_t ws_bytes,
+                       const infllmv2_params* params, void* stream);
+
+int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache, const void* kernel_cache,
+                    const int32_t* kv_len, const void* draft_k, const void* draft_v, const uint64_t* tree_mask,
+                    int B, int n_draft, int Hq, int Hkv, int d, int L_max, int M_max, void* o, float* lse,
+                    int32_t* idx_out, int32_t* counts_out, int S_max, void* workspace, size_t ws_bytes,
+                    const infllmv2_params* params, void* stream) {
+    return decode_impl(true, q, k_cache, v_cache, kernel_cache, kv_len, draft_k, draft_v, tree_mask, B, n_draft, Hq, Hkv,
+                       d, L_max, M_max, o, lse, idx_out, counts_out, S_max, workspace, ws_bytes, params, stream);
+}
+
+int infllmv2_decode_host(const void* q_host, const int32_t* kv_len_host, void* o_host, float* lse_host, void* q_dev,
+                         int32_t* kv_len_dev, void* o_dev, float* lse_dev, const void* k_cache, const void* v_cache,
+                         const void* kernel_cache, int B, int Hq, int Hkv, int d, int L_max, int M_max, void* workspace,
+                         size_t ws_bytes, const infllmv2_params* params, void* stream) {
+    if (lse_host != nullptr && lse_dev == nullptr) return INFLLMV2_ERR_INVALID_ARG;
+    if (int rc = decode_impl(false, q_dev, k_cache, v_cache, kernel_cache, kv_len_dev, nullptr, nullptr, nullptr, B, 1,
+                             Hq, Hkv, d, L_max, M_max, o_dev, lse_dev, nullptr, nullptr, 0, workspace, ws_bytes, params,
+                             stream))
+        return rc;
+    if (B == 0) return INFLLMV2_OK;
+    if (q_host == nullptr || kv_len_host == nullptr || o_host == nullptr) return INFLLMV2_ERR_INVALID_ARG;
+    int* ep = device_error_ptr();
+    if (ep == nullptr) return INFLLMV2_ERR_CUDA;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t nq = static_cast<size_t>(B) * Hq * d * 2, nl = static_cast<size_t>(B) * Hq * sizeof(float);
+    int rc = INFLLMV2_OK;
+    if (cudaMemcpyAsync(q_dev, q_host, nq, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(kv_len_dev, kv_len_host, static_cast<size_t>(B) * sizeof(int32_t), cudaMemcpyHostToDevice,
+                        st) != cudaSuccess)
+        rc = INFLLMV2_ERR_CUDA;
+    if (rc == INFLLMV2_OK)
+        rc = decode_impl(true, q_dev, k_cache, v_cache, kernel_cache, kv_len_dev, nullptr, nullptr, nullptr, B, 1, Hq, Hkv,
+                         d, L_max, M_max, o_dev, lse_dev, nullptr, nullptr, 0, workspace, ws_bytes, params, stream);
+    if (rc == INFLLMV2_OK &&
+        (cudaMemcpyAsync(o_host, o_dev, nq, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+         (lse_host != nullptr && cudaMemcpyAsync(lse_host, lse_dev, nl, cudaMemcpyDeviceToHost, st) != cudaSuccess)))
+        rc = INFLLMV2_ERR_CUDA;
+    // the device error word, in the same round trip (a copy to pageable memory returns when done)
+    int word = 0;
+    if (cudaMemcpyAsync(&word, ep, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess && rc == INFLLMV2_OK)
+        rc = INFLLMV2_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess && rc == INFLLMV2_OK) rc = INFLLMV2_ERR_CUDA;
+    if (word != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(ep, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess && rc == INFLLMV2_OK)
+            rc = INFLLMV2_ERR_CUDA;
+        if (rc == INFLLMV2_OK)
+            rc = (word & infllmv2::kDevErrTimeout) ? INFLLMV2_ERR_DEVICE_TIMEOUT : INFLLMV2_ERR_DEVICE_INDEX;
+    }
+    return rc;
+}
+
 int infllmv2_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                          void* kernel_cache, const int32_t* kv_len, int B, int Hq, int Hkv, int d, int L_max, int M_max,
                          void* o, float* lse, int32_t* idx_out, int32_t* counts_out, int S_max, void* workspace,
@@ -478,11 +535,12 @@ int infllmv2_decode_step(const void* q, const void* k_new, const void* v_new, vo
                            M_max, o, lse, idx_out, counts_out, S_max, workspace, ws_bytes, params, stream);
 }
 
-int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache, const void* kernel_cache,
-                    const int32_t* kv_len, const void* draft_k, const void* draft_v, const uint64_t* tree_mask,
-                    int B, int n_draft, int Hq, int Hkv, int d, int L_max, int M_max, void* o, float* lse,
-                    int32_t* idx_out, int32_t* counts_out, int S_max, void* workspace, size_t ws_bytes,
-                    const infllmv2_params* params, void* stream) {
+// infllmv2_decode's body; with launch == false it only checks the arguments (no CUDA call).
+static int decode_impl(bool launch, const void* q, const void* k_cache, const void* v_cache, const void* kernel_cache,
+                       const int32_t* kv_len, const void* draft_k, const void* draft_v, const uint64_t* tree_mask,
+                       int B, int n_draft, int Hq, int Hkv, int d, int L_max, int M_max, void* o, float* lse,
+                       int32_t* idx_out, int32_t* counts_out, int S_max, void* workspace, size_t ws_bytes,
+                       const infllmv2_params* params, void* stream) {
     Params p;
     if (int rc = check_params(params, d, &p)) return rc;
     if (int rc = check_heads(Hq, Hkv, d)) return rc;
@@ -506,6 +564,7 @@ int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache, con
         return INFLLMV2_ERR_INVALID_ARG;
     const DecodeWs w = decode_ws(B, n_draft, Hkv, d, L_max, p);
     if (workspace == nullptr || ws_bytes < w.total || !aligned16(workspace)) return INFLLMV2_ERR_WORKSPACE;
+    if (!launch) return INFLLMV2_OK;
     int* err = device_error_ptr();
     if (err == nullptr) return INFLLMV2_ERR_CUDA;
     char* ws = static_cast<char*>(workspace);

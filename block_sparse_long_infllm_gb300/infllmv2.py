@@ -95,6 +95,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.infllmv2_decode_noalloc.argtypes = [p, p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, p, p,
                                             p, p, i32, pp, p]
     lib.infllmv2_decode_noalloc.restype = ctypes.c_int
+    lib.infllmv2_decode_host.argtypes = [p, p, p, p, p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, p, sz, pp, p]
+    lib.infllmv2_decode_host.restype = ctypes.c_int
     lib.infllmv2_profile_enable.argtypes = [i32]
     lib.infllmv2_profile_read.argtypes = [p, i32, p]
     lib.infllmv2_profile_stage_name.argtypes = [i32]
@@ -134,6 +136,16 @@ def _ptr(t):
         return None
     if not t.is_cuda:
         raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host_ptr(t):
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("tensor must live in host memory")
     if not t.is_contiguous():
         raise ValueError("tensor must be contiguous")
     return ctypes.c_void_p(t.data_ptr())
@@ -293,6 +305,22 @@ def decode(q, k_cache, v_cache, kernel_cache, kv_len, o, workspace, params, lse=
                                   L_max, M_max, _ptr(o), _ptr(lse), _ptr(idx_out), _ptr(counts_out), S_max,
                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
                                   ctypes.byref(Params.make(params)), _stream(stream)), "infllmv2_decode")
+
+
+def decode_host(q_host, kv_len_host, o_host, q_dev, kv_len_dev, o_dev, k_cache, v_cache, kernel_cache,
+                workspace, params, lse_host=None, lse_dev=None, stream=None):
+    """One single-token decode step with q, kv_len and o in host memory (pinned for asynchronous
+    copies): copy in, decode on the device staging tensors, copy out, wait.  The host output is
+    complete on return; device errors raise."""
+    B, Hq, d = q_host.shape[0], q_host.shape[-2], q_host.shape[-1]
+    Hkv, L_max = k_cache.shape[1], k_cache.shape[2]
+    M_max = kernel_cache.shape[2]
+    _check(load().infllmv2_decode_host(_host_ptr(q_host), _host_ptr(kv_len_host), _host_ptr(o_host),
+                                       _host_ptr(lse_host), _ptr(q_dev), _ptr(kv_len_dev), _ptr(o_dev),
+                                       _ptr(lse_dev), _ptr(k_cache), _ptr(v_cache), _ptr(kernel_cache), B, Hq, Hkv,
+                                       d, L_max, M_max, _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       ctypes.byref(Params.make(params)), _stream(stream)), "infllmv2_decode_host")
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20  # INFLLMV2_NOALLOC_SCRATCH_BYTES

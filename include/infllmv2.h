@@ -285,6 +285,28 @@ int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache,
                     const infllmv2_params* params, void* stream);
 
 /*
+ * infllmv2_decode of one single-token step whose query, cache lengths and
+ * output live in host memory: copies q_host [B, Hq, d] bf16 to q_dev and
+ * kv_len_host [B] to kv_len_dev on `stream` (cudaMemcpyAsync, one per buffer;
+ * page-locked host memory keeps them asynchronous), decodes q_dev over the
+ * resident caches into o_dev (and lse_dev, when not NULL), copies o_dev back to
+ * o_host (and lse_dev [B, Hq] fp32 to lse_host, when not NULL), reads the device
+ * error word in the same round trip and waits for the stream.  On return the
+ * host output is complete.  q_dev, kv_len_dev, o_dev, lse_dev are the caller's
+ * device staging buffers (16-byte aligned; the library allocates nothing);
+ * the other arguments are those of infllmv2_decode (n_draft = 1, no selection
+ * output).  Arguments are checked before anything is enqueued.  Returns the
+ * first of: an argument error, infllmv2_decode's status, INFLLMV2_ERR_CUDA for
+ * a failed copy or wait, and the device error word (as infllmv2_sync_status,
+ * which clears it).
+ */
+int infllmv2_decode_host(const void* q_host, const int32_t* kv_len_host, void* o_host, float* lse_host,
+                         void* q_dev, int32_t* kv_len_dev, void* o_dev, float* lse_dev,
+                         const void* k_cache, const void* v_cache, const void* kernel_cache, int B,
+                         int Hq, int Hkv, int d, int L_max, int M_max, void* workspace,
+                         size_t ws_bytes, const infllmv2_params* params, void* stream);
+
+/*
  * One whole single-token decode step: infllmv2_append (the new token's K and V
  * into row kv_len[b]-1 of the caches, and the semantic kernel it completes),
  * then infllmv2_decode of q over the updated caches ([CPM.cu] section 4: the

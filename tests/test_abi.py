@@ -11,7 +11,7 @@ from block_sparse_long_infllm_gb300 import infllmv2
 def test_exports_every_declared_function(built_lib):
     names = infllmv2.declared_functions()
     assert {"infllmv2_kernel_pool", "infllmv2_append", "infllmv2_block_select", "infllmv2_sparse_attn_fwd",
-            "infllmv2_decode", "infllmv2_sparse_attn_bwd"} <= set(names)
+            "infllmv2_decode", "infllmv2_sparse_attn_bwd", "infllmv2_decode_host"} <= set(names)
     for n in names:
         assert hasattr(built_lib, n), n
 
@@ -113,3 +113,23 @@ def test_empty_calls_are_noops(built_lib):
                                               fake, None, None, 0, _params(), None) == 0
     assert built_lib.infllmv2_kernel_pool(fake, fake, 1, 2, 4096, 255, 128, 100, 100, _params(), None) == 0
     assert built_lib.infllmv2_append(fake, fake, fake, fake, fake, fake, 0, 2, 128, 4096, 255, _params(), None) == 0
+
+
+def test_decode_host_checks_before_enqueueing(built_lib):
+    fake = ctypes.c_void_p(1 << 20)
+    lib = built_lib
+    args = dict(B=1, Hq=32, Hkv=2, d=128, L_max=4096, M_max=255)
+
+    def call(q_h=fake, kv_h=fake, o_h=fake, lse_h=None, q_d=fake, kv_d=fake, o_d=fake, lse_d=None, ws_bytes=1 << 30,
+             B=1, d=128, params=None):
+        return lib.infllmv2_decode_host(q_h, kv_h, o_h, lse_h, q_d, kv_d, o_d, lse_d, fake, fake, fake, B,
+                                        args["Hq"], args["Hkv"], d, args["L_max"], args["M_max"], fake, ws_bytes,
+                                        params or _params(), None)
+    assert call(B=0) == 0                                           # nothing to do
+    assert call(lse_h=fake) == infllmv2.ERR_INVALID_ARG             # lse wanted on the host, no device buffer
+    assert call(q_h=None) == infllmv2.ERR_INVALID_ARG               # missing host query
+    assert call(o_d=None) == infllmv2.ERR_INVALID_ARG               # missing device output
+    assert call(q_d=ctypes.c_void_p((1 << 20) + 4)) == infllmv2.ERR_INVALID_ARG  # misaligned staging buffer
+    assert call(ws_bytes=16) == infllmv2.ERR_WORKSPACE
+    assert call(d=96) == infllmv2.ERR_UNSUPPORTED
+    assert call(params=_params(topk=-1)) == infllmv2.ERR_INVALID_ARG

@@ -270,3 +270,30 @@ def test_decode_output_without_selection_list(cuda_lib, decisive):
     assert torch.equal(lse2, g["lse"])
     o_ref, lse_ref = oracle.attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["kv_len"], oidx, ocnt, p)
     check_output(bf16_to_f64(o2), o_ref)
+
+
+def test_decode_host_buffers_match_device_call(cuda_lib):
+    # infllmv2_decode_host: the same step with q, kv_len, o and lse in pinned host memory gives the
+    # same bits as the device-buffer call, and matches the oracle
+    import torch
+    w = synth.WORKLOADS["decode_128k_b4"].scaled(B=2, L=32768, seed=3500)
+    inp = synth.make_inputs(w)
+    g, oidx, ocnt = _parity(w, inp)
+    L = lib()
+    p = w.params()
+    ws = torch.empty(L.workspace_size(L.ENTRY_DECODE, w.B, w.Tq, w.Hq, w.Hkv, w.d, w.L_max, p),
+                     dtype=torch.uint8, device="cuda")
+    q_host = g["q"].view(w.B, w.Hq, w.d).cpu().pin_memory()
+    kv_host = g["kv_len"].cpu().pin_memory()
+    o_host = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16).pin_memory()
+    lse_host = torch.empty((w.B, w.Hq), dtype=torch.float32).pin_memory()
+    q_dev = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+    kv_dev = torch.empty_like(g["kv_len"])
+    o_dev = torch.empty_like(q_dev)
+    lse_dev = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+    L.decode_host(q_host, kv_host, o_host, q_dev, kv_dev, o_dev, g["k"], g["v"], g["kern"], ws, p,
+                  lse_host=lse_host, lse_dev=lse_dev)
+    assert torch.equal(o_host.view(torch.int16), g["o"].view(w.B, w.Hq, w.d).cpu().view(torch.int16))
+    assert torch.equal(lse_host, g["lse"].view(w.B, w.Hq).cpu())
+    o_ref, _ = oracle.attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["kv_len"], oidx, ocnt, p)
+    check_output(bf16_to_f64(o_host.view(w.B, 1, w.Hq, w.d)), o_ref)
