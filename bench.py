@@ -314,6 +314,13 @@ def run_decode(args, world, rank):
     b.record(stream)
     torch.cuda.synchronize()
     nograph_ms = a.elapsed_time(b) / n_ng
+    # the same, each step also writing its block lists (an optional output of the call)
+    a.record(stream)
+    for i in range(n_ng):
+        decode_call(d, i, selection=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    nograph_sel_ms = a.elapsed_time(b) / n_ng
 
     # ---- stage times: library stage events around each kernel, replicas cycled
     stage_n = min(K, 400)
@@ -376,13 +383,16 @@ def run_decode(args, world, rank):
                              f"({R} x {alg['total'] / 1e6:.1f} MB touched per cycle)",
                        "launch": (f"CUDA graph of {R} steps, replayed; one cluster kernel per step (one thread-block cluster per row, the largest size whose clusters all fit the device: 12 CTAs for 8 rows on a GB300)" if fused else
                                   f"CUDA graph of {R} steps, replayed; kernels chained with programmatic dependent launch"),
-                       "kernel_cache": "resident (pooled before timing)"},
+                       "kernel_cache": "resident (pooled before timing)",
+                       "outputs": "o and lse per step; the block lists are an optional output the timed steps "
+                                  "do not ask for (step.no_graph_with_block_lists_ms_per_step times them)"},
                roofline=roofline, clocks=clk, gpu_launches=(1 if fused else 4) * K, device_status=status)
     out["value"] = world * w.B * w.Tq * K / (total_ms * 1e-3)
     out["step"] = {"algorithmic_bytes": alg["total"], "kernel_cache_bytes": alg["kernel_cache"],
                    "selected_kv_bytes": alg["selected_kv"], "achieved_gbs": round(step_alg_gbs, 1),
                    "frac_hbm": round(step_alg_gbs / pk["hbm_gbs"], 4), "frac_8tbs": round(step_alg_gbs / 8000, 4),
                    "wall_s": round(t_wall, 3), "no_graph_ms_per_step": round(nograph_ms, 5),
+                   "no_graph_with_block_lists_ms_per_step": round(nograph_sel_ms, 5),
                    "latency_ms_l2_flushed": round(statistics.median(lat), 5)}
     out["stages_ms"] = {k: round(v, 5) for k, v in stage_ms.items()}
     out["e2e"] = run_decode_e2e(d, n=min(K, 400))
