@@ -57,6 +57,9 @@ def parse_args():
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--replicas", type=int, default=REPLICAS,
+                    help="copies of the decode inputs cycled step by step (fewer: a smaller footprint for "
+                         "profiler captures; the timed steps then find their inputs in L2)")
     ap.add_argument("--no-decode", action="store_true",
                     help="profiling aid: run only the chunked-prefill part (no headline value)")
     return ap.parse_args()
@@ -265,7 +268,7 @@ def run_decode(args, world, rank):
     import torch
 
     from block_sparse_long_infllm_gb300 import infllmv2
-    d = setup_decode(HEADLINE)
+    d = setup_decode(HEADLINE, replicas=max(1, args.replicas))
     w = d["w"]
     R = len(d["rep"])
     stream = torch.cuda.current_stream()
@@ -379,8 +382,10 @@ def run_decode(args, world, rank):
                        "head_dim": w.d, "block_size": w.block_size, "kernel": [w.kernel_size, w.kernel_stride],
                        "topk": w.topk, "n_init": w.n_init, "n_local": w.n_local, "dense_len": w.dense_len,
                        "parallelism": f"replicas x{world}",
-                       "l2": f"inputs larger than L2: {R} replicas of Q, K/V and kernel caches cycled step by step "
-                             f"({R} x {alg['total'] / 1e6:.1f} MB touched per cycle)",
+                       "l2": (f"inputs larger than L2: {R} replicas of Q, K/V and kernel caches cycled step by step "
+                              f"({R} x {alg['total'] / 1e6:.1f} MB touched per cycle)" if R * alg["total"] > 2 * 129e6
+                              else f"{R} replica(s): the steps find their inputs in L2 (a profiling run, not the "
+                                   f"benchmark)"),
                        "launch": (f"CUDA graph of {R} steps, replayed; one cluster kernel per step (one thread-block cluster per row, the largest size whose clusters all fit the device: 12 CTAs for 8 rows on a GB300)" if fused else
                                   f"CUDA graph of {R} steps, replayed; kernels chained with programmatic dependent launch"),
                        "kernel_cache": "resident (pooled before timing)",
