@@ -206,7 +206,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     pdl_wait();
 
     // ================= 1. scores of this CTA's blocks, pushed as keys to every CTA
-    // Thread 0 issues the TMA copies of a pass's kernel rows in 128-row pieces; warp w scores the
+    // Lane 0 of warp p issues the TMA copy of piece p (128 kernel rows) of a pass; warp w scores the
     // 32-row tiles w, w + 8, ... of the pass as their pieces land: S[head][kernel row] = Q K^T by
     // warp MMAs (the Q fragments of the attention below), then the maximum over the G heads.  (With
     // N = 16 heads a tcgen05 MMA does too little work per issue: one thread issuing the 8 MMAs of a

@@ -96,11 +96,14 @@ def test_append_length_past_cache_sets_error_and_skips_row(cuda_lib):
     assert L.sync_status() == 0                      # the error word was cleared
 
 
-@pytest.mark.parametrize("n_local", [2, 1], ids=["fused", "append_then_decode"])
-def test_decode_step_matches_oracle(cuda_lib, n_local):
+@pytest.mark.parametrize("n_local,lists", [(2, True), (1, True), (2, False)],
+                         ids=["fused", "append_then_decode", "fused_without_block_lists"])
+def test_decode_step_matches_oracle(cuda_lib, n_local, lists):
     """infllmv2_decode_step: one call appends and decodes.  With 2 local blocks the single cluster
     kernel does both (the new kernel overlaps only forced blocks); with 1 the append kernel runs
-    first.  Caches, kernels and outputs as for append followed by decode."""
+    first.  Caches, kernels and outputs as for append followed by decode.  Without the optional
+    block lists: at the checked steps the same step is repeated with them (an append of the same
+    row is idempotent) and both outputs must be the same bits."""
     torch = torch_mod()
     L = lib()
     w = synth.WORKLOADS["decode_32k"].scaled(B=2, L=1600, Hq=32, Hkv=2, d=128, block_size=64, topk=8, n_local=n_local,
@@ -130,8 +133,15 @@ def test_decode_step_matches_oracle(cuda_lib, n_local):
             v_np[b, :, kv[b] - 1] = vn[b]
         q = to_dev(q_bits)
         o = torch.empty_like(q)
-        L.decode_step(q, to_dev(kn), to_dev(vn), k, v, kern, to_dev(kv), o, ws, p, idx_out=idx, counts_out=cnt)
+        L.decode_step(q, to_dev(kn), to_dev(vn), k, v, kern, to_dev(kv), o, ws, p, idx_out=idx if lists else None,
+                      counts_out=cnt if lists else None)
         if step in (0, 9, 17, 31, 39):
+            if not lists:
+                o_lists = torch.empty_like(q)
+                L.decode_step(q, to_dev(kn), to_dev(vn), k, v, kern, to_dev(kv), o_lists, ws, p, idx_out=idx,
+                              counts_out=cnt)
+                torch.cuda.synchronize()
+                assert torch.equal(o.view(torch.int16), o_lists.view(torch.int16)), f"step {step}"
             torch.cuda.synchronize()
             assert L.sync_status() == 0
             kern_ref, _ = oracle.kernel_pool(k_np, kv, c, s, M)
