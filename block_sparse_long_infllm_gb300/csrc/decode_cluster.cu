@@ -373,7 +373,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     // fast path: the attention's list is init blocks [0, r_ainit) | s_byrank[0, r_k) | local blocks
     // from r_lof; otherwise sel[] in block order
     bool by_rank = false;
-    int r_ainit = 0, r_lof = 0, r_k = 0;
+    int r_ainit = 0, r_lof = 0, r_k = 0, r_nc = 0, r_nn = 0;
     auto list_blk = [&](int e) {
         if (!by_rank) return sel[e];
         if (e < r_ainit) return e;
@@ -517,42 +517,14 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                     }
                     for (int i3 = tid; i3 < kDcFastPer * kDcThreads / 32; i3 += kDcThreads) s_bits[i3] = 0u;
                     __syncthreads();
-                    if (idx_out != nullptr) {
-                        // the list in block order: bitmap of the chosen blocks, word prefix popcounts
-                        // (one warp), then one popcount per chosen candidate
-                        for (int i3 = tid; i3 < c_total; i3 += kDcThreads)
-                            if (s_rk[i3] < k) {
-                                const uint32_t blk = ~static_cast<uint32_t>(s_cv[i3]);
-                                atomicOr(&s_bits[blk >> 5], 1u << (blk & 31));
-                            }
-                        __syncthreads();
-                        if (warp == 0) {
-                            const int c0 = __popc(s_bits[2 * lane]), c1 = __popc(s_bits[2 * lane + 1]);
-                            int wi = c0 + c1;
-#pragma unroll
-                            for (int off = 1; off < 32; off <<= 1) {
-                                const int x = __shfl_up_sync(0xffffffffu, wi, off);
-                                if (lane >= off) wi += x;
-                            }
-                            s_wpre[2 * lane] = wi - c0 - c1;
-                            s_wpre[2 * lane + 1] = wi - c1;
-                        }
-                        __syncthreads();
-                        for (int i3 = tid; i3 < c_total; i3 += kDcThreads)
-                            if (s_rk[i3] < k) {
-                                const uint32_t blk = ~static_cast<uint32_t>(s_cv[i3]);
-                                sel[a_init + s_wpre[blk >> 5] + __popc(s_bits[blk >> 5] & ((1u << (blk & 31)) - 1u))] =
-                                    static_cast<int>(blk);
-                            }
-                        for (int i3 = tid; i3 < a_init; i3 += kDcThreads) sel[i3] = i3;
-                        for (int i3 = tid; i3 < nn - lo_f; i3 += kDcThreads) sel[a_init + k + i3] = lo_f + i3;
-                    }
                     total = a_init + k + (nn - lo_f);
                     done = true;
                     by_rank = true;
                     r_ainit = a_init;
                     r_lof = lo_f;
                     r_k = k;
+                    r_nc = c_total;
+                    r_nn = nn;
                 }
             }
             __syncthreads();
@@ -725,13 +697,51 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
         __syncthreads();  // sel complete
         if (rank == 0) {
             if (tid == 0 && (total > sh.S_cap || !len_ok)) raise_error(err, kDevErrIndex);
-            if (idx_out != nullptr) {
+            if (idx_out != nullptr && !by_rank) {  // (fast path: written by the last CTA behind its copies)
                 int* out = idx_out + static_cast<size_t>(row) * idx_stride;
                 for (int i = tid; i < idx_stride; i += kDcThreads) out[i] = i < count ? sel[i] : -1;
                 if (tid == 0) counts_out[row] = count;
             }
         }
     }
+    // The block lists of the fast path, by the last CTA (which attends the fewest blocks) while its
+    // attention copies are in flight: the chosen candidates in block order by a bitmap, word prefix
+    // popcounts (one warp) and one popcount per candidate, framed by the initial and local blocks.
+    bool lists_pending = by_rank && static_cast<int>(rank) == ncta - 1 && idx_out != nullptr;
+    auto write_lists = [&]() {
+        for (int i = tid; i < r_nc; i += kDcThreads)
+            if (s_rk[i] < r_k) {
+                const uint32_t blk = ~static_cast<uint32_t>(s_cv[i]);
+                atomicOr(&s_bits[blk >> 5], 1u << (blk & 31));
+            }
+        __syncthreads();
+        if (warp == 0) {
+            const int c0 = __popc(s_bits[2 * lane]), c1 = __popc(s_bits[2 * lane + 1]);
+            int wi = c0 + c1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int x = __shfl_up_sync(0xffffffffu, wi, off);
+                if (lane >= off) wi += x;
+            }
+            s_wpre[2 * lane] = wi - c0 - c1;
+            s_wpre[2 * lane + 1] = wi - c1;
+        }
+        __syncthreads();
+        int* out = idx_out + static_cast<size_t>(row) * idx_stride;
+        for (int i = tid; i < r_nc; i += kDcThreads)
+            if (s_rk[i] < r_k) {
+                const uint32_t blk = ~static_cast<uint32_t>(s_cv[i]);
+                const int at = r_ainit + s_wpre[blk >> 5] + __popc(s_bits[blk >> 5] & ((1u << (blk & 31)) - 1u));
+                if (at < count) out[at] = static_cast<int>(blk);
+            }
+        for (int i = tid; i < idx_stride; i += kDcThreads) {
+            if (i >= count) out[i] = -1;
+            else if (i < r_ainit) out[i] = i;
+            else if (i >= r_ainit + r_k) out[i] = r_lof + (i - r_ainit - r_k);
+        }
+        if (tid == 0) counts_out[row] = count;
+        lists_pending = false;
+    };
     // second half-barrier: this CTA no longer reads its keys or scores (and its copies of its keys
     // have been read), whose memory takes the peers' partials after the attention
     if (warp == 0) bulk_wait_read_all();
@@ -762,6 +772,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                 }
             }
             __syncthreads();
+            if (lists_pending) write_lists();
             for (int tile = warp; tile < PB * kTilesPerBlock; tile += kDcThreads / 32) {
                 const int k = tile / kTilesPerBlock;
                 const int t = t0 + k;
@@ -788,6 +799,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
             __syncthreads();
         }
     }
+    if (lists_pending) write_lists();  // (a CTA without blocks to attend)
     acc_finish_rowsum(A);
     {
         // merge the 8 warps (scratch in the tile memory) into this CTA's partial
