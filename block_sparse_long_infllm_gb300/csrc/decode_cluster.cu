@@ -27,6 +27,8 @@
 //      after their selection (whose memory the partials reuse); there is no barrier at the end.
 // No global memory is written but the outputs, and nothing is carried between launches.
 #include <algorithm>
+#include <mutex>
+#include <vector>
 
 #include "attn_warp.cuh"
 #include "internal.h"
@@ -926,13 +928,6 @@ static cudaError_t launch_cluster_t(const DecodeArgs& a, const void* kernel_cach
     if (sh.S_cap > kDcMaxSel) return cudaErrorNotSupported;
     const int smem = SM::bytes(sh.nblk_max, sh.S_cap);
     auto kfn = a.k_new != nullptr ? decode_cluster_kernel<D, BS, true> : decode_cluster_kernel<D, BS, false>;
-    cudaFuncAttributes fa{};
-    if (cudaError_t e = cudaFuncGetAttributes(&fa, kfn); e != cudaSuccess) return e;
-    if (smem + static_cast<int>(fa.sharedSizeBytes) > 227 * 1024) return cudaErrorNotSupported;
-    if (cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); e != cudaSuccess)
-        return e;
-    if (cudaFuncSetAttribute(kfn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-        (void)cudaGetLastError();  // then only the portable sizes (<= 8) are offered below
     const int rows = a.B * a.Hkv;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kDcThreads);
@@ -945,28 +940,67 @@ static cudaError_t launch_cluster_t(const DecodeArgs& a, const void* kernel_cach
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;  // (cluster size search without the serialisation attribute)
-    // cluster size: the largest whose clusters all fit on the device at once (one wave of rows);
-    // if none does, the one that keeps the most SMs busy
-    int CL = 0, best_sms = 0, fallback = 0;
-    for (int cand : {16, 12, 8, 4, 2}) {
-        attr[0].val.clusterDim.x = cand;
-        cfg.gridDim = dim3(cand * rows);
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kfn, &cfg) != cudaSuccess) {
-            (void)cudaGetLastError();
-            continue;
-        }
-        if (n >= rows) {
-            CL = cand;
-            break;
-        }
-        if (n * cand > best_sms) {
-            best_sms = n * cand;
-            fallback = cand;
+    int dev = 0;
+    if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
+    // The kernel's attributes and the cluster size for (kernel, device, rows, shared memory) are
+    // settled once (the function-attribute and occupancy queries cost host time on every call);
+    // the dynamic shared-memory limit only ever grows, so earlier choices stay launchable.
+    struct Choice {
+        const void* fn;
+        int dev, rows, smem, CL;
+    };
+    static std::mutex mtx;
+    static std::vector<Choice> choices;
+    static std::vector<Choice> smem_set;  // per (kernel, device): the largest limit set (in .smem)
+    int CL = 0;
+    {
+        std::lock_guard<std::mutex> lock(mtx);
+        for (const Choice& ch : choices)
+            if (ch.fn == reinterpret_cast<const void*>(kfn) && ch.dev == dev && ch.rows == rows && ch.smem == smem)
+                CL = ch.CL;
+        if (CL == 0) {
+            cudaFuncAttributes fa{};
+            if (cudaError_t e = cudaFuncGetAttributes(&fa, kfn); e != cudaSuccess) return e;
+            if (smem + static_cast<int>(fa.sharedSizeBytes) > 227 * 1024) return cudaErrorNotSupported;
+            Choice* lim = nullptr;
+            for (Choice& ch : smem_set)
+                if (ch.fn == reinterpret_cast<const void*>(kfn) && ch.dev == dev) lim = &ch;
+            if (lim == nullptr || lim->smem < smem) {
+                if (cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                    e != cudaSuccess)
+                    return e;
+                if (lim == nullptr)
+                    smem_set.push_back(Choice{reinterpret_cast<const void*>(kfn), dev, 0, smem, 0});
+                else
+                    lim->smem = smem;
+            }
+            if (cudaFuncSetAttribute(kfn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+                (void)cudaGetLastError();  // then only the portable sizes (<= 8) are offered below
+            // cluster size: the largest whose clusters all fit on the device at once (one wave of
+            // rows); if none does, the one that keeps the most SMs busy
+            cfg.numAttrs = 1;  // (the search without the serialisation attribute)
+            int best_sms = 0, fallback = 0;
+            for (int cand : {16, 12, 8, 4, 2}) {
+                attr[0].val.clusterDim.x = cand;
+                cfg.gridDim = dim3(cand * rows);
+                int n = 0;
+                if (cudaOccupancyMaxActiveClusters(&n, kfn, &cfg) != cudaSuccess) {
+                    (void)cudaGetLastError();
+                    continue;
+                }
+                if (n >= rows) {
+                    CL = cand;
+                    break;
+                }
+                if (n * cand > best_sms) {
+                    best_sms = n * cand;
+                    fallback = cand;
+                }
+            }
+            if (CL == 0) CL = fallback;
+            if (CL > 0) choices.push_back(Choice{reinterpret_cast<const void*>(kfn), dev, rows, smem, CL});
         }
     }
-    if (CL == 0) CL = fallback;
     if (CL == 0 || ((16 + CL - 1) / CL) * CL * SM::kPRow * 4 > SM::kSlots) return cudaErrorNotSupported;
     sh.CB = ((sh.nblk_max + CL - 1) / CL + 3) & ~3;  // a multiple of 4: each CTA's keys are 16-byte copies
     attr[0].val.clusterDim.x = CL;
