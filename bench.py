@@ -65,6 +65,17 @@ def parse_args():
     return ap.parse_args()
 
 
+def max_over_ranks(value: float, world: int, device: str = "cuda") -> float:
+    """The largest of the ranks' values (the job's time is its slowest rank's): an all-reduce
+    over the default process group on `device` (the GPU under NCCL, "cpu" under gloo)."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_info():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -301,10 +312,7 @@ def run_decode(args, world, rank):
         torch.distributed.barrier()
     clk = clocks.stop()
     total_ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world)
     status = infllmv2.sync_status()
 
     # ---- the same K steps launched one call at a time (no graph)

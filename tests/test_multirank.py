@@ -1,0 +1,55 @@
+"""The multi-GPU path is replicas only: every rank runs its own copy of the decode workload and
+the job's time is the slowest rank's.  These run on CPU: two gloo ranks reduce their times, and
+the reference arm under two ranks runs on rank 0 alone."""
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank: int, world: int, port: int, values, out):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        out[rank] = bench.max_over_ranks(values[rank], world, device="cpu")
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_time():
+    world, port = 2, _free_port()
+    values = [3.25, 7.5]
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_rank_main, args=(world, port, values, out), nprocs=world, join=True)
+        assert dict(out) == {0: 7.5, 1: 7.5}
+
+
+def test_single_rank_keeps_its_value():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(4.0, 1) == 4.0
+
+
+def test_reference_arm_runs_on_rank_0_only():
+    env = dict(os.environ, RANK="1", LOCAL_RANK="1", WORLD_SIZE="2", MASTER_ADDR="127.0.0.1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
