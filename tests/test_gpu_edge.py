@@ -307,3 +307,15 @@ def test_decode_many_rows_smaller_clusters(cuda_lib, B, Hkv, G, L):
     inp = synth.make_inputs(w)
     inp["kv_len"] = np.array([L - 97 * i for i in range(B)], dtype=np.int32)   # per-sequence lengths
     _parity(w, inp)
+
+
+@pytest.mark.parametrize("B,L", [(1, 262144), (16, 65536)], ids=["256k_rows_over_2048_blocks", "32_rows_at_64k"])
+def test_decode_multi_pass_scoring_and_long_rows(cuda_lib, B, L):
+    # 256K tokens: 4096 blocks per row, past the fast selection path (the two-bit general search
+    # takes over) and several scoring passes per CTA; 32 rows at 64K: clusters of 4 CTAs, each
+    # scoring its 256 blocks in two passes
+    w = synth.WORKLOADS["decode_128k_b4"].scaled(B=B, L=L, seed=3700 + B)
+    inp = synth.make_inputs(w)
+    if B > 1:
+        inp["kv_len"] = np.array([L - 131 * i for i in range(B)], dtype=np.int32)
+    _parity(w, inp)
