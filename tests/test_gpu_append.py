@@ -96,9 +96,10 @@ def test_append_length_past_cache_sets_error_and_skips_row(cuda_lib):
     assert L.sync_status() == 0                      # the error word was cleared
 
 
-@pytest.mark.parametrize("n_local,lists", [(2, True), (1, True), (2, False)],
-                         ids=["fused", "append_then_decode", "fused_without_block_lists"])
-def test_decode_step_matches_oracle(cuda_lib, n_local, lists):
+@pytest.mark.parametrize("n_local,lists,d,bs", [(2, True, 128, 64), (1, True, 128, 64), (2, False, 128, 64),
+                                               (2, True, 64, 128)],
+                         ids=["fused", "append_then_decode", "fused_without_block_lists", "fused_d64_block128"])
+def test_decode_step_matches_oracle(cuda_lib, n_local, lists, d, bs):
     """infllmv2_decode_step: one call appends and decodes.  With 2 local blocks the single cluster
     kernel does both (the new kernel overlaps only forced blocks); with 1 the append kernel runs
     first.  Caches, kernels and outputs as for append followed by decode.  Without the optional
@@ -106,8 +107,8 @@ def test_decode_step_matches_oracle(cuda_lib, n_local, lists):
     row is idempotent) and both outputs must be the same bits."""
     torch = torch_mod()
     L = lib()
-    w = synth.WORKLOADS["decode_32k"].scaled(B=2, L=1600, Hq=32, Hkv=2, d=128, block_size=64, topk=8, n_local=n_local,
-                                              dense_len=0, seed=5300 + n_local)
+    w = synth.WORKLOADS["decode_32k"].scaled(B=2, L=1600, Hq=32, Hkv=2, d=d, block_size=bs, topk=8, n_local=n_local,
+                                              dense_len=0, seed=5300 + n_local + (0 if (d, bs) == (128, 64) else d + bs))
     inp = synth.make_inputs(w)
     p = w.params()
     c, s = w.kernel_size, w.kernel_stride
