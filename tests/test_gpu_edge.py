@@ -319,3 +319,32 @@ def test_decode_multi_pass_scoring_and_long_rows(cuda_lib, B, L):
     if B > 1:
         inp["kv_len"] = np.array([L - 131 * i for i in range(B)], dtype=np.int32)
     _parity(w, inp)
+
+
+def test_decode_host_reports_device_errors(cuda_lib):
+    # a cache length past the cache, staged from host memory: the host-buffer call returns the
+    # device error (and clears the word); the next call with good lengths succeeds
+    import torch
+    L = lib()
+    w = BASE.scaled(L=2048, seed=3800)
+    inp = synth.make_inputs(w)
+    p = w.params()
+    k, v = to_dev(inp["k_cache"]), to_dev(inp["v_cache"])
+    kern = torch.zeros((1, 2, n_kernels(w), 128), dtype=torch.bfloat16, device="cuda")
+    L.kernel_pool(k, kern, 0, w.L, p)
+    ws = torch.empty(L.workspace_size(L.ENTRY_DECODE, 1, 1, 32, 2, 128, w.L_max, p), dtype=torch.uint8,
+                     device="cuda")
+    q_host = torch.from_numpy(np.ascontiguousarray(inp["q"]).view(np.int16)).view(torch.bfloat16).view(1, 32, 128)
+    q_host = q_host.pin_memory()
+    o_host = torch.empty((1, 32, 128), dtype=torch.bfloat16).pin_memory()
+    q_dev = torch.empty((1, 32, 128), dtype=torch.bfloat16, device="cuda")
+    o_dev = torch.empty_like(q_dev)
+    kv_dev = torch.empty(1, dtype=torch.int32, device="cuda")
+    bad = torch.tensor([w.L_max + 5], dtype=torch.int32).pin_memory()
+    with pytest.raises(L.InfLLMv2Error) as e:
+        L.decode_host(q_host, bad, o_host, q_dev, kv_dev, o_dev, k, v, kern, ws, p)
+    assert e.value.status == L.ERR_DEVICE_INDEX
+    assert L.sync_status() == 0                                   # cleared by the call
+    good = torch.from_numpy(inp["kv_len"]).pin_memory()
+    L.decode_host(q_host, good, o_host, q_dev, kv_dev, o_dev, k, v, kern, ws, p)
+    assert L.sync_status() == 0
