@@ -952,60 +952,6 @@ static cudaError_t launch_cluster_t(const DecodeArgs& a, const void* kernel_cach
     static std::mutex mtx;
     static std::vector<Choice> choices;
     static std::vector<Choice> smem_set;  // per (kernel, device): the largest limit set (in .smem)
-    int CL = 0;
-    {
-        std::lock_guard<std::mutex> lock(mtx);
-        for (const Choice& ch : choices)
-            if (ch.fn == reinterpret_cast<const void*>(kfn) && ch.dev == dev && ch.rows == rows && ch.smem == smem)
-                CL = ch.CL;
-        if (CL == 0) {
-            cudaFuncAttributes fa{};
-            if (cudaError_t e = cudaFuncGetAttributes(&fa, kfn); e != cudaSuccess) return e;
-            if (smem + static_cast<int>(fa.sharedSizeBytes) > 227 * 1024) return cudaErrorNotSupported;
-            Choice* lim = nullptr;
-            for (Choice& ch : smem_set)
-                if (ch.fn == reinterpret_cast<const void*>(kfn) && ch.dev == dev) lim = &ch;
-            if (lim == nullptr || lim->smem < smem) {
-                if (cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-                    e != cudaSuccess)
-                    return e;
-                if (lim == nullptr)
-                    smem_set.push_back(Choice{reinterpret_cast<const void*>(kfn), dev, 0, smem, 0});
-                else
-                    lim->smem = smem;
-            }
-            if (cudaFuncSetAttribute(kfn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-                (void)cudaGetLastError();  // then only the portable sizes (<= 8) are offered below
-            // cluster size: the largest whose clusters all fit on the device at once (one wave of
-            // rows); if none does, the one that keeps the most SMs busy
-            cfg.numAttrs = 1;  // (the search without the serialisation attribute)
-            int best_sms = 0, fallback = 0;
-            for (int cand : {16, 12, 8, 4, 2}) {
-                attr[0].val.clusterDim.x = cand;
-                cfg.gridDim = dim3(cand * rows);
-                int n = 0;
-                if (cudaOccupancyMaxActiveClusters(&n, kfn, &cfg) != cudaSuccess) {
-                    (void)cudaGetLastError();
-                    continue;
-                }
-                if (n >= rows) {
-                    CL = cand;
-                    break;
-                }
-                if (n * cand > best_sms) {
-                    best_sms = n * cand;
-                    fallback = cand;
-                }
-            }
-            if (CL == 0) CL = fallback;
-            if (CL > 0) choices.push_back(Choice{reinterpret_cast<const void*>(kfn), dev, rows, smem, CL});
-        }
-    }
-    if (CL == 0 || ((16 + CL - 1) / CL) * CL * SM::kPRow * 4 > SM::kSlots) return cudaErrorNotSupported;
-    sh.CB = ((sh.nblk_max + CL - 1) / CL + 3) & ~3;  // a multiple of 4: each CTA's keys are 16-byte copies
-    attr[0].val.clusterDim.x = CL;
-    cfg.gridDim = dim3(rows * CL);
-    cfg.numAttrs = 2;  // + programmatic stream serialisation: set-up overlaps the previous kernel
     CUtensorMap tkern, tk, tv;
     const uint64_t krows = static_cast<uint64_t>(a.B) * a.Hkv * M_max;
     const uint64_t cache_rows = static_cast<uint64_t>(a.B) * a.Hkv * a.L_max;
@@ -1015,15 +961,85 @@ static cudaError_t launch_cluster_t(const DecodeArgs& a, const void* kernel_cach
         return cudaErrorNotSupported;
     const int G = a.Hq / a.Hkv;
     const float scale_log2 = a.p.scale * 1.4426950408889634f;
-    return cudaLaunchKernelEx(&cfg, kfn, tkern, tk, tv, static_cast<const __nv_bfloat16*>(a.q),
-                              static_cast<const __nv_bfloat16*>(kernel_cache),
-                              static_cast<const __nv_bfloat16*>(a.k_cache), static_cast<const __nv_bfloat16*>(a.v_cache),
-                              a.kv_len, a.Hq, a.Hkv,
-                              G, a.L_max, M_max, a.p, sh, idx_out, idx_stride, counts_out,
-                              static_cast<__nv_bfloat16*>(a.o), a.lse, scale_log2, a.err,
-                              static_cast<const __nv_bfloat16*>(a.k_new), static_cast<const __nv_bfloat16*>(a.v_new),
-                              static_cast<__nv_bfloat16*>(a.k_w), static_cast<__nv_bfloat16*>(a.v_w),
-                              static_cast<__nv_bfloat16*>(a.kern_w));
+    const void* fn = reinterpret_cast<const void*>(kfn);
+    // a launch from a remembered choice that fails (the device was reset and the attributes with
+    // it) settles the choice afresh and launches once more
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        int CL = 0;
+        bool remembered = false;
+        {
+            std::lock_guard<std::mutex> lock(mtx);
+            if (attempt > 0) {
+                auto drop = [&](std::vector<Choice>& v) {
+                    v.erase(std::remove_if(v.begin(), v.end(),
+                                           [&](const Choice& ch) { return ch.fn == fn && ch.dev == dev; }),
+                            v.end());
+                };
+                drop(choices);
+                drop(smem_set);
+            }
+            for (const Choice& ch : choices)
+                if (ch.fn == fn && ch.dev == dev && ch.rows == rows && ch.smem == smem) CL = ch.CL;
+            remembered = CL != 0;
+            if (CL == 0) {
+                cudaFuncAttributes fa{};
+                if (cudaError_t e = cudaFuncGetAttributes(&fa, kfn); e != cudaSuccess) return e;
+                if (smem + static_cast<int>(fa.sharedSizeBytes) > 227 * 1024) return cudaErrorNotSupported;
+                Choice* lim = nullptr;
+                for (Choice& ch : smem_set)
+                    if (ch.fn == fn && ch.dev == dev) lim = &ch;
+                if (lim == nullptr || lim->smem < smem) {
+                    if (cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                        e != cudaSuccess)
+                        return e;
+                    if (lim == nullptr)
+                        smem_set.push_back(Choice{fn, dev, 0, smem, 0});
+                    else
+                        lim->smem = smem;
+                }
+                if (cudaFuncSetAttribute(kfn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+                    (void)cudaGetLastError();  // then only the portable sizes (<= 8) are offered below
+                // cluster size: the largest whose clusters all fit on the device at once (one wave
+                // of rows); if none does, the one that keeps the most SMs busy
+                cfg.numAttrs = 1;  // (the search without the serialisation attribute)
+                int best_sms = 0, fallback = 0;
+                for (int cand : {16, 12, 8, 4, 2}) {
+                    attr[0].val.clusterDim.x = cand;
+                    cfg.gridDim = dim3(cand * rows);
+                    int n = 0;
+                    if (cudaOccupancyMaxActiveClusters(&n, kfn, &cfg) != cudaSuccess) {
+                        (void)cudaGetLastError();
+                        continue;
+                    }
+                    if (n >= rows) {
+                        CL = cand;
+                        break;
+                    }
+                    if (n * cand > best_sms) {
+                        best_sms = n * cand;
+                        fallback = cand;
+                    }
+                }
+                if (CL == 0) CL = fallback;
+                if (CL > 0) choices.push_back(Choice{fn, dev, rows, smem, CL});
+            }
+        }
+        if (CL == 0 || ((16 + CL - 1) / CL) * CL * SM::kPRow * 4 > SM::kSlots) return cudaErrorNotSupported;
+        sh.CB = ((sh.nblk_max + CL - 1) / CL + 3) & ~3;  // a multiple of 4: each CTA's keys are 16-byte copies
+        attr[0].val.clusterDim.x = CL;
+        cfg.gridDim = dim3(rows * CL);
+        cfg.numAttrs = 2;  // + programmatic stream serialisation: set-up overlaps the previous kernel
+        const cudaError_t e = cudaLaunchKernelEx(
+            &cfg, kfn, tkern, tk, tv, static_cast<const __nv_bfloat16*>(a.q),
+            static_cast<const __nv_bfloat16*>(kernel_cache), static_cast<const __nv_bfloat16*>(a.k_cache),
+            static_cast<const __nv_bfloat16*>(a.v_cache), a.kv_len, a.Hq, a.Hkv, G, a.L_max, M_max, a.p, sh, idx_out,
+            idx_stride, counts_out, static_cast<__nv_bfloat16*>(a.o), a.lse, scale_log2, a.err,
+            static_cast<const __nv_bfloat16*>(a.k_new), static_cast<const __nv_bfloat16*>(a.v_new),
+            static_cast<__nv_bfloat16*>(a.k_w), static_cast<__nv_bfloat16*>(a.v_w), static_cast<__nv_bfloat16*>(a.kern_w));
+        if (e == cudaSuccess || !remembered) return e;
+        (void)cudaGetLastError();
+    }
+    return cudaErrorNotSupported;
 }
 
 bool decode_cluster_supported(const DecodeArgs& a, int M_max) {
