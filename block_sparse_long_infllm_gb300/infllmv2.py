@@ -323,6 +323,30 @@ def decode_host(q_host, kv_len_host, o_host, q_dev, kv_len_dev, o_dev, k_cache, 
                                        ctypes.byref(Params.make(params)), _stream(stream)), "infllmv2_decode_host")
 
 
+class DecodeHostStep:
+    """decode_host with its buffers bound once: a serving loop with static buffers (its query,
+    length and output tensors refilled in place each step) pays only the C call per step.  The
+    tensors must stay alive and in place while the object is used."""
+
+    def __init__(self, q_host, kv_len_host, o_host, q_dev, kv_len_dev, o_dev, k_cache, v_cache, kernel_cache,
+                 workspace, params, lse_host=None, lse_dev=None, stream=None):
+        B, Hq, d = q_host.shape[0], q_host.shape[-2], q_host.shape[-1]
+        Hkv, L_max = k_cache.shape[1], k_cache.shape[2]
+        self._fn = load().infllmv2_decode_host
+        self._params = Params.make(params)
+        self._args = (_host_ptr(q_host), _host_ptr(kv_len_host), _host_ptr(o_host), _host_ptr(lse_host), _ptr(q_dev),
+                      _ptr(kv_len_dev), _ptr(o_dev), _ptr(lse_dev), _ptr(k_cache), _ptr(v_cache), _ptr(kernel_cache),
+                      B, Hq, Hkv, d, L_max, kernel_cache.shape[2], _ptr(workspace),
+                      workspace.numel() * workspace.element_size(), ctypes.byref(self._params), _stream(stream))
+        self._keep = (q_host, kv_len_host, o_host, lse_host, q_dev, kv_len_dev, o_dev, lse_dev, k_cache, v_cache,
+                      kernel_cache, workspace)
+
+    def __call__(self):
+        rc = self._fn(*self._args)
+        if rc != OK:
+            raise InfLLMv2Error(rc, "infllmv2_decode_host")
+
+
 NOALLOC_SCRATCH_BYTES = 16 << 20  # INFLLMV2_NOALLOC_SCRATCH_BYTES
 
 

@@ -295,6 +295,13 @@ def test_decode_host_buffers_match_device_call(cuda_lib):
                   lse_host=lse_host, lse_dev=lse_dev)
     assert torch.equal(o_host.view(torch.int16), g["o"].view(w.B, w.Hq, w.d).cpu().view(torch.int16))
     assert torch.equal(lse_host, g["lse"].view(w.B, w.Hq).cpu())
+    # the prepared call (buffers bound once) gives the same bits
+    o_host.zero_()
+    step = L.DecodeHostStep(q_host, kv_host, o_host, q_dev, kv_dev, o_dev, g["k"], g["v"], g["kern"], ws, p,
+                            lse_host=lse_host, lse_dev=lse_dev)
+    step()
+    step()
+    assert torch.equal(o_host.view(torch.int16), g["o"].view(w.B, w.Hq, w.d).cpu().view(torch.int16))
     o_ref, _ = oracle.attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["kv_len"], oidx, ocnt, p)
     check_output(bf16_to_f64(o_host.view(w.B, 1, w.Hq, w.d)), o_ref)
 
