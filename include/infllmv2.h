@@ -25,7 +25,8 @@
  *
  * Conventions for every entry point
  *   - Tensors are plain device pointers, row-major, densely packed, 16-byte
- *     aligned.  bf16 tensors are passed as void*.  Index/length arrays are
+ *     aligned (infllmv2_decode_host also takes host buffers, as its comment
+ *     says).  bf16 tensors are passed as void*.  Index/length arrays are
  *     device int32.  The caller owns every buffer and the stream; the library
  *     never allocates device memory (the static-memory design of [CPM.cu]).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
