@@ -257,22 +257,39 @@ def decode_algorithmic_bytes(d) -> dict:
                 total=kern_bytes + kv_bytes + 2 * q_bytes, kernel_cache=kern_bytes, selected_kv=kv_bytes)
 
 
-def capture_decode_graph(d):
-    """One CUDA graph holding one decode step per replica (4 kernels each)."""
+def capture_graph(step, n: int):
+    """One CUDA graph holding step(0), ..., step(n-1) (the launch path warmed outside capture)."""
     import torch
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        for r in range(len(d["rep"])):   # warm the launch path outside capture
-            decode_call(d, r)
+        for r in range(n):
+            step(r)
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        for r in range(len(d["rep"])):
-            decode_call(d, r)
+        for r in range(n):
+            step(r)
     torch.cuda.synchronize()
     return g
+
+
+class StepGraphs:
+    """Exactly K steps back to back: a graph of one step per replica (R steps) replayed K // R
+    times, then a graph of the first K % R replicas' steps, so the step count is the one asked
+    for and every step still runs on the next replica's inputs."""
+
+    def __init__(self, step, R: int, K: int):
+        self.full = capture_graph(step, R) if K >= R else None
+        self.n_full = K // R
+        self.tail = capture_graph(step, K % R) if K % R else None
+
+    def replay(self):
+        for _ in range(self.n_full):
+            self.full.replay()
+        if self.tail is not None:
+            self.tail.replay()
 
 
 def run_decode(args, world, rank):
@@ -288,13 +305,12 @@ def run_decode(args, world, rank):
     torch.cuda.synchronize()
     if infllmv2.sync_status() != 0:
         raise RuntimeError("device error during warm-up")
-    graph = capture_decode_graph(d)
-    graph.replay()
+    # ---- timed region: exactly K steps back to back (graphs of R steps replayed), each step on the
+    # next replica so no step finds its inputs in L2
+    K = max(1, args.steps)
+    graphs = StepGraphs(lambda r: decode_call(d, r), R, K)
+    graphs.replay()
     torch.cuda.synchronize()
-
-    # ---- timed region: K steps back to back (the graph replays R steps), each step on the next
-    # replica so no step finds its inputs in L2
-    K = max(R, (args.steps // R) * R)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(torch.cuda.current_device())
     if world > 1:
@@ -303,8 +319,7 @@ def run_decode(args, world, rank):
     clocks.start()
     t_wall = time.perf_counter()
     ev0.record(stream)
-    for _ in range(K // R):
-        graph.replay()
+    graphs.replay()
     ev1.record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
@@ -406,10 +421,59 @@ def run_decode(args, world, rank):
                    "frac_hbm": round(step_alg_gbs / pk["hbm_gbs"], 4), "frac_8tbs": round(step_alg_gbs / 8000, 4),
                    "wall_s": round(t_wall, 3), "no_graph_ms_per_step": round(nograph_ms, 5),
                    "no_graph_with_block_lists_ms_per_step": round(nograph_sel_ms, 5),
-                   "latency_ms_l2_flushed": round(statistics.median(lat), 5)}
+                   "latency_ms_l2_flushed": round(statistics.median(lat), 5),
+                   "latency_frac_hbm": round(alg["total"] / (statistics.median(lat) * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
     out["stages_ms"] = {k: round(v, 5) for k, v in stage_ms.items()}
     out["e2e"] = run_decode_e2e(d, n=min(K, 400))
     return out, d
+
+
+def run_decode_32k(args) -> dict:
+    """Single-token decode at 32K context, batch 1 (workload "decode_32k": 64-token blocks, top-64
+    + 1 initial + 2 local blocks): exactly K steps back to back in CUDA graphs, each step on the next
+    of 48 replicas (48 x 5.5 MB touched per cycle, over twice the L2), and the single-step latency
+    with L2 flushed before the step."""
+    import torch
+    d = setup_decode("decode_32k", replicas=48)
+    w = d["w"]
+    R = len(d["rep"])
+    K = max(1, min(args.steps, 2000))
+    for i in range(max(args.warmup, 3)):
+        decode_call(d, i)
+    graphs = StepGraphs(lambda r: decode_call(d, r), R, K)
+    graphs.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    graphs.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / K
+    flush = Flusher()
+    lat = []
+    for i in range(30):
+        flush()
+        a.record(stream)
+        decode_call(d, i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        lat.append(a.elapsed_time(b))
+    del flush
+    decode_call(d, 0, selection=True)
+    torch.cuda.synchronize()
+    from block_sparse_long_infllm_gb300 import infllmv2
+    assert infllmv2.sync_status() == 0
+    alg = decode_algorithmic_bytes(d)
+    pk = peaks()
+    lat_ms = statistics.median(lat)
+    gbs = alg["total"] / (ms * 1e-3) / 1e9
+    return {"workload": "decode_32k", "batch": w.B, "kv_len": w.L, "ms_per_step": ms, "steps": K,
+            "value": w.B * w.Tq / (ms * 1e-3), "unit": UNIT, "algorithmic_bytes": alg["total"],
+            "achieved_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+            "latency_ms_l2_flushed": round(lat_ms, 5),
+            "latency_frac_hbm": round(alg["total"] / (lat_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+            "gpu_launches_per_step": 1}
 
 
 def run_decode_append(args, d) -> dict:
@@ -434,25 +498,14 @@ def run_decode_append(args, d) -> dict:
         infllmv2.decode_step(rep["q"], kn, vn, rep["k"], rep["v"], rep["kern"], d["kv_len"], d["o"], d["ws"], d["p"],
                              lse=d["lse"])
 
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        for r in range(R):
-            step(r)
-    torch.cuda.current_stream().wait_stream(s)
+    K = max(1, min(args.steps, 2000))
+    graphs = StepGraphs(step, R, K)
+    graphs.replay()
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for r in range(R):
-            step(r)
-    g.replay()
-    torch.cuda.synchronize()
-    K = max(R, (min(args.steps, 2000) // R) * R)
     stream = torch.cuda.current_stream()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(K // R):
-        g.replay()
+    graphs.replay()
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / K
@@ -986,6 +1039,7 @@ def main():
     else:
         out, dec = run_decode(args, world, rank)
         out["decode_step_with_append"] = run_decode_append(args, dec)
+        out["decode_32k"] = run_decode_32k(args)
     if not args.no_prefill:
         out["prefill"] = run_prefill(args)
         out["varlen_prefill"] = run_varlen_prefill(args)

@@ -307,6 +307,28 @@ def decode(q, k_cache, v_cache, kernel_cache, kv_len, o, workspace, params, lse=
                                   ctypes.byref(Params.make(params)), _stream(stream)), "infllmv2_decode")
 
 
+def _check_host_step_buffers(q_host, kv_len_host, o_host, q_dev, kv_len_dev, o_dev, lse_host, lse_dev, Hkv):
+    """The host-buffer decode copies B*Hq*d bf16 values of q and o, B int32 lengths and B*Hq fp32
+    lse values between the paired tensors: check their types and sizes once, so a wrong tensor
+    raises here instead of overrunning memory in the C call."""
+    import torch
+    B, Hq, d = q_host.shape[0], q_host.shape[-2], q_host.shape[-1]
+    n = B * Hq * d
+    for name, t in (("q_host", q_host), ("q_dev", q_dev), ("o_host", o_host), ("o_dev", o_dev)):
+        if t.dtype != torch.bfloat16 or t.numel() != n:
+            raise ValueError(f"{name} must be bf16 with {n} elements (B * Hq * d)")
+    for name, t in (("kv_len_host", kv_len_host), ("kv_len_dev", kv_len_dev)):
+        if t.dtype != torch.int32 or t.numel() != B:
+            raise ValueError(f"{name} must be int32 with {B} elements (B)")
+    if (lse_host is None) != (lse_dev is None):
+        raise ValueError("lse_host and lse_dev must be given together")
+    for name, t in (("lse_host", lse_host), ("lse_dev", lse_dev)):
+        if t is not None and (t.dtype != torch.float32 or t.numel() != B * Hq):
+            raise ValueError(f"{name} must be fp32 with {B * Hq} elements (B * Hq)")
+    if Hkv <= 0 or Hq % Hkv != 0:
+        raise ValueError("Hq must be a multiple of the caches' KV heads")
+
+
 def decode_host(q_host, kv_len_host, o_host, q_dev, kv_len_dev, o_dev, k_cache, v_cache, kernel_cache,
                 workspace, params, lse_host=None, lse_dev=None, stream=None):
     """One single-token decode step with q, kv_len and o in host memory (pinned for asynchronous
@@ -315,6 +337,7 @@ def decode_host(q_host, kv_len_host, o_host, q_dev, kv_len_dev, o_dev, k_cache, 
     B, Hq, d = q_host.shape[0], q_host.shape[-2], q_host.shape[-1]
     Hkv, L_max = k_cache.shape[1], k_cache.shape[2]
     M_max = kernel_cache.shape[2]
+    _check_host_step_buffers(q_host, kv_len_host, o_host, q_dev, kv_len_dev, o_dev, lse_host, lse_dev, Hkv)
     _check(load().infllmv2_decode_host(_host_ptr(q_host), _host_ptr(kv_len_host), _host_ptr(o_host),
                                        _host_ptr(lse_host), _ptr(q_dev), _ptr(kv_len_dev), _ptr(o_dev),
                                        _ptr(lse_dev), _ptr(k_cache), _ptr(v_cache), _ptr(kernel_cache), B, Hq, Hkv,
@@ -332,6 +355,7 @@ class DecodeHostStep:
                  workspace, params, lse_host=None, lse_dev=None, stream=None):
         B, Hq, d = q_host.shape[0], q_host.shape[-2], q_host.shape[-1]
         Hkv, L_max = k_cache.shape[1], k_cache.shape[2]
+        _check_host_step_buffers(q_host, kv_len_host, o_host, q_dev, kv_len_dev, o_dev, lse_host, lse_dev, Hkv)
         self._fn = load().infllmv2_decode_host
         self._params = Params.make(params)
         self._args = (_host_ptr(q_host), _host_ptr(kv_len_host), _host_ptr(o_host), _host_ptr(lse_host), _ptr(q_dev),

@@ -131,8 +131,9 @@ size_t infllmv2_workspace_size(int entry, int B, int Tq, int Hq, int Hkv, int d,
  * for every kernel j whose last token lies in [tok_begin, tok_end) -- that is,
  * the kernels that become complete once tokens [tok_begin, tok_end) are in the
  * cache.  Call it after appending tokens (a prefill chunk, or each decode token;
- * a new kernel completes every `stride` tokens).  Sums are exact (fp64) and
- * rounded to bf16 once, nearest-even.
+ * a new kernel completes every `stride` tokens).  Sums are exact -- integer
+ * fixed-point sums of the bf16 inputs under a shared per-column exponent -- and
+ * the mean is rounded to bf16 once, nearest-even.
  * Requires 0 <= tok_begin <= tok_end <= L_max and
  * M_max >= (tok_end - kernel_size)/kernel_stride + 1.  Other kernels are untouched.
  */

@@ -133,3 +133,30 @@ def test_decode_host_checks_before_enqueueing(built_lib):
     assert call(ws_bytes=16) == infllmv2.ERR_WORKSPACE
     assert call(d=96) == infllmv2.ERR_UNSUPPORTED
     assert call(params=_params(topk=-1)) == infllmv2.ERR_INVALID_ARG
+
+
+def test_decode_host_binding_checks_types_and_sizes():
+    """The binding refuses staging tensors whose type or size would make the C call copy past them
+    (checked before any pointer is taken, so CPU tensors stand in here)."""
+    torch = pytest.importorskip("torch")
+    B, Hq, d = 2, 32, 128
+    good = dict(q_host=torch.empty((B, Hq, d), dtype=torch.bfloat16),
+                kv_len_host=torch.empty(B, dtype=torch.int32),
+                o_host=torch.empty((B, Hq, d), dtype=torch.bfloat16),
+                q_dev=torch.empty((B, Hq, d), dtype=torch.bfloat16),
+                kv_len_dev=torch.empty(B, dtype=torch.int32),
+                o_dev=torch.empty((B, Hq, d), dtype=torch.bfloat16),
+                lse_host=torch.empty((B, Hq), dtype=torch.float32),
+                lse_dev=torch.empty((B, Hq), dtype=torch.float32))
+    infllmv2._check_host_step_buffers(Hkv=2, **good)
+    bad_cases = [("o_host", torch.empty((B, Hq, d), dtype=torch.float32)),
+                 ("q_dev", torch.empty((B, Hq, d // 2), dtype=torch.bfloat16)),
+                 ("kv_len_host", torch.empty(B, dtype=torch.int64)),
+                 ("kv_len_dev", torch.empty(B + 1, dtype=torch.int32)),
+                 ("lse_host", torch.empty((B, Hq), dtype=torch.float16)),
+                 ("lse_dev", None)]
+    for name, t in bad_cases:
+        with pytest.raises(ValueError):
+            infllmv2._check_host_step_buffers(Hkv=2, **dict(good, **{name: t}))
+    with pytest.raises(ValueError):
+        infllmv2._check_host_step_buffers(Hkv=3, **good)

@@ -125,3 +125,38 @@ def test_bwd_full_chunk_32k_sampled(cuda_lib):
         got.append(dq_gpu[:, t])
         ref.append(rq[:, 0])
     _check("dq (sampled tokens)", np.stack(got), np.stack(ref))
+
+
+def test_bwd_group16_many_units_per_cta(cuda_lib):
+    """A chunk whose inverse selection holds several times as many work units (a block and up to
+    128 of the tokens that chose it) as the GPU has SMs, so every persistent CTA of the tensor-core
+    gradient kernel takes several units in turn (TMEM, barrier phases and the dK/dV reductions
+    carried from unit to unit).  dq, dk and dv are compared element by element with the oracle;
+    the softmax identity sum_k dV = sum dO is checked beside them."""
+    torch = torch_mod()
+    w = synth.WORKLOADS["chunked_prefill_32k"].scaled(B=4, L=8192, Tq=256, Hq=64, Hkv=4, d=128, block_size=128,
+                                                       topk=16, n_local=4, dense_len=0, seed=4500)
+    inp = synth.make_inputs(w)
+    inp["kv_len"] = np.array([8192, 7000, 8192 - 37, 6500], dtype=np.int32)
+    p = w.params()
+    g, dq, dk, dv, dout_bits = _gpu_bwd(w, inp)
+    gidx, gcnt = g["idx"].cpu().numpy(), g["counts"].cpu().numpy()
+    # work units: per (sequence, KV head, block), the tokens that chose it in slices of 128
+    units = 0
+    for b in range(w.B):
+        for gg in range(w.Hkv):
+            per_block = np.bincount(np.concatenate([gidx[b, gg, t, :gcnt[b, gg, t]] for t in range(w.Tq)]))
+            units += int(np.sum((per_block + 127) // 128))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert units >= 3 * sms, (units, sms)
+    dout = _bf16_as_f64(dout_bits)
+    rq, rk, rv = oracle.attention_bwd(_bf16_as_f64(inp["q"]), _bf16_as_f64(inp["k_cache"]),
+                                      _bf16_as_f64(inp["v_cache"]), inp["kv_len"], gidx, gcnt, p, dout)
+    _check("dq", dq.cpu().numpy().astype(np.float64), rq)
+    _check("dk", dk.cpu().numpy().astype(np.float64), rk)
+    _check("dv", dv.cpu().numpy().astype(np.float64), rv)
+    G = w.Hq // w.Hkv
+    dv_sum = dv.double().sum(dim=2).cpu().numpy()
+    do_sum = dout.reshape(w.B, w.Tq, w.Hkv, G, w.d).sum(axis=(1, 3))
+    do_abs = np.abs(dout).reshape(w.B, w.Tq, w.Hkv, G, w.d).sum(axis=(1, 3))
+    assert np.all(np.abs(dv_sum - do_sum) <= 4e-3 * do_abs + 1e-3)
