@@ -10,12 +10,16 @@
 // CTAs (one per SM) takes the whole row and keeps every intermediate in shared memory:
 //   1. CTA r scores the blocks [r*CB, (r+1)*CB): TMA copies of their kernel rows (issued before
 //      the cache length is read, for the longest cache), warp MMAs q.k for the G heads, max over
-//      the heads, then over the kernels overlapping each block -> its order-preserving keys,
-//      which bulk copies put into every peer's shared memory (counted on the peer's barrier).
-//   2. Every CTA computes the same selection from all of the row's keys: forced initial and
-//      local blocks, and the top-k of the others (a threshold from block-wide counts, then an
-//      exact ranking of the few keys above it; ties go to the lower block), or every block below
-//      dense_len.  The forced blocks' K and V are brought towards L2 at the start, the few
+//      the heads, then over the kernels overlapping each block -> its order-preserving keys.
+//      Keys and lists travel by bulk copies into the peers' shared memory (counted on the
+//      receiving CTA's barrier).
+//   2. Every CTA computes the same selection: forced initial and local blocks, and the top-k of
+//      the others (ties go to the lower block), or every block below dense_len.  Each CTA sorts
+//      its blocks' keys and sends its best 16 to every peer; every candidate of those lists finds
+//      its exact rank in the row by binary searches in the other lists.  That decides the top-k
+//      unless some CTA holds 16 or more of it; then (and for rows the lists do not cover) the
+//      CTAs exchange all their keys and a threshold from block-wide counts plus an exact ranking
+//      of the few keys above it decides.  The forced blocks' K and V are brought towards L2 at the start, the few
 //      candidates' while they are ranked (bulk prefetches), and before the programmatic wait the
 //      CTA prefetches its q and kernel rows: a prefetch reads no value.
 //   3. CTA r attends to the selected blocks r, r+CL, ...: TMA copies of their K and V, the
@@ -42,6 +46,7 @@ constexpr int kDcMaxSel = 4096;   // selection capacity covered (the list lives 
 constexpr int kDcMaxPer = 16;     // keys per thread in the selection: rows of up to 4096 blocks
 constexpr int kDcCand = 384;      // candidates ranked exactly after the pre-threshold
 constexpr int kDcFastPer = 8;     // strided keys per thread on the fast selection path (<= 2048 blocks)
+constexpr int kDcLT = 16;         // best candidates of each CTA sent to every peer (the list path)
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -77,6 +82,46 @@ __device__ __forceinline__ void prefetch_l2_line(const void* p) {
 __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
                  : "memory");
+}
+// Sort one 64-bit value per lane of the warp, largest first (a bitonic network over shuffles).
+__device__ __forceinline__ unsigned long long warp_sort_desc64(unsigned long long v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, j);
+            const bool keep_max = ((lane & k) == 0) == ((lane & j) == 0);
+            v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
+        }
+    return v;
+}
+__device__ __forceinline__ unsigned long long lds_u64(uint32_t addr) {
+    unsigned long long v;
+    asm("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(addr));
+    return v;
+}
+// Number of entries greater than x in the lists l < n_lists, l != skip, of 16 values each (sorted
+// largest first, 128 bytes apart from shared address `base`; all NL lists lie in shared memory):
+// binary searches advanced in lockstep, every load unconditional and every step a select, so the
+// NL searches are independent chains without branches (lanes of a warp differ in `skip`).
+template <int NL>
+__device__ __forceinline__ int count_greater_lists(uint32_t base, int n_lists, int skip, unsigned long long x) {
+    int pos[NL];
+#pragma unroll
+    for (int l = 0; l < NL; ++l) pos[l] = 0;
+#pragma unroll
+    for (int step = 8; step >= 1; step >>= 1)
+#pragma unroll
+        for (int l = 0; l < NL; ++l) pos[l] += lds_u64(base + 128u * l + 8u * (pos[l] + step - 1)) > x ? step : 0;
+    int total = 0;
+#pragma unroll
+    for (int l = 0; l < NL; ++l) {
+        const bool last_greater = lds_u64(base + 128u * l + 120u) > x;
+        const int c = pos[l] + ((pos[l] == 15) & last_greater ? 1 : 0);
+        total += (l < n_lists && l != skip) ? c : 0;
+    }
+    return total;
 }
 // Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from this CTA's shared
 // memory to a cluster address (a peer's shared memory); completion is counted in bytes on the
@@ -155,6 +200,11 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     __shared__ uint32_t s_tau[2];                          // threshold, and whether k maxima are nonzero
     __shared__ int s_nc;                                   // candidates compacted so far
     __shared__ uint64_t s_bar_piece[kDcKRows / 128];       // scoring: kernel rows of piece p landed
+    __shared__ __align__(16) unsigned long long s_wtop[kDcThreads / 32][kDcLT];  // each warp's best, sorted
+    __shared__ __align__(16) unsigned long long s_gcand[16][kDcLT];  // CTA r's best, sorted (filled by CTA r)
+    __shared__ int s_grk[16 * kDcLT];                      // their ranks in the row
+    __shared__ uint64_t s_bar_cand;                        // the peers' lists have landed
+    __shared__ int s_lt_fail;                              // some CTA may hold more of the top-k than it sent
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, cq = lane & 3;
@@ -177,11 +227,14 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
         for (int k = 0; k < kDcKRows / 128; ++k) mbar_init(&s_bar_piece[k], 1);
         mbar_init(bar_keys, 1);
         mbar_init(bar_part, 1);
+        mbar_init(&s_bar_cand, 1);
         fence_mbar_init();
         uint32_t in_keys = 0;
         for (int j = 0; j < ncta; ++j)
             if (j != static_cast<int>(rank)) in_keys += key_bytes(j);
         mbar_arrive_expect_tx(bar_keys, in_keys);
+        mbar_arrive_expect_tx(&s_bar_cand, static_cast<uint32_t>((ncta - 1) * kDcLT * 8));
+        s_lt_fail = 0;
         mbar_arrive_expect_tx(bar_part, static_cast<uint32_t>(nh * ncta * kPRow * 4));
     }
     if (tid < 12) (&s_cnt[0][0])[tid] = 0;
@@ -356,19 +409,70 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
         __syncthreads();  // tiles and ks free for the next pass
         if (sub0 + sh.SC < blkA1) issue_pass(sub0 + sh.SC);
     }
-    // this CTA's keys -> every peer: bulk copies into the same offsets of the peers' shared memory,
-    // counted on their key barriers; then wait for the peers' keys
+    // The row's selection parameters (the same in every CTA of the cluster)
+    const int n = bt + 1;
+    const int a_init = min(p.n_init, max(n, 0));
+    const int lo_local = max(bt - p.n_local + 1, 0);
+    const int n_forced = len_ok ? a_init + (n - max(lo_local, a_init)) : 0;
+    const int nc = n - n_forced;
+    const bool take_all = len_ok && (dense || nc <= p.topk);
+    const bool select = len_ok && !take_all && p.topk > 0;
+    const int nn = max(n, 0);
+    const int lo_f = max(lo_local, a_init);  // first local block not already an initial one
+    // the list path (below) decides from the CTAs' lists alone; the keys travel only without it
+    const bool list_path = select && sh.CB <= kDcThreads && p.topk < ncta * kDcLT &&
+                           nn <= kDcFastPer * kDcThreads;  // (s_bits: 2048 blocks)
+    // This CTA's best candidates: the kDcLT largest of its blocks' 64-bit values key << 32 | ~block
+    // (0: not a candidate; larger = better, ties to the lower block), sorted: each warp sorts 32 of
+    // them, then each of the warps' kDcLT best finds its rank among the warps' lists by binary
+    // searches.  The lists of all CTAs decide the row's top-k exactly unless some CTA holds more of
+    // it than it sent (checked below).
+    unsigned long long* my_cand = &s_gcand[rank][0];
+    if (tid < kDcLT) my_cand[tid] = 0ull;
+    if (list_path) {  // (one block per thread: CB <= 256)
+        const int blk = blkA0 + tid;
+        unsigned long long v = 0ull;
+        if (len_ok && !dense && blk < blkA1 && blk <= bt && !forced(blk)) {
+            const uint32_t kk = keys[blk];
+            if (kk != 0u) v = (static_cast<unsigned long long>(kk) << 32) | static_cast<uint32_t>(~blk);
+        }
+        v = warp_sort_desc64(v);
+        if (lane < kDcLT) s_wtop[warp][lane] = v;
+    }
+    __syncthreads();
+    if (list_path && tid < (kDcThreads / 32) * kDcLT) {
+        const int w0 = tid / kDcLT;
+        const unsigned long long x = s_wtop[w0][tid % kDcLT];
+        const int r = tid % kDcLT + count_greater_lists<kDcThreads / 32>(smem_u32(&s_wtop[0][0]), kDcThreads / 32, w0, x);
+        if (x != 0ull && r < kDcLT) my_cand[r] = x;
+    }
+    // this CTA's list (and, without the list path, its keys) -> every peer: bulk copies into the
+    // same offsets of the peers' shared memory, counted on their barriers
     fence_proxy_async_shared();
     __syncthreads();
     cluster_wait();
-    if (warp == 0) {  // lane j copies to peer j
+    auto send_keys = [&]() {  // by warp 0: lane j copies to peer j
         const uint32_t nb = key_bytes(static_cast<int>(rank));
         if (nb > 0 && lane < ncta && lane != static_cast<int>(rank))
             bulk_copy_to_peer(dsmem_addr(keys_base + 4u * blkA0, lane), keys_base + 4u * blkA0, nb,
                               dsmem_addr(smem_u32(bar_keys), lane));
+    };
+    if (warp == 0) {
+        if (lane < ncta && lane != static_cast<int>(rank))
+            bulk_copy_to_peer(dsmem_addr(smem_u32(my_cand), lane), smem_u32(my_cand), kDcLT * 8,
+                              dsmem_addr(smem_u32(&s_bar_cand), lane));
+        if (!list_path) send_keys();
         bulk_commit();
     }
-    if (!mbar_wait(bar_keys, 0) && tid == 0) raise_error(err, kDevErrTimeout);
+    bool keys_sent = !list_path, keys_in = false, cand_in = false;  // (uniform over the cluster)
+    auto wait_keys = [&]() {
+        if (keys_sent && !keys_in && !mbar_wait(bar_keys, 0) && tid == 0) raise_error(err, kDevErrTimeout);
+        keys_in = true;
+    };
+    auto wait_cand = [&]() {
+        if (!cand_in && !mbar_wait(&s_bar_cand, 0) && tid == 0) raise_error(err, kDevErrTimeout);
+        cand_in = true;
+    };
 
     // ================= 2. the row's selection, computed by every CTA from all the keys
     int count = 0;
@@ -376,6 +480,8 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     // from r_lof; otherwise sel[] in block order
     bool by_rank = false;
     int r_ainit = 0, r_lof = 0, r_k = 0, r_nc = 0, r_nn = 0;
+    const unsigned long long* r_cv = s_cv;  // the ranked candidates (value, rank) of the fast paths
+    const int* r_rk = s_rk;
     auto list_blk = [&](int e) {
         if (!by_rank) return sel[e];
         if (e < r_ainit) return e;
@@ -383,18 +489,64 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
         return r_lof + (e - r_ainit - r_k);
     };
     {
-        const int n = bt + 1;
-        const int a_init = min(p.n_init, max(n, 0));
-        const int lo_local = max(bt - p.n_local + 1, 0);
-        const int n_forced = len_ok ? a_init + (n - max(lo_local, a_init)) : 0;
-        const int nc = n - n_forced;
-        const bool take_all = len_ok && (dense || nc <= p.topk);
-        const bool select = len_ok && !take_all && p.topk > 0;
-        const int nn = max(n, 0);
-        const int lo_f = max(lo_local, a_init);  // first local block not already an initial one
         int total = 0;
         bool done = false;
-        if (select && nn <= kDcFastPer * kDcThreads && p.topk <= kDcThreads) {
+        if (list_path) {
+            // List path.  While the lists travel, this CTA's likely share of the chosen blocks (its
+            // best ceil(k * blocks here / blocks) candidates) goes towards L2 ahead of the attention's
+            // copies.  Then every candidate of the lists finds its rank in the row by binary
+            // searches in the other lists; ranks below k are the chosen ones.  A CTA that sent a full
+            // list whose last entry is chosen may hold more chosen blocks than it sent: then the
+            // threshold path below decides from all the keys instead (sent now, by every CTA).
+            const int k = p.topk;
+            const int mine = max(0, min(blkA1, nn) - blkA0);
+            const int n_pf = min(kDcLT, (k * mine + nn - 1) / max(nn, 1));
+            if (tid >= 32 && tid < 32 + 2 * n_pf) {
+                const unsigned long long x = my_cand[(tid - 32) >> 1];
+                if (x != 0ull) {
+                    const int blk = static_cast<int>(~static_cast<uint32_t>(x));
+                    const size_t off = (static_cast<size_t>(row) * L_max + static_cast<size_t>(blk) * BS) * D;
+                    bulk_prefetch_l2((tid & 1) ? vc + off : kc + off, static_cast<uint32_t>(min(BS, L - blk * BS) * D * 2));
+                }
+            }
+            wait_cand();
+            const int n_all = ncta * kDcLT;
+            if (tid < n_all) {
+                const int r0 = tid / kDcLT, p0 = tid % kDcLT;
+                const unsigned long long x = s_gcand[r0][p0];
+                int rk = 0x7fffffff;
+                if (x != 0ull) {
+                    rk = p0 + count_greater_lists<16>(smem_u32(&s_gcand[0][0]), ncta, r0, x);
+                    if (rk < k) {
+                        s_byrank[rk] = static_cast<int>(~static_cast<uint32_t>(x));
+                        if (p0 == kDcLT - 1) s_lt_fail = 1;
+                    }
+                }
+                s_grk[tid] = rk;
+            }
+            for (int i3 = tid; i3 < kDcFastPer * kDcThreads / 32; i3 += kDcThreads) s_bits[i3] = 0u;
+            __syncthreads();
+            if (s_lt_fail == 0) {
+                total = a_init + k + (nn - lo_f);
+                done = true;
+                by_rank = true;
+                r_ainit = a_init;
+                r_lof = lo_f;
+                r_k = k;
+                r_nc = n_all;
+                r_cv = &s_gcand[0][0];
+                r_rk = s_grk;
+                r_nn = nn;
+            } else {
+                if (warp == 0) {
+                    send_keys();
+                    bulk_commit();
+                }
+                keys_sent = true;
+            }
+        }
+        if (!done && select && nn <= kDcFastPer * kDcThreads && p.topk <= kDcThreads) {
+            wait_keys();
             // Fast path.  tau = the k-th largest of the threads' maxima over the strided keys
             // t, t + 256, ... (neighbouring blocks have correlated scores: a stride spreads each
             // thread over the row), found bit by bit by one warp.  At least k keys are >= tau and,
@@ -532,6 +684,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
             __syncthreads();
         }
         if (!done) {
+            wait_keys();
             // General path: thread t holds the keys of blocks [t*per, t*per + per); the k-th
             // largest key T is decided two bits per round from block-wide counts; the list is
             // compacted in block order.
@@ -712,8 +865,8 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     bool lists_pending = by_rank && static_cast<int>(rank) == ncta - 1 && idx_out != nullptr;
     auto write_lists = [&]() {
         for (int i = tid; i < r_nc; i += kDcThreads)
-            if (s_rk[i] < r_k) {
-                const uint32_t blk = ~static_cast<uint32_t>(s_cv[i]);
+            if (r_rk[i] < r_k) {
+                const uint32_t blk = ~static_cast<uint32_t>(r_cv[i]);
                 atomicOr(&s_bits[blk >> 5], 1u << (blk & 31));
             }
         __syncthreads();
@@ -731,8 +884,8 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
         __syncthreads();
         int* out = idx_out + static_cast<size_t>(row) * idx_stride;
         for (int i = tid; i < r_nc; i += kDcThreads)
-            if (s_rk[i] < r_k) {
-                const uint32_t blk = ~static_cast<uint32_t>(s_cv[i]);
+            if (r_rk[i] < r_k) {
+                const uint32_t blk = ~static_cast<uint32_t>(r_cv[i]);
                 const int at = r_ainit + s_wpre[blk >> 5] + __popc(s_bits[blk >> 5] & ((1u << (blk & 31)) - 1u));
                 if (at < count) out[at] = static_cast<int>(blk);
             }
@@ -746,6 +899,9 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
     };
     // second half-barrier: this CTA no longer reads its keys or scores (and its copies of its keys
     // have been read), whose memory takes the peers' partials after the attention
+    // (and every peer's copies into this CTA's keys and lists have landed)
+    wait_keys();
+    wait_cand();
     if (warp == 0) bulk_wait_read_all();
     cluster_arrive_relaxed();
 
