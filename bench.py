@@ -553,10 +553,11 @@ def run_decode_e2e(d, n: int) -> dict:
     d2h = o_host.numel() * o_host.element_size() + lse_host.numel() * lse_host.element_size()
     return {"value": w.B * w.Tq / statistics.mean(times), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * statistics.mean(times),
-            "note": "wall clock per step of infllmv2_decode_host through the binding's prepared call (q and "
-                    "lengths copied in from pinned host memory, one decode launch, o and lse copied out, the "
-                    "device error word read, the stream waited for); replicas cycled; KV and kernel caches "
-                    "resident"}
+            "note": "wall clock per step of infllmv2_decode_host through the binding's prepared call: q and the "
+                    "lengths come from page-locked host memory and o and lse go back to it (the decode kernel "
+                    "reads and writes those mapped host buffers directly, over NVLink-C2C on this Grace host: "
+                    "one launch, its error word in page-locked host memory, one wait); replicas cycled; KV and "
+                    "kernel caches resident"}
 
 
 # ------------------------------------------------------------------ prefill (secondary)

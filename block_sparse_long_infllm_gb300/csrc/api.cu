@@ -40,6 +40,46 @@ int* device_error_ptr() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The device-side address of a host buffer that is page-locked and mapped into the device's
+// address space (cudaHostAlloc / cudaMallocHost / cudaHostRegister with mapping), else nullptr.
+void* mapped_host(const void* p) {
+    if (p == nullptr) return nullptr;
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+// This host thread's page-locked, mapped error word (allocated on first use, kept until the process
+// exits): the zero-copy host-buffer decode gives it to its kernel and reads it back after the wait.
+// *dev receives its address on the current device.
+volatile int* host_error_word(int** dev) {
+    thread_local int* word = nullptr;
+    thread_local int* word_dev[kMaxDevices] = {};
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur < 0 || cur >= kMaxDevices) return nullptr;
+    if (word == nullptr) {
+        void* h = nullptr;
+        if (cudaHostAlloc(&h, 64, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        word = static_cast<int*>(h);
+    }
+    if (word_dev[cur] == nullptr) {
+        void* d = nullptr;
+        if (cudaHostGetDevicePointer(&d, word, 0) != cudaSuccess || d == nullptr) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        word_dev[cur] = static_cast<int*>(d);
+    }
+    *dev = word_dev[cur];
+    return word;
+}
+
 bool supported_group(int G) { return G == 1 || G == 2 || G == 4 || G == 8 || G == 16; }
 
 // Checks the parameter struct; fills the kernel-side copy (with the scale resolved for d).
@@ -436,7 +476,8 @@ static int decode_impl(bool launch, const void* q, const void* k_cache, const vo
                        const int32_t* kv_len, const void* draft_k, const void* draft_v, const uint64_t* tree_mask,
                        int B, int n_draft, int Hq, int Hkv, int d, int L_max, int M_max, void* o, float* lse,
                        int32_t* idx_out, int32_t* counts_out, int S_max, void* workspace, size_t ws_bytes,
-                       const infllmv2_params* params, void* stream);
+                       const infllmv2_params* params, void* stream, int* err_word = nullptr,
+                       bool cluster_only = false);
 
 int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache, const void* kernel_cache,
                     const int32_t* kv_len, const void* draft_k, const void* draft_v, const uint64_t* tree_mask,
@@ -458,9 +499,36 @@ int infllmv2_decode_host(const void* q_host, const int32_t* kv_len_host, void* o
         return rc;
     if (B == 0) return INFLLMV2_OK;
     if (q_host == nullptr || kv_len_host == nullptr || o_host == nullptr) return INFLLMV2_ERR_INVALID_ARG;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // Zero-copy: when every host buffer is page-locked and mapped (and 16-byte aligned), the
+    // single-kernel decode reads q and the lengths and writes o and lse straight through host
+    // memory (NVLink-C2C between Grace and the GPU), its errors go to this thread's page-locked
+    // error word, and the call is one launch and one wait.
+    {
+        void* qm = mapped_host(q_host);
+        void* km = qm != nullptr ? mapped_host(kv_len_host) : nullptr;
+        void* om = km != nullptr ? mapped_host(o_host) : nullptr;
+        void* lm = (om != nullptr && lse_host != nullptr) ? mapped_host(lse_host) : nullptr;
+        int* wd = nullptr;
+        volatile int* wh = (om != nullptr && (lse_host == nullptr || lm != nullptr)) ? host_error_word(&wd) : nullptr;
+        if (wh != nullptr && aligned16(qm) && aligned16(km) && aligned16(om) && (lm == nullptr || aligned16(lm))) {
+            *wh = 0;
+            const int rc = decode_impl(true, qm, k_cache, v_cache, kernel_cache, static_cast<const int32_t*>(km), nullptr,
+                                       nullptr, nullptr, B, 1, Hq, Hkv, d, L_max, M_max, om, static_cast<float*>(lm),
+                                       nullptr, nullptr, 0, workspace, ws_bytes, params, stream, wd, true);
+            if (rc != INFLLMV2_ERR_UNSUPPORTED) {
+                if (rc != INFLLMV2_OK) return rc;
+                if (cudaStreamSynchronize(st) != cudaSuccess) return INFLLMV2_ERR_CUDA;
+                const int word = *wh;
+                if (word != 0)
+                    return (word & infllmv2::kDevErrTimeout) ? INFLLMV2_ERR_DEVICE_TIMEOUT : INFLLMV2_ERR_DEVICE_INDEX;
+                return INFLLMV2_OK;
+            }
+        }
+    }
+    // Otherwise: the caller's device staging buffers, one copy per buffer each way.
     int* ep = device_error_ptr();
     if (ep == nullptr) return INFLLMV2_ERR_CUDA;
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t nq = static_cast<size_t>(B) * Hq * d * 2, nl = static_cast<size_t>(B) * Hq * sizeof(float);
     int rc = INFLLMV2_OK;
     if (cudaMemcpyAsync(q_dev, q_host, nq, cudaMemcpyHostToDevice, st) != cudaSuccess ||
@@ -536,11 +604,15 @@ int infllmv2_decode_step(const void* q, const void* k_new, const void* v_new, vo
 }
 
 // infllmv2_decode's body; with launch == false it only checks the arguments (no CUDA call).
+// err_word: the error word the kernels set (default: the library's device word).  cluster_only:
+// return INFLLMV2_ERR_UNSUPPORTED (having launched nothing) unless the single-kernel decode covers
+// the call -- the zero-copy host path uses it, because that kernel reads q and the lengths and
+// writes o and lse with plain loads and stores only.
 static int decode_impl(bool launch, const void* q, const void* k_cache, const void* v_cache, const void* kernel_cache,
                        const int32_t* kv_len, const void* draft_k, const void* draft_v, const uint64_t* tree_mask,
                        int B, int n_draft, int Hq, int Hkv, int d, int L_max, int M_max, void* o, float* lse,
                        int32_t* idx_out, int32_t* counts_out, int S_max, void* workspace, size_t ws_bytes,
-                       const infllmv2_params* params, void* stream) {
+                       const infllmv2_params* params, void* stream, int* err_word, bool cluster_only) {
     Params p;
     if (int rc = check_params(params, d, &p)) return rc;
     if (int rc = check_heads(Hq, Hkv, d)) return rc;
@@ -565,7 +637,7 @@ static int decode_impl(bool launch, const void* q, const void* k_cache, const vo
     const DecodeWs w = decode_ws(B, n_draft, Hkv, d, L_max, p);
     if (workspace == nullptr || ws_bytes < w.total || !aligned16(workspace)) return INFLLMV2_ERR_WORKSPACE;
     if (!launch) return INFLLMV2_OK;
-    int* err = device_error_ptr();
+    int* err = err_word != nullptr ? err_word : device_error_ptr();
     if (err == nullptr) return INFLLMV2_ERR_CUDA;
     char* ws = static_cast<char*>(workspace);
     int* idx = idx_out != nullptr ? idx_out : reinterpret_cast<int*>(ws + w.idx);
@@ -574,6 +646,7 @@ static int decode_impl(bool launch, const void* q, const void* k_cache, const vo
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     infllmv2::DecodeArgs da{q, k_cache, v_cache, kv_len, draft_k, draft_v, tree_mask, B, n_draft, Hq, Hkv, d, L_max,
                             o, lse, p, err, st};
+    if (cluster_only && !infllmv2::decode_cluster_supported(da, M_max)) return INFLLMV2_ERR_UNSUPPORTED;
     prof_begin(st);
     if (infllmv2::decode_cluster_supported(da, M_max)) {
         const cudaError_t e = infllmv2::launch_decode_cluster(da, kernel_cache, M_max, idx_out, S_max, counts_out);
@@ -582,6 +655,7 @@ static int decode_impl(bool launch, const void* q, const void* k_cache, const vo
             return cuda_status(e);
         }
         (void)cudaGetLastError();  // not launched: take the separate kernels
+        if (cluster_only) return INFLLMV2_ERR_UNSUPPORTED;
     }
     infllmv2::SelectArgs sa{q, kernel_cache, kv_len, B, n_draft, Hq, Hkv, d, L_max, M_max, tree ? 1 : 0, idx, counts,
                             stride, blocks_per_score_cta(p), p, err, st};

@@ -288,19 +288,30 @@ int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache,
 
 /*
  * infllmv2_decode of one single-token step whose query, cache lengths and
- * output live in host memory: copies q_host [B, Hq, d] bf16 to q_dev and
- * kv_len_host [B] to kv_len_dev on `stream` (cudaMemcpyAsync, one per buffer;
- * page-locked host memory keeps them asynchronous), decodes q_dev over the
- * resident caches into o_dev (and lse_dev, when not NULL), copies o_dev back to
- * o_host (and lse_dev [B, Hq] fp32 to lse_host, when not NULL), reads the device
- * error word in the same round trip and waits for the stream.  On return the
- * host output is complete.  q_dev, kv_len_dev, o_dev, lse_dev are the caller's
- * device staging buffers (16-byte aligned; the library allocates nothing);
- * the other arguments are those of infllmv2_decode (n_draft = 1, no selection
- * output).  Arguments are checked before anything is enqueued.  Returns the
- * first of: an argument error, infllmv2_decode's status, INFLLMV2_ERR_CUDA for
- * a failed copy or wait, and the device error word (as infllmv2_sync_status,
- * which clears it).
+ * output live in host memory: q_host [B, Hq, d] bf16 and kv_len_host [B] in,
+ * o_host [B, Hq, d] bf16 (and lse_host [B, Hq] fp32, when not NULL) out; on
+ * return the host output is complete.  Two ways, chosen per call:
+ *   - zero-copy: when every host buffer is page-locked and mapped into the
+ *     device's address space (cudaHostAlloc / cudaMallocHost, or registered
+ *     with mapping; 16-byte aligned) and the single-kernel decode covers the
+ *     shape, that kernel reads q and the lengths and writes o and lse straight
+ *     through host memory (on a Grace host, over NVLink-C2C); device errors go
+ *     to a page-locked error word of the calling host thread (allocated on its
+ *     first such call, kept until the process exits); one launch and one wait.
+ *     The staging buffers are not touched.
+ *   - staged: otherwise q and kv_len are copied to the caller's device staging
+ *     buffers q_dev, kv_len_dev on `stream` (cudaMemcpyAsync, one per buffer),
+ *     infllmv2_decode runs on them into o_dev (and lse_dev), o and lse are
+ *     copied back, the device error word is read in the same round trip and
+ *     the stream is waited for.
+ * q_dev, kv_len_dev, o_dev, lse_dev are the caller's device staging buffers
+ * (16-byte aligned; lse_dev is required when lse_host is given; the library
+ * allocates no device memory); the other arguments are those of
+ * infllmv2_decode (n_draft = 1, no selection output).  Arguments are checked
+ * before anything is enqueued.  Returns the first of: an argument error,
+ * infllmv2_decode's status, INFLLMV2_ERR_CUDA for a failed copy or wait, and
+ * the call's device error (INFLLMV2_ERR_DEVICE_INDEX or _TIMEOUT; the staged
+ * way reads and clears the device error word as infllmv2_sync_status does).
  */
 int infllmv2_decode_host(const void* q_host, const int32_t* kv_len_host, void* o_host, float* lse_host,
                          void* q_dev, int32_t* kv_len_dev, void* o_dev, float* lse_dev,

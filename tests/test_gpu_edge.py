@@ -355,3 +355,37 @@ def test_decode_host_reports_device_errors(cuda_lib):
     good = torch.from_numpy(inp["kv_len"]).pin_memory()
     L.decode_host(q_host, good, o_host, q_dev, kv_dev, o_dev, k, v, kern, ws, p)
     assert L.sync_status() == 0
+
+
+def test_decode_host_pageable_buffers_take_the_staged_copies(cuda_lib):
+    # pageable host buffers cannot be read by a kernel: the call stages them through the caller's
+    # device buffers and gives the same bits as the device-buffer call (and as the zero-copy call
+    # on page-locked buffers)
+    import torch
+    w = synth.WORKLOADS["decode_128k_b4"].scaled(B=2, L=16384, seed=3900)
+    inp = synth.make_inputs(w)
+    g = run_gpu(w, inp)
+    L = lib()
+    p = w.params()
+    ws = torch.empty(L.workspace_size(L.ENTRY_DECODE, w.B, w.Tq, w.Hq, w.Hkv, w.d, w.L_max, p),
+                     dtype=torch.uint8, device="cuda")
+    ref_o = g["o"].view(w.B, w.Hq, w.d).cpu().view(torch.int16)
+    ref_lse = g["lse"].view(w.B, w.Hq).cpu()
+    for pinned in (False, True):
+        q_host = g["q"].view(w.B, w.Hq, w.d).cpu()
+        kv_host = g["kv_len"].cpu()
+        o_host = torch.zeros((w.B, w.Hq, w.d), dtype=torch.bfloat16)
+        lse_host = torch.zeros((w.B, w.Hq), dtype=torch.float32)
+        if pinned:
+            q_host, kv_host, o_host, lse_host = (t.pin_memory() for t in (q_host, kv_host, o_host, lse_host))
+        q_dev = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+        kv_dev = torch.empty_like(g["kv_len"])
+        o_dev = torch.full_like(q_dev, float("nan"))
+        lse_dev = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+        L.decode_host(q_host, kv_host, o_host, q_dev, kv_dev, o_dev, g["k"], g["v"], g["kern"], ws, p,
+                      lse_host=lse_host, lse_dev=lse_dev)
+        assert torch.equal(o_host.view(torch.int16), ref_o), f"pinned={pinned}"
+        assert torch.equal(lse_host, ref_lse), f"pinned={pinned}"
+        # the staged call used the staging buffers; the zero-copy one left them alone
+        assert bool(torch.isnan(o_dev.float()).any()) == pinned
+    assert L.sync_status() == 0
