@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build", "infllmv2")
 LIB_PATH = os.path.join(HERE, "libinfllmv2.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "kernel_pool.cu", "select.cu", "decode.cu", "prefill.cu", "decode_noalloc.cu", "tmap.cu", "prefill_tc.cu", "score_tc.cu", "decode_cluster.cu", "bwd.cu", "bwd_tc.cu"]
+SOURCES = ["api.cu", "kernel_pool.cu", "select.cu", "decode.cu", "prefill.cu", "decode_noalloc.cu", "tmap.cu", "prefill_tc.cu", "score_tc.cu", "decode_cluster.cu", "bwd.cu", "bwd_tc.cu", "tree_attn.cu"]
 
 
 def _nvcc() -> str:

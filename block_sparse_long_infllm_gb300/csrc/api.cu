@@ -660,6 +660,8 @@ static int decode_impl(bool launch, const void* q, const void* k_cache, const vo
     infllmv2::SelectArgs sa{q, kernel_cache, kv_len, B, n_draft, Hq, Hkv, d, L_max, M_max, tree ? 1 : 0, idx, counts,
                             stride, blocks_per_score_cta(p), p, err, st};
     if (int rc = cuda_status(infllmv2::launch_block_select(sa, reinterpret_cast<float*>(ws + w.scores)))) return rc;
+    if (tree && infllmv2::tree_attention_supported(da))
+        return cuda_status(infllmv2::launch_tree_attention(da, idx, counts, stride));
     return cuda_status(
         infllmv2::launch_decode_attention(da, idx, counts, stride, reinterpret_cast<float*>(ws + w.part)));
 }

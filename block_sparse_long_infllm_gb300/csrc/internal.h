@@ -145,6 +145,10 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, const BwdTcWork& w);
 
 cudaError_t launch_decode_attention(const DecodeArgs& a, const int* idx, const int* counts, int idx_stride,
                                     float* part);
+// Tree verification's attention (draft tree, uint64 masks) with one thread-block cluster per
+// (sequence, KV head, draft) row merging in shared memory: o and lse written directly.
+bool tree_attention_supported(const DecodeArgs& a);
+cudaError_t launch_tree_attention(const DecodeArgs& a, const int* idx, const int* counts, int idx_stride);
 
 // Single-token decode (no draft tree) with one thread-block cluster per row: scores, selection,
 // attention and merge, every intermediate in shared memory.  cudaErrorNotSupported when the
