@@ -277,12 +277,12 @@ __device__ __forceinline__ bool is_forced(int blk, int bt, const Params& p) {
 
 // Top-k selection, one CTA per (b, g, t) row.  Thread t owns the contiguous blocks
 // [t*PER, t*PER + PER) and keeps their candidate keys (the order-preserving 32-bit image of each
-// non-forced block's score) in registers.  The k-th largest key T is found bit by bit from the
-// first bit where candidate keys differ: for each bit, the number of keys >= (T | bit) is one
-// per-thread count, one warp reduction and one barrier; the search stops as soon as exactly k
-// keys clear the threshold.  Keys above T are taken, and of the keys equal to T (exact ties)
-// the `rem` with the lowest block ids.  One block-wide scan of (chosen, tied) counts then
-// places every chosen block in ascending order.
+// non-forced block's score) in registers.  The k-th largest key T is found below the bits all
+// candidate keys share: for long rows by a radix select, 8 bits per round from a shared histogram
+// of the next digit (three barriers a round); for short rows bit by bit (one count, one warp
+// reduction and one barrier per bit, stopping once exactly k keys clear).  Keys above T are taken, and of the keys equal to T (exact ties) the
+// `rem` with the lowest block ids.  One block-wide scan of (chosen, tied) counts then places
+// every chosen block in ascending order.
 template <int NT, int PER>
 __global__ void __launch_bounds__(NT)
 topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, SeqMap sm, int B, int Hkv, int nblk_max,
@@ -290,7 +290,9 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, SeqMap 
             int* __restrict__ err) {
     constexpr int NW = NT / 32;
     __shared__ uint32_t s_and[NW], s_or[NW];
+    __shared__ int s_hist[256];
     __shared__ int s_cnt[2][NW];
+    __shared__ int s_sel[2];  // this round's digit, keys with a larger one
     __shared__ int s_wsel[NW], s_wtie[NW];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int row = blockIdx.x;
@@ -298,6 +300,11 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, SeqMap 
     sm.row_of(row, B, Hkv, &b, &g_unused, &t);
     pdl_wait();
     pdl_trigger();
+    // the row's scores, loaded before (and independently of) the cache length that bounds them
+    const float* srow = S + static_cast<size_t>(row) * nblk_max;
+    float sv[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) sv[u] = tid * PER + u < nblk_max ? __ldcg(srow + tid * PER + u) : 0.f;
     const int L = kv_len[b];
     const int Tq = sm.len(b);
     int* out = idx + static_cast<size_t>(row) * S_max;
@@ -313,7 +320,6 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, SeqMap 
     const int pos = tree ? L - 1 : L - Tq + t;
     const int bt = pos / p.block_size;
     const int n = bt + 1;
-    const float* srow = S + static_cast<size_t>(row) * nblk_max;
     const int a_init = min(p.n_init, n);
     const int lo_local = max(bt - p.n_local + 1, 0);
     const int n_forced = a_init + (n - max(lo_local, a_init));
@@ -329,7 +335,7 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, SeqMap 
     for (int u = 0; u < PER; ++u) {
         const int blk = blk_base + u;
         cand[u] = select && blk < n && !is_forced(blk, bt, p);
-        key[u] = cand[u] ? ordered_key(__ldcg(srow + blk)) : 0u;
+        key[u] = cand[u] ? ordered_key(sv[u]) : 0u;
     }
 
     // threshold: keys >= T are taken (all of them when tie_limit is not hit)
@@ -362,39 +368,104 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, SeqMap 
         }
         const uint32_t diff = k_and ^ k_or;
         const int k = p.topk;
-        int top = diff == 0 ? -1 : 31 - __clz(diff);
+        const int top = diff == 0 ? -1 : 31 - __clz(diff);
         T = top >= 31 ? 0u : (k_and & (~0u << (top + 1)));  // bits above `top` are common to all
-        bool exact = false;
-        int buf = 0;
-        for (int bit = top; bit >= 0; --bit, buf ^= 1) {
-            const uint32_t trial = T | (1u << bit);
-            int c = 0;
-#pragma unroll
-            for (int u = 0; u < PER; ++u) c += (cand[u] && key[u] >= trial) ? 1 : 0;
-            c = __reduce_add_sync(0xffffffffu, c);
-            if (lane == 0) s_cnt[buf][warp] = c;
+        // Radix select of the k-th largest key below the common bits, 8 bits per round: a histogram
+        // of the next digit over the keys that match T on the bits decided so far (shared atomics,
+        // one per distinct digit of a warp), then warp 0 walks the bins from the largest digit down
+        // to the one where the count reaches the rank still sought.  At the end T is the k-th
+        // largest key and `kr` of the keys equal to T are taken (the lowest blocks).
+        int kr = k;
+        // Long rows (few CTAs, each on its own SM: tree drafts, decode rows) take the radix select;
+        // short rows (prefill chunks: many CTAs per SM hide each other's barriers) decide one bit
+        // per round, which costs fewer instructions there.
+        const bool radix = n > 512;
+        for (int lo = radix ? top + 1 : 0; lo > 0;) {
+            const int nb = lo < 8 ? lo : 8;
+            const int shift = lo - nb;
+            const uint32_t hi_mask = lo >= 32 ? 0u : (~0u << lo);
+            for (int x = tid; x < 256; x += NT) s_hist[x] = 0;
             __syncthreads();
-            int total = 0;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) total += s_cnt[buf][w];
-            if (total >= k) T = trial;  // the k-th largest key has this bit set
-            if (total == k) {          // exactly k keys clear `trial`: no ties to break
-                exact = true;
-                break;
+            for (int u = 0; u < PER; ++u) {
+                const bool in = cand[u] && ((key[u] ^ T) & hi_mask) == 0u;
+                const uint32_t dg = in ? (key[u] >> shift) & ((1u << nb) - 1u) : 0xffffffffu;
+                const unsigned grp = __match_any_sync(0xffffffffu, dg);
+                if (in && (__ffs(grp) - 1) == lane) atomicAdd(&s_hist[dg], __popc(grp));
             }
-        }
-        if (!exact) {
-            // T is the k-th largest key itself; take the keys above it and enough of its ties
-            int c = 0;
-#pragma unroll
-            for (int u = 0; u < PER; ++u) c += (cand[u] && key[u] > T) ? 1 : 0;
-            c = __reduce_add_sync(0xffffffffu, c);
-            if (lane == 0) s_cnt[buf][warp] = c;
             __syncthreads();
-            int above = 0;
+            if (warp == 0) {
+                int c[8], sum = 0;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) above += s_cnt[buf][w];
-            rem = k - above;
+                for (int j = 0; j < 8; ++j) {
+                    c[j] = s_hist[255 - 8 * lane - j];
+                    sum += c[j];
+                }
+                int incl = sum;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int x = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += x;
+                }
+                int acc = incl - sum;  // keys with a larger digit than this lane's bins
+                if (acc < kr && kr <= incl) {
+                    int jf = 0, above = 0;
+                    bool found = false;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (!found && acc + c[j] >= kr) {
+                            found = true;
+                            jf = j;
+                            above = acc;
+                        }
+                        acc += c[j];
+                    }
+                    s_sel[0] = 255 - 8 * lane - jf;
+                    s_sel[1] = above;
+                }
+            }
+            __syncthreads();
+            T |= static_cast<uint32_t>(s_sel[0]) << shift;
+            kr -= s_sel[1];
+            lo = shift;
+        }
+        if (radix) {
+            rem = kr;
+        } else {
+            // bit by bit: for each bit, the number of keys >= (T | bit) by one count, one warp
+            // reduction and one barrier; stop as soon as exactly k keys clear the trial value
+            bool exact = false;
+            int buf = 0;
+            for (int bit = top; bit >= 0; --bit, buf ^= 1) {
+                const uint32_t trial = T | (1u << bit);
+                int c = 0;
+#pragma unroll
+                for (int u = 0; u < PER; ++u) c += (cand[u] && key[u] >= trial) ? 1 : 0;
+                c = __reduce_add_sync(0xffffffffu, c);
+                if (lane == 0) s_cnt[buf][warp] = c;
+                __syncthreads();
+                int total = 0;
+#pragma unroll
+                for (int w = 0; w < NW; ++w) total += s_cnt[buf][w];
+                if (total >= k) T = trial;  // the k-th largest key has this bit set
+                if (total == k) {          // exactly k keys clear `trial`: no ties to break
+                    exact = true;
+                    break;
+                }
+            }
+            if (!exact) {
+                // T is the k-th largest key itself; take the keys above it and enough of its ties
+                int c = 0;
+#pragma unroll
+                for (int u = 0; u < PER; ++u) c += (cand[u] && key[u] > T) ? 1 : 0;
+                c = __reduce_add_sync(0xffffffffu, c);
+                if (lane == 0) s_cnt[buf][warp] = c;
+                __syncthreads();
+                int above = 0;
+#pragma unroll
+                for (int w = 0; w < NW; ++w) above += s_cnt[buf][w];
+                rem = k - above;
+            }
         }
     }
     const uint32_t mask = ~0u;

@@ -389,3 +389,40 @@ def test_decode_host_pageable_buffers_take_the_staged_copies(cuda_lib):
         # the staged call used the staging buffers; the zero-copy one left them alone
         assert bool(torch.isnan(o_dev.float()).any()) == pinned
     assert L.sync_status() == 0
+
+
+@pytest.mark.parametrize("L", [5000, 40000], ids=["short_rows_bitwise", "long_rows_radix"])
+def test_tree_fully_tied_scores_take_the_lowest_blocks(cuda_lib, L):
+    # zero semantic kernels: every candidate block of every draft ties, so each draft's selection
+    # is its forced blocks plus the lowest-numbered candidates -- through the separate top-k kernel
+    # on rows of 79 blocks (bit-by-bit threshold) and of 625 blocks (radix select)
+    torch = pytest.importorskip("torch")
+    Lb = lib()
+    w = synth.WORKLOADS["tree_verify_64k"].scaled(B=1, L=L, Tq=12, topk=16, seed=3980 + L % 97)
+    inp = synth.make_inputs(w)
+    p = w.params()
+    q, k, v, kv = (to_dev(inp[x]) for x in ("q", "k_cache", "v_cache", "kv_len"))
+    dk, dv, mask = to_dev(inp["draft_k"]), to_dev(inp["draft_v"]), to_dev(inp["tree_mask"])
+    M = max(n_kernels(w), 1)
+    kern = torch.zeros((w.B, w.Hkv, M, w.d), dtype=torch.bfloat16, device="cuda")
+    S_cap = Lb.selection_capacity(p, w.L_max)
+    idx = torch.empty((w.B, w.Hkv, w.Tq, S_cap), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((w.B, w.Hkv, w.Tq), dtype=torch.int32, device="cuda")
+    ws = torch.empty(Lb.workspace_size(Lb.ENTRY_DECODE, w.B, w.Tq, w.Hq, w.Hkv, w.d, w.L_max, p),
+                     dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(q)
+    Lb.decode(q, k, v, kern, kv, o, ws, p, draft_k=dk, draft_v=dv, tree_mask=mask, idx_out=idx, counts_out=cnt)
+    torch.cuda.synchronize()
+    assert Lb.sync_status() == 0
+    kern_ref = np.zeros((w.B, w.Hkv, M, w.d), dtype=np.uint16)
+    S = oracle.block_scores(inp["q"], kern_ref, inp["kv_len"], w.Hkv, p, tree=True)
+    oidx, ocnt, _, _ = oracle.select(S, inp["kv_len"], w.Tq, p, tree=True, S_max=S_cap)
+    gidx, gcnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    assert np.array_equal(gcnt, ocnt)
+    for t in range(w.Tq):
+        for g in range(w.Hkv):
+            n = int(ocnt[0, g, t])
+            assert gidx[0, g, t, :n].tolist() == oidx[0, g, t, :n].tolist()
+    o_ref, _ = oracle.attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["kv_len"], gidx, gcnt, p,
+                                draft_k=inp["draft_k"], draft_v=inp["draft_v"], tree_mask=inp["tree_mask"])
+    check_output(bf16_to_f64(o), o_ref)
