@@ -6,11 +6,13 @@
 //
 // One row is (sequence b, KV head g, draft i): the G query heads of draft i that share its
 // selection (the selection kernel's row order).  A thread-block cluster of CL CTAs takes a row:
-//   * CTA r attends the row's list entries r, r + CL, ...: a producer warp streams their K and V
-//     blocks through a ring of shared-memory slots by TMA (full / empty mbarriers per slot), and
-//     eight consumer warps each feed 32-key tiles through the warp-MMA online softmax of
-//     attn_warp.cuh; the last CTA (which has the fewest entries) also attends the draft keys
-//     whose mask bits are set.
+//   * CTA r attends the row's list entries r, r + CL, ...: their K and V blocks stream through a
+//     ring of shared-memory slots by TMA (full / empty mbarriers per slot) and eight warps each
+//     feed 32-key tiles through the warp-MMA online softmax of attn_warp.cuh.  A copy issue holds
+//     its thread for a while, so the issues are spread over the warps: warp k fills slot k at the
+//     start, and the warp that reads a block's first tile refills its slot with the block NS
+//     later once every tile of the slot has been read.  The last CTA (which has the fewest
+//     entries) also attends the draft keys whose mask bits are set.
 //   * The eight warps merge into one fp32 (m, l, o) partial per head; CTA r copies its partial of
 //     head h into a slot of CTA h mod CL (bulk copies into the peer's shared memory, counted on
 //     its barrier), which merges the CL partials of its heads and writes o (bf16) and lse.
@@ -25,14 +27,22 @@
 
 namespace infllmv2 {
 
-constexpr int kTaConsumers = 8;                      // warps attending 32-key tiles
-constexpr int kTaThreads = (kTaConsumers + 1) * 32;  // + the producer warp
+constexpr int kTaWarps = 8;                          // warps attending 32-key tiles
+constexpr int kTaThreads = kTaWarps * 32;
 constexpr int kTaRingBytes = 6 * 32768;              // K/V slots
+constexpr int kTaList = 512;                         // entries of a CTA's list staged in shared memory
 
 template <int D, int BS>
 struct TreeSmem {
     static constexpr int kTile = BS * D * 2;  // one block of K (or V)
-    static constexpr int kSlots = kTaRingBytes / (2 * kTile) < 8 ? kTaRingBytes / (2 * kTile) : 8;
+    // Warp w reads tile w of every group of eight, so it meets blocks w/TPB, w/TPB + kStride, ...
+    // (TPB tiles per block).  The slots are a multiple of kStride: a slot's successive blocks are
+    // then read by the same warps, in order, and a warp waiting on a slot's next phase has always
+    // seen the previous one complete (a parity wait can never be a phase ahead).
+    static constexpr int kStride = kTaWarps / (BS / 32);
+    static constexpr int kFit = kTaRingBytes / (2 * kTile);
+    static constexpr int kSlots = (kFit < 8 ? kFit : 8) / kStride * kStride;
+    static_assert(kSlots >= kStride, "a ring of at least one stride of blocks");
     static constexpr int kPRow = D + 4;        // a head's partial: m, l, 2 unused, o[D]
     static constexpr int kMergeRow = D + D / 8;  // the 8-warp merge scratch: 4 floats of pad per 32 columns
     static constexpr int kMerge = (8 * 16 * 2 + 8 * 16 * kMergeRow) * 4;
@@ -100,6 +110,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const int g = (row / n_draft) % Hkv;
     const int b = row / (n_draft * Hkv);
     const int nh = rank < G ? (G - 1 - rank) / ncta + 1 : 0;  // heads merged here
+    __shared__ int s_list[kTaList];  // this CTA's blocks (-1: out of range), read once
 
     if (tid == 0) {
         prefetch_tmap(&tm_k);
@@ -117,8 +128,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
     // Q of the draft's G heads (an input of the call, not written by the selection kernels)
     QFrag<D> Q;
-    if (warp < kTaConsumers)
-        load_q(Q, q + ((static_cast<size_t>(b) * n_draft + i) * Hq + static_cast<size_t>(g) * G) * D, D, G);
+    load_q(Q, q + ((static_cast<size_t>(b) * n_draft + i) * Hq + static_cast<size_t>(g) * G) * D, D, G);
     pdl_wait();
     pdl_trigger();
     const int L = kv_len[b];
@@ -128,65 +138,73 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const int* list = idx + static_cast<size_t>(row) * idx_stride;
     const int mine = cnt > rank ? (cnt - rank + ncta - 1) / ncta : 0;
     if (!len_ok && rank == 0 && tid == 0) raise_error(err, kDevErrIndex);
-    auto entry = [&](int t) {  // the block of this CTA's t-th entry, -1 if it is out of range
+    auto entry_g = [&](int t) {  // the block of this CTA's t-th entry, -1 if it is out of range
         const int blk = list[rank + ncta * t];  // (written by the selection kernel before this one)
         return (blk >= 0 && blk <= bt) ? blk : -1;
     };
+    // every thread loads a share of the list once (independent loads), so that neither the
+    // producer's issue loop nor the consumers wait on a global load per block
+    for (int t = tid; t < min(mine, kTaList); t += kTaThreads) s_list[t] = entry_g(t);
+    __syncthreads();
+    auto entry = [&](int t) { return t < kTaList ? s_list[t] : entry_g(t); };
 
     WarpAcc<D> A;
     acc_init(A);
-    if (warp == kTaConsumers) {
-        // ---- producer: block t into slot t % NS once its previous occupant has been read
-        if (lane == 0) {
-            for (int t = 0; t < mine; ++t) {
-                const int s = t % NS;
-                if (t >= NS && !mbar_wait(&empty[s], ((t / NS) - 1) & 1u)) raise_error(err, kDevErrTimeout);
-                const int blk = entry(t);
-                if (blk >= 0) {
-                    const int krow = (b * Hkv + g) * L_max + blk * BS;
-                    mbar_arrive_expect_tx(&full[s], 2 * kTile);
+    // block t (its entry already checked) into slot t % NS, counted on full[t % NS]
+    auto issue = [&](int t) {
+        const int s = t % NS;
+        const int blk = entry(t);
+        if (blk >= 0) {
+            const int krow = (b * Hkv + g) * L_max + blk * BS;
+            mbar_arrive_expect_tx(&full[s], 2 * kTile);
 #pragma unroll
-                    for (int sub = 0; sub < D / 64; ++sub) {
-                        tma_load_2d(base + (2 * s) * kTile + sub * BS * 128, &tm_k, 64 * sub, krow, &full[s]);
-                        tma_load_2d(base + (2 * s + 1) * kTile + sub * BS * 128, &tm_v, 64 * sub, krow, &full[s]);
-                    }
-                } else {
-                    raise_error(err, kDevErrIndex);
-                    mbar_arrive(&full[s]);  // nothing to load: the consumers skip the block
-                }
+            for (int sub = 0; sub < D / 64; ++sub) {
+                tma_load_2d(base + (2 * s) * kTile + sub * BS * 128, &tm_k, 64 * sub, krow, &full[s]);
+                tma_load_2d(base + (2 * s + 1) * kTile + sub * BS * 128, &tm_v, 64 * sub, krow, &full[s]);
             }
+        } else {
+            raise_error(err, kDevErrIndex);
+            mbar_arrive(&full[s]);  // nothing to load: the tiles skip the block
         }
-    } else {
-        // ---- consumers.  The last CTA of the row also attends the drafts the mask bits name
-        // (warp w: draft keys 32w .. 32w + 31), ahead of its block tiles.
-        if (rank == ncta - 1 && len_ok && 32 * warp < n_draft) {
-            const uint64_t bits = tree_mask[static_cast<size_t>(b) * n_draft + i] >> (32 * warp);
-            const int n_rows = n_draft - 32 * warp;
-            uint32_t valid = static_cast<uint32_t>(bits);
-            if (n_rows < 32) valid &= (1u << n_rows) - 1u;
-            const size_t off = ((static_cast<size_t>(b) * Hkv + g) * n_draft + 32 * warp) * D;
-            attend32(A, Q, dk + off, dv + off, valid, scale_log2);
-        }
-        // block tiles: tile tau = t * TPB + h of block t; warp w takes tau = w, w + 8, ...
-        for (int tau = warp; tau < mine * TPB; tau += kTaConsumers) {
-            const int t = tau / TPB, h = tau % TPB, s = t % NS;
-            const int blk = entry(t);
-            if (mbar_wait(&full[s], (t / NS) & 1u)) {
-                const int r0 = h * 32;
-                const int n_ok = blk >= 0 ? L - (blk * BS + r0) : 0;
-                if (n_ok > 0) {
-                    const uint32_t valid = n_ok >= 32 ? 0xffffffffu : ((1u << n_ok) - 1u);
-                    attend32_smem<D>(A, Q, smem_u32(base + (2 * s) * kTile), smem_u32(base + (2 * s + 1) * kTile), BS,
-                                     r0, valid, scale_log2);
-                }
-            } else if (lane == 0) {
-                raise_error(err, kDevErrTimeout);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);  // this tile of slot s has been read
-        }
-        acc_finish_rowsum(A);
+    };
+    if (lane == 0 && warp < NS && warp < mine) issue(warp);
+    // The last CTA of the row also attends the drafts the mask bits name (warp w: draft keys
+    // 32w .. 32w + 31), ahead of its block tiles.
+    if (rank == ncta - 1 && len_ok && 32 * warp < n_draft) {
+        const uint64_t bits = tree_mask[static_cast<size_t>(b) * n_draft + i] >> (32 * warp);
+        const int n_rows = n_draft - 32 * warp;
+        uint32_t valid = static_cast<uint32_t>(bits);
+        if (n_rows < 32) valid &= (1u << n_rows) - 1u;
+        const size_t off = ((static_cast<size_t>(b) * Hkv + g) * n_draft + 32 * warp) * D;
+        attend32(A, Q, dk + off, dv + off, valid, scale_log2);
     }
+    // block tiles: tile tau = t * TPB + h of block t; warp w takes tau = w, w + 8, ...
+    for (int tau = warp; tau < mine * TPB; tau += kTaWarps) {
+        const int t = tau / TPB, h = tau % TPB, s = t % NS;
+        const uint32_t ph = (t / NS) & 1u;
+        const int blk = entry(t);
+        if (mbar_wait(&full[s], ph)) {
+            const int r0 = h * 32;
+            const int n_ok = blk >= 0 ? L - (blk * BS + r0) : 0;
+            if (n_ok > 0) {
+                const uint32_t valid = n_ok >= 32 ? 0xffffffffu : ((1u << n_ok) - 1u);
+                attend32_smem<D>(A, Q, smem_u32(base + (2 * s) * kTile), smem_u32(base + (2 * s + 1) * kTile), BS,
+                                 r0, valid, scale_log2);
+            }
+        } else if (lane == 0) {
+            raise_error(err, kDevErrTimeout);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&empty[s]);  // this tile of slot s has been read
+            if (h == 0 && t + NS < mine) {  // refill once every tile of the slot has been read
+                if (!mbar_wait(&empty[s], ph)) raise_error(err, kDevErrTimeout);
+                issue(t + NS);
+            }
+        }
+        __syncwarp();
+    }
+    acc_finish_rowsum(A);
     // every slot has landed and been read: every block's tiles waited for it
     __syncthreads();
 
@@ -196,7 +214,7 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         float* sm_l = sm_m + 8 * 16;
         float* sm_o = sm_l + 8 * 16;  // [8][16][kMergeRow]
         auto mpad = [](int col) { return col + 4 * (col >> 5); };
-        if (warp < kTaConsumers) {
+        {
             if (cq == 0) {
                 sm_m[warp * 16 + gq] = A.m[0];
                 sm_m[warp * 16 + gq + 8] = A.m[1];
