@@ -409,8 +409,11 @@ def run_decode(args, world, rank):
                               f"({R} x {alg['total'] / 1e6:.1f} MB touched per cycle)" if R * alg["total"] > 2 * 129e6
                               else f"{R} replica(s): the steps find their inputs in L2 (a profiling run, not the "
                                    f"benchmark)"),
-                       "launch": (f"CUDA graph of {R} steps, replayed; one cluster kernel per step (one thread-block cluster per row, the largest size whose clusters all fit the device: 12 CTAs for 8 rows on a GB300)" if fused else
-                                  f"CUDA graph of {R} steps, replayed; kernels chained with programmatic dependent launch"),
+                       "launch": (f"exactly {K} steps: a CUDA graph of one step per replica ({R} steps) replayed "
+                                  f"{K // R} times, then a graph of the first {K % R}; " +
+                                  ("one cluster kernel per step (one thread-block cluster per row, the largest size whose "
+                                   "clusters all fit the device: 12 CTAs for 8 rows on a GB300)" if fused else
+                                   "kernels chained with programmatic dependent launch")),
                        "kernel_cache": "resident (pooled before timing)",
                        "outputs": "o and lse per step; the block lists are an optional output the timed steps "
                                   "do not ask for (step.no_graph_with_block_lists_ms_per_step times them)"},
