@@ -28,6 +28,7 @@ constexpr int kScN = kScTokens * 16;
 constexpr int kScM = 128;                // kernels per chunk
 constexpr int kScThreads = 288;  // 8 epilogue warps + the producer warp
 constexpr int kScEpi = 256;      // epilogue threads
+constexpr int kScSpan = 16;      // kernels a block may overlap on the division-free block-max pass
 
 template <int D>
 struct ScSmem {
@@ -186,6 +187,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int r = 32 * (warp % 4) + lane;
         const int th = warp / 4;
         const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
+        // the block-max pass without divisions: block size a power of two and a multiple of the
+        // stride, a block overlapping at most kScSpan kernels, at most 32 blocks per chunk
+        const int kr = bs / s, kcs = (c + s - 1) / s, bs_shift = __ffs(bs) - 1;
+        const int nb_log = blocks_per_chunk <= 16 ? 4 : 5;
+        const bool kr_fast = bs % s == 0 && (bs & (bs - 1)) == 0 && kr + kcs - 1 <= kScSpan && blocks_per_chunk <= 32;
         for (int ch = 0; ch < n_chunks; ++ch) {
             const int st = ch & 1;
             const bool waited = !*s_abort && mbar_wait(&bar_acc[st], (ch >> 1) & 1);
@@ -237,15 +243,39 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             asm volatile("bar.sync 1, 256;" ::: "memory");
             // block max over the kernels each block overlaps, for every token of the tile
             const int nb = min(blocks_per_chunk, bt_max + 1 - b0);
-            for (int e = tid; e < n_tok * nb; e += kScEpi) {
-                const int tk = e / nb, blk = b0 + e % nb;
+            if (kr_fast) {
+                // block size a multiple of the stride (r kernels per block): block blk overlaps
+                // kernels max(0, blk*r - ceil(c/s) + 1) .. (blk+1)*r - 1, at most kScSpan of them;
+                // item e = (token e >> nb_log, block e & (2^nb_log - 1)), no divisions, the span's
+                // loads all in flight before the maximum
+                for (int e = tid; e < (kScTokens << nb_log); e += kScEpi) {
+                const int tk = e >> nb_log, i = e & ((1 << nb_log) - 1);
+                const int blk = b0 + i;
                 const int pos = tree ? pos0 : pos0 + t0 + tk;
-                if (blk > pos / bs) continue;
-                const int ja = first_kernel_of_block(blk, bs, c, s) - j0;
-                const int jz = min(last_kernel_of_block(blk, bs, s) - j0, kScM - 1);
-                float m = -INFINITY;
-                for (int jj = ja; jj <= jz; ++jj) m = fmaxf(m, kmax[tk * kScM + jj]);
-                S[sm.sel(b, g, Hkv, t0 + tk) * nblk_max + blk] = m;
+                if (tk < n_tok && i < nb && blk <= (pos >> bs_shift)) {
+                    const int ja = max(0, blk * kr - kcs + 1) - j0;
+                    const int jz = min((blk + 1) * kr - 1 - j0, kScM - 1);
+                    float v[kScSpan];
+#pragma unroll
+                    for (int u = 0; u < kScSpan; ++u) v[u] = ja + u <= jz ? kmax[tk * kScM + ja + u] : -INFINITY;
+#pragma unroll
+                    for (int w2 = kScSpan / 2; w2 > 0; w2 >>= 1)
+#pragma unroll
+                        for (int u = 0; u < w2; ++u) v[u] = fmaxf(v[u], v[u + w2]);
+                    S[sm.sel(b, g, Hkv, t0 + tk) * nblk_max + blk] = v[0];
+                }
+                }
+            } else {
+                for (int e = tid; e < n_tok * nb; e += kScEpi) {
+                    const int tk = e / nb, blk = b0 + e % nb;
+                    const int pos = tree ? pos0 : pos0 + t0 + tk;
+                    if (blk > pos / bs) continue;
+                    const int ja = first_kernel_of_block(blk, bs, c, s) - j0;
+                    const int jz = min(last_kernel_of_block(blk, bs, s) - j0, kScM - 1);
+                    float m = -INFINITY;
+                    for (int jj = ja; jj <= jz; ++jj) m = fmaxf(m, kmax[tk * kScM + jj]);
+                    S[sm.sel(b, g, Hkv, t0 + tk) * nblk_max + blk] = m;
+                }
             }
             asm volatile("bar.sync 1, 256;" ::: "memory");  // kmax is rewritten by the next chunk
         }
