@@ -11,7 +11,8 @@
 //     feed 32-key tiles through the warp-MMA online softmax of attn_warp.cuh.  A copy issue holds
 //     its thread for a while, so the issues are spread over the warps: warp k fills slot k at the
 //     start, and the warp that reads a block's first tile refills its slot with the block NS
-//     later once every tile of the slot has been read.  The last CTA (which has the fewest
+//     later once every tile of the slot has been read (a per-slot generation count tells the
+//     readers which block a slot's current phase holds).  The last CTA (which has the fewest
 //     entries) also attends the draft keys whose mask bits are set.
 //   * The eight warps merge into one fp32 (m, l, o) partial per head; CTA r copies its partial of
 //     head h into a slot of CTA h mod CL (bulk copies into the peer's shared memory, counted on
@@ -35,14 +36,8 @@ constexpr int kTaList = 512;                         // entries of a CTA's list 
 template <int D, int BS>
 struct TreeSmem {
     static constexpr int kTile = BS * D * 2;  // one block of K (or V)
-    // Warp w reads tile w of every group of eight, so it meets blocks w/TPB, w/TPB + kStride, ...
-    // (TPB tiles per block).  The slots are a multiple of kStride: a slot's successive blocks are
-    // then read by the same warps, in order, and a warp waiting on a slot's next phase has always
-    // seen the previous one complete (a parity wait can never be a phase ahead).
-    static constexpr int kStride = kTaWarps / (BS / 32);
     static constexpr int kFit = kTaRingBytes / (2 * kTile);
-    static constexpr int kSlots = (kFit < 8 ? kFit : 8) / kStride * kStride;
-    static_assert(kSlots >= kStride, "a ring of at least one stride of blocks");
+    static constexpr int kSlots = kFit < 8 ? kFit : 8;
     static constexpr int kPRow = D + 4;        // a head's partial: m, l, 2 unused, o[D]
     static constexpr int kMergeRow = D + D / 8;  // the 8-warp merge scratch: 4 floats of pad per 32 columns
     static constexpr int kMerge = (8 * 16 * 2 + 8 * 16 * kMergeRow) * 4;
@@ -111,7 +106,9 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const int b = row / (n_draft * Hkv);
     const int nh = rank < G ? (G - 1 - rank) / ncta + 1 : 0;  // heads merged here
     __shared__ int s_list[kTaList];  // this CTA's blocks (-1: out of range), read once
+    __shared__ int s_gen[8];         // per slot: blocks issued into it so far
 
+    if (tid < 8) s_gen[tid] = 0;
     if (tid == 0) {
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
@@ -166,6 +163,8 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             raise_error(err, kDevErrIndex);
             mbar_arrive(&full[s]);  // nothing to load: the tiles skip the block
         }
+        __threadfence_block();
+        *reinterpret_cast<volatile int*>(&s_gen[s]) = t / NS + 1;  // block t is the slot's next phase
     };
     if (lane == 0 && warp < NS && warp < mine) issue(warp);
     // The last CTA of the row also attends the drafts the mask bits name (warp w: draft keys
@@ -178,12 +177,29 @@ tree_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         const size_t off = ((static_cast<size_t>(b) * Hkv + g) * n_draft + 32 * warp) * D;
         attend32(A, Q, dk + off, dv + off, valid, scale_log2);
     }
-    // block tiles: tile tau = t * TPB + h of block t; warp w takes tau = w, w + 8, ...
+    // block tiles: tile tau = t * TPB + h of block t; warp w takes tau = w, w + 8, ...  A warp may
+    // reach block t before the block NS earlier in its slot has been read by other warps; it first
+    // waits for the slot's generation to show block t issued, so that the parity wait below is on
+    // the slot's current phase, never one ahead (which the parity test would take for the last
+    // completed one).
     for (int tau = warp; tau < mine * TPB; tau += kTaWarps) {
         const int t = tau / TPB, h = tau % TPB, s = t % NS;
         const uint32_t ph = (t / NS) & 1u;
         const int blk = entry(t);
-        if (mbar_wait(&full[s], ph)) {
+        bool issued = true;
+        if (lane == 0) {
+            const volatile int* gen = &s_gen[s];
+            if (*gen <= t / NS) {
+                const long long t0 = clock64();
+                while (*gen <= t / NS)
+                    if (clock64() - t0 > kWaitBudgetCycles) {
+                        issued = false;
+                        break;
+                    }
+            }
+        }
+        issued = __shfl_sync(0xffffffffu, issued, 0);
+        if (issued && mbar_wait(&full[s], ph)) {
             const int r0 = h * 32;
             const int n_ok = blk >= 0 ? L - (blk * BS + r0) : 0;
             if (n_ok > 0) {
