@@ -7,14 +7,22 @@
 // the MMA's N) and walks the kernel cache in chunks of 128 kernels (the MMA's M), so each
 // accumulator lane holds one kernel against all 256 rows: the max over a token's 16 heads and
 // the visibility test (the kernel ends at or before the token's position) are thread-local.
-// The per-(token, kernel) maxima go to shared memory, where the block max over the kernels a
-// block overlaps is taken and written to S[b, g, t, block].  Chunks cover whole blocks (31
-// blocks of 64 tokens or 15 of 128), so no block straddles two chunks.
+// Chunks cover whole blocks (31 blocks of 64 tokens or 15 of 128), so no block straddles two
+// chunks.  When the block size is a power-of-two multiple r of the stride, a chunk starts
+// ceil(c/s) - 1 kernels before its first block (a negative kernel index reads the TMA fill value
+// and is masked), so block i of the chunk overlaps kernel rows r*i .. r*i + r + ceil(c/s) - 2: the
+// block max is a max over r aligned accumulator lanes and the first ceil(c/s) - 1 lanes after
+// them, taken by warp shuffles (the lanes past a warp's last come from the next warp through a
+// small shared array, one barrier per chunk).  Otherwise the per-(token, kernel) maxima go to
+// shared memory, where each block's max over its kernels is taken.  The result goes to
+// S[b, g, t, block].
 //   * producer warp (warp 8, one lane): TMA of the Q tile once and of each chunk's kernel rows
-//     into two shared stages; one tcgen05 MMA group per chunk into one of two TMEM buffers;
-//   * epilogue warps (warps 0-7, two per TMEM lane quarter, one half of the 16 tokens each):
-//     TMEM -> registers (all four loads of a thread in flight before one wait) -> maxima ->
-//     shared -> S.
+//     into a ring of four shared stages; one tcgen05 MMA group per chunk into one of two TMEM
+//     buffers; a stage is refilled once the MMA group after the one reading it is queued;
+//   * epilogue warps (warps 0-15, four per TMEM lane quarter, 4 of the 16 tokens each: with
+//     two warps per scheduler the dependent steps of the maxima were not hidden): TMEM ->
+//     registers (both loads of a thread in flight before one wait) -> maxima over the heads
+//     (three-input max) -> block maxima -> S.
 // Waits are bounded (device error word + abort flag), TMEM is freed before exit.
 #include <algorithm>
 
@@ -26,33 +34,44 @@ namespace infllmv2 {
 constexpr int kScTokens = 16;            // query tokens per CTA: N = 16 x 16 heads = 256
 constexpr int kScN = kScTokens * 16;
 constexpr int kScM = 128;                // kernels per chunk
-constexpr int kScThreads = 288;  // 8 epilogue warps + the producer warp
-constexpr int kScEpi = 256;      // epilogue threads
-constexpr int kScSpan = 16;      // kernels a block may overlap on the division-free block-max pass
+constexpr int kScEpiWarps = 16;  // epilogue warps: four per TMEM lane quarter
+constexpr int kScEpi = 32 * kScEpiWarps;          // epilogue threads
+constexpr int kScThreads = kScEpi + 32;           // + the producer warp
+constexpr int kScTpt = kScTokens * 4 / kScEpiWarps;  // tokens per epilogue thread
+constexpr int kScStages = 4;     // kernel-row chunks in flight
+constexpr int kScTail = 3;       // most kernels a block overlaps past its stride-aligned group (shuffle pass)
 
 template <int D>
 struct ScSmem {
     static constexpr int kQ = kScN * D * 2;       // Q tile (B operand)
     static constexpr int kK = kScM * D * 2;       // one chunk of kernel rows (A operand)
     static constexpr int kQOff = 0;
-    static constexpr int kKOff = kQ;              // 2 stages
-    static constexpr int kMaxOff = kQ + 2 * kK;   // [kScTokens][kScM] floats
-    static constexpr int kBarOff = kMaxOff + kScTokens * kScM * 4;
+    static constexpr int kKOff = kQ;              // kScStages stages
+    static constexpr int kMaxOff = kQ + kScStages * kK;  // [kScTokens][kScM] floats (general pass)
+    static constexpr int kXOff = kMaxOff + kScTokens * kScM * 4;  // [2][4][kScTail][kScTokens] floats
+    static constexpr int kBarOff = kXOff + 2 * 4 * kScTail * kScTokens * 4;
     static constexpr int kBytes = kBarOff + 128 + 1024;
 };
 
-// AND of `v` over the 256 epilogue threads (named barrier 1; also synchronises them).
+// max(a, b, c) in one instruction (the three-input form of max.f32).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// AND of `v` over the epilogue threads (named barrier 1; also synchronises them).
 __device__ __forceinline__ bool epilogue_all(bool v) {
     uint32_t r;
     asm volatile(
         "{\n"
         " .reg .pred p, q;\n"
         " setp.ne.u32 q, %1, 0;\n"
-        " bar.red.and.pred p, 1, 256, q;\n"
+        " bar.red.and.pred p, 1, %2, q;\n"
         " selp.u32 %0, 1, 0, p;\n"
         "}\n"
         : "=r"(r)
-        : "r"(static_cast<uint32_t>(v))
+        : "r"(static_cast<uint32_t>(v)), "n"(kScEpi)
         : "memory");
     return r != 0;
 }
@@ -70,12 +89,14 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
     float* kmax = reinterpret_cast<float*>(base + SM::kMaxOff);  // [token][kernel row]
+    float* xrow = reinterpret_cast<float*>(base + SM::kXOff);    // [chunk parity][quarter][lane][token]
     uint64_t* bar_q = reinterpret_cast<uint64_t*>(base + SM::kBarOff);
-    uint64_t* bar_k = bar_q + 1;     // [2] kernel chunk landed
-    uint64_t* bar_acc = bar_q + 3;   // [2] MMA of a chunk done
-    uint64_t* bar_free = bar_q + 5;  // [2] epilogue done with a TMEM buffer (256 arrivals)
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_q + 8);
-    volatile int* s_abort = reinterpret_cast<volatile int*>(bar_q + 9);
+    uint64_t* bar_k = bar_q + 1;                 // [kScStages] kernel chunk landed
+    uint64_t* bar_acc = bar_k + kScStages;       // [2] MMA of a chunk done
+    uint64_t* bar_free = bar_acc + 2;            // [2] epilogue done with a TMEM buffer (kScEpi arrivals)
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_free + 2);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(bar_free + 3);
+    static_assert((1 + kScStages + 4) * 8 + 16 <= 128, "barrier area");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bg = blockIdx.y;
@@ -101,11 +122,29 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int n_chunks_all = bt_max / blocks_per_chunk + 1;
     const int n_chunks = n_chunks_all > split ? (n_chunks_all - split + n_split - 1) / n_split : 0;
     if (n_chunks == 0) return;
+    // the shuffle pass: block size a power-of-two multiple kr of the stride (kr <= 32), at most
+    // kScTail kernels past a block's group, and a chunk's blocks within its 128 kernel rows
+    const int kr = bs / s, kcs = (c + s - 1) / s;
+    const bool kr_fast = bs % s == 0 && kr <= 32 && (kr & (kr - 1)) == 0 && kcs - 1 <= kScTail &&
+                         kcs - 1 <= kr && blocks_per_chunk * kr + kcs - 1 <= kScM;
+    // Local chunk k is chunk split + n_split * ((k + rot) % n_chunks) of the tile: the CTAs of a
+    // wave (consecutive tiles of one KV head, all reading the same kernel rows) start at different
+    // chunks, so that they do not all request the same 32 KB from L2 at the same time.
+    const int rot = (blockIdx.x + 5 * blockIdx.y) % n_chunks;
+    auto chunk_b0 = [&](int k) {
+        const int kk = k + rot < n_chunks ? k + rot : k + rot - n_chunks;
+        return (split + n_split * kk) * blocks_per_chunk;
+    };
+    // first kernel row of local chunk k; may be negative
+    auto chunk_row = [&](int k) {
+        const int b0 = chunk_b0(k);
+        return kr_fast ? b0 * kr - (kcs - 1) : first_kernel_of_block(b0, bs, c, s);
+    };
 
     if (tid == 0) {
         mbar_init(bar_q, 1);
+        for (int i = 0; i < kScStages; ++i) mbar_init(&bar_k[i], 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar_k[i], 1);
             mbar_init(&bar_acc[i], 1);
             mbar_init(&bar_free[i], kScEpi);
         }
@@ -121,21 +160,19 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
-    if (warp == 8) {
+    if (warp == kScEpiWarps) {
         // ======================= producer
         if (lane == 0) {
             const uint32_t sQ = smem_u32(base + SM::kQOff);
-            int k_issued[2] = {0, 0}, mma_issued = 0;
-            // local chunk k is chunk split + n_split * k of the tile
-            auto chunk_row = [&](int k) { return first_kernel_of_block((split + n_split * k) * blocks_per_chunk, bs, c, s); };
+            int n_loaded = 0, mma_issued = 0;  // chunks are loaded in order: stage st holds loads st, st + kScStages, ...
             auto load = [&](int ch) {
-                const int st = ch & 1;
+                const int st = ch % kScStages;
                 mbar_arrive_expect_tx(&bar_k[st], SM::kK);
 #pragma unroll
                 for (int sub = 0; sub < D / 64; ++sub)
                     tma_load_2d(base + SM::kKOff + st * SM::kK + sub * (kScM * 128), &tm_kern, 64 * sub,
                                 bg * M_max + chunk_row(ch), &bar_k[st]);
-                ++k_issued[st];
+                ++n_loaded;
             };
             auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
                 if (*s_abort) return false;
@@ -153,121 +190,169 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int sub = 0; sub < D / 64; ++sub)
                     tma_load_2d(base + SM::kQOff + sub * (kScN * 128) + tk * (G * 128), &tm_q, 64 * sub, qrow, bar_q);
             }
-            load(0);
-            if (n_chunks > 1) load(1);
+            for (int ch = 0; ch < kScStages && ch < n_chunks; ++ch) load(ch);
             bool ok = wait(bar_q, 0);
             for (int ch = 0; ok && ch < n_chunks; ++ch) {
-                const int st = ch & 1;
-                if (!(ok = wait(&bar_k[st], (ch >> 1) & 1))) break;
-                if (ch >= 2 && !(ok = wait(&bar_free[st], ((ch - 2) >> 1) & 1))) break;
+                const int st = ch % kScStages, tb = ch & 1;
+                if (!(ok = wait(&bar_k[st], (ch / kScStages) & 1))) break;
+                if (ch >= 2 && !(ok = wait(&bar_free[tb], ((ch - 2) >> 1) & 1))) break;
                 tc_fence_after();
                 const uint32_t ka = smem_u32(base + SM::kKOff + st * SM::kK);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t ao = (kk / 4) * (kScM * 128) + (kk % 4) * 32;
                     const uint32_t bo = (kk / 4) * (kScN * 128) + (kk % 4) * 32;
-                    mma_ss(tmem + st * kScN, sw128_desc(ka + ao, 16, 1024), sw128_desc(sQ + bo, 16, 1024), kIdesc,
+                    mma_ss(tmem + tb * kScN, sw128_desc(ka + ao, 16, 1024), sw128_desc(sQ + bo, 16, 1024), kIdesc,
                            kk > 0 ? 1u : 0u);
                 }
-                mma_commit(&bar_acc[st]);
+                mma_commit(&bar_acc[tb]);
                 ++mma_issued;
-                if (ch + 2 < n_chunks) {  // the stage is free once this chunk's MMA is done
-                    if (!(ok = wait(&bar_acc[st], (ch >> 1) & 1))) break;
-                    load(ch + 2);
+                // the previous chunk's stage is free once its MMA group is done (this group is
+                // already queued behind it, so the tensor pipe does not wait for the refill)
+                if (ch >= 1 && ch - 1 + kScStages < n_chunks) {
+                    if (!(ok = wait(&bar_acc[(ch - 1) & 1], ((ch - 1) >> 1) & 1))) break;
+                    load(ch - 1 + kScStages);
                 }
             }
             const long long drain = kWaitBudgetCycles / 8;
-            for (int st = 0; st < 2; ++st)
-                if (k_issued[st] > 0) mbar_wait(&bar_k[st], (k_issued[st] - 1) & 1, drain);
+            for (int st = 0; st < kScStages && st < n_loaded; ++st) {
+                const int uses = (n_loaded - st + kScStages - 1) / kScStages;  // loads into stage st
+                mbar_wait(&bar_k[st], (uses - 1) & 1, drain);
+            }
             if (mma_issued > 0) mbar_wait(&bar_acc[(mma_issued - 1) & 1], ((mma_issued - 1) >> 1) & 1, drain);
         }
     } else {
         // ======================= epilogue: thread r = 32*(warp%4) + lane owns kernel row r of each
-        // chunk; warps w and w+4 take tokens 0-7 and 8-15 (TMEM columns 128*(w/4) ...)
-        const int r = 32 * (warp % 4) + lane;
+        // chunk; warps w, w+4, w+8, w+12 take tokens 0-3, 4-7, 8-11, 12-15 (TMEM columns 64*(w/4) ...)
+        const int q4 = warp % 4;
+        const int r = 32 * q4 + lane;
         const int th = warp / 4;
-        const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
-        // the block-max pass without divisions: block size a power of two and a multiple of the
-        // stride, a block overlapping at most kScSpan kernels, at most 32 blocks per chunk
-        const int kr = bs / s, kcs = (c + s - 1) / s, bs_shift = __ffs(bs) - 1;
-        const int nb_log = blocks_per_chunk <= 16 ? 4 : 5;
-        const bool kr_fast = bs % s == 0 && (bs & (bs - 1)) == 0 && kr + kcs - 1 <= kScSpan && blocks_per_chunk <= 32;
-        for (int ch = 0; ch < n_chunks; ++ch) {
-            const int st = ch & 1;
-            const bool waited = !*s_abort && mbar_wait(&bar_acc[st], (ch >> 1) & 1);
-            // all eight epilogue warps leave together: they meet at the named barrier below
-            if (!epilogue_all(waited)) {
-                if (tid == 0 && !*s_abort) raise_error(err, kDevErrTimeout);
-                *s_abort = 1;
-                break;
+        const int tk0 = th * kScTpt;  // this thread's first token
+        const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
+        // this thread's kernel row r of a chunk: maxima over the 16 heads of tokens tk0 .. tk0 + 3
+        auto row_maxima = [&](int tb, float (&mx)[kScTpt]) {
+            static_assert(kScTpt == 4, "two 32-column loads");
+            uint32_t ra[32], rb[32];
+            const uint32_t ta = tmem + tb * kScN + lane_off + tk0 * G;
+            tmem_ld32(ta, ra);
+            tmem_ld32(ta + 32, rb);
+            tmem_ld_wait(ra);
+            reg_fence(rb);
+            auto head_max = [&](const uint32_t (&v)[32], int u) {  // three-input maxima: 8 steps for 16 heads
+                float m = max3f(__uint_as_float(v[16 * u]), __uint_as_float(v[16 * u + 1]),
+                                __uint_as_float(v[16 * u + 2]));
+#pragma unroll
+                for (int h = 3; h < G; h += 2)
+                    m = h + 1 < G ? max3f(m, __uint_as_float(v[16 * u + h]), __uint_as_float(v[16 * u + h + 1]))
+                                  : fmaxf(m, __uint_as_float(v[16 * u + h]));
+                return m;
+            };
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                mx[u] = head_max(ra, u);
+                mx[2 + u] = head_max(rb, u);
             }
-            tc_fence_after();
-            const int b0 = (split + n_split * ch) * blocks_per_chunk;
-            const int j0 = first_kernel_of_block(b0, bs, c, s);
-            const int j = j0 + r;
-            const int jend = j * s + c - 1;  // last token of kernel j
-            {
-                uint32_t ra[32], rb[32], rc[32], rd[32];
-                const uint32_t ta = tmem + st * kScN + lane_off + th * 128;
-                tmem_ld32(ta, ra);
-                tmem_ld32(ta + 32, rb);
-                tmem_ld32(ta + 64, rc);
-                tmem_ld32(ta + 96, rd);
-                tmem_ld_wait(ra);
-                reg_fence(rb);
-                reg_fence(rc);
-                reg_fence(rd);
-                auto head_max = [&](const uint32_t (&v)[32], int u) {
-                    float m = __uint_as_float(v[16 * u]);
+        };
+        if (kr_fast) {
+            // per token of this thread: its position's last block and last visible kernel (-1: no
+            // such token), and its row of S
+            int bt_tok[kScTpt], jv_tok[kScTpt];
+            float* srow[kScTpt];
 #pragma unroll
-                    for (int h = 1; h < G; ++h) m = fmaxf(m, __uint_as_float(v[16 * u + h]));
-                    return m;
-                };
-                float mx[8];
+            for (int u = 0; u < kScTpt; ++u) {
+                const int tk = tk0 + u;
+                const int pos = tree ? pos0 : pos0 + t0 + tk;
+                bt_tok[u] = tk < n_tok ? pos / bs : -1;
+                jv_tok[u] = tk < n_tok && pos + 1 >= c ? (pos + 1 - c) / s : -1;
+                srow[u] = S + (tk < n_tok ? sm.sel(b, g, Hkv, t0 + tk) * nblk_max : 0);
+            }
+            const int kr_log = __ffs(kr) - 1;
+            for (int ch = 0; ch < n_chunks; ++ch) {
+                const int tb = ch & 1;
+                const bool waited = !*s_abort && mbar_wait(&bar_acc[tb], (ch >> 1) & 1);
+                tc_fence_after();
+                const int b0 = chunk_b0(ch);
+                const int j = b0 * kr - (kcs - 1) + r;  // this thread's kernel (negative: before the cache)
+                float mx[kScTpt];
+                row_maxima(tb, mx);
+                tc_fence_before();
+                mbar_arrive(&bar_free[tb]);  // this thread is done with the TMEM buffer
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    mx[u] = head_max(ra, u);
-                    mx[2 + u] = head_max(rb, u);
-                    mx[4 + u] = head_max(rc, u);
-                    mx[6 + u] = head_max(rd, u);
+                for (int u = 0; u < kScTpt; ++u)
+                    if (j < 0 || j > jv_tok[u]) mx[u] = -INFINITY;  // before the cache, or ends past the token
+                // lanes 0 .. ceil(c/s) - 2 are the tail of the previous warp's last block
+                float* xw = xrow + (tb * 4 + q4) * kScTail * kScTokens;
+                if (lane < kcs - 1)
+#pragma unroll
+                    for (int u = 0; u < kScTpt; ++u) xw[lane * kScTokens + tk0 + u] = mx[u];
+                // max over the kr aligned lanes of each block, then its tail lanes inside this warp
+                float bm[kScTpt];
+#pragma unroll
+                for (int u = 0; u < kScTpt; ++u) bm[u] = mx[u];
+                for (int off = 1; off < kr; off <<= 1)
+#pragma unroll
+                    for (int u = 0; u < kScTpt; ++u) bm[u] = fmaxf(bm[u], __shfl_xor_sync(0xffffffffu, bm[u], off));
+                for (int t = 0; t < kcs - 1; ++t) {
+                    const int src = lane + kr + t;
+#pragma unroll
+                    for (int u = 0; u < kScTpt; ++u) {
+                        const float v = __shfl_sync(0xffffffffu, mx[u], src & 31);
+                        if (src < 32) bm[u] = fmaxf(bm[u], v);
+                    }
                 }
+                // all eight epilogue warps meet here (the tails are published; a failed wait ends all)
+                if (!epilogue_all(waited)) {
+                    if (tid == 0 && !*s_abort) raise_error(err, kDevErrTimeout);
+                    *s_abort = 1;
+                    break;
+                }
+                // tail lanes in the next warp (none past the last: its last group is no block)
+                if (q4 < 3)
+                    for (int t = 0; t < kcs - 1; ++t) {
+                        const int src = lane + kr + t;
+                        if (src >= 32) {
+                            const float* xn = xrow + ((tb * 4 + q4 + 1) * kScTail + src - 32) * kScTokens + tk0;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int tk = th * 8 + u;
+                            for (int u = 0; u < kScTpt; ++u) bm[u] = fmaxf(bm[u], xn[u]);
+                        }
+                    }
+                const int i = r >> kr_log;  // the block this lane's group starts
+                const int blk = b0 + i;
+                if ((lane & (kr - 1)) == 0 && i < blocks_per_chunk)
+#pragma unroll
+                    for (int u = 0; u < kScTpt; ++u)
+                        if (blk <= bt_tok[u]) srow[u][blk] = bm[u];
+            }
+        } else {
+            for (int ch = 0; ch < n_chunks; ++ch) {
+                const int tb = ch & 1;
+                const bool waited = !*s_abort && mbar_wait(&bar_acc[tb], (ch >> 1) & 1);
+                // all eight epilogue warps leave together: they meet at the named barrier below
+                if (!epilogue_all(waited)) {
+                    if (tid == 0 && !*s_abort) raise_error(err, kDevErrTimeout);
+                    *s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const int b0 = chunk_b0(ch);
+                const int j0 = first_kernel_of_block(b0, bs, c, s);
+                const int j = j0 + r;
+                const int jend = j * s + c - 1;  // last token of kernel j
+                float mx[kScTpt];
+                row_maxima(tb, mx);
+#pragma unroll
+                for (int u = 0; u < kScTpt; ++u) {
+                    const int tk = tk0 + u;
                     const int pos = tree ? pos0 : pos0 + t0 + tk;
                     kmax[tk * kScM + r] = (tk < n_tok && jend <= pos) ? mx[u] : -INFINITY;
                 }
-            }
-            tc_fence_before();
-            mbar_arrive(&bar_free[st]);  // this thread is done with the TMEM buffer
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-            // block max over the kernels each block overlaps, for every token of the tile
-            const int nb = min(blocks_per_chunk, bt_max + 1 - b0);
-            if (kr_fast) {
-                // block size a multiple of the stride (r kernels per block): block blk overlaps
-                // kernels max(0, blk*r - ceil(c/s) + 1) .. (blk+1)*r - 1, at most kScSpan of them;
-                // item e = (token e >> nb_log, block e & (2^nb_log - 1)), no divisions, the span's
-                // loads all in flight before the maximum
-                for (int e = tid; e < (kScTokens << nb_log); e += kScEpi) {
-                const int tk = e >> nb_log, i = e & ((1 << nb_log) - 1);
-                const int blk = b0 + i;
-                const int pos = tree ? pos0 : pos0 + t0 + tk;
-                if (tk < n_tok && i < nb && blk <= (pos >> bs_shift)) {
-                    const int ja = max(0, blk * kr - kcs + 1) - j0;
-                    const int jz = min((blk + 1) * kr - 1 - j0, kScM - 1);
-                    float v[kScSpan];
-#pragma unroll
-                    for (int u = 0; u < kScSpan; ++u) v[u] = ja + u <= jz ? kmax[tk * kScM + ja + u] : -INFINITY;
-#pragma unroll
-                    for (int w2 = kScSpan / 2; w2 > 0; w2 >>= 1)
-#pragma unroll
-                        for (int u = 0; u < w2; ++u) v[u] = fmaxf(v[u], v[u + w2]);
-                    S[sm.sel(b, g, Hkv, t0 + tk) * nblk_max + blk] = v[0];
-                }
-                }
-            } else {
-                for (int e = tid; e < n_tok * nb; e += kScEpi) {
-                    const int tk = e / nb, blk = b0 + e % nb;
+                tc_fence_before();
+                mbar_arrive(&bar_free[tb]);  // this thread is done with the TMEM buffer
+                asm volatile("bar.sync 1, %0;" ::"n"(kScEpi) : "memory");
+                // block max over the kernels each block overlaps, for every token of the tile
+                const int nb = min(blocks_per_chunk, bt_max + 1 - b0);
+                for (int e2 = tid; e2 < n_tok * nb; e2 += kScEpi) {
+                    const int tk = e2 / nb, blk = b0 + e2 % nb;
                     const int pos = tree ? pos0 : pos0 + t0 + tk;
                     if (blk > pos / bs) continue;
                     const int ja = first_kernel_of_block(blk, bs, c, s) - j0;
@@ -276,8 +361,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     for (int jj = ja; jj <= jz; ++jj) m = fmaxf(m, kmax[tk * kScM + jj]);
                     S[sm.sel(b, g, Hkv, t0 + tk) * nblk_max + blk] = m;
                 }
+                asm volatile("bar.sync 1, %0;" ::"n"(kScEpi) : "memory");  // kmax is rewritten by the next chunk
             }
-            asm volatile("bar.sync 1, 256;" ::: "memory");  // kmax is rewritten by the next chunk
         }
     }
     tc_fence_before();

@@ -214,6 +214,10 @@ int infllmv2_append(const void* k_new, const void* v_new, void* k_cache, void* v
  * Needs S_max >= infllmv2_selection_capacity(params, L_max), kernels pooled up
  * to kv_len[b], kv_len[b] in [Tq, L_max], and
  * ws_bytes >= infllmv2_workspace_size(INFLLMV2_ENTRY_BLOCK_SELECT, ...).
+ * Once the call's work is done, the workspace starts with the scores S as float
+ * [B, Hkv, Tq, ceil(L_max / block_size)]: entries of blocks 0..bt of each query
+ * of a sequence with kv_len[b] >= dense_len are written, the others are
+ * unspecified; they stay there until the workspace is used again.
  */
 int infllmv2_block_select(const void* q, const void* kernel_cache, const int32_t* kv_len, int B,
                           int Tq, int Hq, int Hkv, int d, int L_max, int M_max, int32_t* idx,

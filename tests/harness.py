@@ -76,6 +76,7 @@ def run_gpu(w, inp: dict, pool_split: int | None = None, params: dict | None = N
         ws = torch.empty(L.workspace_size(L.ENTRY_BLOCK_SELECT, w.B, w.Tq, w.Hq, w.Hkv, w.d, w.L_max, p),
                          dtype=torch.uint8, device="cuda")
         L.block_select(q, kern, kv_len, idx, counts, ws, p, w.L_max)
+        out["ws"] = ws  # starts with the block scores
         o = torch.empty_like(q)
         lse = torch.empty((w.B, w.Hq, w.Tq), dtype=torch.float32, device="cuda")
         L.sparse_attn_fwd(q, k, v, idx, counts, kv_len, o, p, lse=lse)

@@ -426,3 +426,44 @@ def test_tree_fully_tied_scores_take_the_lowest_blocks(cuda_lib, L):
     o_ref, _ = oracle.attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["kv_len"], gidx, gcnt, p,
                                 draft_k=inp["draft_k"], draft_v=inp["draft_v"], tree_mask=inp["tree_mask"])
     check_output(bf16_to_f64(o), o_ref)
+
+
+@pytest.mark.parametrize("bs,c,s,d", [
+    (128, 32, 16, 128),  # 8 kernels per block, one past the group: the shuffle pass (prefill shape)
+    (64, 32, 16, 64),    # 4 per block, one past
+    (128, 16, 16, 128),  # kernels as wide as the stride: no lane past the group
+    (64, 64, 16, 128),   # three past the group (the most the shuffle pass takes)
+    (128, 40, 16, 64),   # kernel not a multiple of the stride, two past
+    (128, 32, 32, 128),  # 4 per block, kernel = stride
+    (128, 32, 24, 128),  # block not a multiple of the stride: the shared-memory pass
+    (64, 64, 8, 128),    # seven past the group: the shared-memory pass
+])
+def test_chunk_block_scores_for_kernel_shapes(cuda_lib, bs, c, s, d):
+    # the tensor-core scorer's block scores (16 heads per KV head), read from the start of the
+    # workspace, against the oracle's for every visible block of every query; two sequences of
+    # different lengths and a ragged last tile of 11 queries
+    w = synth.WORKLOADS["chunked_prefill_32k"].scaled(B=2, L=3000, Tq=203, Hq=32, Hkv=2, d=d, block_size=bs,
+                                                       kernel_size=c, kernel_stride=s, topk=4, n_local=2,
+                                                       dense_len=0, seed=4600 + bs + c + s + d)
+    inp = synth.make_inputs(w)
+    inp["kv_len"] = np.array([3000, 1777], dtype=np.int32)
+    p = w.params()
+    g = run_gpu(w, inp, pool_split=0, params=p)
+    kern_ref, _ = oracle.kernel_pool(inp["k_cache"], inp["kv_len"], c, s, n_kernels(w))
+    nblk = (w.L_max - 1) // bs + 1
+    S = oracle.block_scores(inp["q"], kern_ref, inp["kv_len"], w.Hkv, p, nblk_max=nblk)
+    Sg = g["ws"][: w.B * w.Hkv * w.Tq * nblk * 4].view(dtype=__import__("torch").float32).cpu().numpy()
+    Sg = Sg.reshape(w.B, w.Hkv, w.Tq, nblk)
+    checked = 0
+    for b in range(w.B):
+        for t in range(w.Tq):
+            bt = (int(inp["kv_len"][b]) - w.Tq + t) // bs
+            ref, got = S[b, :, t, :bt + 1], Sg[b, :, t, :bt + 1].astype(np.float64)
+            fin = np.isfinite(ref)
+            assert np.array_equal(fin, np.isfinite(got)), (b, t)
+            assert np.array_equal(ref[~fin], got[~fin]), (b, t)
+            assert np.max(np.abs(ref[fin] - got[fin]), initial=0.0) < 1e-3, (b, t)
+            checked += int(fin.sum())
+    assert checked > 0
+    oidx, ocnt, kth, _ = oracle.select(S, inp["kv_len"], w.Tq, p, S_max=g["S_cap"])
+    assert compare_selection(g["idx"].cpu().numpy(), g["counts"].cpu().numpy(), oidx, ocnt, S, kth)[3] == 0
