@@ -52,6 +52,27 @@ void* mapped_host(const void* p) {
     return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
 }
 
+// Whether the current device reads and writes pageable host memory coherently through the host's
+// page tables (address translation services, as between Grace and the GPU over NVLink-C2C): then
+// every host buffer is usable by a kernel at its own address, page-locked or not.  Asked once per
+// device.
+bool host_memory_direct() {
+    static std::once_flag once[kMaxDevices];
+    static bool direct[kMaxDevices] = {};
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur < 0 || cur >= kMaxDevices) return false;
+    std::call_once(once[cur], [cur] {
+        int pageable = 0, host_tables = 0;
+        if (cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, cur) != cudaSuccess ||
+            cudaDeviceGetAttribute(&host_tables, cudaDevAttrPageableMemoryAccessUsesHostPageTables, cur) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return;
+        }
+        direct[cur] = pageable != 0 && host_tables != 0;
+    });
+    return direct[cur];
+}
+
 // This host thread's page-locked, mapped error word (allocated on first use, kept until the process
 // exits): the zero-copy host-buffer decode gives it to its kernel and reads it back after the wait.
 // *dev receives its address on the current device.
@@ -488,6 +509,12 @@ int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache, con
                        d, L_max, M_max, o, lse, idx_out, counts_out, S_max, workspace, ws_bytes, params, stream);
 }
 
+int infllmv2_host_memory_direct(int* direct) {
+    if (direct == nullptr) return INFLLMV2_ERR_INVALID_ARG;
+    *direct = host_memory_direct() ? 1 : 0;
+    return INFLLMV2_OK;
+}
+
 int infllmv2_decode_host(const void* q_host, const int32_t* kv_len_host, void* o_host, float* lse_host, void* q_dev,
                          int32_t* kv_len_dev, void* o_dev, float* lse_dev, const void* k_cache, const void* v_cache,
                          const void* kernel_cache, int B, int Hq, int Hkv, int d, int L_max, int M_max, void* workspace,
@@ -505,10 +532,12 @@ int infllmv2_decode_host(const void* q_host, const int32_t* kv_len_host, void* o
     // memory (NVLink-C2C between Grace and the GPU), its errors go to this thread's page-locked
     // error word, and the call is one launch and one wait.
     {
-        void* qm = mapped_host(q_host);
-        void* km = qm != nullptr ? mapped_host(kv_len_host) : nullptr;
-        void* om = km != nullptr ? mapped_host(o_host) : nullptr;
-        void* lm = (om != nullptr && lse_host != nullptr) ? mapped_host(lse_host) : nullptr;
+        const bool direct = host_memory_direct();
+        auto dev_view = [direct](const void* h) { return direct ? const_cast<void*>(h) : mapped_host(h); };
+        void* qm = dev_view(q_host);
+        void* km = qm != nullptr ? dev_view(kv_len_host) : nullptr;
+        void* om = km != nullptr ? dev_view(o_host) : nullptr;
+        void* lm = (om != nullptr && lse_host != nullptr) ? dev_view(lse_host) : nullptr;
         int* wd = nullptr;
         volatile int* wh = (om != nullptr && (lse_host == nullptr || lm != nullptr)) ? host_error_word(&wd) : nullptr;
         if (wh != nullptr && aligned16(qm) && aligned16(km) && aligned16(om) && (lm == nullptr || aligned16(lm))) {

@@ -31,8 +31,32 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
+// The last few maps this thread encoded, by their arguments: a map is a pure function of them (the
+// driver only checks and packs them), so a repeated call copies the earlier result instead of
+// paying the encode again on every launch.
+struct TmapKey {
+    int type;
+    const void* base;
+    uint64_t inner, rows;
+    uint32_t box_inner, box_rows;
+    bool operator==(const TmapKey& o) const {
+        return type == o.type && base == o.base && inner == o.inner && rows == o.rows && box_inner == o.box_inner &&
+               box_rows == o.box_rows;
+    }
+};
+constexpr int kTmapCache = 64;
+
 static bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType type, uint64_t elem_bytes, const void* base,
                          uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
+    thread_local TmapKey keys[kTmapCache];
+    thread_local CUtensorMap maps[kTmapCache];
+    thread_local int n_cached = 0, next = 0;
+    const TmapKey key{static_cast<int>(type), base, inner, rows, box_inner, box_rows};
+    for (int i = 0; i < n_cached; ++i)
+        if (keys[i] == key) {
+            *map = maps[i];
+            return true;
+        }
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint64_t dims[2] = {inner, rows};
@@ -42,7 +66,12 @@ static bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType type, uint64_t el
     const CUresult r = fn(map, type, 2, const_cast<void*>(base), dims, strides, box, estride,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    if (r != CUDA_SUCCESS) return false;
+    keys[next] = key;
+    maps[next] = *map;
+    next = (next + 1) % kTmapCache;
+    if (n_cached < kTmapCache) ++n_cached;
+    return true;
 }
 
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,

@@ -97,6 +97,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.infllmv2_decode_noalloc.restype = ctypes.c_int
     lib.infllmv2_decode_host.argtypes = [p, p, p, p, p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, p, sz, pp, p]
     lib.infllmv2_decode_host.restype = ctypes.c_int
+    lib.infllmv2_host_memory_direct.argtypes = [p]
+    lib.infllmv2_host_memory_direct.restype = ctypes.c_int
     lib.infllmv2_profile_enable.argtypes = [i32]
     lib.infllmv2_profile_read.argtypes = [p, i32, p]
     lib.infllmv2_profile_stage_name.argtypes = [i32]
@@ -344,6 +346,14 @@ def decode_host(q_host, kv_len_host, o_host, q_dev, kv_len_dev, o_dev, k_cache, 
                                        d, L_max, M_max, _ptr(workspace),
                                        workspace.numel() * workspace.element_size(),
                                        ctypes.byref(Params.make(params)), _stream(stream)), "infllmv2_decode_host")
+
+
+def host_memory_direct() -> bool:
+    """Whether decode_host's zero-copy way also takes pageable host buffers on the current device
+    (the device reads host memory through the host's page tables)."""
+    v = ctypes.c_int(0)
+    _check(load().infllmv2_host_memory_direct(ctypes.byref(v)), "infllmv2_host_memory_direct")
+    return v.value != 0
 
 
 class DecodeHostStep:

@@ -295,11 +295,16 @@ int infllmv2_decode(const void* q, const void* k_cache, const void* v_cache,
  * output live in host memory: q_host [B, Hq, d] bf16 and kv_len_host [B] in,
  * o_host [B, Hq, d] bf16 (and lse_host [B, Hq] fp32, when not NULL) out; on
  * return the host output is complete.  Two ways, chosen per call:
- *   - zero-copy: when every host buffer is page-locked and mapped into the
- *     device's address space (cudaHostAlloc / cudaMallocHost, or registered
- *     with mapping; 16-byte aligned) and the single-kernel decode covers the
- *     shape, that kernel reads q and the lengths and writes o and lse straight
- *     through host memory (on a Grace host, over NVLink-C2C); device errors go
+ *   - zero-copy: when every host buffer is 16-byte aligned and usable by the
+ *     device -- any host memory on a device that reads pageable memory through
+ *     the host's page tables (cudaDevAttrPageableMemoryAccess and
+ *     ...UsesHostPageTables, as a GPU attached to a Grace CPU), else memory
+ *     page-locked and mapped into the device's address space (cudaHostAlloc /
+ *     cudaMallocHost, or registered with mapping) -- and the single-kernel
+ *     decode covers the shape, that kernel reads q and the lengths and writes
+ *     o and lse straight through host memory (on a Grace host, over
+ *     NVLink-C2C); the buffers must then be valid host memory of the stated
+ *     sizes (the device reads and writes them as they are); device errors go
  *     to a page-locked error word of the calling host thread (allocated on its
  *     first such call, kept until the process exits); one launch and one wait.
  *     The staging buffers are not touched.
@@ -322,6 +327,16 @@ int infllmv2_decode_host(const void* q_host, const int32_t* kv_len_host, void* o
                          const void* k_cache, const void* v_cache, const void* kernel_cache, int B,
                          int Hq, int Hkv, int d, int L_max, int M_max, void* workspace,
                          size_t ws_bytes, const infllmv2_params* params, void* stream);
+
+/*
+ * Whether infllmv2_decode_host's zero-copy way takes pageable host buffers on
+ * the current device: *direct = 1 when the device reads and writes pageable
+ * memory coherently through the host's page tables (a GPU attached to a Grace
+ * CPU over NVLink-C2C), else 0 (then only page-locked, mapped buffers avoid the
+ * staged copies; also 0 when no device can be queried).  Returns INFLLMV2_OK,
+ * or INFLLMV2_ERR_INVALID_ARG when direct is NULL.
+ */
+int infllmv2_host_memory_direct(int* direct);
 
 /*
  * One whole single-token decode step: infllmv2_append (the new token's K and V

@@ -135,6 +135,10 @@ def test_decode_host_checks_before_enqueueing(built_lib):
     assert call(params=_params(topk=-1)) == infllmv2.ERR_INVALID_ARG
 
 
+def test_host_memory_direct_checks_its_argument(built_lib):
+    assert built_lib.infllmv2_host_memory_direct(None) == infllmv2.ERR_INVALID_ARG
+
+
 def test_decode_host_binding_checks_types_and_sizes():
     """The binding refuses staging tensors whose type or size would make the C call copy past them
     (checked before any pointer is taken, so CPU tensors stand in here)."""
