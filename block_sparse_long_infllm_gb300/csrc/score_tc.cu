@@ -98,6 +98,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     volatile int* s_abort = reinterpret_cast<volatile int*>(bar_free + 3);
     static_assert((1 + kScStages + 4) * 8 + 16 <= 128, "barrier area");
 
+    // the top-k kernel after this one may start launching now: it waits (griddepcontrol.wait) for
+    // this whole grid to complete before it reads the scores
+    pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bg = blockIdx.y;
     const int b = bg / Hkv, g = bg % Hkv;

@@ -292,7 +292,7 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, SeqMap 
     __shared__ uint32_t s_and[NW], s_or[NW];
     __shared__ int s_hist[256];
     __shared__ int s_cnt[2][NW];
-    __shared__ int s_sel[2];  // this round's digit, keys with a larger one
+    __shared__ int s_sel[3];  // this round's digit, keys with a larger one, whether its bin is exactly the rest
     __shared__ int s_wsel[NW], s_wtie[NW];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int row = blockIdx.x;
@@ -376,6 +376,7 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, SeqMap 
         // to the one where the count reaches the rank still sought.  At the end T is the k-th
         // largest key and `kr` of the keys equal to T are taken (the lowest blocks).
         int kr = k;
+        bool bin_exact = false;  // a round's bin held exactly the keys still sought: all of them are taken
         // Long rows (few CTAs, each on its own SM: tree drafts, decode rows) take the radix select;
         // short rows (prefill chunks: many CTAs per SM hide each other's barriers) decide one bit
         // per round, which costs fewer instructions there.
@@ -422,15 +423,20 @@ topk_kernel(const float* __restrict__ S, const int* __restrict__ kv_len, SeqMap 
                     }
                     s_sel[0] = 255 - 8 * lane - jf;
                     s_sel[1] = above;
+                    s_sel[2] = above + c[jf] == kr;
                 }
             }
             __syncthreads();
             T |= static_cast<uint32_t>(s_sel[0]) << shift;
             kr -= s_sel[1];
             lo = shift;
+            if (s_sel[2]) {  // every key with T's bits so far is taken: the lower digits need no rounds
+                bin_exact = true;
+                break;
+            }
         }
         if (radix) {
-            rem = kr;
+            rem = bin_exact ? (1 << 30) : kr;  // keys equal to T: all of the bin, or the kr lowest blocks
         } else {
             // bit by bit: for each bit, the number of keys >= (T | bit) by one count, one warp
             // reduction and one barrier; stop as soon as exactly k keys clear the trial value
@@ -627,16 +633,19 @@ cudaError_t launch_block_select(const SelectArgs& a, float* S) {
     const SeqMap sm = a.seqmap();
     const int rows = a.Hkv * sm.total;
     if (nblk_max <= 128 * 4)
-        e = launch_kernel(topk_kernel<128, 4>, dim3(rows), dim3(128), 0, a.stream, decode_shaped, S, a.kv_len, sm,
+        e = launch_kernel(topk_kernel<128, 4>, dim3(rows), dim3(128), 0, a.stream, true, S, a.kv_len, sm,
+                          a.B, a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
+    else if (nblk_max <= 512 * 2)
+        e = launch_kernel(topk_kernel<512, 2>, dim3(rows), dim3(512), 0, a.stream, true, S, a.kv_len, sm,
                           a.B, a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
     else if (nblk_max <= 256 * 8)
-        e = launch_kernel(topk_kernel<256, 8>, dim3(rows), dim3(256), 0, a.stream, decode_shaped, S, a.kv_len, sm,
+        e = launch_kernel(topk_kernel<256, 8>, dim3(rows), dim3(256), 0, a.stream, true, S, a.kv_len, sm,
                           a.B, a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
     else if (nblk_max <= 512 * 16)
-        e = launch_kernel(topk_kernel<512, 16>, dim3(rows), dim3(512), 0, a.stream, decode_shaped, S, a.kv_len, sm,
+        e = launch_kernel(topk_kernel<512, 16>, dim3(rows), dim3(512), 0, a.stream, true, S, a.kv_len, sm,
                           a.B, a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
     else
-        e = launch_kernel(topk_kernel<1024, 32>, dim3(rows), dim3(1024), 0, a.stream, decode_shaped, S, a.kv_len,
+        e = launch_kernel(topk_kernel<1024, 32>, dim3(rows), dim3(1024), 0, a.stream, true, S, a.kv_len,
                           sm, a.B, a.Hkv, nblk_max, a.L_max, a.tree, p, a.idx, a.counts, a.S_max, a.err);
     prof_mark(a.stream, "topk");
     return e;
