@@ -1156,10 +1156,14 @@ static cudaError_t launch_cluster_t(const DecodeArgs& a, const void* kernel_cach
                 if (cudaFuncSetAttribute(kfn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
                     (void)cudaGetLastError();  // then only the portable sizes (<= 8) are offered below
                 // cluster size: the largest whose clusters all fit on the device at once (one wave
-                // of rows); if none does, the one that keeps the most SMs busy
+                // of rows); if none does, the one that keeps the most SMs busy.  Every size from 16
+                // down is tried whose partial slots fit (the heads a CTA merges x CL <= 24): the
+                // clusters must fit in the GPU's processing clusters, so which sizes fit depends on
+                // the row count (8 rows: 12; 16 rows: 9 on a GB300).
                 cfg.numAttrs = 1;  // (the search without the serialisation attribute)
                 int best_sms = 0, fallback = 0;
-                for (int cand : {16, 12, 8, 4, 2}) {
+                for (int cand = 16; cand >= 2; --cand) {
+                    if (((16 + cand - 1) / cand) * cand * SM::kPRow * 4 > SM::kSlots) continue;
                     attr[0].val.clusterDim.x = cand;
                     cfg.gridDim = dim3(cand * rows);
                     int n = 0;
