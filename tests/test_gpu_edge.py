@@ -309,7 +309,8 @@ def test_decode_host_buffers_match_device_call(cuda_lib):
 @pytest.mark.parametrize("B,Hkv,G,L", [(8, 2, 16, 16384), (12, 4, 4, 8192), (3, 8, 2, 4096)])
 def test_decode_many_rows_smaller_clusters(cuda_lib, B, Hkv, G, L):
     # more (sequence, KV head) rows than 12-CTA clusters fit at once: the single-kernel decode
-    # takes clusters of 8, 4 or 2 CTAs (each CTA then merges more heads and scores more blocks)
+    # takes the largest smaller cluster whose clusters all fit (16 rows: 9 or 10 CTAs on a GB300;
+    # 24 and 48 rows: fewer), each CTA then merging more heads and scoring more blocks
     w = BASE.scaled(B=B, L=L, Hq=G * Hkv, Hkv=Hkv, topk=16, dense_len=0, seed=3600 + B + Hkv + G)
     inp = synth.make_inputs(w)
     inp["kv_len"] = np.array([L - 97 * i for i in range(B)], dtype=np.int32)   # per-sequence lengths
