@@ -18,6 +18,24 @@
 
 namespace infllmv2 {
 
+// Key order inside an n-tile of 8 keys: MMA column j holds key key_perm<D>(j) of the tile's 8.
+// The B fragments of QK^T give lane (g, c) column g; those of PV give it columns 2c, 2c + 1 (+8).
+// In a 128-byte-swizzled shared tile (16-byte chunk x of row y stored at chunk x ^ (y & 7)) the
+// eight lanes of one shared-memory wavefront must read eight different chunk positions:
+//   * K rows: a lane pair (columns 2q, 2q + 1) reads the same four chunks of two rows, so the two
+//     rows must differ in bit 2;
+//   * V rows (lanes read head-dim chunks 2 apart for d = 128, 1 apart for d = 64, over the four
+//     rows of the even or of the odd columns): the even columns map to rows {0, 1, 4, 5} for
+//     d = 128 and {0, 2, 4, 6} for d = 64, the odd ones to the rest.
+// In the identity order the K reads (and for d = 128 the V reads) were 2-way bank conflicts.  The
+// order of the keys does not change the result: every place that maps a column to a key (loads,
+// the valid mask, the scoring's kernel rows) uses this one table.
+template <int D>
+__device__ __forceinline__ int key_perm(int j) {
+    constexpr uint32_t kTable = D == 128 ? 0x35247160u : 0x36147250u;  // [0,6,1,7,4,2,5,3], [0,5,2,7,4,1,6,3]
+    return static_cast<int>((kTable >> (4 * j)) & 7u);
+}
+
 // One split's fp32 partial of a decode row: running maxima m[16] (log2 domain), row sums l[16]
 // and unnormalised outputs o[16][D] for the (up to 16) heads of the row.
 template <int D>
@@ -79,7 +97,7 @@ __device__ __forceinline__ void softmax_pv(WarpAcc<D>& A, float (&s)[4][4], cons
     for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const int key = nt * 8 + 2 * c + (e & 1);
+            const int key = nt * 8 + key_perm<D>(2 * c + (e & 1));
             s[nt][e] = ((valid >> key) & 1u) ? s[nt][e] * scale_log2 : -INFINITY;
             mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
         }
@@ -155,7 +173,7 @@ __device__ __forceinline__ void attend32(WarpAcc<D>& A, const QFrag<D>& Q, const
     for (int kk = 0; kk < 2; ++kk) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            const int key = 16 * kk + 2 * c + (r & 1) + 8 * (r >> 1);
+            const int key = 16 * kk + 8 * (r >> 1) + key_perm<D>(2 * c + (r & 1));
             const bool ok = (valid >> key) & 1u;
             const uint4* src = reinterpret_cast<const uint4*>(v_rows + static_cast<size_t>(key) * D + (D / 8) * g);
 #pragma unroll
@@ -171,7 +189,7 @@ __device__ __forceinline__ void attend32(WarpAcc<D>& A, const QFrag<D>& Q, const
     uint4 kw[4][D / 32];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
-        const int key = nt * 8 + g;
+        const int key = nt * 8 + key_perm<D>(g);
         const bool ok = (valid >> key) & 1u;
         const __nv_bfloat16* src = k_rows + static_cast<size_t>(key) * D + 8 * c;
 #pragma unroll
@@ -197,7 +215,7 @@ __device__ __forceinline__ void attend32_smem(WarpAcc<D>& A, const QFrag<D>& Q, 
     for (int kk = 0; kk < 2; ++kk) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            const int key = 16 * kk + 2 * c + (r & 1) + 8 * (r >> 1);
+            const int key = 16 * kk + 8 * (r >> 1) + key_perm<D>(2 * c + (r & 1));
             const bool ok = (valid >> key) & 1u;
             const int row = row0 + key;
 #pragma unroll
@@ -216,7 +234,7 @@ __device__ __forceinline__ void attend32_smem(WarpAcc<D>& A, const QFrag<D>& Q, 
     uint4 kw[4][D / 32];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
-        const int row = row0 + nt * 8 + g;
+        const int row = row0 + nt * 8 + key_perm<D>(g);
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) {
             const int col = 32 * i + 8 * c;

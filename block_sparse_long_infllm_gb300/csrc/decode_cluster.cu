@@ -368,7 +368,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
             uint4 kw[4][D / 32];
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
-                const int r = 32 * t + 8 * nt + gq;
+                const int r = 32 * t + 8 * nt + key_perm<D>(gq);  // (the key order of attn_warp.cuh)
 #pragma unroll
                 for (int i = 0; i < D / 32; ++i) {
                     const int col = 32 * i + 8 * cq;
@@ -377,7 +377,8 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
             }
             float sc[4][4];
             qk_tiles<D>(sc, Q, kw);
-            // column 2cq + j of n-tile nt is kernel row 32t + 8nt + 2cq + j; rows gq and gq + 8 are heads
+            // column 2cq + j of n-tile nt is kernel row 32t + 8nt + key_perm<D>(2cq + j); rows gq and gq + 8
+            // are heads
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -386,7 +387,7 @@ decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_kern, const __grid_
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                    const int r = 32 * t + 8 * nt + 2 * cq + j;
+                    const int r = 32 * t + 8 * nt + key_perm<D>(2 * cq + j);
                     if (gq == 0 && r < nj) ks[r] = m;
                 }
         }
