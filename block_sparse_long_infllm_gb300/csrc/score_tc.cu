@@ -36,7 +36,7 @@ constexpr int kScN = kScTokens * 16;
 constexpr int kScM = 128;                // kernels per chunk
 constexpr int kScEpiWarps = 16;  // epilogue warps: four per TMEM lane quarter
 constexpr int kScEpi = 32 * kScEpiWarps;          // epilogue threads
-constexpr int kScThreads = kScEpi + 32;           // + the producer warp
+constexpr int kScThreads = kScEpi + 64;           // + the MMA warp and the loader warp
 constexpr int kScTpt = kScTokens * 4 / kScEpiWarps;  // tokens per epilogue thread
 constexpr int kScStages = 4;     // kernel-row chunks in flight
 constexpr int kScTail = 3;       // most kernels a block overlaps past its stride-aligned group (shuffle pass)
@@ -50,7 +50,7 @@ struct ScSmem {
     static constexpr int kMaxOff = kQ + kScStages * kK;  // [kScTokens][kScM] floats (general pass)
     static constexpr int kXOff = kMaxOff + kScTokens * kScM * 4;  // [2][4][kScTail][kScTokens] floats
     static constexpr int kBarOff = kXOff + 2 * 4 * kScTail * kScTokens * 4;
-    static constexpr int kBytes = kBarOff + 128 + 1024;
+    static constexpr int kBytes = kBarOff + 192 + 1024;
 };
 
 // max(a, b, c) in one instruction (the three-input form of max.f32).
@@ -94,9 +94,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint64_t* bar_k = bar_q + 1;                 // [kScStages] kernel chunk landed
     uint64_t* bar_acc = bar_k + kScStages;       // [2] MMA of a chunk done
     uint64_t* bar_free = bar_acc + 2;            // [2] epilogue done with a TMEM buffer (kScEpi arrivals)
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_free + 2);
-    volatile int* s_abort = reinterpret_cast<volatile int*>(bar_free + 3);
-    static_assert((1 + kScStages + 4) * 8 + 16 <= 128, "barrier area");
+    uint64_t* bar_kfree = bar_free + 2;          // [kScStages] the MMA group reading a stage is done
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_kfree + kScStages);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(bar_kfree + kScStages + 1);
+    static_assert((1 + 2 * kScStages + 4) * 8 + 16 <= 192, "barrier area");
 
     // the top-k kernel after this one may start launching now: it waits (griddepcontrol.wait) for
     // this whole grid to complete before it reads the scores
@@ -146,7 +147,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     if (tid == 0) {
         mbar_init(bar_q, 1);
-        for (int i = 0; i < kScStages; ++i) mbar_init(&bar_k[i], 1);
+        for (int i = 0; i < kScStages; ++i) {
+            mbar_init(&bar_k[i], 1);
+            mbar_init(&bar_kfree[i], 1);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar_acc[i], 1);
             mbar_init(&bar_free[i], kScEpi);
@@ -163,37 +167,62 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
-    if (warp == kScEpiWarps) {
-        // ======================= producer
-        if (lane == 0) {
-            const uint32_t sQ = smem_u32(base + SM::kQOff);
-            int n_loaded = 0, mma_issued = 0;  // chunks are loaded in order: stage st holds loads st, st + kScStages, ...
-            auto load = [&](int ch) {
-                const int st = ch % kScStages;
-                mbar_arrive_expect_tx(&bar_k[st], SM::kK);
-#pragma unroll
-                for (int sub = 0; sub < D / 64; ++sub)
-                    tma_load_2d(base + SM::kKOff + st * SM::kK + sub * (kScM * 128), &tm_kern, 64 * sub,
-                                bg * M_max + chunk_row(ch), &bar_k[st]);
-                ++n_loaded;
-            };
-            auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-                if (*s_abort) return false;
-                if (mbar_wait(bar, parity)) return true;
-                raise_error(err, kDevErrTimeout);
-                *s_abort = 1;
-                return false;
-            };
-            // Q tile: 16 tokens x 16 heads, one 16-row box per token and 64-column half
-            mbar_arrive_expect_tx(bar_q, SM::kQ);
-            for (int tk = 0; tk < kScTokens; ++tk) {
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (*s_abort) return false;
+        if (mbar_wait(bar, parity)) return true;
+        raise_error(err, kDevErrTimeout);
+        *s_abort = 1;
+        return false;
+    };
+    if (warp == kScEpiWarps + 1) {
+        // ======================= loader warp: the copies, issued apart from the MMA issuer (a thread
+        // that issues an MMA group is held for about its duration, so copies issued by the same
+        // warp waited behind it); the boxes of a copy go out from different lanes
+        int n_loaded = 0;  // chunks are loaded in order: stage st holds loads st, st + kScStages, ...
+        // Q tile: 16 tokens x 16 heads, one 16-row box per token and 64-column half (lane 16 sub + tk)
+        if (lane == 0) mbar_arrive_expect_tx(bar_q, SM::kQ);
+        __syncwarp();
+        {
+            static_assert(kScTokens * 2 <= 32, "a lane per Q box");
+            const int tk = lane % kScTokens, sub = lane / kScTokens;
+            if (sub < D / 64) {
                 const int t = min(t0 + tk, Tq - 1);
                 const int qrow = (tok + t) * Hq + g * G;
-#pragma unroll
-                for (int sub = 0; sub < D / 64; ++sub)
-                    tma_load_2d(base + SM::kQOff + sub * (kScN * 128) + tk * (G * 128), &tm_q, 64 * sub, qrow, bar_q);
+                tma_load_2d(base + SM::kQOff + sub * (kScN * 128) + tk * (G * 128), &tm_q, 64 * sub, qrow, bar_q);
             }
-            for (int ch = 0; ch < kScStages && ch < n_chunks; ++ch) load(ch);
+        }
+        // chunk ch into stage ch % kScStages once the MMA group of chunk ch - kScStages is done:
+        // lane 2 sub + rh issues rows 64 rh .. 64 rh + 63 of column half sub
+        for (int ch = 0; ch < n_chunks; ++ch) {
+            const int st = ch % kScStages;
+            bool ok = true;
+            if (lane == 0 && ch >= kScStages) ok = wait(&bar_kfree[st], (ch / kScStages - 1) & 1);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            if (lane == 0) mbar_arrive_expect_tx(&bar_k[st], SM::kK);
+            __syncwarp();
+            if (lane < 2 * (D / 64)) {
+                const int sub = lane >> 1, rh = lane & 1;
+                tma_load_2d(base + SM::kKOff + st * SM::kK + sub * (kScM * 128) + rh * (64 * 128), &tm_kern, 64 * sub,
+                            bg * M_max + chunk_row(ch) + 64 * rh, &bar_k[st]);
+            }
+            ++n_loaded;
+        }
+        // every copy has landed before shared memory goes away
+        if (lane == 0) {
+            const long long drain = kWaitBudgetCycles / 8;
+            mbar_wait(bar_q, 0, drain);
+            for (int st = 0; st < kScStages && st < n_loaded; ++st) {
+                const int uses = (n_loaded - st + kScStages - 1) / kScStages;  // loads into stage st
+                mbar_wait(&bar_k[st], (uses - 1) & 1, drain);
+            }
+        }
+    } else if (warp == kScEpiWarps) {
+        // ======================= MMA warp (one lane): one tcgen05 group per chunk into TMEM buffer
+        // ch & 1; a commit frees the chunk's stage for the loader, another hands the buffer to the
+        // epilogue
+        if (lane == 0) {
+            const uint32_t sQ = smem_u32(base + SM::kQOff);
+            int mma_issued = 0;
             bool ok = wait(bar_q, 0);
             for (int ch = 0; ok && ch < n_chunks; ++ch) {
                 const int st = ch % kScStages, tb = ch & 1;
@@ -209,20 +238,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                            kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&bar_acc[tb]);
+                mma_commit(&bar_kfree[st]);
                 ++mma_issued;
-                // the previous chunk's stage is free once its MMA group is done (this group is
-                // already queued behind it, so the tensor pipe does not wait for the refill)
-                if (ch >= 1 && ch - 1 + kScStages < n_chunks) {
-                    if (!(ok = wait(&bar_acc[(ch - 1) & 1], ((ch - 1) >> 1) & 1))) break;
-                    load(ch - 1 + kScStages);
-                }
             }
-            const long long drain = kWaitBudgetCycles / 8;
-            for (int st = 0; st < kScStages && st < n_loaded; ++st) {
-                const int uses = (n_loaded - st + kScStages - 1) / kScStages;  // loads into stage st
-                mbar_wait(&bar_k[st], (uses - 1) & 1, drain);
-            }
-            if (mma_issued > 0) mbar_wait(&bar_acc[(mma_issued - 1) & 1], ((mma_issued - 1) >> 1) & 1, drain);
+            if (mma_issued > 0)
+                mbar_wait(&bar_acc[(mma_issued - 1) & 1], ((mma_issued - 1) >> 1) & 1, kWaitBudgetCycles / 8);
         }
     } else {
         // ======================= epilogue: thread r = 32*(warp%4) + lane owns kernel row r of each
@@ -398,7 +418,7 @@ cudaError_t launch_score_tc(const SelectArgs& a, float* S) {
     const SeqMap sm = a.seqmap();
     const uint64_t q_rows = static_cast<uint64_t>(sm.total) * a.Hq;
     const uint64_t k_rows = static_cast<uint64_t>(a.B) * a.Hkv * a.M_max;
-    if (!make_tmap_bf16_2d(&tq, a.q, a.d, q_rows, 64, 16) || !make_tmap_bf16_2d(&tk, a.kernel_cache, a.d, k_rows, 64, kScM))
+    if (!make_tmap_bf16_2d(&tq, a.q, a.d, q_rows, 64, 16) || !make_tmap_bf16_2d(&tk, a.kernel_cache, a.d, k_rows, 64, kScM / 2))
         return cudaErrorInvalidValue;
     // few query tiles (a draft tree, a short chunk): split each tile's chunks of blocks over CTAs
     const int tiles = ((a.Tq + kScTokens - 1) / kScTokens) * a.B * a.Hkv;
