@@ -76,6 +76,23 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
     return r != 0;
 }
 
+// AND of `v` over the four epilogue warps that take tokens 4 th .. 4 th + 3, one per TMEM lane
+// quarter (named barrier 2 + th; also synchronises them).
+__device__ __forceinline__ bool token_group_all(bool v, int th) {
+    uint32_t r;
+    asm volatile(
+        "{\n"
+        " .reg .pred p, q;\n"
+        " setp.ne.u32 q, %1, 0;\n"
+        " bar.red.and.pred p, %2, %3, q;\n"
+        " selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(2 + th), "n"(128)
+        : "memory");
+    return r != 0;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kScThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kern,
@@ -323,8 +340,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         if (src < 32) bm[u] = fmaxf(bm[u], v);
                     }
                 }
-                // all eight epilogue warps meet here (the tails are published; a failed wait ends all)
-                if (!epilogue_all(waited)) {
+                // the four warps of these tokens meet here (the tails are published; a failed wait ends
+                // all of them, the other groups see the abort flag at their next wait)
+                if (!token_group_all(waited, th)) {
                     if (tid == 0 && !*s_abort) raise_error(err, kDevErrTimeout);
                     *s_abort = 1;
                     break;
