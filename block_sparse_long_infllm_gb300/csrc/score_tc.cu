@@ -269,42 +269,31 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int th = warp / 4;
         const int tk0 = th * kScTpt;  // this thread's first token
         const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
-        // this thread's kernel row r of a chunk: maxima over the 16 heads of tokens tk0 .. tk0 + 3
+        // this thread's kernel row r of a chunk: maxima over the 16 heads of tokens tk0 .. tk0 + 3,
+        // one load-reduce of 16 columns per token
         auto row_maxima = [&](int tb, float (&mx)[kScTpt]) {
-            static_assert(kScTpt == 4, "two 32-column loads");
-            uint32_t ra[32], rb[32];
+            static_assert(kScTpt == 4, "four 16-column load-reduces");
+            uint32_t r0[16], r1[16], r2[16], r3[16];  // the columns (unused), written by the loads
             const uint32_t ta = tmem + tb * kScN + lane_off + tk0 * G;
-            tmem_ld32(ta, ra);
-            tmem_ld32(ta + 32, rb);
-            tmem_ld_wait(ra);
-            reg_fence(rb);
-            auto head_max = [&](const uint32_t (&v)[32], int u) {  // three-input maxima: 8 steps for 16 heads
-                float m = max3f(__uint_as_float(v[16 * u]), __uint_as_float(v[16 * u + 1]),
-                                __uint_as_float(v[16 * u + 2]));
-#pragma unroll
-                for (int h = 3; h < G; h += 2)
-                    m = h + 1 < G ? max3f(m, __uint_as_float(v[16 * u + h]), __uint_as_float(v[16 * u + h + 1]))
-                                  : fmaxf(m, __uint_as_float(v[16 * u + h]));
-                return m;
-            };
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                mx[u] = head_max(ra, u);
-                mx[2 + u] = head_max(rb, u);
-            }
+            tmem_ld16_max(ta, r0, mx[0]);
+            tmem_ld16_max(ta + G, r1, mx[1]);
+            tmem_ld16_max(ta + 2 * G, r2, mx[2]);
+            tmem_ld16_max(ta + 3 * G, r3, mx[3]);
+            tmem_ld_wait_max2(r0, r1, mx[0], mx[1]);
+            tmem_ld_wait_max2(r2, r3, mx[2], mx[3]);
         };
         if (kr_fast) {
             // per token of this thread: its position's last block and last visible kernel (-1: no
             // such token), and its row of S
             int bt_tok[kScTpt], jv_tok[kScTpt];
-            float* srow[kScTpt];
+            int srow[kScTpt];  // row of S (sequence, KV head, token)
 #pragma unroll
             for (int u = 0; u < kScTpt; ++u) {
                 const int tk = tk0 + u;
                 const int pos = tree ? pos0 : pos0 + t0 + tk;
                 bt_tok[u] = tk < n_tok ? pos / bs : -1;
                 jv_tok[u] = tk < n_tok && pos + 1 >= c ? (pos + 1 - c) / s : -1;
-                srow[u] = S + (tk < n_tok ? sm.sel(b, g, Hkv, t0 + tk) * nblk_max : 0);
+                srow[u] = tk < n_tok ? sm.sel(b, g, Hkv, t0 + tk) : 0;
             }
             const int kr_log = __ffs(kr) - 1;
             for (int ch = 0; ch < n_chunks; ++ch) {
@@ -362,7 +351,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if ((lane & (kr - 1)) == 0 && i < blocks_per_chunk)
 #pragma unroll
                     for (int u = 0; u < kScTpt; ++u)
-                        if (blk <= bt_tok[u]) srow[u][blk] = bm[u];
+                        if (blk <= bt_tok[u]) S[static_cast<size_t>(srow[u]) * nblk_max + blk] = bm[u];
             }
         } else {
             for (int ch = 0; ch < n_chunks; ++ch) {
