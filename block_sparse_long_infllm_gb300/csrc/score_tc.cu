@@ -146,7 +146,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // the shuffle pass: block size a power-of-two multiple kr of the stride (kr <= 32), at most
     // kScTail kernels past a block's group, and a chunk's blocks within its 128 kernel rows
     const int kr = bs / s, kcs = (c + s - 1) / s;
-    const bool kr_fast = bs % s == 0 && kr <= 32 && (kr & (kr - 1)) == 0 && kcs - 1 <= kScTail &&
+    const bool kr_fast = bs % s == 0 && kr >= 4 && kr <= 32 && (kr & (kr - 1)) == 0 && kcs - 1 <= kScTail &&
                          kcs - 1 <= kr && blocks_per_chunk * kr + kcs - 1 <= kScM;
     // Local chunk k is chunk split + n_split * ((k + rot) % n_chunks) of the tile: the CTAs of a
     // wave (consecutive tiles of one KV head, all reading the same kernel rows) start at different
@@ -283,52 +283,69 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tmem_ld_wait_max2(r2, r3, mx[2], mx[3]);
         };
         if (kr_fast) {
-            // per token of this thread: its position's last block and last visible kernel (-1: no
-            // such token), and its row of S
-            int bt_tok[kScTpt], jv_tok[kScTpt];
-            int srow[kScTpt];  // row of S (sequence, KV head, token)
+            // the tile's first query's last visible kernel: no row of a chunk that ends at or
+            // before it needs the mask (that query has the tile's smallest position)
+            const int pos_first = tree ? pos0 : pos0 + t0;
+            const int jv_first = pos_first + 1 >= c ? (pos_first + 1 - c) / s : -1;
+            // After the block maxima below, lane l of a group of kr holds token tau(l) = 2 (l & 1) +
+            // ((l >> 1) & 1) of this thread's four (lanes l and l + 4, l + 8 ... hold the same one):
+            // that token's last block and row of S.
+            const int tau = 2 * (lane & 1) + ((lane >> 1) & 1);
+            int my_bt = -1, my_row = 0;
 #pragma unroll
-            for (int u = 0; u < kScTpt; ++u) {
-                const int tk = tk0 + u;
-                const int pos = tree ? pos0 : pos0 + t0 + tk;
-                bt_tok[u] = tk < n_tok ? pos / bs : -1;
-                jv_tok[u] = tk < n_tok && pos + 1 >= c ? (pos + 1 - c) / s : -1;
-                srow[u] = tk < n_tok ? sm.sel(b, g, Hkv, t0 + tk) : 0;
-            }
+            for (int u = 0; u < kScTpt; ++u)
+                if (u == tau && tk0 + u < n_tok) {
+                    const int pos = tree ? pos0 : pos0 + t0 + tk0 + u;
+                    my_bt = pos / bs;
+                    my_row = sm.sel(b, g, Hkv, t0 + tk0 + u);
+                }
             const int kr_log = __ffs(kr) - 1;
+            const int T = kcs - 1;  // kernels of a block past its aligned group of kr
+            // the group that ends this lane quarter takes its T tail rows from the next quarter
+            const bool takes_tail = T > 0 && q4 < 3 && lane >= 32 - kr && (lane & (kr - 1)) < 4;
             for (int ch = 0; ch < n_chunks; ++ch) {
                 const int tb = ch & 1;
                 const bool waited = !*s_abort && mbar_wait(&bar_acc[tb], (ch >> 1) & 1);
                 tc_fence_after();
                 const int b0 = chunk_b0(ch);
-                const int j = b0 * kr - (kcs - 1) + r;  // this thread's kernel (negative: before the cache)
+                const int jlo = b0 * kr - T;  // kernel of row 0 (negative: before the cache)
                 float mx[kScTpt];
                 row_maxima(tb, mx);
                 tc_fence_before();
                 mbar_arrive(&bar_free[tb]);  // this thread is done with the TMEM buffer
-#pragma unroll
-                for (int u = 0; u < kScTpt; ++u)
-                    if (j < 0 || j > jv_tok[u]) mx[u] = -INFINITY;  // before the cache, or ends past the token
-                // lanes 0 .. ceil(c/s) - 2 are the tail of the previous warp's last block
-                float* xw = xrow + (tb * 4 + q4) * kScTail * kScTokens;
-                if (lane < kcs - 1)
-#pragma unroll
-                    for (int u = 0; u < kScTpt; ++u) xw[lane * kScTokens + tk0 + u] = mx[u];
-                // max over the kr aligned lanes of each block, then its tail lanes inside this warp
-                float bm[kScTpt];
-#pragma unroll
-                for (int u = 0; u < kScTpt; ++u) bm[u] = mx[u];
-                for (int off = 1; off < kr; off <<= 1)
-#pragma unroll
-                    for (int u = 0; u < kScTpt; ++u) bm[u] = fmaxf(bm[u], __shfl_xor_sync(0xffffffffu, bm[u], off));
-                for (int t = 0; t < kcs - 1; ++t) {
-                    const int src = lane + kr + t;
+                if (jlo < 0 || jlo + kScM - 1 > jv_first) {  // (uniform) a row before the cache or past a query
+                    const int j = jlo + r;
 #pragma unroll
                     for (int u = 0; u < kScTpt; ++u) {
-                        const float v = __shfl_sync(0xffffffffu, mx[u], src & 31);
-                        if (src < 32) bm[u] = fmaxf(bm[u], v);
+                        // the token's last visible kernel (-1: no such token)
+                        const int tk = tk0 + u;
+                        const int pos = tree ? pos0 : pos0 + t0 + tk;
+                        const int jv = tk < n_tok && pos + 1 >= c ? (pos + 1 - c) / s : -1;
+                        if (j < 0 || j > jv) mx[u] = -INFINITY;
                     }
                 }
+                // Block i of the chunk is rows kr i .. kr i + kr - 1 + T.  Each lane takes the maxima
+                // of the T rows after it: a group's lanes then cover its block, except that the rows
+                // past lane 31 come from the next quarter's lanes 0 .. T - 1, published here (rows of
+                // the other lanes of a group are in the block already, so the fold needs no mask).
+                float f[kScTpt];
+#pragma unroll
+                for (int u = 0; u < kScTpt; ++u) f[u] = mx[u];
+                for (int t = 1; t <= T; ++t) {
+                    if (t == T && lane == 0)
+                        *reinterpret_cast<float4*>(xrow + (tb * 4 + q4) * kScTokens + tk0) =
+                            make_float4(f[0], f[1], f[2], f[3]);
+#pragma unroll
+                    for (int u = 0; u < kScTpt; ++u) f[u] = fmaxf(f[u], __shfl_down_sync(0xffffffffu, mx[u], t));
+                }
+                // maxima over each group of kr lanes (kr >= 4), exchanging tokens on the way: after
+                // the xor-1 step a lane keeps two tokens, after the xor-2 step one (tau)
+                const bool o1 = lane & 1, o2 = lane & 2;
+                float k0 = o1 ? f[2] : f[0], k1 = o1 ? f[3] : f[1];
+                k0 = fmaxf(k0, __shfl_xor_sync(0xffffffffu, o1 ? f[0] : f[2], 1));
+                k1 = fmaxf(k1, __shfl_xor_sync(0xffffffffu, o1 ? f[1] : f[3], 1));
+                float m = fmaxf(o2 ? k1 : k0, __shfl_xor_sync(0xffffffffu, o2 ? k0 : k1, 2));
+                for (int off = 4; off < kr; off <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
                 // the four warps of these tokens meet here (the tails are published; a failed wait ends
                 // all of them, the other groups see the abort flag at their next wait)
                 if (!token_group_all(waited, th)) {
@@ -336,22 +353,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     *s_abort = 1;
                     break;
                 }
-                // tail lanes in the next warp (none past the last: its last group is no block)
-                if (q4 < 3)
-                    for (int t = 0; t < kcs - 1; ++t) {
-                        const int src = lane + kr + t;
-                        if (src >= 32) {
-                            const float* xn = xrow + ((tb * 4 + q4 + 1) * kScTail + src - 32) * kScTokens + tk0;
-#pragma unroll
-                            for (int u = 0; u < kScTpt; ++u) bm[u] = fmaxf(bm[u], xn[u]);
-                        }
-                    }
-                const int i = r >> kr_log;  // the block this lane's group starts
+                if (takes_tail) m = fmaxf(m, xrow[(tb * 4 + q4 + 1) * kScTokens + tk0 + tau]);
+                const int i = r >> kr_log;  // this lane's block in the chunk
                 const int blk = b0 + i;
-                if ((lane & (kr - 1)) == 0 && i < blocks_per_chunk)
-#pragma unroll
-                    for (int u = 0; u < kScTpt; ++u)
-                        if (blk <= bt_tok[u]) S[static_cast<size_t>(srow[u]) * nblk_max + blk] = bm[u];
+                if ((lane & (kr - 1)) < 4 && i < blocks_per_chunk && blk <= my_bt)
+                    S[static_cast<size_t>(my_row) * nblk_max + blk] = m;
             }
         } else {
             for (int ch = 0; ch < n_chunks; ++ch) {

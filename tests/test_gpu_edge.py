@@ -439,6 +439,9 @@ def test_tree_fully_tied_scores_take_the_lowest_blocks(cuda_lib, L):
     (128, 32, 32, 128),  # 4 per block, kernel = stride
     (128, 32, 24, 128),  # block not a multiple of the stride: the shared-memory pass
     (64, 64, 8, 128),    # seven past the group: the shared-memory pass
+    (128, 16, 8, 128),   # 16 per block: the shuffle pass with a fourth exchange step
+    (128, 12, 4, 64),    # 32 per block (a whole lane quarter), two past
+    (64, 48, 32, 128),   # 2 per block: the shared-memory pass
 ])
 def test_chunk_block_scores_for_kernel_shapes(cuda_lib, bs, c, s, d):
     # the tensor-core scorer's block scores (16 heads per KV head), read from the start of the
