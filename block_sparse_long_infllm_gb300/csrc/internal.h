@@ -98,6 +98,10 @@ bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint6
 // The same over fp32 elements (row stride inner*4 bytes; box_inner*4 must be at most 128).
 bool make_tmap_f32_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
                       uint32_t box_rows);
+// 3-D bf16 tensor map over [d2][d1][d0] packed elements (strides d0*2 and d0*d1*2 bytes) with
+// box [box2][box1][box0] and the 128-byte swizzle (box0*2 at most 128); false if the driver refuses.
+bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
+                       uint32_t box1, uint32_t box2);
 
 // Stage timing (infllmv2_profile_*): no-ops unless profiling is enabled.
 void prof_begin(cudaStream_t stream);

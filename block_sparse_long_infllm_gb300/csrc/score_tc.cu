@@ -25,6 +25,7 @@
 //     (three-input max) -> block maxima -> S.
 // Waits are bounded (device error word + abort flag), TMEM is freed before exit.
 #include <algorithm>
+#include <climits>
 
 #include "internal.h"
 #include "umma.cuh"
@@ -93,12 +94,97 @@ __device__ __forceinline__ bool token_group_all(bool v, int th) {
     return r != 0;
 }
 
+// A query tile: 16 tokens of one sequence against the kernels of one KV head.
+struct ScTile {
+    int b, g;      // sequence, KV head
+    int t0;        // first token (within the sequence's chunk)
+    int n_tok;     // tokens in the tile
+    int tok;       // the sequence's first token row
+    int pos0;      // position of the sequence's query 0 (every draft's, for a tree)
+    int n_chunks;  // chunks of blocks to score (0: nothing, e.g. a dense sequence)
+};
+
+struct ScArgs {
+    const int* kv_len;
+    SeqMap sm;
+    int tree, Hkv, L_max, M_max;
+    Params p;
+    int blocks_per_chunk;
+    int tiles_x;   // tiles per (sequence, KV head): ceil(longest chunk / 16)
+    int c_max;     // chunks of the longest cache
+    int n_virt;    // tiles x c_max: the work space the CTAs split into contiguous ranges
+};
+
+// Tile `tile` (KV-head-major: consecutive tiles read the same kernel rows).  A sequence outside the
+// entry point's limits has no chunks and, with `report`, raises kDevErrIndex.
+__device__ __forceinline__ ScTile sc_tile(const ScArgs& a, int tile, bool report, int* err) {
+    ScTile t;
+    const int x = tile % a.tiles_x, bg = tile / a.tiles_x;
+    t.b = bg / a.Hkv;
+    t.g = bg % a.Hkv;
+    t.t0 = x * kScTokens;
+    t.n_tok = 0;
+    t.n_chunks = 0;
+    const int Lb = a.kv_len[t.b], Tq = a.sm.len(t.b);
+    t.tok = a.sm.tok0(t.b);
+    // query t sits at Lb - Tq + t (a chunk) or, for tree drafts, all at the last cached position
+    t.pos0 = a.tree ? Lb - 1 : Lb - Tq;
+    if (Tq < 0 || Tq > a.sm.Tq ||
+        (Tq > 0 && (Lb < (a.tree ? 1 : Tq) || Lb > a.L_max ||
+                    kernels_in(Lb, a.p.kernel_size, a.p.kernel_stride) > a.M_max))) {
+        if (report && x == 0) raise_error(err, kDevErrIndex);
+        return t;
+    }
+    // packed chunks shorter than the longest; dense sequences (every block selected) need no scores
+    if (t.t0 >= Tq || Lb < a.p.dense_len) return t;
+    t.n_tok = min(kScTokens, Tq - t.t0);
+    const int pos_last = a.tree ? t.pos0 : t.pos0 + t.t0 + t.n_tok - 1;
+    t.n_chunks = pos_last / a.p.block_size / a.blocks_per_chunk + 1;
+    return t;
+}
+
+// Walks a CTA's range of the work space (tile x c_max + chunk): next() moves to the next chunk that
+// exists (a tile's chunks past its last block are skipped), `first` tells a tile's first chunk in
+// the range.  Every role of the CTA walks the same sequence.
+struct ScCursor {
+    int v, v_end;  // next work-space index, end of the range
+    int tile, kk;  // its tile and chunk
+    int k = 0;     // the chunk next() returned
+    bool first = false, fresh = false, loaded = false;
+    ScTile t;
+    __device__ __forceinline__ ScCursor(int v0, int v1, int c_max)
+        : v(v0), v_end(v1), tile(v0 / c_max), kk(v0 - (v0 / c_max) * c_max) {}
+    __device__ __forceinline__ bool next(const ScArgs& a, bool report, int* err) {
+        while (v < v_end) {
+            if (!loaded) {
+                t = sc_tile(a, tile, report, err);
+                loaded = fresh = true;
+            }
+            if (kk < t.n_chunks) {  // (a tile's chunks are 0 .. n_chunks - 1)
+                k = kk;
+                first = fresh;
+                fresh = false;
+                ++v;
+                if (++kk == a.c_max) {
+                    ++tile;
+                    kk = 0;
+                    loaded = false;
+                }
+                return true;
+            }
+            v += a.c_max - kk;  // the rest of this tile has no chunks
+            ++tile;
+            kk = 0;
+            loaded = false;
+        }
+        return false;
+    }
+};
+
 template <int D>
 __global__ void __launch_bounds__(kScThreads, 1)
-score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kern,
-                const int* __restrict__ kv_len, SeqMap sm, int tree, int Hq, int Hkv, int L_max, int M_max, int nblk_max,
-                Params p,
-                int blocks_per_chunk, float* __restrict__ S, int* __restrict__ err) {
+score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kern, ScArgs a,
+                int Hq, int nblk_max, float* __restrict__ S, int* __restrict__ err) {
     using SM = ScSmem<D>;
     constexpr int G = 16;
     constexpr uint32_t kIdesc = idesc_bf16_f32(kScM, kScN, 0, 0);
@@ -106,64 +192,42 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
     float* kmax = reinterpret_cast<float*>(base + SM::kMaxOff);  // [token][kernel row]
-    float* xrow = reinterpret_cast<float*>(base + SM::kXOff);    // [chunk parity][quarter][lane][token]
-    uint64_t* bar_q = reinterpret_cast<uint64_t*>(base + SM::kBarOff);
+    float* xrow = reinterpret_cast<float*>(base + SM::kXOff);    // [chunk parity][quarter][token]
+    uint64_t* bar_q = reinterpret_cast<uint64_t*>(base + SM::kBarOff);  // the tile's Q landed (a phase per tile)
     uint64_t* bar_k = bar_q + 1;                 // [kScStages] kernel chunk landed
     uint64_t* bar_acc = bar_k + kScStages;       // [2] MMA of a chunk done
     uint64_t* bar_free = bar_acc + 2;            // [2] epilogue done with a TMEM buffer (kScEpi arrivals)
     uint64_t* bar_kfree = bar_free + 2;          // [kScStages] the MMA group reading a stage is done
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_kfree + kScStages);
-    volatile int* s_abort = reinterpret_cast<volatile int*>(bar_kfree + kScStages + 1);
-    static_assert((1 + 2 * kScStages + 4) * 8 + 16 <= 192, "barrier area");
+    uint64_t* bar_qfree = bar_kfree + kScStages; // the MMAs of a tile are done with Q
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_qfree + 1);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(bar_qfree + 2);
+    static_assert((2 + 2 * kScStages + 4) * 8 + 16 <= 192, "barrier area");
 
     // the top-k kernel after this one may start launching now: it waits (griddepcontrol.wait) for
     // this whole grid to complete before it reads the scores
     pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bg = blockIdx.y;
-    const int b = bg / Hkv, g = bg % Hkv;
-    const int t0 = blockIdx.x * kScTokens;
+    const Params& p = a.p;
     const int bs = p.block_size, c = p.kernel_size, s = p.kernel_stride;
-    const int Lb = kv_len[b];
-    const int Tq = sm.len(b), tok = sm.tok0(b);  // this sequence's chunk: token rows tok .. tok + Tq - 1
-    // query t sits at Lb - Tq + t (a chunk) or, for tree drafts, all at the last cached position Lb - 1
-    const int pos0 = tree ? Lb - 1 : Lb - Tq;  // position of query t is pos0 + (tree ? 0 : t)
-    if (Tq < 0 || Tq > sm.Tq ||
-        (Tq > 0 && (Lb < (tree ? 1 : Tq) || Lb > L_max || kernels_in(Lb, c, s) > M_max))) {
-        if (tid == 0 && blockIdx.x == 0) raise_error(err, kDevErrIndex);
-        return;
-    }
-    if (t0 >= Tq) return;  // packed chunks shorter than the longest
-    if (Lb < p.dense_len) return;  // dense sequence: every block is selected, no scores needed
-    const int n_tok = min(kScTokens, Tq - t0);
-    const int pos_last = tree ? pos0 : pos0 + t0 + n_tok - 1;
-    const int bt_max = pos_last / bs;
-    // chunks split, split + n_split, ... of the blocks are this CTA's (blockIdx.z = split)
-    const int split = blockIdx.z, n_split = gridDim.z;
-    const int n_chunks_all = bt_max / blocks_per_chunk + 1;
-    const int n_chunks = n_chunks_all > split ? (n_chunks_all - split + n_split - 1) / n_split : 0;
-    if (n_chunks == 0) return;
-    // the shuffle pass: block size a power-of-two multiple kr of the stride (kr <= 32), at most
-    // kScTail kernels past a block's group, and a chunk's blocks within its 128 kernel rows
+    const int bpc = a.blocks_per_chunk;
+    // this CTA's contiguous range of the work space: the tiles' chunks are split over the grid
+    // evenly (a tile may be shared by two CTAs), whatever the number of tiles
+    const int v0 = static_cast<int>(static_cast<long long>(a.n_virt) * blockIdx.x / gridDim.x);
+    const int v1 = static_cast<int>(static_cast<long long>(a.n_virt) * (blockIdx.x + 1) / gridDim.x);
+    // the shuffle pass: block size a power-of-two multiple kr of the stride (4 <= kr <= 32), at
+    // most kScTail kernels past a block's group, and a chunk's blocks within its 128 kernel rows
     const int kr = bs / s, kcs = (c + s - 1) / s;
     const bool kr_fast = bs % s == 0 && kr >= 4 && kr <= 32 && (kr & (kr - 1)) == 0 && kcs - 1 <= kScTail &&
-                         kcs - 1 <= kr && blocks_per_chunk * kr + kcs - 1 <= kScM;
-    // Local chunk k is chunk split + n_split * ((k + rot) % n_chunks) of the tile: the CTAs of a
-    // wave (consecutive tiles of one KV head, all reading the same kernel rows) start at different
-    // chunks, so that they do not all request the same 32 KB from L2 at the same time.
-    const int rot = (blockIdx.x + 5 * blockIdx.y) % n_chunks;
-    auto chunk_b0 = [&](int k) {
-        const int kk = k + rot < n_chunks ? k + rot : k + rot - n_chunks;
-        return (split + n_split * kk) * blocks_per_chunk;
-    };
-    // first kernel row of local chunk k; may be negative
+                         kcs - 1 <= kr && bpc * kr + kcs - 1 <= kScM;
+    // first kernel row of chunk k of a tile; may be negative
     auto chunk_row = [&](int k) {
-        const int b0 = chunk_b0(k);
+        const int b0 = k * bpc;
         return kr_fast ? b0 * kr - (kcs - 1) : first_kernel_of_block(b0, bs, c, s);
     };
 
     if (tid == 0) {
         mbar_init(bar_q, 1);
+        mbar_init(bar_qfree, 1);
         for (int i = 0; i < kScStages; ++i) {
             mbar_init(&bar_k[i], 1);
             mbar_init(&bar_kfree[i], 1);
@@ -191,43 +255,38 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         *s_abort = 1;
         return false;
     };
+    // A tile's Q is one 3-D box {64 columns, 16 heads, 16 tokens} per 64-column half, rows (token,
+    // head) in the MMA's layout.  A ragged tile's last box rows hold the next sequence's queries or
+    // the fill value: their scores are never stored.
     if (warp == kScEpiWarps + 1) {
-        // ======================= loader warp: the copies, issued apart from the MMA issuer (a thread
-        // that issues an MMA group is held for about its duration, so copies issued by the same
-        // warp waited behind it); the boxes of a copy go out from different lanes
+        // ======================= loader warp: the kernel-row copies, issued apart from the MMA
+        // issuer (a thread that issues an MMA group is held for about its duration, so copies
+        // issued by the same warp waited behind it); the boxes of a copy go out from different lanes
+        ScCursor cur(v0, v1, a.c_max);
         int n_loaded = 0;  // chunks are loaded in order: stage st holds loads st, st + kScStages, ...
-        // Q tile: 16 tokens x 16 heads, one 16-row box per token and 64-column half (lane 16 sub + tk)
-        if (lane == 0) mbar_arrive_expect_tx(bar_q, SM::kQ);
-        __syncwarp();
-        {
-            static_assert(kScTokens * 2 <= 32, "a lane per Q box");
-            const int tk = lane % kScTokens, sub = lane / kScTokens;
-            if (sub < D / 64) {
-                const int t = min(t0 + tk, Tq - 1);
-                const int qrow = (tok + t) * Hq + g * G;
-                tma_load_2d(base + SM::kQOff + sub * (kScN * 128) + tk * (G * 128), &tm_q, 64 * sub, qrow, bar_q);
-            }
-        }
-        // chunk ch into stage ch % kScStages once the MMA group of chunk ch - kScStages is done:
-        // lane 2 sub + rh issues rows 64 rh .. 64 rh + 63 of column half sub
-        for (int ch = 0; ch < n_chunks; ++ch) {
-            const int st = ch % kScStages;
+        while (cur.next(a, false, err)) {
+            const ScTile& t = cur.t;
+            // a new tile: start its Q rows towards L2, for the MMA warp's copy when the previous
+            // tile's MMAs are done (this warp runs up to kScStages chunks ahead of them)
+            if (cur.first && n_loaded > 0 && lane < D / 64) tma_prefetch_3d(&tm_q, 64 * lane, t.g * G, t.tok + t.t0);
+            // chunk n_loaded into stage n_loaded % kScStages once the MMA group of the chunk before
+            // it in that stage is done: lane 2 sub + rh issues rows 64 rh .. 64 rh + 63 of column half sub
+            const int st = n_loaded % kScStages;
             bool ok = true;
-            if (lane == 0 && ch >= kScStages) ok = wait(&bar_kfree[st], (ch / kScStages - 1) & 1);
+            if (lane == 0 && n_loaded >= kScStages) ok = wait(&bar_kfree[st], (n_loaded / kScStages - 1) & 1);
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             if (lane == 0) mbar_arrive_expect_tx(&bar_k[st], SM::kK);
             __syncwarp();
             if (lane < 2 * (D / 64)) {
                 const int sub = lane >> 1, rh = lane & 1;
                 tma_load_2d(base + SM::kKOff + st * SM::kK + sub * (kScM * 128) + rh * (64 * 128), &tm_kern, 64 * sub,
-                            bg * M_max + chunk_row(ch) + 64 * rh, &bar_k[st]);
+                            (t.b * a.Hkv + t.g) * a.M_max + chunk_row(cur.k) + 64 * rh, &bar_k[st]);
             }
             ++n_loaded;
         }
         // every copy has landed before shared memory goes away
         if (lane == 0) {
             const long long drain = kWaitBudgetCycles / 8;
-            mbar_wait(bar_q, 0, drain);
             for (int st = 0; st < kScStages && st < n_loaded; ++st) {
                 const int uses = (n_loaded - st + kScStages - 1) / kScStages;  // loads into stage st
                 mbar_wait(&bar_k[st], (uses - 1) & 1, drain);
@@ -236,12 +295,27 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     } else if (warp == kScEpiWarps) {
         // ======================= MMA warp (one lane): one tcgen05 group per chunk into TMEM buffer
         // ch & 1; a commit frees the chunk's stage for the loader, another hands the buffer to the
-        // epilogue
+        // epilogue.  At a tile's first chunk it copies the tile's Q once the previous tile's MMAs
+        // are done with the one buffer.
         if (lane == 0) {
             const uint32_t sQ = smem_u32(base + SM::kQOff);
-            int mma_issued = 0;
-            bool ok = wait(bar_q, 0);
-            for (int ch = 0; ok && ch < n_chunks; ++ch) {
+            ScCursor cur(v0, v1, a.c_max);
+            int ch = 0, n_q = 0;  // chunks issued, Q tiles copied
+            bool ok = true;
+            while (ok && cur.next(a, false, err)) {
+                if (cur.first) {
+                    if (n_q > 0) {
+                        mma_commit(bar_qfree);
+                        if (!(ok = wait(bar_qfree, (n_q - 1) & 1))) break;
+                    }
+                    mbar_arrive_expect_tx(bar_q, SM::kQ);
+#pragma unroll
+                    for (int sub = 0; sub < D / 64; ++sub)
+                        tma_load_3d(base + SM::kQOff + sub * (kScN * 128), &tm_q, 64 * sub, cur.t.g * G,
+                                    cur.t.tok + cur.t.t0, bar_q);
+                    ++n_q;
+                    if (!(ok = wait(bar_q, (n_q - 1) & 1))) break;
+                }
                 const int st = ch % kScStages, tb = ch & 1;
                 if (!(ok = wait(&bar_k[st], (ch / kScStages) & 1))) break;
                 if (ch >= 2 && !(ok = wait(&bar_free[tb], ((ch - 2) >> 1) & 1))) break;
@@ -256,10 +330,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 mma_commit(&bar_acc[tb]);
                 mma_commit(&bar_kfree[st]);
-                ++mma_issued;
+                ++ch;
             }
-            if (mma_issued > 0)
-                mbar_wait(&bar_acc[(mma_issued - 1) & 1], ((mma_issued - 1) >> 1) & 1, kWaitBudgetCycles / 8);
+            const long long drain = kWaitBudgetCycles / 8;
+            if (n_q > 0) mbar_wait(bar_q, (n_q - 1) & 1, drain);  // the last Q copy has landed
+            if (ch > 0) mbar_wait(&bar_acc[(ch - 1) & 1], ((ch - 1) >> 1) & 1, drain);
         }
     } else {
         // ======================= epilogue: thread r = 32*(warp%4) + lane owns kernel row r of each
@@ -282,32 +357,37 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tmem_ld_wait_max2(r0, r1, mx[0], mx[1]);
             tmem_ld_wait_max2(r2, r3, mx[2], mx[3]);
         };
+        ScCursor cur(v0, v1, a.c_max);
+        const bool report = tid == 0;
+        int ch = 0;  // chunks taken (TMEM buffer ch & 1)
         if (kr_fast) {
-            // the tile's first query's last visible kernel: no row of a chunk that ends at or
-            // before it needs the mask (that query has the tile's smallest position)
-            const int pos_first = tree ? pos0 : pos0 + t0;
-            const int jv_first = pos_first + 1 >= c ? (pos_first + 1 - c) / s : -1;
             // After the block maxima below, lane l of a group of kr holds token tau(l) = 2 (l & 1) +
-            // ((l >> 1) & 1) of this thread's four (lanes l and l + 4, l + 8 ... hold the same one):
-            // that token's last block and row of S.
+            // ((l >> 1) & 1) of this thread's four (lanes l and l + 4, l + 8 ... hold the same one).
             const int tau = 2 * (lane & 1) + ((lane >> 1) & 1);
-            int my_bt = -1, my_row = 0;
-#pragma unroll
-            for (int u = 0; u < kScTpt; ++u)
-                if (u == tau && tk0 + u < n_tok) {
-                    const int pos = tree ? pos0 : pos0 + t0 + tk0 + u;
-                    my_bt = pos / bs;
-                    my_row = sm.sel(b, g, Hkv, t0 + tk0 + u);
-                }
             const int kr_log = __ffs(kr) - 1;
             const int T = kcs - 1;  // kernels of a block past its aligned group of kr
             // the group that ends this lane quarter takes its T tail rows from the next quarter
             const bool takes_tail = T > 0 && q4 < 3 && lane >= 32 - kr && (lane & (kr - 1)) < 4;
-            for (int ch = 0; ch < n_chunks; ++ch) {
+            int my_bt = -1, my_row = 0, jv_first = -1;
+            while (cur.next(a, report, err)) {
+                const ScTile& t = cur.t;
+                if (cur.first) {
+                    // token tau's last block and row of S; the tile's first query's last visible
+                    // kernel (no row of a chunk that ends at or before it needs the mask: that query
+                    // has the tile's smallest position)
+                    my_bt = -1;
+                    if (tk0 + tau < t.n_tok) {
+                        const int pos = a.tree ? t.pos0 : t.pos0 + t.t0 + tk0 + tau;
+                        my_bt = pos / bs;
+                        my_row = static_cast<int>(a.sm.sel(t.b, t.g, a.Hkv, t.t0 + tk0 + tau));
+                    }
+                    const int pos_first = a.tree ? t.pos0 : t.pos0 + t.t0;
+                    jv_first = pos_first + 1 >= c ? (pos_first + 1 - c) / s : -1;
+                }
                 const int tb = ch & 1;
                 const bool waited = !*s_abort && mbar_wait(&bar_acc[tb], (ch >> 1) & 1);
                 tc_fence_after();
-                const int b0 = chunk_b0(ch);
+                const int b0 = cur.k * bpc;
                 const int jlo = b0 * kr - T;  // kernel of row 0 (negative: before the cache)
                 float mx[kScTpt];
                 row_maxima(tb, mx);
@@ -319,8 +399,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     for (int u = 0; u < kScTpt; ++u) {
                         // the token's last visible kernel (-1: no such token)
                         const int tk = tk0 + u;
-                        const int pos = tree ? pos0 : pos0 + t0 + tk;
-                        const int jv = tk < n_tok && pos + 1 >= c ? (pos + 1 - c) / s : -1;
+                        const int pos = a.tree ? t.pos0 : t.pos0 + t.t0 + tk;
+                        const int jv = tk < t.n_tok && pos + 1 >= c ? (pos + 1 - c) / s : -1;
                         if (j < 0 || j > jv) mx[u] = -INFINITY;
                     }
                 }
@@ -331,12 +411,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 float f[kScTpt];
 #pragma unroll
                 for (int u = 0; u < kScTpt; ++u) f[u] = mx[u];
-                for (int t = 1; t <= T; ++t) {
-                    if (t == T && lane == 0)
+                for (int tt = 1; tt <= T; ++tt) {
+                    if (tt == T && lane == 0)
                         *reinterpret_cast<float4*>(xrow + (tb * 4 + q4) * kScTokens + tk0) =
                             make_float4(f[0], f[1], f[2], f[3]);
 #pragma unroll
-                    for (int u = 0; u < kScTpt; ++u) f[u] = fmaxf(f[u], __shfl_down_sync(0xffffffffu, mx[u], t));
+                    for (int u = 0; u < kScTpt; ++u) f[u] = fmaxf(f[u], __shfl_down_sync(0xffffffffu, mx[u], tt));
                 }
                 // maxima over each group of kr lanes (kr >= 4), exchanging tokens on the way: after
                 // the xor-1 step a lane keeps two tokens, after the xor-2 step one (tau)
@@ -356,21 +436,23 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (takes_tail) m = fmaxf(m, xrow[(tb * 4 + q4 + 1) * kScTokens + tk0 + tau]);
                 const int i = r >> kr_log;  // this lane's block in the chunk
                 const int blk = b0 + i;
-                if ((lane & (kr - 1)) < 4 && i < blocks_per_chunk && blk <= my_bt)
+                if ((lane & (kr - 1)) < 4 && i < bpc && blk <= my_bt)
                     S[static_cast<size_t>(my_row) * nblk_max + blk] = m;
+                ++ch;
             }
         } else {
-            for (int ch = 0; ch < n_chunks; ++ch) {
+            while (cur.next(a, report, err)) {
+                const ScTile& t = cur.t;
                 const int tb = ch & 1;
                 const bool waited = !*s_abort && mbar_wait(&bar_acc[tb], (ch >> 1) & 1);
-                // all eight epilogue warps leave together: they meet at the named barrier below
+                // all epilogue warps leave together: they meet at the named barrier below
                 if (!epilogue_all(waited)) {
                     if (tid == 0 && !*s_abort) raise_error(err, kDevErrTimeout);
                     *s_abort = 1;
                     break;
                 }
                 tc_fence_after();
-                const int b0 = chunk_b0(ch);
+                const int b0 = cur.k * bpc;
                 const int j0 = first_kernel_of_block(b0, bs, c, s);
                 const int j = j0 + r;
                 const int jend = j * s + c - 1;  // last token of kernel j
@@ -379,25 +461,27 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int u = 0; u < kScTpt; ++u) {
                     const int tk = tk0 + u;
-                    const int pos = tree ? pos0 : pos0 + t0 + tk;
-                    kmax[tk * kScM + r] = (tk < n_tok && jend <= pos) ? mx[u] : -INFINITY;
+                    const int pos = a.tree ? t.pos0 : t.pos0 + t.t0 + tk;
+                    kmax[tk * kScM + r] = (tk < t.n_tok && jend <= pos) ? mx[u] : -INFINITY;
                 }
                 tc_fence_before();
                 mbar_arrive(&bar_free[tb]);  // this thread is done with the TMEM buffer
                 asm volatile("bar.sync 1, %0;" ::"n"(kScEpi) : "memory");
                 // block max over the kernels each block overlaps, for every token of the tile
-                const int nb = min(blocks_per_chunk, bt_max + 1 - b0);
-                for (int e2 = tid; e2 < n_tok * nb; e2 += kScEpi) {
+                const int pos_last = a.tree ? t.pos0 : t.pos0 + t.t0 + t.n_tok - 1;
+                const int nb = min(bpc, pos_last / bs + 1 - b0);
+                for (int e2 = tid; e2 < t.n_tok * nb; e2 += kScEpi) {
                     const int tk = e2 / nb, blk = b0 + e2 % nb;
-                    const int pos = tree ? pos0 : pos0 + t0 + tk;
+                    const int pos = a.tree ? t.pos0 : t.pos0 + t.t0 + tk;
                     if (blk > pos / bs) continue;
                     const int ja = first_kernel_of_block(blk, bs, c, s) - j0;
                     const int jz = min(last_kernel_of_block(blk, bs, s) - j0, kScM - 1);
-                    float m = -INFINITY;
-                    for (int jj = ja; jj <= jz; ++jj) m = fmaxf(m, kmax[tk * kScM + jj]);
-                    S[sm.sel(b, g, Hkv, t0 + tk) * nblk_max + blk] = m;
+                    float mm = -INFINITY;
+                    for (int jj = ja; jj <= jz; ++jj) mm = fmaxf(mm, kmax[tk * kScM + jj]);
+                    S[a.sm.sel(t.b, t.g, a.Hkv, t.t0 + tk) * nblk_max + blk] = mm;
                 }
                 asm volatile("bar.sync 1, %0;" ::"n"(kScEpi) : "memory");  // kmax is rewritten by the next chunk
+                ++ch;
             }
         }
     }
@@ -419,39 +503,62 @@ int score_tc_blocks_per_chunk(const Params& p) {
     return 0;
 }
 
+// The work space of a launch: tiles x chunks of the longest cache (0 when there is nothing to
+// score; -1 when it does not fit the kernel's int indexing).
+static long long score_tc_work(const SelectArgs& a, int blocks_per_chunk) {
+    const int nblk_max = (a.L_max + a.p.block_size - 1) / a.p.block_size;
+    if (nblk_max <= 0 || a.Tq <= 0) return 0;
+    const long long n = static_cast<long long>((a.Tq + kScTokens - 1) / kScTokens) * a.B * a.Hkv *
+                        ((nblk_max - 1) / blocks_per_chunk + 1);
+    return n <= INT_MAX / 2 ? n : -1;
+}
+
 bool score_tc_supported(const SelectArgs& a) {
     return a.Hq / a.Hkv == 16 && (a.d == 64 || a.d == 128) && a.M_max > 0 &&
-           score_tc_blocks_per_chunk(a.p) > 0;
+           score_tc_blocks_per_chunk(a.p) > 0 && score_tc_work(a, score_tc_blocks_per_chunk(a.p)) >= 0;
 }
 
 cudaError_t launch_score_tc(const SelectArgs& a, float* S) {
     const int nb = score_tc_blocks_per_chunk(a.p);
     const int nblk_max = (a.L_max + a.p.block_size - 1) / a.p.block_size;
+    const long long n_virt = score_tc_work(a, nb);
+    if (n_virt < 0) return cudaErrorInvalidValue;
+    if (n_virt == 0) return cudaSuccess;
     CUtensorMap tq, tk;
     const SeqMap sm = a.seqmap();
-    const uint64_t q_rows = static_cast<uint64_t>(sm.total) * a.Hq;
     const uint64_t k_rows = static_cast<uint64_t>(a.B) * a.Hkv * a.M_max;
-    if (!make_tmap_bf16_2d(&tq, a.q, a.d, q_rows, 64, 16) || !make_tmap_bf16_2d(&tk, a.kernel_cache, a.d, k_rows, 64, kScM / 2))
+    if (!make_tmap_bf16_3d(&tq, a.q, a.d, a.Hq, sm.total, 64, 16, kScTokens) ||
+        !make_tmap_bf16_2d(&tk, a.kernel_cache, a.d, k_rows, 64, kScM / 2))
         return cudaErrorInvalidValue;
-    // few query tiles (a draft tree, a short chunk): split each tile's chunks of blocks over CTAs
-    const int tiles = ((a.Tq + kScTokens - 1) / kScTokens) * a.B * a.Hkv;
-    const int chunks_max = (nblk_max - 1) / nb + 1;
-    const int n_split = std::max(1, std::min(chunks_max, 300 / std::max(tiles, 1)));
-    dim3 grid((a.Tq + kScTokens - 1) / kScTokens, a.B * a.Hkv, n_split);
+    ScArgs sa;
+    sa.kv_len = a.kv_len;
+    sa.sm = sm;
+    sa.tree = a.tree;
+    sa.Hkv = a.Hkv;
+    sa.L_max = a.L_max;
+    sa.M_max = a.M_max;
+    sa.p = a.p;
+    sa.blocks_per_chunk = nb;
+    sa.tiles_x = (a.Tq + kScTokens - 1) / kScTokens;
+    sa.c_max = (nblk_max - 1) / nb + 1;
+    sa.n_virt = static_cast<int>(n_virt);
+    // one CTA per SM (shared memory and TMEM allow no second), each a contiguous share of the work
+    int dev = 0, n_sm = 0;
+    if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
+    if (cudaError_t e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev); e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>(std::min<long long>(std::max(n_sm, 1), n_virt)));
     if (a.d == 128) {
         auto kfn = score_tc_kernel<128>;
         constexpr int smem = ScSmem<128>::kBytes;
         if (cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); e != cudaSuccess)
             return e;
-        return launch_kernel(kfn, grid, dim3(kScThreads), smem, a.stream, false, tq, tk, a.kv_len, sm, a.tree, a.Hq, a.Hkv,
-                             a.L_max, a.M_max, nblk_max, a.p, nb, S, a.err);
+        return launch_kernel(kfn, grid, dim3(kScThreads), smem, a.stream, false, tq, tk, sa, a.Hq, nblk_max, S, a.err);
     }
     auto kfn = score_tc_kernel<64>;
     constexpr int smem = ScSmem<64>::kBytes;
     if (cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); e != cudaSuccess)
         return e;
-    return launch_kernel(kfn, grid, dim3(kScThreads), smem, a.stream, false, tq, tk, a.kv_len, sm, a.tree, a.Hq, a.Hkv,
-                         a.L_max, a.M_max, nblk_max, a.p, nb, S, a.err);
+    return launch_kernel(kfn, grid, dim3(kScThreads), smem, a.stream, false, tq, tk, sa, a.Hq, nblk_max, S, a.err);
 }
 
 }  // namespace infllmv2
