@@ -28,6 +28,7 @@
 #include <climits>
 
 #include "internal.h"
+#include "tc_extra.cuh"
 #include "umma.cuh"
 
 namespace infllmv2 {
