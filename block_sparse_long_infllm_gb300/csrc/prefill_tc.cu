@@ -28,6 +28,7 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "tc_extra.cuh"
 #include "umma.cuh"
 
 namespace infllmv2 {
@@ -348,13 +349,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // warp waits for its P(j) stores, so the two latencies overlap.  Both warps of a pair
         // see the same tokens, so they take the same branches and meet at the same barriers.
         uint32_t ra[32], rb[32];
+        float ma = -INFINITY, mb = -INFINITY;  // the loaded columns' maxima (load-reduce)
         auto chooses = [&](int jj) -> bool {  // warp-uniform: does any row of this warp attend block jj?
             return __any_sync(0xffffffffu, live && ((umask[jj] >> tk) & 1u));
         };
         auto load_s = [&](int sbuf) {
             const uint32_t tS = tmem + sbuf * BS + lane_off + h * HB;
-            tmem_ld32(tS, ra);
-            if constexpr (HB == 64) tmem_ld32(tS + 32, rb);
+            tmem_ld32_max(tS, ra, ma);
+            if constexpr (HB == 64) tmem_ld32_max(tS + 32, rb, mb);
         };
         if (U > 0) {
             const bool waited = !*s_abort && mbar_wait(&bar_s[0], 0);
@@ -374,30 +376,36 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const uint32_t sph1 = sb1 == 0 ? sph ^ 1u : sph;
             if (__any_sync(0xffffffffu, chose)) {
                 // S(j) of this half, in place in the load registers (column c in ra / rb)
-                tmem_ld_wait(ra);
-                if constexpr (HB == 64) reg_fence(rb);
+                tmem_ld_wait_max32(ra, ma);
+                if constexpr (HB == 64) {
+                    reg_fence(rb);
+                    asm volatile("" : "+f"(mb));
+                }
                 auto sv = [&](int c) -> float { return __uint_as_float(c < 32 ? ra[c] : rb[c - 32]); };
                 // valid keys of a row that chose the block: x = blk*BS + c <= pos (only the
                 // query's own block is partial); rows that did not choose it get p = 0 below
                 const int n_valid = min(BS, pos - ublk[j] * BS + 1) - h * HB;
+                // row maximum of this half: from the load-reduces, except in the query's own
+                // (partial) block, whose keys past the query are masked first
+                float mh = HB == 64 ? fmaxf(ma, mb) : ma;
                 if (__any_sync(0xffffffffu, chose && n_valid < HB)) {
 #pragma unroll
                     for (int c = 0; c < HB; ++c) {
                         uint32_t& x = c < 32 ? ra[c] : rb[c - 32];
                         x = c < n_valid ? x : __float_as_uint(-INFINITY);
                     }
+                    // eight independent chains of three-input maxima
+                    float mc[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mc[k] = sv(k);
+#pragma unroll
+                    for (int c = 8; c + 16 <= HB; c += 16)
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) mc[k] = fmax3f(mc[k], sv(c + k), sv(c + 8 + k));
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mc[k] = fmaxf(mc[k], sv(HB - 8 + k));
+                    mh = fmax3f(fmax3f(mc[0], mc[1], mc[2]), fmax3f(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
                 }
-                // row maximum of this half: eight independent chains of three-input maxima
-                float mc[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) mc[k] = sv(k);
-#pragma unroll
-                for (int c = 8; c + 16 <= HB; c += 16)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) mc[k] = fmax3f(mc[k], sv(c + k), sv(c + 8 + k));
-#pragma unroll
-                for (int k = 0; k < 8; ++k) mc[k] = fmaxf(mc[k], sv(HB - 8 + k));
-                const float mh = fmax3f(fmax3f(mc[0], mc[1], mc[2]), fmax3f(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
                 pmax[h * 128 + r] = mh;
                 asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
                 const float mb = fmaxf(mh, pmax[(1 - h) * 128 + r]);

@@ -1,6 +1,6 @@
-// tc_extra.cuh -- device helpers for the 3-D TMA boxes and the TMEM load-reduce (sm_103a) of the
-// tensor-core block scorer: 3-D tiled copies and L2 prefetches, and 16-column TMEM loads that also
-// return the columns' maximum.
+// tc_extra.cuh -- device helpers of the tensor-core scorer and attention: 3-D tiled copies and L2
+// prefetches, and TMEM loads that also return the loaded columns' maximum (the load-reduce form
+// of tcgen05.ld, sm_103a).
 #pragma once
 
 #include "tma.cuh"
@@ -45,6 +45,33 @@ __device__ __forceinline__ void tmem_ld_wait_max2(uint32_t (&a)[16], uint32_t (&
                    "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]),
                    "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15]),
                    "+f"(ma), "+f"(mb)
+                 :
+                 : "memory");
+}
+
+// 32 consecutive 32-bit columns of this thread's TMEM lane read as f32, and their maximum (written
+// asynchronously: valid after tmem_ld_wait_max32).
+__device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, uint32_t (&r)[32], float& m) {
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, %32, [%33];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=f"(m)
+        : "r"(taddr));
+}
+// Wait for this thread's outstanding TMEM loads with one load-reduce's columns and maximum tied to
+// the wait.
+__device__ __forceinline__ void tmem_ld_wait_max32(uint32_t (&r)[32], float& m) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+                   "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]),
+                   "+f"(m)
                  :
                  : "memory");
 }
