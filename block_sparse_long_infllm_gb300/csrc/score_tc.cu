@@ -215,6 +215,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // evenly (a tile may be shared by two CTAs), whatever the number of tiles
     const int v0 = static_cast<int>(static_cast<long long>(a.n_virt) * blockIdx.x / gridDim.x);
     const int v1 = static_cast<int>(static_cast<long long>(a.n_virt) * (blockIdx.x + 1) / gridDim.x);
+    {
+        // a range without a chunk to score (e.g. one tile past a packed sequence's end) ends here,
+        // before any setup; an invalid sequence is reported by the CTA holding its first tile
+        ScCursor probe(v0, v1, a.c_max);
+        if (!probe.next(a, tid == 0, err)) return;
+    }
     // the shuffle pass: block size a power-of-two multiple kr of the stride (4 <= kr <= 32), at
     // most kScTail kernels past a block's group, and a chunk's blocks within its 128 kernel rows
     const int kr = bs / s, kcs = (c + s - 1) / s;
@@ -543,11 +549,14 @@ cudaError_t launch_score_tc(const SelectArgs& a, float* S) {
     sa.tiles_x = (a.Tq + kScTokens - 1) / kScTokens;
     sa.c_max = (nblk_max - 1) / nb + 1;
     sa.n_virt = static_cast<int>(n_virt);
-    // one CTA per SM (shared memory and TMEM allow no second), each a contiguous share of the work
+    // Equal-length sequences: one CTA per SM (shared memory and TMEM allow no second), each a
+    // contiguous share of the work.  Packed sequences of different lengths leave most of the work
+    // space empty and unevenly so: one CTA per tile there, balanced by the hardware's scheduling.
     int dev = 0, n_sm = 0;
     if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
     if (cudaError_t e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev); e != cudaSuccess) return e;
-    const dim3 grid(static_cast<unsigned>(std::min<long long>(std::max(n_sm, 1), n_virt)));
+    const long long n_tiles = n_virt / sa.c_max;
+    const dim3 grid(static_cast<unsigned>(sm.cu != nullptr ? n_tiles : std::min<long long>(std::max(n_sm, 1), n_virt)));
     if (a.d == 128) {
         auto kfn = score_tc_kernel<128>;
         constexpr int smem = ScSmem<128>::kBytes;
