@@ -650,7 +650,7 @@ def run_prefill(args) -> dict:
             "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": round(att_tf, 2),
                          "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(att_tf / pk["bf16_tflops"], 4),
                          "traffic": ncu_traffic("prefill_tc_kernel",
-                                                source_sha("prefill_tc.cu", "umma.cuh", "common.cuh", "tma.cuh"))},
+                                                source_sha("prefill_tc.cu", "umma.cuh", "common.cuh", "tma.cuh", "tc_extra.cuh"))},
             "step_tflops": round(step_tf, 2), "step_frac": round(step_tf / pk["bf16_tflops"], 4),
             "gpu_launches": 4 * K, "backward": backward}
 
