@@ -3,26 +3,30 @@
 // at kernel granularity, max over the kernels of a block and over a group's heads).
 //
 // The scoring is a GEMM per KV head: every (query token, head) row against every visible
-// semantic kernel.  One CTA owns 16 query tokens x the 16 heads of one KV head (256 Q rows,
-// the MMA's N) and walks the kernel cache in chunks of 128 kernels (the MMA's M), so each
-// accumulator lane holds one kernel against all 256 rows: the max over a token's 16 heads and
-// the visibility test (the kernel ends at or before the token's position) are thread-local.
-// Chunks cover whole blocks (31 blocks of 64 tokens or 15 of 128), so no block straddles two
-// chunks.  When the block size is a power-of-two multiple r of the stride, a chunk starts
-// ceil(c/s) - 1 kernels before its first block (a negative kernel index reads the TMA fill value
-// and is masked), so block i of the chunk overlaps kernel rows r*i .. r*i + r + ceil(c/s) - 2: the
-// block max is a max over r aligned accumulator lanes and the first ceil(c/s) - 1 lanes after
-// them, taken by warp shuffles (the lanes past a warp's last come from the next warp through a
-// small shared array, one barrier per chunk).  Otherwise the per-(token, kernel) maxima go to
-// shared memory, where each block's max over its kernels is taken.  The result goes to
-// S[b, g, t, block].
-//   * producer warp (warp 8, one lane): TMA of the Q tile once and of each chunk's kernel rows
-//     into a ring of four shared stages; one tcgen05 MMA group per chunk into one of two TMEM
-//     buffers; a stage is refilled once the MMA group after the one reading it is queued;
-//   * epilogue warps (warps 0-15, four per TMEM lane quarter, 4 of the 16 tokens each: with
-//     two warps per scheduler the dependent steps of the maxima were not hidden): TMEM ->
-//     registers (both loads of a thread in flight before one wait) -> maxima over the heads
-//     (three-input max) -> block maxima -> S.
+// semantic kernel.  A work unit is a tile of 16 query tokens x the 16 heads of one KV head (256 Q
+// rows, the MMA's N) against one chunk of 128 kernels (the MMA's M), so each accumulator lane
+// holds one kernel against all 256 rows: the max over a token's 16 heads and the visibility test
+// (the kernel ends at or before the token's position) are thread-local.  Chunks cover whole
+// blocks (31 blocks of 64 tokens or 15 of 128), so no block straddles two chunks.  When the block
+// size is a power-of-two multiple r >= 4 of the stride, a chunk starts ceil(c/s) - 1 kernels
+// before its first block (a negative kernel index reads the TMA fill value and is masked), so
+// block i of the chunk overlaps kernel rows r*i .. r*i + r + ceil(c/s) - 2: each lane folds in the
+// rows after it, then warp shuffles take the max over the r aligned lanes while handing tokens
+// between lanes (the rows past a warp's last come from the next warp through a small shared
+// array, one barrier per chunk among the four warps of the same tokens).  Otherwise the
+// per-(token, kernel) maxima go to shared memory, where each block's max over its kernels is
+// taken.  The result goes to S[b, g, t, block].
+//
+// The kernel is persistent: one CTA per SM walks a contiguous share of the (tile x chunk) space,
+// so a tile's chunks may be split between two CTAs (packed sequences of uneven lengths take one
+// CTA per tile instead).  Per CTA:
+//   * loader warp: TMA of each chunk's kernel rows into a ring of four shared stages (a stage is
+//     refilled once the MMA group reading it is done), four lanes issuing the boxes; at a new
+//     tile, its Q rows started towards L2;
+//   * MMA warp (one lane): at a new tile, its Q (two 3-D boxes) once the previous tile's MMAs are
+//     done with the buffer; one tcgen05 MMA group per chunk into one of two TMEM buffers;
+//   * epilogue warps (warps 0-15, four per TMEM lane quarter, 4 of the 16 tokens each): TMEM
+//     load-reduces (each token's 16 columns and their maximum in one load) -> block maxima -> S.
 // Waits are bounded (device error word + abort flag), TMEM is freed before exit.
 #include <algorithm>
 #include <climits>
