@@ -54,7 +54,9 @@ struct ScSmem {
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQ;              // kScStages stages
     static constexpr int kMaxOff = kQ + kScStages * kK;  // [kScTokens][kScM] floats (general pass)
-    static constexpr int kXOff = kMaxOff + kScTokens * kScM * 4;  // [2][4][kScTail][kScTokens] floats
+    // [2][4][kScTokens] floats: the tail maxima each lane quarter publishes, per chunk parity
+    // (the area has room for kScTail rows of them)
+    static constexpr int kXOff = kMaxOff + kScTokens * kScM * 4;
     static constexpr int kBarOff = kXOff + 2 * 4 * kScTail * kScTokens * 4;
     static constexpr int kBytes = kBarOff + 192 + 1024;
 };
